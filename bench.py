@@ -1,0 +1,531 @@
+"""Benchmark of the fused ZeRO optimizer step on GB300.
+
+Default workload: the GPT-2-small parameter list (124,356,864 parameters, flattened) with
+N = 8 simulated data-parallel ranks, ZeRO-2, 25 MiB buckets. One step = one launch of the
+fused reduce-scatter + Adam + bf16 all-gather kernel over every rank's shard: it reads the
+8 ranks' bf16 gradients and the fp32 master / m / v and writes master / m / v and the full
+bf16 parameter buffer: P * (2N + 26) = 5.22 GB of HBM traffic per step, far above the
+129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
+
+Prints ONE JSON line (rank 0). Under torchrun each rank runs an independent replica on
+its own GPU (the simulated ranks live on one GPU; there is no inter-GPU exchange), and
+`value` is the parameters all GPUs updated per second over the slowest rank's time.
+--impl reference times the CPU oracle on the host cores on a bounded sample of the same
+workload. --sweep prints one line per point of the 1.5B-parameter bandwidth sweep.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "fused ZeRO step params/s and HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "params/s"
+MIB = 1 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def workload_config(psi, n, stage, bb):
+    return {
+        "workload": f"GPT-2-small parameter list ({psi:,} params) flattened, N={n} simulated data-parallel ranks, "
+                    f"{stage.upper()} fused reduce-scatter + Adam + bf16 param all-gather, {bb // MIB} MiB buckets, "
+                    "every rank's shard in one launch per step",
+        "psi": psi, "n_ranks": n, "stage": stage, "bucket_bytes": bb,
+        "adam": {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0},
+        "grads": "bf16 N(0,1e-3) per rank", "master": "fp32 N(0,0.02)",
+        "l2": "inputs larger than L2 (5.22 GB per step vs 129 MB L2): no flush",
+    }
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        mhz, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------------------
+# traffic from the committed ncu summary (valid only while the kernel source is unchanged)
+# ---------------------------------------------------------------------------------------
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for name in ("step_kernels.cu", "device_common.cuh"):
+        h.update((ROOT / "fsdp_sharded_optimizer_zero_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, bytes_per_unit_launch: float):
+    """dram read + write bytes per launch of `kernel` from profiles/ncu_traffic.txt, scaled
+    to this launch by units processed, or None when absent or taken on other source."""
+    p = ROOT / "profiles" / "ncu_traffic.txt"
+    if not p.exists():
+        return None
+    for line in p.read_text().splitlines():
+        if line.startswith("#") or not line.strip():
+            continue
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") == kernel and f.get("source") == kernel_source_digest():
+            return float(f["dram_bytes_per_unit"]) * bytes_per_unit_launch
+    return None
+
+
+# ---------------------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------------------
+
+def init_dist(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_ours(args):
+    import torch
+
+    import fsdp_sharded_optimizer_zero_gb300 as z
+    import synth
+
+    world, rank, local = init_dist(args)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hbm_peak, tf_burst, tf_sust, peak_src = peaks()
+    psi, n, stage, bb = synth.GPT2_SMALL_PSI, 8, "zero2", 25 * MIB
+    plan = z.zero_plan(psi, n, stage, bb)
+    P = plan.psi_padded
+    bytes_per_step = plan.fused_step_bytes
+    grads = [synth.rank_grads(psi, P, r, 1, device=dev) for r in range(n)]
+    master = synth.master_params(psi, P, device=dev)
+    m = torch.zeros(P, device=dev)
+    v = torch.zeros(P, device=dev)
+    param = torch.empty(P, dtype=torch.bfloat16, device=dev)
+    hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+    stream = torch.cuda.current_stream()
+    step_no = 0
+
+    def step():
+        nonlocal step_no
+        step_no += 1
+        z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, step_no, stream)
+
+    for _ in range(args.warmup):
+        step()
+    z.zero_device_status(stream)
+    torch.cuda.synchronize()
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(K):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    z.zero_device_status(stream)
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world)
+    ms_step = ms_total / K
+    launch_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    value = world * psi * K / (ms_total / 1e3)
+    achieved = bytes_per_step / (launch_ms / 1e3) / 1e9
+    clocks = clk.summary()
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; GPT-2-small tensor shapes, random values; no dataset, no weights)",
+        "config": workload_config(psi, n, stage, bb),
+        "hbm_gbs": bytes_per_step * K * world / (ms_total / 1e3) / 1e9,
+        "hbm_pct_of_peak": 100.0 * (bytes_per_step * K / (ms_total / 1e3) / 1e9) / hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": "fused_tma_kernel", "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "traffic": ncu_traffic("fused_tma_kernel", P),
+                     "algorithmic_bytes_per_launch": bytes_per_step, "launch_ms": launch_ms},
+        "clocks": clocks,
+        "gpu_launches": K,
+    }
+    # end to end through the public API: grads from pinned host memory, params back
+    out["e2e"] = e2e_leg(z, synth, plan, psi, n, dev, hp, world, args)
+    if not args.no_legs:
+        out["legs"] = extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_leg(z, synth, plan, psi, n, dev, hp, world, args):
+    import torch
+    P = plan.psi_padded
+    host_grads = [synth.rank_grads(psi, P, r, 2).pin_memory() for r in range(n)]
+    dgrads = [torch.empty(P, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    master = synth.master_params(psi, P, device=dev)
+    m = torch.zeros(P, device=dev)
+    v = torch.zeros(P, device=dev)
+    param = torch.empty(P, dtype=torch.bfloat16, device=dev)
+    host_param = torch.empty(P, dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream()
+    steps = max(3, args.e2e_steps)
+
+    def step(t):
+        for q in range(n):
+            dgrads[q].copy_(host_grads[q], non_blocking=True)
+        z.zero_fused_step(plan, z.ZERO_ALL_RANKS, dgrads, master, m, v, param, hp, t, stream)
+        host_param.copy_(param, non_blocking=True)
+
+    for t in range(1, 4):
+        step(t)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for t in range(4, 4 + steps):
+        step(t)
+    torch.cuda.synchronize()
+    el = max_over_ranks(time.perf_counter() - t0, world)
+    z.zero_device_status(stream)
+    return {"value": world * psi * steps / el, "unit": UNIT, "h2d_bytes_per_step": 2 * P * n,
+            "d2h_bytes_per_step": 2 * P, "steps": steps, "ms_per_step": 1e3 * el / steps,
+            "how": "per step: cudaMemcpyAsync of the 8 ranks' bf16 grads from pinned host memory, the fused step, "
+                   "cudaMemcpyAsync of the bf16 params back; wall clock over the steps"}
+
+
+def time_launches(fn, iters, stream):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for s, e in evs:
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return statistics.fmean(s.elapsed_time(e) for s, e in evs)
+
+
+def extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args):
+    """The other rows of the path, each timed on its own after the main region:
+    the DDP all-reduce + replica Adam, the unfused reduce-scatter -> Adam -> all-gather
+    pipeline (ablation), and the FSDP unit forward on the Mistral-7B MLP shapes."""
+    import torch
+    legs = {}
+    stream = torch.cuda.current_stream()
+    psi, n = synth.GPT2_SMALL_PSI, 8
+    hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+    plan = z.zero_plan(psi, n, "ddp", 25 * MIB)
+    P, S = plan.psi_padded, plan.shard_elems
+    grads = [synth.rank_grads(psi, P, r, 1, device=dev) for r in range(n)]
+    master = synth.master_params(psi, P, device=dev)
+    m = torch.zeros(P, device=dev)
+    v = torch.zeros(P, device=dev)
+    param = torch.empty(P, dtype=torch.bfloat16, device=dev)
+    g = torch.empty(P, device=dev)
+    it = 50
+    ms_ar = time_launches(lambda: z.ddp_allreduce(plan, grads, g, stream), it, stream)
+    ms_ad = time_launches(lambda: z.zero_adam_step(plan, z.ZERO_ALL_RANKS, g, master, m, v, None, hp, 1, stream),
+                          it, stream)
+    ms_ag = time_launches(lambda: z.zero_allgather_params(plan, [master[r * S:(r + 1) * S] for r in range(n)], param,
+                                                          stream), it, stream)
+    b_ar, b_ad, b_ag = P * (2 * n + 4), P * 28, P * 6
+    legs["ddp_allreduce"] = {"ms": ms_ar, "gbs": b_ar / ms_ar / 1e6, "frac": b_ar / ms_ar / 1e6 / hbm_peak,
+                             "bytes": b_ar}
+    legs["adam_step"] = {"ms": ms_ad, "gbs": b_ad / ms_ad / 1e6, "frac": b_ad / ms_ad / 1e6 / hbm_peak, "bytes": b_ad}
+    legs["allgather_params"] = {"ms": ms_ag, "gbs": b_ag / ms_ag / 1e6, "frac": b_ag / ms_ag / 1e6 / hbm_peak,
+                                "bytes": b_ag}
+    legs["unfused_pipeline_ms"] = ms_ar + ms_ad + ms_ag
+    z.zero_set_fused_kernel(2)
+    ms_vec = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1,
+                                                     stream), it, stream)
+    z.zero_set_fused_kernel(0)
+    b_f = P * (2 * n + 26)
+    legs["fused_register_variant"] = {"ms": ms_vec, "gbs": b_f / ms_vec / 1e6, "frac": b_f / ms_vec / 1e6 / hbm_peak}
+    del grads, master, m, v, param, g
+    torch.cuda.empty_cache()
+    legs["fsdp_unit_forward"] = fsdp_leg(z, synth, dev, tf_burst, peak_src, stream)
+    return legs
+
+
+def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
+    """Mistral-7B MLP unit, N = 8 row shards: W_up, W_gate [14336, 4096] times X [8192,
+    4096]; W_down [4096, 14336] times H [8192, 14336]; fp32 out. Gather fused into the
+    GEMM's loads (no scratch) and, separately, materialised into a scratch W."""
+    import torch
+    n, M = 8, 8192
+    X = synth.activations(M, 4096, device=dev)
+    H = synth.activations(M, 14336, device=dev, seed_key=1)
+    mats = {"up": (14336, 4096, X), "gate": (14336, 4096, X), "down": (4096, 14336, H)}
+    res = {}
+    try:
+        total_ms, total_flop = 0.0, 0.0
+        for name, (R, K, A) in mats.items():
+            shards = synth.weight_shards(R, K, n, device=dev, seed_key=hash(name) % 1000)
+            Y = torch.empty(M, R, device=dev)
+            ms = time_launches(lambda: z.fsdp_unit_forward(shards, A, Y, stream=stream), 10, stream)
+            flop = 2.0 * M * R * K
+            res[name] = {"ms": ms, "tflops": flop / ms / 1e9}
+            total_ms += ms
+            total_flop += flop
+            del shards, Y
+        res["total_ms"] = total_ms
+        res["tflops"] = total_flop / total_ms / 1e9
+        res["roofline"] = {"bound": "tensor", "achieved": res["tflops"], "peak": tf_peak, "unit": "TFLOP/s",
+                           "frac": res["tflops"] / tf_peak,
+                           "peak_source": f"{peak_src} bf16_tflops (burst)" if peak_src == "measured" else "fallback"}
+    except Exception as e:  # the GEMM leg must not hide the step's line
+        res["error"] = str(e)[:300]
+    return res
+
+
+# ---------------------------------------------------------------------------------------
+# the CPU oracle as baseline / reference arm
+# ---------------------------------------------------------------------------------------
+
+def oracle_rate(n_params: int, n_ranks: int = 8, reps: int = 1):
+    """Oracle params/s on the first n_params of the workload: N bf16 gradient slices,
+    fp32 master / m / v, one fused step (reduce, Adam, cast) in plain numpy."""
+    import numpy as np
+    import torch
+
+    import synth
+    from oracle import zero_oracle as O
+    psi = synth.GPT2_SMALL_PSI
+    master = synth.master_params(n_params, n_params).numpy()
+    m = np.zeros(n_params, np.float32)
+    v = np.zeros(n_params, np.float32)
+    grads = [synth.rank_grads(n_params, n_params, r, 1).view(torch.int16).numpy().view(np.uint16)
+             for r in range(n_ranks)]
+    hp = O.AdamHyper()
+    t0 = time.perf_counter()
+    for t in range(1, reps + 1):
+        master, m, v, _ = O.fused_step_elements(grads, master, m, v, hp, t)
+    el = time.perf_counter() - t0
+    assert psi > n_params
+    return n_params * reps / el, el
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    n_params = 4 * MIB
+    rate, el = oracle_rate(n_params)
+    reps = max(1, int(budget_s / max(el, 1e-3)))
+    rate, el = oracle_rate(n_params, reps=reps)
+    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {n_params:,} of 124,356,864 GPT-2-small parameters, N=8 gradient slices, "
+                      f"{reps} fused steps ({el:.1f} s; numpy elementwise, single-threaded)"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    psi, n, stage, bb = synth.GPT2_SMALL_PSI, 8, "zero2", 25 * MIB
+    # size each step's sample so the whole run stays near args.ref_seconds
+    rate, _ = oracle_rate(1 << 18)
+    per_step = args.ref_seconds / max(1, args.steps + args.warmup)
+    n_params = int(min(psi, max(4096, rate * per_step)))
+    for _ in range(args.warmup):
+        oracle_rate(n_params)
+    t_total = 0.0
+    for _ in range(args.steps):
+        _, el = oracle_rate(n_params)
+        t_total += el
+    value = n_params * args.steps / t_total
+    cb = {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+          "sample": f"{n_params:,} of {psi:,} parameters per step (N=8), numpy single-threaded"}
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": 1e3 * psi / value, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; GPT-2-small tensor shapes)",
+           "config": workload_config(psi, n, stage, bb), "impl": "reference", "cpu_baseline": cb,
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# the 1.5B-parameter bandwidth sweep
+# ---------------------------------------------------------------------------------------
+
+def run_sweep(args):
+    """psi = 1.5e9, N in {2,4,8,16,64}, buckets {1,5,25,100} MiB. For each point: one launch
+    over all buckets, and one launch per bucket (as DDP reduces each bucket once backward
+    produced it) captured in a CUDA graph. N <= 16: all N ranks' shards (full simulation);
+    N = 64: one rank's view (its 64 incoming chunks), which bounds device memory."""
+    import torch
+
+    import fsdp_sharded_optimizer_zero_gb300 as z
+    import synth
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream()
+    hbm_peak, _, _, peak_src = peaks()
+    psi = 1_500_000_000
+    hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+    for n in (2, 4, 8, 16, 64):
+        full = n <= 16
+        plan0 = z.zero_plan(psi, n, "zero2", MIB)
+        P, S = plan0.psi_padded, plan0.shard_elems
+        L = P if full else S
+        if full:
+            grads = [synth.rank_grads(psi, P, r, 1, device=dev) for r in range(n)]
+        else:
+            ch = synth.chunk_grads(S, n, 1, device=dev)
+            grads = [ch[q] for q in range(n)]
+        master = synth.master_params(L, L, device=dev)
+        m = torch.zeros(L, device=dev)
+        v = torch.zeros(L, device=dev)
+        param = torch.empty(L, dtype=torch.bfloat16, device=dev)
+        rank = z.ZERO_ALL_RANKS if full else z.ZERO_RANK_VIEW
+        byts = L * (2 * n + 26)
+        for bmib in (1, 5, 25, 100):
+            plan = z.zero_plan(psi, n, "zero2", bmib * MIB)
+            NB = plan.n_buckets
+            with torch.cuda.stream(stream):
+                one = time_launches(lambda: z.zero_fused_step(plan, rank, grads, master, m, v, param, hp, 1, stream),
+                                    10, stream)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for k in range(NB):
+                        z.zero_fused_step_buckets(plan, rank, k, k + 1, grads, master, m, v, param, hp, 1, stream)
+                per_bucket = time_launches(lambda: g.replay(), 10, stream)
+            z.zero_device_status(stream)
+            line = {"sweep": "fused step", "psi": psi, "n_ranks": n, "bucket_mib": bmib, "n_buckets": NB,
+                    "mode": "all ranks" if full else "rank view", "bytes_per_step": byts,
+                    "single_launch_ms": one, "single_launch_gbs": byts / one / 1e6,
+                    "single_launch_frac": byts / one / 1e6 / hbm_peak,
+                    "per_bucket_graph_ms": per_bucket, "per_bucket_graph_gbs": byts / per_bucket / 1e6,
+                    "per_bucket_graph_frac": byts / per_bucket / 1e6 / hbm_peak,
+                    "state_bytes_per_rank": {s: z.zero_plan(psi, n, s, bmib * MIB).state_total_bytes
+                                             for s in ("ddp", "zero1", "zero2", "zero3")},
+                    "peak": hbm_peak, "peak_source": peak_src}
+            print(json.dumps(line), flush=True)
+            del g
+        del grads, master, m, v, param
+        torch.cuda.empty_cache()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--no-legs", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and not args.sweep:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import __graft_entry__ as g
+    g.build()
+    if args.sweep:
+        run_sweep(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,12 @@
+"""GB300-native data-parallel optimizer step (DDP / ZeRO-1/2/3 / FSDP) on one GPU.
+
+The N data-parallel ranks are simulated as separate device buffers. The work is done by
+hand-written sm_103a CUDA kernels behind a C ABI (include/zero.h, libzero_gb300.so); this
+package is the thin Python binding with the same entry-point names.
+"""
+from ._lib import (  # noqa: F401
+    EXPORTS, LIB_PATH, STAGE_IDS, ZERO_ALL_RANKS, ZERO_MAX_RANKS, ZERO_RANK_VIEW, Plan, ZeroError,
+    ddp_allreduce, fsdp_gather_rows, fsdp_unit_forward, library, zero_adam_step, zero_allgather_params,
+    zero_bucket_range, zero_device_status, zero_fused_step, zero_fused_step_buckets, zero_last_error,
+    zero_plan, zero_plan_query, zero_reduce_scatter, zero_set_fused_kernel, zero_version,
+)

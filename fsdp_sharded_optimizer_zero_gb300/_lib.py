@@ -1,0 +1,262 @@
+"""ctypes binding of libzero_gb300.so: argument marshalling only.
+
+Each function below has the name of the C entry point it calls. Tensors are torch CUDA
+tensors (PyTorch supplies device memory and streams); the binding checks dtype, device and
+contiguity, passes raw pointers and the current stream, and raises ZeroError on a
+non-zero status. Every arithmetic step runs in the library's CUDA kernels; there is no
+Python or CPU fallback: if the shared library is missing the import fails.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libzero_gb300.so"
+
+ZERO_OK = 0
+ZERO_ERR_INVALID_ARG = -1
+ZERO_ERR_OOM = -2
+ZERO_ERR_CUDA = -3
+ZERO_ERR_UNSUPPORTED = -4
+ZERO_ERR_DEVICE = -5
+ZERO_RANK_VIEW = -1
+ZERO_ALL_RANKS = -2
+ZERO_MAX_RANKS = 64
+STAGE_IDS = {"ddp": 0, "zero1": 1, "zero2": 2, "zero3": 3}
+
+# every symbol declared in include/zero.h
+EXPORTS = (
+    "zero_plan", "zero_plan_query", "zero_bucket_range", "zero_plan_destroy",
+    "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_buckets",
+    "zero_allgather_params", "ddp_allreduce", "fsdp_gather_rows", "fsdp_unit_forward",
+    "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
+)
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+class zero_layout(C.Structure):
+    _fields_ = [
+        ("psi", C.c_uint64), ("psi_padded", C.c_uint64), ("shard_elems", C.c_uint64),
+        ("bucket_bytes", C.c_uint64), ("bucket_elems", C.c_uint64), ("n_buckets", C.c_uint64),
+        ("n_ranks", C.c_int32), ("stage", C.c_int32),
+        ("state_param_bytes", C.c_uint64), ("state_grad_bytes", C.c_uint64),
+        ("state_master_bytes", C.c_uint64), ("state_m_bytes", C.c_uint64), ("state_v_bytes", C.c_uint64),
+        ("state_total_bytes", C.c_uint64),
+        ("comm_reduce_scatter", C.c_uint64), ("comm_all_gather_fwd", C.c_uint64),
+        ("comm_all_gather_bwd", C.c_uint64), ("comm_total", C.c_uint64),
+        ("ring_sent_elems", C.c_uint64), ("fused_step_bytes", C.c_uint64),
+    ]
+
+
+class zero_adam(C.Structure):
+    _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
+                ("weight_decay", C.c_float)]
+
+
+def _load():
+    if not LIB_PATH.exists():
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(nvcc, sm_103a). There is no fallback path.")
+    lib = C.CDLL(str(LIB_PATH))
+    P, I, U64, I64, VP = C.c_void_p, C.c_int, C.c_uint64, C.c_int64, C.c_void_p
+    PP = C.POINTER(C.c_void_p)
+    sig = {
+        "zero_plan": (I, [U64, I, I, U64, C.POINTER(C.c_void_p)]),
+        "zero_plan_query": (I, [P, C.POINTER(zero_layout)]),
+        "zero_bucket_range": (I, [P, I, U64, C.POINTER(U64), C.POINTER(U64)]),
+        "zero_plan_destroy": (I, [P]),
+        "zero_reduce_scatter": (I, [P, I, PP, VP, VP]),
+        "zero_adam_step": (I, [P, I, VP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
+        "zero_fused_step": (I, [P, I, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
+        "zero_fused_step_buckets": (I, [P, I, U64, U64, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
+        "zero_allgather_params": (I, [P, PP, VP, VP]),
+        "ddp_allreduce": (I, [P, PP, VP, VP]),
+        "fsdp_gather_rows": (I, [I, PP, I64, I64, VP, VP]),
+        "fsdp_unit_forward": (I, [I, PP, I64, I64, VP, I64, VP, VP, VP, VP]),
+        "zero_last_error": (C.c_char_p, []),
+        "zero_device_status": (I, [VP]),
+        "zero_set_fused_kernel": (I, [I]),
+        "zero_version": (I, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    return lib
+
+
+_lib = _load()
+
+
+def _check(rc: int):
+    if rc != ZERO_OK:
+        raise ZeroError(rc, _lib.zero_last_error().decode(errors="replace"))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _ptr_array(ts, dtype, name):
+    arr = (C.c_void_p * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = _dev(t, dtype, f"{name}[{i}]")
+    return arr
+
+
+def _adam(hp) -> zero_adam:
+    if isinstance(hp, zero_adam):
+        return hp
+    d = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    if hp is not None:
+        d.update({k: getattr(hp, k) for k in d if hasattr(hp, k)} if not isinstance(hp, dict) else hp)
+    return zero_adam(**d)
+
+
+class Plan:
+    """Owns a zero_plan_t handle."""
+
+    def __init__(self, handle: int):
+        self.handle = C.c_void_p(handle)
+        self.layout = zero_plan_query(self)
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h and _lib is not None:
+            _lib.zero_plan_destroy(h)
+
+    def __getattr__(self, k):
+        lay = self.__dict__.get("layout")
+        if lay is not None and k in lay:
+            return lay[k]
+        raise AttributeError(k)
+
+
+# ---------------------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------------------
+
+def zero_plan(psi: int, n_ranks: int, stage, bucket_bytes: int) -> Plan:
+    stage = STAGE_IDS.get(stage, stage)
+    h = C.c_void_p()
+    _check(_lib.zero_plan(psi, n_ranks, stage, bucket_bytes, C.byref(h)))
+    return Plan(h.value)
+
+
+def zero_plan_query(plan: Plan) -> dict:
+    lay = zero_layout()
+    _check(_lib.zero_plan_query(plan.handle, C.byref(lay)))
+    return {name: getattr(lay, name) for name, _ in zero_layout._fields_}
+
+
+def zero_bucket_range(plan: Plan, rank: int, bucket: int):
+    b, e = C.c_uint64(), C.c_uint64()
+    _check(_lib.zero_bucket_range(plan.handle, rank, bucket, C.byref(b), C.byref(e)))
+    return b.value, e.value
+
+
+def zero_reduce_scatter(plan: Plan, rank: int, grads, g_shard, stream=None):
+    _check(_lib.zero_reduce_scatter(plan.handle, rank, _ptr_array(grads, torch.bfloat16, "grads"),
+                                    _dev(g_shard, torch.float32, "g_shard"), _stream(stream)))
+
+
+def zero_adam_step(plan: Plan, rank: int, g_shard, master, m, v, param_out, hp, step: int, stream=None):
+    a = _adam(hp)
+    _check(_lib.zero_adam_step(plan.handle, rank, _dev(g_shard, torch.float32, "g_shard"),
+                               _dev(master, torch.float32, "master"), _dev(m, torch.float32, "m"),
+                               _dev(v, torch.float32, "v"), _dev(param_out, torch.bfloat16, "param_out"),
+                               C.byref(a), step, _stream(stream)))
+
+
+def zero_fused_step(plan: Plan, rank: int, grads, master, m, v, param_out, hp, step: int, stream=None):
+    a = _adam(hp)
+    _check(_lib.zero_fused_step(plan.handle, rank, _ptr_array(grads, torch.bfloat16, "grads"),
+                                _dev(master, torch.float32, "master"), _dev(m, torch.float32, "m"),
+                                _dev(v, torch.float32, "v"), _dev(param_out, torch.bfloat16, "param_out"),
+                                C.byref(a), step, _stream(stream)))
+
+
+def zero_fused_step_buckets(plan: Plan, rank: int, bucket_begin: int, bucket_end: int, grads, master, m, v,
+                            param_out, hp, step: int, stream=None):
+    a = _adam(hp)
+    _check(_lib.zero_fused_step_buckets(plan.handle, rank, bucket_begin, bucket_end,
+                                        _ptr_array(grads, torch.bfloat16, "grads"),
+                                        _dev(master, torch.float32, "master"), _dev(m, torch.float32, "m"),
+                                        _dev(v, torch.float32, "v"), _dev(param_out, torch.bfloat16, "param_out"),
+                                        C.byref(a), step, _stream(stream)))
+
+
+def zero_allgather_params(plan: Plan, masters, full_param, stream=None):
+    _check(_lib.zero_allgather_params(plan.handle, _ptr_array(masters, torch.float32, "masters"),
+                                      _dev(full_param, torch.bfloat16, "full_param"), _stream(stream)))
+
+
+def ddp_allreduce(plan: Plan, grads, g_full, stream=None):
+    _check(_lib.ddp_allreduce(plan.handle, _ptr_array(grads, torch.bfloat16, "grads"),
+                              _dev(g_full, torch.float32, "g_full"), _stream(stream)))
+
+
+def fsdp_gather_rows(w_shards, w_full, stream=None):
+    n = len(w_shards)
+    rows, k = w_full.shape
+    _check(_lib.fsdp_gather_rows(n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, k,
+                                 _dev(w_full, torch.bfloat16, "w_full"), _stream(stream)))
+
+
+def fsdp_unit_forward(w_shards, A, Y, Y_bf16=None, scratch_w=None, stream=None):
+    n = len(w_shards)
+    rows = sum(int(s.shape[0]) for s in w_shards)
+    k = int(A.shape[1])
+    m_tok = int(A.shape[0])
+    _check(_lib.fsdp_unit_forward(n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, k,
+                                  _dev(A, torch.bfloat16, "A"), m_tok, _dev(Y, torch.float32, "Y"),
+                                  _dev(Y_bf16, torch.bfloat16, "Y_bf16"),
+                                  _dev(scratch_w, torch.bfloat16, "scratch_w"), _stream(stream)))
+
+
+def zero_device_status(stream=None):
+    _check(_lib.zero_device_status(_stream(stream)))
+
+
+def zero_set_fused_kernel(which: int):
+    _check(_lib.zero_set_fused_kernel(which))
+
+
+def zero_version() -> int:
+    return _lib.zero_version()
+
+
+def zero_last_error() -> str:
+    return _lib.zero_last_error().decode(errors="replace")
+
+
+def library():
+    """The loaded ctypes library (for tests that call the C ABI directly)."""
+    return _lib

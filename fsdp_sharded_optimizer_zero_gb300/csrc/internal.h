@@ -1,0 +1,62 @@
+// Internal declarations shared by the library's translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/zero.h"
+
+struct zero_plan {
+  zero_layout lay;
+};
+
+namespace zgb {
+
+// Scalars of one Adam step, prepared once on the host (bias corrections, 1 - beta,
+// lr * wd, 1 / N) and passed by value to every kernel that updates state.
+struct AdamScalars {
+  float lr, beta1, beta2, omb1, omb2, eps, bc1, bc2, lr_wd, inv_n;
+  int wd_on;
+};
+
+// N device pointers carried in kernel parameter space.
+struct GradPtrs {
+  const uint16_t* p[ZERO_MAX_RANKS];
+};
+struct MasterPtrs {
+  const float* p[ZERO_MAX_RANKS];
+};
+
+// The elements a launch covers: n_seg segments of seg_len elements; element e of segment
+// s is at flat offset s * seg_stride + e of EVERY stream of the launch (the host offsets
+// each stream's base pointer before the launch).
+struct Domain {
+  uint64_t n_seg, seg_len, seg_stride;
+};
+
+// ---- launchers (step_kernels.cu) ----
+cudaError_t launch_reduce(const GradPtrs& gp, int n, float* out, const Domain& d, float inv_n, bool vec,
+                          cudaStream_t st);
+cudaError_t launch_adam(const float* g, float* master, float* m, float* v, uint16_t* param, const Domain& d,
+                        const AdamScalars& sc, bool vec, cudaStream_t st);
+// variant: 1 = TMA bulk pipeline, 2 = register streaming, 3 = scalar (unaligned inputs)
+cudaError_t launch_fused(const GradPtrs& gp, int n, float* master, float* m, float* v, uint16_t* param,
+                         const Domain& d, const AdamScalars& sc, int variant, cudaStream_t st);
+cudaError_t launch_allgather(const MasterPtrs& mp, int n, uint64_t shard, uint16_t* full, bool vec,
+                             cudaStream_t st);
+cudaError_t launch_gather_rows(const GradPtrs& shards, int n, uint64_t shard_elems, uint16_t* full, bool vec,
+                               cudaStream_t st);
+unsigned int step_kernels_read_clear_error();
+
+// ---- FSDP GEMM (fsdp_gemm.cu) ----
+// Y[M, R] = A[M, K] * W^T with W given as n_ranks row shards of R/n_ranks rows each
+// (n_ranks = 1 with the full W for the materialised path).
+int launch_fsdp_gemm(int n_ranks, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
+                     const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, cudaStream_t st);
+unsigned int fsdp_gemm_read_clear_error();
+
+// ---- errors (capi.cu) ----
+int set_error(int code, const char* fmt, ...);
+int num_sms();
+
+}  // namespace zgb

@@ -1,0 +1,249 @@
+/*
+ * zero.h — C ABI of the GB300 data-parallel optimizer-step library (libzero_gb300.so).
+ *
+ * What it computes: the per-step state update of DDP / ZeRO-1/2/3 / FSDP with the N
+ * data-parallel ranks simulated as separate buffers on ONE GPU, plus the FSDP unit's
+ * gather + linear. Sources (cited by page title and section):
+ *   [Wiring]    "Behind the scenes of distributed training, and why your GPU wiring matters as
+ *               much as your strategy" (automationscribe.com), Part 1: DDP, FSDP, "ZeRO: The
+ *               Dial Between DDP and FSDP".
+ *   [Interview] "DP、ZeRO-1/2/3、FSDP:每卡显存多少、通信多多少?" (charliedreemur.github.io,
+ *               ml-interview / dp-zero-fsdp): concepts, Fig. 1, Fig. 2, key formulas, the
+ *               7B / N = 8 worked table, and the follow-up on a hand-written FSDP linear.
+ *   [Concepts]  "Data Parallel, ZeRO and FSDP" (k8ai.app): DDP steps, communication cost,
+ *               the ZeRO / FSDP stage table, full sharding.
+ *
+ * Conventions (every call):
+ *   - Returns zero_status: ZERO_OK (0) or a negative error. On error nothing is launched
+ *     and zero_last_error() returns a thread-local message describing the cause.
+ *   - Tensor arguments are raw DEVICE pointers owned by the caller (e.g. allocated by
+ *     PyTorch). bf16 tensors are passed as zero_bf16 (raw IEEE bfloat16 bits).
+ *     Any alignment is accepted; 16-byte-aligned buffers take the vectorised / TMA path,
+ *     others a scalar path with bit-identical results.
+ *   - Arrays of per-rank pointers (grads[], masters[], w_shards[]) are HOST arrays of
+ *     n_ranks device pointers; they are copied into the kernel's parameters, so the host
+ *     array may be reused as soon as the call returns.
+ *   - Every launch is asynchronous on the caller's stream (cudaStream_t; NULL = legacy
+ *     default stream). Nothing on the step path allocates device memory.
+ *   - Device-side checks (bounded waits in the pipelined kernels) never trap: they set a
+ *     device error word that zero_device_status() reads.
+ *   - Thread safety: calls may be made from several host threads; a plan is read-only
+ *     after zero_plan() and may be shared.
+ *
+ * Arithmetic of the step (identical in every call that performs it; bit-exact with the
+ * CPU oracle when buffers hold the same bytes):
+ *   reduced gradient g = ((grad_0 + grad_1) + ... + grad_{N-1}) in fp32, rank order,
+ *                        times f32(1/N) (the fp32 nearest 1/N);
+ *   Adam (Kingma & Ba, bias-corrected, eps outside the root, decoupled weight decay),
+ *   one IEEE fp32 operation per line, no fused multiply-add:
+ *        m  = b1*m + (1-b1)*g;         v  = b2*v + (1-b2)*(g*g)
+ *        mh = m / bc1;                 vh = v / bc2       bc_i = f32(1 - b_i^t), t >= 1
+ *        den = sqrt(vh) + eps
+ *        if (wd != 0) master = master - f32(lr*wd)*master
+ *        master = master - lr*(mh/den)
+ *   bf16 param = round-to-nearest-even(master).
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ZERO_API __attribute__((visibility("default")))
+#else
+#define ZERO_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* zero_stream_t; /* the same type as cudaStream_t */
+typedef uint16_t zero_bf16;                /* raw bfloat16 bits */
+
+typedef enum {
+  ZERO_OK = 0,
+  ZERO_ERR_INVALID_ARG = -1, /* a bad argument; nothing launched */
+  ZERO_ERR_OOM = -2,         /* host allocation failed (plan object) */
+  ZERO_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed; message has the code */
+  ZERO_ERR_UNSUPPORTED = -4, /* valid request this build / device cannot run */
+  ZERO_ERR_DEVICE = -5       /* a kernel's device-side check fired (see zero_device_status) */
+} zero_status;
+
+/* Strategies ([Concepts] "ZeRO and FSDP" stage table; [Interview] Fig. 1). */
+enum {
+  ZERO_STAGE_DDP = 0, /* nothing sharded */
+  ZERO_STAGE_1 = 1,   /* optimizer state sharded */
+  ZERO_STAGE_2 = 2,   /* + gradients */
+  ZERO_STAGE_3 = 3    /* + parameters (ZeRO-3 / FSDP full shard) */
+};
+
+/* `rank` argument values besides 0..N-1 */
+#define ZERO_RANK_VIEW (-1) /* one rank's view: per-rank pointers address S-element chunks */
+#define ZERO_ALL_RANKS (-2) /* every rank's shard in one launch (full simulation) */
+#define ZERO_MAX_RANKS 64
+
+typedef struct zero_plan zero_plan_t; /* opaque; owned by the library until destroyed */
+
+/* Layout and accounting of a plan. Element counts unless named *_bytes. */
+typedef struct {
+  uint64_t psi;          /* parameters */
+  uint64_t psi_padded;   /* P = ceil(psi/N)*N; entries [psi, P) are padding (kept zero) */
+  uint64_t shard_elems;  /* S = P/N; rank r owns flat [r*S, (r+1)*S) */
+  uint64_t bucket_bytes; /* as passed to zero_plan */
+  uint64_t bucket_elems; /* C = floor(bucket_bytes/(2N)) elements of every rank's shard */
+  uint64_t n_buckets;    /* ceil(S/C); bucket k of rank r = flat [r*S+k*C, r*S+min((k+1)*C,S)) */
+  int32_t n_ranks;
+  int32_t stage;
+  /* model-state bytes ONE rank keeps between steps for this stage ([Interview] "手算例子:
+   * 7B、N = 8" / Fig. 1; [Concepts] stage table): DDP 16P; ZeRO-1 4P+12S; ZeRO-2 2P+14S;
+   * ZeRO-3 16S. Transient buffers (incoming gradient chunks, fp32 reduced gradient) are
+   * not model state and are not counted. */
+  uint64_t state_param_bytes, state_grad_bytes, state_master_bytes, state_m_bytes, state_v_bytes;
+  uint64_t state_total_bytes;
+  /* elements ONE rank moves per step per collective ([Interview] "每卡通信量"):
+   * DDP and ZeRO-1/2: reduce-scatter P + all-gather P = 2P; ZeRO-3: + backward all-gather P = 3P */
+  uint64_t comm_reduce_scatter, comm_all_gather_fwd, comm_all_gather_bwd, comm_total;
+  /* elements one rank sends per step when each collective is a ring: (N-1)/N * comm_total
+   * ([Concepts] "Communication cost": 2(N-1)/N * S bytes for an all-reduce) */
+  uint64_t ring_sent_elems;
+  /* algorithmic HBM bytes of one fused step over all P elements: P*(2N + 26)
+   * (read N bf16 grads, read+write fp32 master/m/v, write bf16 param) */
+  uint64_t fused_step_bytes;
+} zero_layout;
+
+/* Adam hyper-parameters (fp32). beta1, beta2 in [0, 1); eps > 0; lr, weight_decay >= 0. */
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+} zero_adam;
+
+/* ------------------------------------------------------------------------------------ */
+/* plan: flat-buffer shard / bucket layout (host only; launches nothing)                  */
+/* ------------------------------------------------------------------------------------ */
+
+/* Build the layout for psi parameters over n_ranks (1..ZERO_MAX_RANKS) at `stage`, with
+ * gradient buckets of bucket_bytes (bf16 bytes across all N rank segments; must be
+ * >= 2*n_ranks). [Interview] "ZeRO-1 / 2 / 3": model states are cut by data-parallel rank
+ * into N parts, each card keeps and updates only its 1/N; [Interview] follow-up "FSDP2 和
+ * FSDP1": the flat parameter is flattened and concatenated before it is cut; [Concepts]
+ * "Plain data parallel (DDP)": gradients are reduced in buckets. psi is padded to a
+ * multiple of N. *out receives a new plan (free it with zero_plan_destroy). */
+ZERO_API int zero_plan(uint64_t psi, int n_ranks, int stage, uint64_t bucket_bytes, zero_plan_t** out);
+
+/* Copy the plan's layout and accounting into *out. */
+ZERO_API int zero_plan_query(const zero_plan_t* plan, zero_layout* out);
+
+/* Flat index range [*begin, *end) of bucket `bucket` in rank `rank`'s shard. */
+ZERO_API int zero_bucket_range(const zero_plan_t* plan, int rank, uint64_t bucket, uint64_t* begin, uint64_t* end);
+
+/* Free a plan (NULL is accepted). */
+ZERO_API int zero_plan_destroy(zero_plan_t* plan);
+
+/* ------------------------------------------------------------------------------------ */
+/* the step                                                                              */
+/* ------------------------------------------------------------------------------------ */
+/* Pointer conventions by `rank` (S = shard_elems, P = psi_padded):
+ *   rank = r in [0, N): grads[q] = rank q's full P-element bf16 gradient; the call reads
+ *       elements [r*S, (r+1)*S) of each. g_shard / master / m / v address rank r's
+ *       S-element shard. param_out: stages 0-2 = the full P-element bf16 parameter buffer,
+ *       written at [r*S, (r+1)*S) (the all-gather's destination); stage 3 = rank r's own
+ *       S-element bf16 shard.
+ *   rank = ZERO_RANK_VIEW: grads[q] = the S-element chunk rank q contributes to this shard;
+ *       every other buffer is S elements.
+ *   rank = ZERO_ALL_RANKS: every rank's shard at once; grads[q] full P-element buffers and
+ *       g / master / m / v / param_out all P-element flat buffers (rank r's shard at r*S).
+ */
+
+/* Reduce-scatter ([Wiring] "ZeRO: The Dial Between DDP and FSDP": sums everyone's gradients
+ * but gives each GPU only its slice; [Interview] "reduce-scatter 与 all-gather"):
+ * g_shard[i] = fp32 rank-order sum of the N bf16 contributions times f32(1/N). */
+ZERO_API int zero_reduce_scatter(const zero_plan_t* plan, int rank, const zero_bf16* const grads[],
+                        float* g_shard, zero_stream_t stream);
+
+/* Adam on a shard's fp32 master/m/v with the fp32 reduced gradient g_shard (updated in
+ * place). step counts from 1. param_out may be NULL (no bf16 cast); otherwise it receives
+ * bf16(master) as described above. ([Interview] DDP item: bf16 param + bf16 grad + fp32
+ * master, m, v = 16 bytes per parameter; [Wiring] Adam keeps momentum and variance.) */
+ZERO_API int zero_adam_step(const zero_plan_t* plan, int rank, const float* g_shard, float* master, float* m,
+                   float* v, zero_bf16* param_out, const zero_adam* hp, int64_t step,
+                   zero_stream_t stream);
+
+/* Reduce-scatter + Adam + bf16 cast / all-gather write in ONE pass over HBM: each byte of
+ * gradient and state is read once and each result written once. Same arguments as the two
+ * calls above without g_shard. Results are bit-identical to zero_reduce_scatter followed
+ * by zero_adam_step. */
+ZERO_API int zero_fused_step(const zero_plan_t* plan, int rank, const zero_bf16* const grads[], float* master,
+                    float* m, float* v, zero_bf16* param_out, const zero_adam* hp, int64_t step,
+                    zero_stream_t stream);
+
+/* As zero_fused_step, restricted to buckets [bucket_begin, bucket_end) of the shard(s):
+ * the unit DDP / ZeRO reduce as soon as backward has produced a bucket ([Concepts] "Plain
+ * data parallel (DDP)"). Pointers follow the same convention (whole-shard / whole-buffer
+ * bases); the call offsets them to the buckets. */
+ZERO_API int zero_fused_step_buckets(const zero_plan_t* plan, int rank, uint64_t bucket_begin, uint64_t bucket_end,
+                            const zero_bf16* const grads[], float* master, float* m, float* v,
+                            zero_bf16* param_out, const zero_adam* hp, int64_t step, zero_stream_t stream);
+
+/* Parameter all-gather ([Interview] "reduce-scatter 与 all-gather"; ZeRO-1/2 after the
+ * update): full_param[r*S + i] = bf16(masters[r][i]) for every rank r, masters[r] being
+ * rank r's S-element fp32 master shard. full_param has P elements. */
+ZERO_API int zero_allgather_params(const zero_plan_t* plan, const float* const masters[], zero_bf16* full_param,
+                          zero_stream_t stream);
+
+/* DDP all-reduce = reduce-scatter + all-gather ([Wiring] "ZeRO: The Dial Between DDP and
+ * FSDP"; [Concepts] "Plain data parallel (DDP)" step 2): g_full[j] = fp32 rank-order sum
+ * of grads[q][j] times f32(1/N) for all j < P. Each rank's reduce-scatter result lands at
+ * its own offset r*S of g_full, so the all-gather is in place. */
+ZERO_API int ddp_allreduce(const zero_plan_t* plan, const zero_bf16* const grads[], float* g_full,
+                  zero_stream_t stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* FSDP unit ([Interview] follow-up "手写 FSDP 的一层 linear"; Fig. 2)                     */
+/* ------------------------------------------------------------------------------------ */
+
+/* All-gather of dim-0 row shards: w_full[r*R/N + j][c] = w_shards[r][j][c] (bit copy).
+ * w_shards[r]: row-major [rows_out/N, k_in] bf16; w_full: row-major [rows_out, k_in].
+ * rows_out % n_ranks must be 0. */
+ZERO_API int fsdp_gather_rows(int n_ranks, const zero_bf16* const w_shards[], int64_t rows_out, int64_t k_in,
+                     zero_bf16* w_full, zero_stream_t stream);
+
+/* Forward of an FSDP unit's linear on the local batch: Y = A * W^T with W [rows_out, k_in]
+ * (the [out, in] layout of a linear layer) assembled from its N row shards, fp32
+ * accumulation on the tensor cores. A: row-major [m_tokens, k_in] bf16. Y: row-major
+ * [m_tokens, rows_out] fp32. Y_bf16 (nullable): bf16 copy of Y (round-to-nearest-even).
+ * scratch_w (nullable): a [rows_out, k_in] bf16 buffer; if given, the shards are first
+ * gathered into it (fsdp_gather_rows) and the GEMM reads the gathered W, which the caller
+ * frees after use; if NULL the gather is fused into the GEMM's loads (each tile is loaded
+ * straight from its shard), which needs (rows_out/n_ranks) % 256 == 0.
+ * Requires k_in % 8 == 0 (16-byte rows for the tensor-memory copies), and 16-byte-aligned
+ * A, shards and scratch_w. Results are fp32 sums of exact bf16 products in an unspecified
+ * order: within K * 2^-23 * sum|a*w| of the exact value. */
+ZERO_API int fsdp_unit_forward(int n_ranks, const zero_bf16* const w_shards[], int64_t rows_out, int64_t k_in,
+                      const zero_bf16* A, int64_t m_tokens, float* Y, zero_bf16* Y_bf16, zero_bf16* scratch_w,
+                      zero_stream_t stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* status                                                                                */
+/* ------------------------------------------------------------------------------------ */
+
+/* Message for the last error on this host thread ("" if none). Valid until the next call
+ * on this thread. */
+ZERO_API const char* zero_last_error(void);
+
+/* Synchronise `stream`, then read and clear the device error word that bounded waits set
+ * (current device). Returns ZERO_OK, ZERO_ERR_DEVICE (message names the kernel and wait)
+ * or ZERO_ERR_CUDA. */
+ZERO_API int zero_device_status(zero_stream_t stream);
+
+/* Select the fused-step kernel: 0 = automatic (default), 1 = TMA bulk-copy pipeline,
+ * 2 = register-streaming kernel. Both give bit-identical results; used for ablations. */
+ZERO_API int zero_set_fused_kernel(int which);
+
+/* Library version, e.g. 100 for 0.1.0. */
+ZERO_API int zero_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_GB300_H */

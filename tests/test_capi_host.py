@@ -1,0 +1,114 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every entry point
+include/zero.h declares; the plan's layout, per-stage bytes and communication counts equal
+the oracle's exactly; invalid arguments are rejected before anything is launched."""
+from __future__ import annotations
+
+import ctypes as C
+import re
+from pathlib import Path
+
+import pytest
+
+import oracle.zero_oracle as O
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def z():
+    import __graft_entry__ as g
+    g.build()
+    import fsdp_sharded_optimizer_zero_gb300 as z
+    return z
+
+
+def declared_symbols():
+    names = set()
+    for h in (ROOT / "include").glob("*.h"):
+        names |= set(re.findall(r"^ZERO_API\s+[\w\s\*]+?\b(\w+)\s*\(", h.read_text(), flags=re.M))
+    return names
+
+
+def test_header_declares_the_boundary():
+    want = {"zero_plan", "zero_plan_query", "zero_plan_destroy", "zero_reduce_scatter", "zero_adam_step",
+            "zero_fused_step", "zero_allgather_params", "ddp_allreduce", "fsdp_unit_forward"}
+    assert want <= declared_symbols()
+
+
+def test_library_exports_every_declared_symbol(z):
+    lib = C.CDLL(str(z.LIB_PATH))
+    names = declared_symbols()
+    assert names == set(z.EXPORTS)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+STAGES = ["ddp", "zero1", "zero2", "zero3"]
+
+
+@pytest.mark.parametrize("psi,n,bb", [(1, 1, 2), (7, 2, 4), (13, 3, 6), (1000, 8, 40), (1_000_003, 64, 1 << 20),
+                                      (1_048_576, 4, 25 << 20), (124_356_864, 8, 25 << 20),
+                                      (7_241_732_096, 8, 50 << 20), (1_500_000_000, 64, 1 << 20)])
+@pytest.mark.parametrize("stage", STAGES)
+def test_plan_matches_oracle(z, psi, n, bb, stage):
+    p = z.zero_plan(psi, n, stage, bb)
+    lay = O.make_layout(psi, n, bb)
+    L = p.layout
+    assert (L["psi"], L["psi_padded"], L["shard_elems"], L["bucket_elems"], L["n_buckets"]) == \
+        (lay.psi, lay.psi_padded, lay.shard, lay.bucket_elems, lay.n_buckets)
+    mb = O.model_state_bytes(stage, lay)
+    assert (L["state_param_bytes"], L["state_grad_bytes"], L["state_master_bytes"], L["state_m_bytes"],
+            L["state_v_bytes"], L["state_total_bytes"]) == (mb["param"], mb["grad"], mb["master"], mb["m"], mb["v"],
+                                                            mb["total"])
+    c = O.comm_elements(stage, lay)
+    assert (L["comm_reduce_scatter"], L["comm_all_gather_fwd"], L["comm_all_gather_bwd"], L["comm_total"]) == \
+        (c["reduce_scatter"], c["all_gather_fwd"], c["all_gather_bwd"], c["total"])
+    assert L["ring_sent_elems"] == O.ring_sent_elements(c["total"], n)
+    assert L["fused_step_bytes"] == lay.psi_padded * (2 * n + 26)
+
+
+@pytest.mark.parametrize("psi,n,bb", [(13, 3, 6), (1000, 8, 48), (4099, 5, 1 << 10)])
+def test_bucket_ranges_match_oracle(z, psi, n, bb):
+    p = z.zero_plan(psi, n, "zero2", bb)
+    lay = O.make_layout(psi, n, bb)
+    for r in range(n):
+        for k in range(lay.n_buckets):
+            assert z.zero_bucket_range(p, r, k) == O.bucket_range(lay, r, k)
+    with pytest.raises(z.ZeroError):
+        z.zero_bucket_range(p, n, 0)
+    with pytest.raises(z.ZeroError):
+        z.zero_bucket_range(p, 0, lay.n_buckets)
+
+
+@pytest.mark.parametrize("args", [(0, 4, 2, 1 << 20), (10, 0, 2, 1 << 20), (10, 65, 2, 1 << 20), (10, 4, 4, 1 << 20),
+                                  (10, 4, -1, 1 << 20), (10, 4, 2, 7)])
+def test_plan_rejects_bad_arguments(z, args):
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_plan(*args)
+    assert e.value.code == -1
+
+
+def test_step_calls_reject_missing_rank_before_launch(z):
+    """A NULL among the N rank pointers (a missing replica) is an argument error: nothing
+    is launched, so this runs without a GPU."""
+    lib = z.library()
+    p = z.zero_plan(1024, 4, "zero2", 1 << 20)
+    grads = (C.c_void_p * 4)(16, 32, None, 64)
+    adam = z._lib.zero_adam(1e-4, 0.9, 0.999, 1e-8, 0.0)
+    rc = lib.zero_fused_step(p.handle, 0, grads, 256, 512, 768, 1024, C.byref(adam), 1, None)
+    assert rc == -1 and b"grads[2] is NULL" in lib.zero_last_error()
+    rc = lib.zero_reduce_scatter(p.handle, 0, grads, 256, None)
+    assert rc == -1
+    rc = lib.ddp_allreduce(p.handle, grads, 256, None)
+    assert rc == -1
+    good = (C.c_void_p * 4)(16, 32, 48, 64)
+    for bad_rank in (4, -3):
+        assert lib.zero_fused_step(p.handle, bad_rank, good, 256, 512, 768, 1024, C.byref(adam), 1, None) == -1
+    assert lib.zero_fused_step(p.handle, 0, good, 256, 512, 768, 1024, C.byref(adam), 0, None) == -1  # step 0
+    bad_adam = z._lib.zero_adam(1e-4, 1.0, 0.999, 1e-8, 0.0)
+    assert lib.zero_fused_step(p.handle, 0, good, 256, 512, 768, 1024, C.byref(bad_adam), 1, None) == -1
+    assert lib.zero_fused_step_buckets(p.handle, 0, 1, 1, good, 256, 512, 768, 1024, C.byref(adam), 1, None) == -1
+    assert lib.fsdp_unit_forward(3, good, 8, 16, 128, 4, 256, None, None, None) == -1   # rows % N
+    assert lib.fsdp_unit_forward(4, good, 8, 12, 128, 4, 256, None, None, None) == -1   # k % 8
+    assert lib.fsdp_gather_rows(4, grads, 8, 16, 256, None) == -1
+    assert lib.zero_set_fused_kernel(3) == -1
