@@ -1,12 +1,312 @@
-// FSDP unit GEMM (tcgen05 / TMEM / TMA) — under construction.
+// FSDP unit GEMM on the 5th-generation tensor cores: Y[M, R] = A[M, K] * W^T, where W
+// [R, K] (the [out, in] layout of a linear layer) is held as N dim-0 row shards.
+//
+// The all-gather of W is fused into the operand loads: each 256-row tile of W lies inside
+// one shard (shard rows are a multiple of 256), so the TMA producer picks that shard's
+// tensor map and loads the tile straight from the shard; the full W is never assembled.
+// (With a caller scratch buffer the host instead gathers W first and passes one map.)
+//
+// Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0        TMA producer: A tile 128x64 and W tile 256x64 (bf16, 128-byte swizzle)
+//                 per 64-wide K block into a 4-stage shared-memory ring;
+//   warp 1        allocates 512 TMEM columns, then one lane issues tcgen05.mma
+//                 (M=128, N=256, K=16; fp32 accumulators in TMEM, two 256-column buffers)
+//                 and tcgen05.commit frees each stage and publishes each finished tile;
+//   warps 2-5     epilogue: tcgen05.ld 32 columns at a time, fp32 (and optional bf16)
+//                 streaming stores to HBM, then release the accumulator buffer, so the
+//                 epilogue of tile i overlaps the main loop of tile i+1.
+// Every mbarrier wait is bounded (error word + CTA abort flag, no trap); after an abort
+// the producer drains its copies and the MMA warp its MMAs before TMEM is released.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "device_common.cuh"
+#include "tcgen05.cuh"
 
 namespace zgb {
+
 ZGB_DECLARE_ERROR_WORD();
 
-int launch_fsdp_gemm(int, const uint16_t* const*, int64_t, int64_t, const uint16_t*, int64_t, float*, uint16_t*,
-                     cudaStream_t) {
-  return set_error(ZERO_ERR_UNSUPPORTED, "fsdp_unit_forward: GEMM kernel not built yet");
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int kMaxShards = 16;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;  // two accumulators of BN fp32 columns
+constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t kSmemBytes = STAGES * STAGE_BYTES + 1024;  // + alignment slack
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+
+constexpr unsigned int kErrEmpty = (2u << 8) | 1u;  // producer waiting for a free stage
+constexpr unsigned int kErrFull = (2u << 8) | 2u;   // MMA waiting for a loaded stage
+constexpr unsigned int kErrAccE = (2u << 8) | 3u;   // MMA waiting for a drained accumulator
+constexpr unsigned int kErrAccF = (2u << 8) | 4u;   // epilogue waiting for a finished tile
+constexpr unsigned int kErrDrain = (2u << 8) | 5u;  // draining after an abort
+
+struct GemmParams {
+  CUtensorMap a;                 // A [M, K] bf16, box 64 x 128
+  CUtensorMap w[kMaxShards];     // shard s [shard_rows, K] bf16, box 64 x 256
+  float* y;                      // [M, R] fp32
+  uint16_t* yb;                  // [M, R] bf16 or null
+  int m, r, k, shard_rows, n_shards;
+};
+
+// warp-uniform bounded wait: lane 0 polls, the whole warp gets the verdict
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int code) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, &g_zgb_dev_error, code) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok != 0;
+}
+
+__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, int col0, const uint32_t (&r)[32]) {
+  float* yrow = p.y + static_cast<size_t>(row) * p.r;
+  const bool full = col0 + 32 <= p.r;
+  if (full && (p.r & 3) == 0) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      __stcs(reinterpret_cast<float4*>(yrow + col0 + j),
+             make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                         __uint_as_float(r[j + 3])));
+  } else {
+    for (int j = 0; j < 32; ++j)
+      if (col0 + j < p.r) yrow[col0 + j] = __uint_as_float(r[j]);
+  }
+  if (p.yb) {
+    uint16_t* brow = p.yb + static_cast<size_t>(row) * p.r;
+    if (full && (p.r & 7) == 0) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8)
+        __stcs(reinterpret_cast<uint4*>(brow + col0 + j),
+               make_uint4(pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                          pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                          pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                          pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]))));
+    } else {
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < p.r) brow[col0 + j] = f32_to_bf16_bits(__uint_as_float(r[j]));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t accf_bar[2];
+  __shared__ __align__(8) uint64_t acce_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  volatile int* abort = &abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (p.m + BM - 1) / BM;
+  const int num_n = (p.r + BN - 1) / BN;
+  const int num_k = (p.k + BK - 1) / BK;
+  const int tiles = num_m * num_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&accf_bar[a]), 1);
+      mbar_init(smem_u32(&acce_bar[a]), 128);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.a);
+    for (int s = 0; s < p.n_shards; ++s) prefetch_tmap(&p.w[s]);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int64_t last_issue[STAGES];
+      for (int s = 0; s < STAGES; ++s) last_issue[s] = -1;
+      uint32_t it = 0;
+      bool stop = false;
+      for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x) {
+        const int m0 = (tile % num_m) * BM;
+        const int n0 = (tile / num_m) * BN;
+        const int shard = n0 / p.shard_rows;
+        const int nl = n0 - shard * p.shard_rows;
+        const void* wmap = &p.w[shard];
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (it >= STAGES &&
+              !mbar_wait_bounded(smem_u32(&empty_bar[s]), ph ^ 1u, abort, &g_zgb_dev_error, kErrEmpty)) {
+            stop = true;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full_bar[s]);
+          uint8_t* sa = smem + s * STAGE_BYTES;
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          tma_load_2d(smem_u32(sa), &p.a, kb * BK, m0, fb);
+          tma_load_2d(smem_u32(sa + A_BYTES), wmap, kb * BK, nl, fb);
+          last_issue[s] = it;
+        }
+      }
+      if (*abort) {
+        int never = 0;
+        for (int s = 0; s < STAGES; ++s)
+          if (last_issue[s] >= 0)
+            mbar_wait_bounded(smem_u32(&full_bar[s]), static_cast<uint32_t>(last_issue[s] / STAGES) & 1u, &never,
+                              &g_zgb_dev_error, kErrDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0, i = 0;
+      bool stop = false, issued = false;
+      for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x, ++i) {
+        const uint32_t a = i & 1u, u = i >> 1;
+        if (u >= 1 && !mbar_wait_bounded(smem_u32(&acce_bar[a]), (u - 1) & 1u, abort, &g_zgb_dev_error, kErrAccE))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + a * BN;
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, abort, &g_zgb_dev_error, kErrFull)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+          const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)  // K = 16 per MMA: +32 bytes = +2 in the address field
+            umma_bf16(d, ad + 2u * k, bd + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit(smem_u32(&empty_bar[s]));
+          issued = true;
+        }
+        if (!stop) umma_commit(smem_u32(&accf_bar[a]));
+      }
+      if (*abort && issued) {
+        int never = 0;
+        umma_commit(smem_u32(&drain_bar));
+        mbar_wait_bounded(smem_u32(&drain_bar), 0, &never, &g_zgb_dev_error, kErrDrain);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2-5) ----------------
+    const int q = warp & 3;  // a warp reads TMEM lanes [32q, 32q+32)
+    const int row_in_tile = q * 32 + lane;
+    uint32_t i = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
+      const uint32_t a = i & 1u, u = i >> 1;
+      if (!warp_wait(smem_u32(&accf_bar[a]), u & 1u, abort, kErrAccF)) break;
+      tc_fence_after();
+      const int m0 = (tile % num_m) * BM;
+      const int n0 = (tile / num_m) * BN;
+      const int row = m0 + row_in_tile;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32cols(taddr + c, r);
+        if (row < p.m && n0 + c < p.r) store_row_chunk(p, row, n0 + c, r);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&acce_bar[a]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---- host side ----
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+std::once_flag g_attr_once[64];
+
+int get_encode() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? ZERO_OK : set_error(ZERO_ERR_CUDA, "fsdp_unit_forward: cuTensorMapEncodeTiled unavailable");
+}
+
+int encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+              uint32_t box_rows) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(ZERO_ERR_CUDA, "fsdp_unit_forward: cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return ZERO_OK;
+}
+
+}  // namespace
+
+int launch_fsdp_gemm(int n_shards, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
+                     const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, cudaStream_t st) {
+  if (m_tokens > INT32_MAX / 2 || rows_out > INT32_MAX / 2 || k_in > INT32_MAX / 2)
+    return set_error(ZERO_ERR_INVALID_ARG, "fsdp_unit_forward: sizes must be below 2^30");
+  const int64_t shard_rows = rows_out / n_shards;
+  if (n_shards > 1 && (shard_rows % BN != 0 || n_shards > kMaxShards))
+    return set_error(ZERO_ERR_UNSUPPORTED,
+                     "fsdp_unit_forward: the fused gather needs rows_out/n_ranks (%lld) to be a multiple of %d and "
+                     "n_ranks <= %d; pass scratch_w to gather first",
+                     (long long)shard_rows, BN, kMaxShards);
+  int rc = get_encode();
+  if (rc) return rc;
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  if ((rc = encode_2d(&p.a, A, k_in, m_tokens, BK, BM))) return rc;
+  for (int s = 0; s < n_shards; ++s)
+    if ((rc = encode_2d(&p.w[s], w_shards[s], k_in, shard_rows, BK, BN))) return rc;
+  p.y = Y;
+  p.yb = Y_bf16;
+  p.m = static_cast<int>(m_tokens);
+  p.r = static_cast<int>(rows_out);
+  p.k = static_cast<int>(k_in);
+  p.shard_rows = static_cast<int>(shard_rows);
+  p.n_shards = n_shards;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "fsdp_unit_forward: %s", cudaGetErrorString(e));
+  cudaError_t attr = cudaSuccess;
+  std::call_once(g_attr_once[dev & 63], [&] {
+    attr = cudaFuncSetAttribute(fsdp_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "fsdp_unit_forward: %s", cudaGetErrorString(attr));
+  const int64_t tiles = ((m_tokens + BM - 1) / BM) * ((rows_out + BN - 1) / BN);
+  const unsigned int grid = static_cast<unsigned int>(std::min<int64_t>(tiles, num_sms()));
+  fsdp_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "fsdp_unit_forward: launch: %s", cudaGetErrorString(e));
+  return ZERO_OK;
 }
 
 unsigned int fsdp_gemm_read_clear_error() {
@@ -15,4 +315,5 @@ unsigned int fsdp_gemm_read_clear_error() {
   if (v) cudaMemcpyToSymbol(g_zgb_dev_error, &zero, sizeof(zero));
   return v;
 }
+
 }  // namespace zgb

@@ -1,0 +1,158 @@
+"""GPU parity of the FSDP unit (row-shard gather + tcgen05 GEMM) against the CPU oracle.
+
+The gather is a bit copy: compared bit for bit. The GEMM sums exact bf16 x bf16 products
+in fp32 in an order the tensor cores choose, so it is compared with the oracle's float64
+result under the rounding bound of any fp32 summation order:
+    |Y - Y_exact| <= (K + 1) * 2^-23 * sum_k |a_k w_k|
+(first-order bound of recursive summation with unit roundoff 2^-23, which also covers
+round-toward-zero accumulation). The bf16 output must be the round-to-nearest-even of the
+kernel's own fp32 output, bit for bit. The fused-gather path and the scratch-gather path
+load identical tiles, so their outputs must agree bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.zero_oracle as O
+import synth
+from _util import assert_bf16_identical, bits16, f32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def z():
+    import __graft_entry__ as g
+    g.build()
+    import fsdp_sharded_optimizer_zero_gb300 as z
+    return z
+
+
+def gemm_bound(a64, w64, K):
+    return (K + 1) * 2.0 ** -23 * (np.abs(a64) @ np.abs(w64).T)
+
+
+def check_gemm(y_gpu, a_bits, shards_bits, what):
+    y64, _, _ = O.fsdp_linear_forward(a_bits, shards_bits)
+    a64 = O.bf16_to_f32(a_bits).astype(np.float64)
+    w64 = O.bf16_to_f32(O.gather_rows(shards_bits)).astype(np.float64)
+    bound = gemm_bound(a64, w64, a64.shape[1])
+    err = np.abs(y_gpu.astype(np.float64) - y64)
+    bad = err > bound + 1e-30
+    assert not bad.any(), f"{what}: {bad.sum()} outputs outside the bound; worst err {err.max()} at {np.unravel_index(err.argmax(), err.shape)}"
+
+
+@pytest.mark.parametrize("rows,k,n", [(2048, 1024, 8), (77 * 8, 520, 8), (999, 40, 3), (64, 8, 64), (5, 3, 5)])
+def test_gather_rows_bit_exact(z, rows, k, n):
+    shards = synth.weight_shards(rows, k, n, device=DEV)
+    full = torch.empty(rows, k, dtype=torch.bfloat16, device=DEV)
+    z.fsdp_gather_rows(shards, full)
+    z.zero_device_status()
+    assert_bf16_identical(bits16(full), O.gather_rows([bits16(s) for s in shards]), "gather")
+
+
+def test_gather_rows_misaligned_scalar_path(z):
+    rows, k, n = 12, 7, 4
+    base = torch.zeros(rows * k + 1, dtype=torch.bfloat16, device=DEV)
+    full = base[1:].view(rows, k)
+    shards = synth.weight_shards(rows, k, n, device=DEV)
+    z.fsdp_gather_rows(shards, full)
+    z.zero_device_status()
+    assert_bf16_identical(bits16(full), O.gather_rows([bits16(s) for s in shards]), "gather misaligned")
+
+
+@pytest.mark.parametrize("m,rows,k,n", [(128, 256, 64, 1), (256, 2048, 512, 8), (200, 2048, 520, 8),
+                                        (384, 512, 1024, 2), (1, 256, 8, 1), (130, 4096, 136, 16)])
+def test_gemm_fused_gather_vs_oracle(z, m, rows, k, n):
+    shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=m)
+    A = synth.activations(m, k, device=DEV, seed_key=k)
+    Y = torch.full((m, rows), float("nan"), device=DEV)
+    Yb = torch.zeros(m, rows, dtype=torch.bfloat16, device=DEV)
+    z.fsdp_unit_forward(shards, A, Y, Y_bf16=Yb)
+    z.zero_device_status()
+    y = f32(Y)
+    check_gemm(y, bits16(A), [bits16(s) for s in shards], f"fused m={m} rows={rows} k={k} n={n}")
+    assert_bf16_identical(bits16(Yb), O.f32_to_bf16(y), "bf16 output = RNE(fp32 output)")
+
+
+@pytest.mark.parametrize("m,rows,k,n", [(300, 1024, 264, 8), (129, 300, 72, 3), (256, 2048, 512, 8)])
+def test_gemm_scratch_gather_vs_oracle(z, m, rows, k, n):
+    shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=rows)
+    A = synth.activations(m, k, device=DEV, seed_key=m)
+    Y = torch.full((m, rows), float("nan"), device=DEV)
+    scratch = torch.empty(rows, k, dtype=torch.bfloat16, device=DEV)
+    z.fsdp_unit_forward(shards, A, Y, scratch_w=scratch)
+    z.zero_device_status()
+    check_gemm(f32(Y), bits16(A), [bits16(s) for s in shards], f"scratch m={m} rows={rows} k={k}")
+    assert_bf16_identical(bits16(scratch), O.gather_rows([bits16(s) for s in shards]), "scratch holds gathered W")
+    if (rows // n) % 256 == 0:
+        Y2 = torch.empty_like(Y)
+        z.fsdp_unit_forward(shards, A, Y2)
+        z.zero_device_status()
+        assert torch.equal(Y.view(torch.int32), Y2.view(torch.int32)), "fused and scratch gathers disagree"
+
+
+def test_gemm_integer_values_exact(z):
+    """Small integers: every product and partial sum is exact in fp32, so any summation
+    order gives the exact result; checks orientation (Y = A W^T) and shard order."""
+    m, rows, k, n = 128, 512, 128, 2
+    rng = np.random.default_rng(0)
+    a = rng.integers(-3, 4, (m, k)).astype(np.float32)
+    w = rng.integers(-3, 4, (rows, k)).astype(np.float32)
+    A = torch.from_numpy(O.f32_to_bf16(a).view(np.int16)).view(torch.bfloat16).to(DEV)
+    wb = O.f32_to_bf16(w)
+    shards = [torch.from_numpy(wb[r * 256:(r + 1) * 256].view(np.int16).copy()).view(torch.bfloat16).to(DEV)
+              for r in range(n)]
+    Y = torch.empty(m, rows, device=DEV)
+    z.fsdp_unit_forward(shards, A, Y)
+    z.zero_device_status()
+    assert np.array_equal(f32(Y), a @ w.T)
+
+
+def test_gemm_needs_scratch_when_shards_do_not_tile(z):
+    shards = synth.weight_shards(8 * 128, 64, 8, device=DEV)
+    A = synth.activations(128, 64, device=DEV)
+    Y = torch.empty(128, 1024, device=DEV)
+    with pytest.raises(z.ZeroError) as e:
+        z.fsdp_unit_forward(shards, A, Y)
+    assert e.value.code == -4
+
+
+def test_mistral_mlp_unit_sampled(z):
+    """Mistral-7B MLP unit, N = 8 row shards: W_up / W_gate [14336, 4096] with X [8192,
+    4096] and W_down [4096, 14336] with H [8192, 14336]; gather fused into the loads. 4096
+    sampled outputs per matrix plus every output column at the shard seams for a few rows,
+    each against the float64 oracle under the fp32 summation bound. Memory stays at the
+    shards plus activations and output: no gathered W is ever allocated."""
+    n, M = 8, 8192
+    rng = np.random.default_rng(42)
+    X = synth.activations(M, 4096, device=DEV)
+    H = synth.activations(M, 14336, device=DEV, seed_key=1)
+    for name, R, K, A, key in (("up", 14336, 4096, X, 11), ("gate", 14336, 4096, X, 12), ("down", 4096, 14336, H, 13)):
+        shards = synth.weight_shards(R, K, n, device=DEV, seed_key=key)
+        Y = torch.empty(M, R, device=DEV)
+        torch.cuda.synchronize()
+        before = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        z.fsdp_unit_forward(shards, A, Y)
+        z.zero_device_status()
+        assert torch.cuda.max_memory_allocated() <= before, "the fused gather allocated memory"
+        rs = R // n
+        rows = rng.integers(0, M, 4096)
+        cols = rng.integers(0, R, 4096)
+        seam_cols = np.array([c for r in range(1, n) for c in (r * rs - 1, r * rs)] + [0, R - 1])
+        seam_rows = rng.integers(0, M, 8)
+        rows = np.concatenate([rows, np.repeat(seam_rows, seam_cols.size)])
+        cols = np.concatenate([cols, np.tile(seam_cols, seam_rows.size)])
+        a64 = O.bf16_to_f32(bits16(A[torch.from_numpy(rows).to(DEV)])).astype(np.float64)
+        w_full = torch.cat(shards, 0)
+        w64 = O.bf16_to_f32(bits16(w_full[torch.from_numpy(cols).to(DEV)])).astype(np.float64)
+        exact = np.einsum("ik,ik->i", a64, w64)
+        bound = (K + 1) * 2.0 ** -23 * np.einsum("ik,ik->i", np.abs(a64), np.abs(w64))
+        got = f32(Y[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)]).astype(np.float64)
+        bad = np.abs(got - exact) > bound
+        assert not bad.any(), f"{name}: {bad.sum()} sampled outputs outside the bound"
+        del shards, Y, w_full
