@@ -33,7 +33,7 @@ EXPORTS = (
     "zero_plan", "zero_plan_query", "zero_bucket_range", "zero_plan_destroy",
     "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_buckets",
     "zero_allgather_params", "ddp_allreduce", "fsdp_gather_rows", "fsdp_unit_forward",
-    "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
+    "fsdp_unit_forward_static_scratch", "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
 )
 
 
@@ -83,6 +83,7 @@ def _load():
         "ddp_allreduce": (I, [P, PP, VP, VP]),
         "fsdp_gather_rows": (I, [I, PP, I64, I64, VP, VP]),
         "fsdp_unit_forward": (I, [I, PP, I64, I64, VP, I64, VP, VP, VP, VP]),
+        "fsdp_unit_forward_static_scratch": (I, [I, PP, I64, I64, VP, I64, VP, VP, VP]),
         "zero_last_error": (C.c_char_p, []),
         "zero_device_status": (I, [VP]),
         "zero_set_fused_kernel": (I, [I]),
@@ -239,6 +240,16 @@ def fsdp_unit_forward(w_shards, A, Y, Y_bf16=None, scratch_w=None, stream=None):
                                   _dev(A, torch.bfloat16, "A"), m_tok, _dev(Y, torch.float32, "Y"),
                                   _dev(Y_bf16, torch.bfloat16, "Y_bf16"),
                                   _dev(scratch_w, torch.bfloat16, "scratch_w"), _stream(stream)))
+
+
+def fsdp_unit_forward_static_scratch(w_shards, A, Y, Y_bf16=None, stream=None):
+    """fsdp_unit_forward with the gathered W in the library's own 16 MiB device array
+    (for callers that cannot allocate); no scratch argument."""
+    n = len(w_shards)
+    rows = sum(int(s.shape[0]) for s in w_shards)
+    _check(_lib.fsdp_unit_forward_static_scratch(
+        n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, int(A.shape[1]), _dev(A, torch.bfloat16, "A"),
+        int(A.shape[0]), _dev(Y, torch.float32, "Y"), _dev(Y_bf16, torch.bfloat16, "Y_bf16"), _stream(stream)))
 
 
 def zero_device_status(stream=None):

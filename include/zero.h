@@ -223,6 +223,21 @@ ZERO_API int fsdp_unit_forward(int n_ranks, const zero_bf16* const w_shards[], i
                       const zero_bf16* A, int64_t m_tokens, float* Y, zero_bf16* Y_bf16, zero_bf16* scratch_w,
                       zero_stream_t stream);
 
+/* Allocation-free variant of fsdp_unit_forward, for callers that cannot allocate device
+ * memory where they run the unit (e.g. a plug-in inside a framework that owns all device
+ * memory through its own pool, or a latency-critical path that cannot take cudaMalloc's
+ * device-wide synchronisation). The pages have no counterpart to this call.
+ * Arguments as fsdp_unit_forward without scratch_w: it always gathers W first, into a
+ * 16 MiB array inside this library (8,388,608 bf16 elements; rows_out * k_in above that
+ * returns ZERO_ERR_INVALID_ARG), then runs the same GEMM. It allocates nothing. Every GPU
+ * that loads the library holds the array until the process exits. The first call on a
+ * device (with that device current) looks up the array's address: make it before any
+ * stream capture. All calls share the array and it keeps the last call's W; calls that
+ * overlap on the GPU race on it. */
+ZERO_API int fsdp_unit_forward_static_scratch(int n_ranks, const zero_bf16* const w_shards[], int64_t rows_out,
+                                              int64_t k_in, const zero_bf16* A, int64_t m_tokens, float* Y,
+                                              zero_bf16* Y_bf16, zero_stream_t stream);
+
 /* ------------------------------------------------------------------------------------ */
 /* status                                                                                */
 /* ------------------------------------------------------------------------------------ */
