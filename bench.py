@@ -232,10 +232,10 @@ def run_ours(args):
         "config": workload_config(psi, n, stage, bb),
         "hbm_gbs": bytes_per_step * K * world / (ms_total / 1e3) / 1e9,
         "hbm_pct_of_peak": 100.0 * (bytes_per_step * K / (ms_total / 1e3) / 1e9) / hbm_peak,
-        "roofline": {"bound": "hbm", "kernel": "fused_tma_kernel", "achieved": achieved, "peak": hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": "fused_vec_kernel<8>", "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "traffic": ncu_traffic("fused_tma_kernel", P),
+                     "traffic": ncu_traffic("fused_vec_kernel", P),
                      "algorithmic_bytes_per_launch": bytes_per_step, "launch_ms": launch_ms},
         "clocks": clocks,
         "gpu_launches": K,
@@ -331,12 +331,12 @@ def extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args):
     legs["allgather_params"] = {"ms": ms_ag, "gbs": b_ag / ms_ag / 1e6, "frac": b_ag / ms_ag / 1e6 / hbm_peak,
                                 "bytes": b_ag}
     legs["unfused_pipeline_ms"] = ms_ar + ms_ad + ms_ag
-    z.zero_set_fused_kernel(2)
-    ms_vec = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1,
+    z.zero_set_fused_kernel(1)
+    ms_tma = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1,
                                                      stream), it, stream)
     z.zero_set_fused_kernel(0)
     b_f = P * (2 * n + 26)
-    legs["fused_register_variant"] = {"ms": ms_vec, "gbs": b_f / ms_vec / 1e6, "frac": b_f / ms_vec / 1e6 / hbm_peak}
+    legs["fused_tma_pipeline_variant"] = {"ms": ms_tma, "gbs": b_f / ms_tma / 1e6, "frac": b_f / ms_tma / 1e6 / hbm_peak}
     del grads, master, m, v, param, g
     torch.cuda.empty_cache()
     legs["fsdp_unit_forward"] = fsdp_leg(z, synth, dev, tf_burst, peak_src, stream)
@@ -501,8 +501,46 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_case(args):
+    """Small cases for ncu captures (a few launches, about 1 GB on the device, inputs larger
+    than L2). fused_small: psi = 33,554,432 flat, N = 8, all ranks, 5 fused launches.
+    gemm_small: Y[2048, 14336] = X W^T with W 14336 x 4096 in 8 row shards, 5 launches."""
+    import torch
+
+    import fsdp_sharded_optimizer_zero_gb300 as z
+    import synth
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    out = {"case": args.case}
+    if args.case == "fused_small":
+        psi, n = 1 << 25, 8
+        plan = z.zero_plan(psi, n, "zero2", 25 * MIB)
+        grads = [synth.rank_grads(psi, psi, r, 1, device=dev) for r in range(n)]
+        master = synth.master_params(psi, psi, device=dev)
+        m = torch.zeros(psi, device=dev)
+        v = torch.zeros(psi, device=dev)
+        param = torch.empty(psi, dtype=torch.bfloat16, device=dev)
+        hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+        ms = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1, stream),
+                           4, stream)
+        out.update(psi=psi, n_ranks=n, ms=ms, bytes=plan.fused_step_bytes, gbs=plan.fused_step_bytes / ms / 1e6)
+    elif args.case == "gemm_small":
+        M, R, K, n = 2048, 14336, 4096, 8
+        X = synth.activations(M, K, device=dev)
+        shards = synth.weight_shards(R, K, n, device=dev)
+        Y = torch.empty(M, R, device=dev)
+        ms = time_launches(lambda: z.fsdp_unit_forward(shards, X, Y, stream=stream), 4, stream)
+        out.update(M=M, R=R, K=K, ms=ms, tflops=2.0 * M * R * K / ms / 1e9)
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    z.zero_device_status(stream)
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--case", default=None, help="small profiling case: fused_small | gemm_small")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
@@ -521,7 +559,9 @@ def main():
         return
     import __graft_entry__ as g
     g.build()
-    if args.sweep:
+    if args.case:
+        run_case(args)
+    elif args.sweep:
         run_sweep(args)
     else:
         run_ours(args)

@@ -278,9 +278,11 @@ static int fused_impl(const zero_plan_t* plan, int rank, uint64_t b0, uint64_t b
   const bool state16 = aligned(w, 16) && aligned(mm, 16) && aligned(vv, 16) && aligned(p, 8);
   const bool tma_ok = state16 && grads_aligned(gp, L.n_ranks, 16) && stride_ok(r.d, 8);
   const bool vec_ok = state16 && grads_aligned(gp, L.n_ranks, 8) && stride_ok(r.d, 4);
-  int want = g_fused_variant.load(std::memory_order_relaxed);
+  // default (0) and 2: register streaming, at the copy roofline for every N on GB300;
+  // 1: the TMA bulk pipeline (ablation). Misaligned buffers take the scalar kernel.
+  const int want = g_fused_variant.load(std::memory_order_relaxed);
   int variant;
-  if (want == 1 || want == 0)
+  if (want == 1)
     variant = tma_ok ? 1 : (vec_ok ? 2 : 3);
   else
     variant = vec_ok ? 2 : 3;

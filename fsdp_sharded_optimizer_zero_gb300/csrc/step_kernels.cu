@@ -158,20 +158,34 @@ __global__ void __launch_bounds__(kThreads) fused_scalar_kernel(GradPtrs gp, int
 
 // ------------------------------------------------------------------------------------
 // fused step, TMA bulk-copy pipeline.
-// One CTA per SM, persistent over tiles of `tile` elements. Warp 8 (one elected lane) is
-// the producer: for each tile it issues N + 3 one-dimensional bulk copies (the N ranks'
-// gradient chunks and the master / m / v slices) into a shared-memory stage and arms the
-// stage's "full" mbarrier with the byte count. Warps 0-7 consume: they wait for the
-// stage, reduce the N chunks in rank order, run Adam, store master / m / v / param to
-// HBM with streaming stores, and release the stage through its "empty" mbarrier.
+// One CTA per SM, persistent over tiles of `tile` elements. The last warp (one elected
+// lane) is the producer: for each tile it issues N + 3 one-dimensional bulk copies (the N
+// ranks' gradient chunks and the master / m / v slices) into a shared-memory stage and
+// arms the stage's "full" mbarrier with the byte count. The other warps consume: they
+// wait for the stage, reduce the N chunks in rank order, run Adam, store master / m / v /
+// param to HBM with streaming stores, and release the stage through its "empty" mbarrier.
 // A tile's ragged end (< 8 elements, below the 16-byte copy granule) is read directly
 // from global memory by the consumers.
+// Measured on GB300 (GPT-2-small list, N = 8): 16 consumer warps reach 97.5 % of the
+// copy bandwidth (8 warps: 88 %, the IEEE divide / square-root chains need the extra
+// warps); at large N the per-rank chunk of a tile shrinks (512 B at N = 64) and the
+// pipeline falls far behind the register-streaming kernel, which is therefore the default.
 // ------------------------------------------------------------------------------------
-constexpr int kTmaConsumerWarps = 8;
+#ifndef ZGB_TMA_CONSUMER_WARPS
+#define ZGB_TMA_CONSUMER_WARPS 16
+#endif
+#ifndef ZGB_TMA_CTAS_PER_SM
+#define ZGB_TMA_CTAS_PER_SM 1
+#endif
+#ifndef ZGB_TMA_SMEM_BUDGET
+#define ZGB_TMA_SMEM_BUDGET (200u * 1024u)
+#endif
+constexpr int kTmaConsumerWarps = ZGB_TMA_CONSUMER_WARPS;
 constexpr int kTmaThreads = (kTmaConsumerWarps + 1) * 32;
+constexpr int kTmaCtasPerSm = ZGB_TMA_CTAS_PER_SM;
 constexpr int kTmaMaxStages = 8;
-constexpr uint32_t kTmaStageBudget = 64u * 1024u;  // bytes of one stage at most
-constexpr uint32_t kTmaSmemBudget = 200u * 1024u;  // bytes of all stages
+constexpr uint32_t kTmaSmemBudget = ZGB_TMA_SMEM_BUDGET;  // bytes of all stages of one CTA
+constexpr uint32_t kTmaStageBudget = kTmaSmemBudget / 3 < 64u * 1024u ? kTmaSmemBudget / 3 : 64u * 1024u;
 
 struct TileSpan {
   uint64_t base;  // flat index of the tile's first element
@@ -187,7 +201,7 @@ __device__ __forceinline__ TileSpan tile_span(const Domain& d, uint64_t tiles_pe
   return {seg * d.seg_stride + e0, static_cast<uint32_t>(rem < tile ? rem : tile)};
 }
 
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(kTmaThreads, kTmaCtasPerSm)
     fused_tma_kernel(GradPtrs gp, int n, float* __restrict__ master, float* __restrict__ m, float* __restrict__ v,
                      uint16_t* __restrict__ param, Domain d, AdamScalars sc, uint32_t tile, uint32_t stages) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -477,7 +491,8 @@ cudaError_t launch_fused(const GradPtrs& gp, int n, float* master, float* m, flo
     if (attr_err != cudaSuccess) return attr_err;
     const TmaConfig c = tma_config(n);
     const uint64_t tiles = (d.seg_len + c.tile - 1) / c.tile * d.n_seg;
-    const unsigned int grid = static_cast<unsigned int>(std::max<uint64_t>(1, std::min<uint64_t>(tiles, num_sms())));
+    const unsigned int grid =
+        static_cast<unsigned int>(std::max<uint64_t>(1, std::min<uint64_t>(tiles, num_sms() * kTmaCtasPerSm)));
     fused_tma_kernel<<<grid, kTmaThreads, c.smem, st>>>(gp, n, master, m, v, param, d, sc, c.tile, c.stages);
     return cudaGetLastError();
   }

@@ -251,8 +251,9 @@ ZERO_API const char* zero_last_error(void);
  * or ZERO_ERR_CUDA. */
 ZERO_API int zero_device_status(zero_stream_t stream);
 
-/* Select the fused-step kernel: 0 = automatic (default), 1 = TMA bulk-copy pipeline,
- * 2 = register-streaming kernel. Both give bit-identical results; used for ablations. */
+/* Select the fused-step kernel: 0 = default (the register-streaming kernel), 1 = TMA
+ * bulk-copy pipeline staging the N rank chunks in shared memory, 2 = register-streaming.
+ * All give bit-identical results (misaligned buffers always take a scalar kernel). */
 ZERO_API int zero_set_fused_kernel(int which);
 
 /* Library version, e.g. 100 for 0.1.0. */
