@@ -156,13 +156,22 @@ def init_dist(args):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (the slowest rank's time). Host bookkeeping only: NCCL
+    on the GPU machine, gloo in the CPU tests."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank: float, steps: int, world: int, seconds_max: float) -> float:
+    """Whole-job throughput of N independent replicas: every rank's units over the slowest
+    rank's time."""
+    return world * units_per_rank * steps / seconds_max
 
 
 def barrier(world):
@@ -221,7 +230,7 @@ def run_ours(args):
     ms_total = max_over_ranks(t0.elapsed_time(t1), world)
     ms_step = ms_total / K
     launch_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    value = world * psi * K / (ms_total / 1e3)
+    value = job_throughput(psi, K, world, ms_total / 1e3)
     achieved = bytes_per_step / (launch_ms / 1e3) / 1e9
     clocks = clk.summary()
 
@@ -282,7 +291,7 @@ def e2e_leg(z, synth, plan, psi, n, dev, hp, world, args):
     torch.cuda.synchronize()
     el = max_over_ranks(time.perf_counter() - t0, world)
     z.zero_device_status(stream)
-    return {"value": world * psi * steps / el, "unit": UNIT, "h2d_bytes_per_step": 2 * P * n,
+    return {"value": job_throughput(psi, steps, world, el), "unit": UNIT, "h2d_bytes_per_step": 2 * P * n,
             "d2h_bytes_per_step": 2 * P, "steps": steps, "ms_per_step": 1e3 * el / steps,
             "how": "per step: cudaMemcpyAsync of the 8 ranks' bf16 grads from pinned host memory, the fused step, "
                    "cudaMemcpyAsync of the bf16 params back; wall clock over the steps"}

@@ -1,0 +1,63 @@
+"""The multi-process bench path on CPU: two gloo ranks (127.0.0.1), as torchrun would
+launch them. Each rank times its own replica; rank 0 reports every rank's units over the
+slowest rank's time. The reference arm under torchrun runs on rank 0 only."""
+from __future__ import annotations
+
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+from pathlib import Path
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def worker(rank, world, port, q):
+    sys.path.insert(0, str(ROOT))
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    local_seconds = [0.5, 2.0][rank]
+    slowest = bench.max_over_ranks(local_seconds, world)
+    value = bench.job_throughput(1000, 10, world, slowest)
+    bench.barrier(world)
+    # --impl reference: only rank 0 prints; the others return without work
+    buf = io.StringIO()
+    args = type("A", (), dict(steps=1, warmup=0, ref_seconds=0.5))()
+    with redirect_stdout(buf):
+        bench.run_reference(args)
+    q.put((rank, slowest, value, buf.getvalue()))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_aggregate_like_the_bench():
+    world, port = 2, free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = {}
+    for _ in range(world):
+        rank, slowest, value, printed = q.get(timeout=240)
+        out[rank] = (slowest, value, printed)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank in range(world):
+        assert out[rank][0] == 2.0                     # max over ranks
+        assert out[rank][1] == pytest.approx(2 * 1000 * 10 / 2.0)
+    assert '"impl": "reference"' in out[0][2]
+    assert out[1][2] == ""
