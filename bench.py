@@ -346,7 +346,16 @@ def extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args):
     z.zero_set_fused_kernel(0)
     b_f = P * (2 * n + 26)
     legs["fused_tma_pipeline_variant"] = {"ms": ms_tma, "gbs": b_f / ms_tma / 1e6, "frac": b_f / ms_tma / 1e6 / hbm_peak}
-    del grads, master, m, v, param, g
+    del grads, g
+    # Megatron distributed optimizer: the same fused step on fp32 gradients, 4N + 26 B/param
+    plan_mg = z.zero_plan(psi, n, "megatron", 25 * MIB)
+    grads32 = [synth.rank_grads_f32(psi, P, r, 1, device=dev) for r in range(n)]
+    ms_mg = time_launches(lambda: z.zero_fused_step_fp32_grads(plan_mg, z.ZERO_ALL_RANKS, grads32, master, m, v, param,
+                                                               hp, 1, stream), it, stream)
+    b_mg = plan_mg.fused_step_bytes
+    legs["megatron_fp32_grads"] = {"ms": ms_mg, "gbs": b_mg / ms_mg / 1e6, "frac": b_mg / ms_mg / 1e6 / hbm_peak,
+                                   "bytes": b_mg, "params_per_s": P / ms_mg * 1e3}
+    del grads32, master, m, v, param
     torch.cuda.empty_cache()
     legs["fsdp_unit_forward"] = fsdp_leg(z, synth, dev, tf_burst, peak_src, stream)
     return legs

@@ -26,12 +26,13 @@ ZERO_ERR_DEVICE = -5
 ZERO_RANK_VIEW = -1
 ZERO_ALL_RANKS = -2
 ZERO_MAX_RANKS = 64
-STAGE_IDS = {"ddp": 0, "zero1": 1, "zero2": 2, "zero3": 3}
+STAGE_IDS = {"ddp": 0, "zero1": 1, "zero2": 2, "zero3": 3, "megatron": 4}
 
 # every symbol declared in include/zero.h
 EXPORTS = (
     "zero_plan", "zero_plan_query", "zero_bucket_range", "zero_plan_destroy",
-    "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_buckets",
+    "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_fp32_grads",
+    "zero_fused_step_buckets",
     "zero_allgather_params", "ddp_allreduce", "fsdp_gather_rows", "fsdp_unit_forward",
     "fsdp_unit_forward_static_scratch", "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
 )
@@ -78,6 +79,7 @@ def _load():
         "zero_reduce_scatter": (I, [P, I, PP, VP, VP]),
         "zero_adam_step": (I, [P, I, VP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
         "zero_fused_step": (I, [P, I, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
+        "zero_fused_step_fp32_grads": (I, [P, I, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
         "zero_fused_step_buckets": (I, [P, I, U64, U64, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
         "zero_allgather_params": (I, [P, PP, VP, VP]),
         "ddp_allreduce": (I, [P, PP, VP, VP]),
@@ -202,6 +204,14 @@ def zero_fused_step(plan: Plan, rank: int, grads, master, m, v, param_out, hp, s
                                 _dev(master, torch.float32, "master"), _dev(m, torch.float32, "m"),
                                 _dev(v, torch.float32, "v"), _dev(param_out, torch.bfloat16, "param_out"),
                                 C.byref(a), step, _stream(stream)))
+
+
+def zero_fused_step_fp32_grads(plan: Plan, rank: int, grads, master, m, v, param_out, hp, step: int, stream=None):
+    a = _adam(hp)
+    _check(_lib.zero_fused_step_fp32_grads(plan.handle, rank, _ptr_array(grads, torch.float32, "grads"),
+                                           _dev(master, torch.float32, "master"), _dev(m, torch.float32, "m"),
+                                           _dev(v, torch.float32, "v"), _dev(param_out, torch.bfloat16, "param_out"),
+                                           C.byref(a), step, _stream(stream)))
 
 
 def zero_fused_step_buckets(plan: Plan, rank: int, bucket_begin: int, bucket_end: int, grads, master, m, v,

@@ -69,7 +69,7 @@ extern "C" int zero_plan(uint64_t psi, int n_ranks, int stage, uint64_t bucket_b
   CHECK_ARG(psi <= (1ull << 50), "zero_plan: psi %llu too large", (unsigned long long)psi);
   CHECK_ARG(n_ranks >= 1 && n_ranks <= ZERO_MAX_RANKS, "zero_plan: n_ranks %d outside 1..%d", n_ranks,
             ZERO_MAX_RANKS);
-  CHECK_ARG(stage >= ZERO_STAGE_DDP && stage <= ZERO_STAGE_3, "zero_plan: stage %d outside 0..3", stage);
+  CHECK_ARG(stage >= ZERO_STAGE_DDP && stage <= ZERO_STAGE_MEGATRON, "zero_plan: stage %d outside 0..4", stage);
   CHECK_ARG(bucket_bytes >= 2ull * (uint64_t)n_ranks,
             "zero_plan: bucket_bytes %llu holds less than one bf16 element per rank (need >= %d)",
             (unsigned long long)bucket_bytes, 2 * n_ranks);
@@ -88,8 +88,10 @@ extern "C" int zero_plan(uint64_t psi, int n_ranks, int stage, uint64_t bucket_b
 
   const uint64_t P = L.psi_padded, S = L.shard_elems;
   // bytes one rank keeps: bf16 param (2), bf16 grad (2), fp32 master/m/v (4 each)
-  L.state_param_bytes = 2 * (stage >= ZERO_STAGE_3 ? S : P);
-  L.state_grad_bytes = 2 * (stage >= ZERO_STAGE_2 ? S : P);
+  const bool megatron = stage == ZERO_STAGE_MEGATRON;
+  L.state_param_bytes = 2 * (stage == ZERO_STAGE_3 ? S : P);
+  // Megatron keeps the full gradient in fp32; ZeRO-2/3 keep a bf16 slice
+  L.state_grad_bytes = megatron ? 4 * P : 2 * (stage == ZERO_STAGE_2 || stage == ZERO_STAGE_3 ? S : P);
   const uint64_t opt_elems = stage >= ZERO_STAGE_1 ? S : P;
   L.state_master_bytes = L.state_m_bytes = L.state_v_bytes = 4 * opt_elems;
   L.state_total_bytes =
@@ -100,7 +102,7 @@ extern "C" int zero_plan(uint64_t psi, int n_ranks, int stage, uint64_t bucket_b
   L.comm_all_gather_bwd = stage == ZERO_STAGE_3 ? P : 0;
   L.comm_total = L.comm_reduce_scatter + L.comm_all_gather_fwd + L.comm_all_gather_bwd;
   L.ring_sent_elems = (n - 1) * (L.comm_total / n);
-  L.fused_step_bytes = P * (2 * n + 26);
+  L.fused_step_bytes = P * ((megatron ? 4 : 2) * n + 26);
 
   zero_plan_t* p = new (std::nothrow) zero_plan_t;
   if (!p) return set_error(ZERO_ERR_OOM, "zero_plan: host allocation failed");
@@ -163,7 +165,7 @@ int resolve(const zero_layout& L, int rank, uint64_t b0, uint64_t b1, const char
     r->d = {1, len, 0};
     r->grad_off = rs + lo;
     r->state_off = lo;
-    r->param_off = (L.stage <= ZERO_STAGE_2 ? rs : 0) + lo;
+    r->param_off = (L.stage == ZERO_STAGE_3 ? 0 : rs) + lo;
   } else if (rank == ZERO_RANK_VIEW) {
     r->d = {1, len, 0};
     r->grad_off = r->state_off = r->param_off = lo;
@@ -297,6 +299,37 @@ extern "C" int zero_fused_step(const zero_plan_t* plan, int rank, const zero_bf1
   if (!plan) return set_error(ZERO_ERR_INVALID_ARG, "zero_fused_step: plan is NULL");
   return fused_impl(plan, rank, 0, plan->lay.n_buckets, grads, master, m, v, param_out, hp, step, stream,
                     "zero_fused_step");
+}
+
+extern "C" int zero_fused_step_fp32_grads(const zero_plan_t* plan, int rank, const float* const grads[],
+                                          float* master, float* m, float* v, zero_bf16* param_out,
+                                          const zero_adam* hp, int64_t step, zero_stream_t stream) {
+  clear_error();
+  const char* who = "zero_fused_step_fp32_grads";
+  CHECK_ARG(plan != nullptr, "%s: plan is NULL", who);
+  const zero_layout& L = plan->lay;
+  Resolved r;
+  int rc = resolve(L, rank, 0, L.n_buckets, who, &r);
+  if (rc) return rc;
+  CHECK_ARG(master && m && v && param_out, "%s: master / m / v / param_out must not be NULL", who);
+  CHECK_ARG(grads != nullptr, "%s: grads array is NULL", who);
+  AdamScalars sc;
+  if ((rc = make_scalars(hp, step, L.n_ranks, who, &sc))) return rc;
+  F32GradPtrs gp;
+  memset(&gp, 0, sizeof(gp));
+  bool grads16 = true;
+  for (int q = 0; q < L.n_ranks; ++q) {
+    CHECK_ARG(grads[q] != nullptr, "%s: grads[%d] is NULL (missing rank)", who, q);
+    gp.p[q] = grads[q] + r.grad_off;
+    grads16 = grads16 && aligned(gp.p[q], 16);
+  }
+  float *w = master + r.state_off, *mm = m + r.state_off, *vv = v + r.state_off;
+  uint16_t* p = param_out + r.param_off;
+  const bool vec = grads16 && aligned(w, 16) && aligned(mm, 16) && aligned(vv, 16) && aligned(p, 8) &&
+                   stride_ok(r.d, 4);
+  CUDA_LAUNCH(launch_fused_f32g(gp, L.n_ranks, w, mm, vv, p, r.d, sc, vec ? 2 : 3,
+                                reinterpret_cast<cudaStream_t>(stream)));
+  return ZERO_OK;
 }
 
 extern "C" int zero_fused_step_buckets(const zero_plan_t* plan, int rank, uint64_t bucket_begin, uint64_t bucket_end,

@@ -20,12 +20,13 @@ struct AdamScalars {
 };
 
 // N device pointers carried in kernel parameter space.
-struct GradPtrs {
-  const uint16_t* p[ZERO_MAX_RANKS];
+template <typename T>
+struct RankPtrs {
+  const T* p[ZERO_MAX_RANKS];
 };
-struct MasterPtrs {
-  const float* p[ZERO_MAX_RANKS];
-};
+using GradPtrs = RankPtrs<uint16_t>;   // bf16 gradients (raw bits)
+using F32GradPtrs = RankPtrs<float>;   // fp32 gradients (Megatron distributed optimizer)
+using MasterPtrs = RankPtrs<float>;
 
 // The elements a launch covers: n_seg segments of seg_len elements; element e of segment
 // s is at flat offset s * seg_stride + e of EVERY stream of the launch (the host offsets
@@ -42,6 +43,9 @@ cudaError_t launch_adam(const float* g, float* master, float* m, float* v, uint1
 // variant: 1 = TMA bulk pipeline, 2 = register streaming, 3 = scalar (unaligned inputs)
 cudaError_t launch_fused(const GradPtrs& gp, int n, float* master, float* m, float* v, uint16_t* param,
                          const Domain& d, const AdamScalars& sc, int variant, cudaStream_t st);
+// fused step with fp32 gradients: variant 2 = register streaming, 3 = scalar
+cudaError_t launch_fused_f32g(const F32GradPtrs& gp, int n, float* master, float* m, float* v, uint16_t* param,
+                              const Domain& d, const AdamScalars& sc, int variant, cudaStream_t st);
 cudaError_t launch_allgather(const MasterPtrs& mp, int n, uint64_t shard, uint16_t* full, bool vec,
                              cudaStream_t st);
 cudaError_t launch_gather_rows(const GradPtrs& shards, int n, uint64_t shard_elems, uint16_t* full, bool vec,

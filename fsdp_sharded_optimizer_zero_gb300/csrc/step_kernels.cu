@@ -42,25 +42,44 @@ __device__ __forceinline__ void accum4(uint2 u, float s[4]) {
   s[2] = __fadd_rn(s[2], bf16_lo(u.y));
   s[3] = __fadd_rn(s[3], bf16_hi(u.y));
 }
+// fp32 gradients: widening is the identity
+__device__ __forceinline__ void widen4(float4 u, float s[4]) {
+  s[0] = u.x;
+  s[1] = u.y;
+  s[2] = u.z;
+  s[3] = u.w;
+}
+__device__ __forceinline__ void accum4(float4 u, float s[4]) {
+  s[0] = __fadd_rn(s[0], u.x);
+  s[1] = __fadd_rn(s[1], u.y);
+  s[2] = __fadd_rn(s[2], u.z);
+  s[3] = __fadd_rn(s[3], u.w);
+}
+// 4 consecutive gradient elements of one rank (8 B of bf16 or 16 B of fp32)
+__device__ __forceinline__ uint2 load4(const uint16_t* p) { return __ldcs(reinterpret_cast<const uint2*>(p)); }
+__device__ __forceinline__ float4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float to_f32(uint16_t b) { return bf16_bits_to_f32(b); }
+__device__ __forceinline__ float to_f32(float x) { return x; }
 
 // NR > 0: rank count known at compile time, all N loads in flight at once.
 // NR == 0: any N; loads issued in groups of 8 ranks, added strictly in rank order.
-template <int NR>
-__device__ __forceinline__ void reduce4(const GradPtrs& gp, int n, uint64_t idx, float s[4]) {
+template <int NR, typename G>
+__device__ __forceinline__ void reduce4(const RankPtrs<G>& gp, int n, uint64_t idx, float s[4]) {
+  using V = decltype(load4(gp.p[0]));
   if constexpr (NR > 0) {
-    uint2 u[NR];
+    V u[NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) u[r] = __ldcs(reinterpret_cast<const uint2*>(gp.p[r] + idx));
+    for (int r = 0; r < NR; ++r) u[r] = load4(gp.p[r] + idx);
     widen4(u[0], s);
 #pragma unroll
     for (int r = 1; r < NR; ++r) accum4(u[r], s);
   } else {
     for (int r0 = 0; r0 < n; r0 += 8) {
       const int cnt = min(8, n - r0);
-      uint2 u[8];
+      V u[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (j < cnt) u[j] = __ldcs(reinterpret_cast<const uint2*>(gp.p[r0 + j] + idx));
+        if (j < cnt) u[j] = load4(gp.p[r0 + j] + idx);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (j < cnt) {
@@ -74,13 +93,15 @@ __device__ __forceinline__ void reduce4(const GradPtrs& gp, int n, uint64_t idx,
   }
 }
 
-__device__ __forceinline__ float reduce1(const GradPtrs& gp, int n, uint64_t j) {
-  float s = bf16_bits_to_f32(gp.p[0][j]);
-  for (int r = 1; r < n; ++r) s = __fadd_rn(s, bf16_bits_to_f32(gp.p[r][j]));
+template <typename G>
+__device__ __forceinline__ float reduce1(const RankPtrs<G>& gp, int n, uint64_t j) {
+  float s = to_f32(gp.p[0][j]);
+  for (int r = 1; r < n; ++r) s = __fadd_rn(s, to_f32(gp.p[r][j]));
   return s;
 }
 
-__device__ __forceinline__ void fused_elem(const GradPtrs& gp, int n, float* master, float* m, float* v,
+template <typename G>
+__device__ __forceinline__ void fused_elem(const RankPtrs<G>& gp, int n, float* master, float* m, float* v,
                                            uint16_t* param, uint64_t j, const AdamScalars& sc) {
   const float g = __fmul_rn(reduce1(gp, n, j), sc.inv_n);
   float w = master[j], mm = m[j], vv = v[j];
@@ -123,8 +144,8 @@ __device__ __forceinline__ UnitPos unit_pos(const Domain& d, uint64_t units_per_
 // fused step, register-streaming variant: every thread loads its N gradient vectors and
 // its state straight into registers (no shared memory)
 // ------------------------------------------------------------------------------------
-template <int NR>
-__global__ void __launch_bounds__(kThreads) fused_vec_kernel(GradPtrs gp, int n, float* __restrict__ master,
+template <int NR, typename G>
+__global__ void __launch_bounds__(kThreads) fused_vec_kernel(RankPtrs<G> gp, int n, float* __restrict__ master,
                                                              float* __restrict__ m, float* __restrict__ v,
                                                              uint16_t* __restrict__ param, Domain d,
                                                              AdamScalars sc) {
@@ -136,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) fused_vec_kernel(GradPtrs gp, int n,
       const float4 mm = __ldcs(reinterpret_cast<const float4*>(m + p.base));
       const float4 vv = __ldcs(reinterpret_cast<const float4*>(v + p.base));
       float g[4];
-      reduce4<NR>(gp, n, p.base, g);
+      reduce4<NR, G>(gp, n, p.base, g);
       adam4_store(g, w, mm, vv, master, m, v, param, p.base, sc);
     } else {
       for (uint32_t k = 0; k < p.count; ++k) fused_elem(gp, n, master, m, v, param, p.base + k, sc);
@@ -145,7 +166,8 @@ __global__ void __launch_bounds__(kThreads) fused_vec_kernel(GradPtrs gp, int n,
 }
 
 // scalar variant for buffers whose alignment rules out vector accesses
-__global__ void __launch_bounds__(kThreads) fused_scalar_kernel(GradPtrs gp, int n, float* master, float* m,
+template <typename G>
+__global__ void __launch_bounds__(kThreads) fused_scalar_kernel(RankPtrs<G> gp, int n, float* master, float* m,
                                                                 float* v, uint16_t* param, Domain d,
                                                                 AdamScalars sc) {
   const uint64_t total = d.seg_len * d.n_seg;
@@ -302,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) reduce_vec_kernel(GradPtrs gp, int n
     const UnitPos p = unit_pos(d, ups, u);
     if (p.count == 4) {
       float g[4];
-      reduce4<NR>(gp, n, p.base, g);
+      reduce4<NR, uint16_t>(gp, n, p.base, g);
       __stcs(reinterpret_cast<float4*>(out + p.base),
              make_float4(__fmul_rn(g[0], inv_n), __fmul_rn(g[1], inv_n), __fmul_rn(g[2], inv_n),
                          __fmul_rn(g[3], inv_n)));
@@ -499,11 +521,26 @@ cudaError_t launch_fused(const GradPtrs& gp, int n, float* master, float* m, flo
   if (variant == 2) {
     const unsigned int grid = grid_for((d.seg_len + 3) / 4 * d.n_seg);
     return dispatch_nr(n, [&](auto nr) {
-      fused_vec_kernel<decltype(nr)::value><<<grid, kThreads, 0, st>>>(gp, n, master, m, v, param, d, sc);
+      fused_vec_kernel<decltype(nr)::value, uint16_t><<<grid, kThreads, 0, st>>>(gp, n, master, m, v, param, d, sc);
       return cudaGetLastError();
     });
   }
-  fused_scalar_kernel<<<grid_for(total), kThreads, 0, st>>>(gp, n, master, m, v, param, d, sc);
+  fused_scalar_kernel<uint16_t><<<grid_for(total), kThreads, 0, st>>>(gp, n, master, m, v, param, d, sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fused_f32g(const F32GradPtrs& gp, int n, float* master, float* m, float* v, uint16_t* param,
+                              const Domain& d, const AdamScalars& sc, int variant, cudaStream_t st) {
+  const uint64_t total = d.seg_len * d.n_seg;
+  if (total == 0) return cudaSuccess;
+  if (variant == 2) {
+    const unsigned int grid = grid_for((d.seg_len + 3) / 4 * d.n_seg);
+    return dispatch_nr(n, [&](auto nr) {
+      fused_vec_kernel<decltype(nr)::value, float><<<grid, kThreads, 0, st>>>(gp, n, master, m, v, param, d, sc);
+      return cudaGetLastError();
+    });
+  }
+  fused_scalar_kernel<float><<<grid_for(total), kThreads, 0, st>>>(gp, n, master, m, v, param, d, sc);
   return cudaGetLastError();
 }
 

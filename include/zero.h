@@ -76,7 +76,10 @@ enum {
   ZERO_STAGE_DDP = 0, /* nothing sharded */
   ZERO_STAGE_1 = 1,   /* optimizer state sharded */
   ZERO_STAGE_2 = 2,   /* + gradients */
-  ZERO_STAGE_3 = 3    /* + parameters (ZeRO-3 / FSDP full shard) */
+  ZERO_STAGE_3 = 3,   /* + parameters (ZeRO-3 / FSDP full shard) */
+  ZERO_STAGE_MEGATRON = 4 /* Megatron distributed optimizer: bf16 params and fp32 gradients
+                             kept in full, fp32 master / m / v sharded ([Interview] worked
+                             table, Megatron row: 6P + 12P/N bytes) */
 };
 
 /* `rank` argument values besides 0..N-1 */
@@ -98,8 +101,8 @@ typedef struct {
   int32_t stage;
   /* model-state bytes ONE rank keeps between steps for this stage ([Interview] "手算例子:
    * 7B、N = 8" / Fig. 1; [Concepts] stage table): DDP 16P; ZeRO-1 4P+12S; ZeRO-2 2P+14S;
-   * ZeRO-3 16S. Transient buffers (incoming gradient chunks, fp32 reduced gradient) are
-   * not model state and are not counted. */
+   * ZeRO-3 16S; Megatron 6P+12S. Transient buffers (incoming gradient chunks, fp32 reduced
+   * gradient) are not model state and are not counted. */
   uint64_t state_param_bytes, state_grad_bytes, state_master_bytes, state_m_bytes, state_v_bytes;
   uint64_t state_total_bytes;
   /* elements ONE rank moves per step per collective ([Interview] "每卡通信量"):
@@ -108,8 +111,9 @@ typedef struct {
   /* elements one rank sends per step when each collective is a ring: (N-1)/N * comm_total
    * ([Concepts] "Communication cost": 2(N-1)/N * S bytes for an all-reduce) */
   uint64_t ring_sent_elems;
-  /* algorithmic HBM bytes of one fused step over all P elements: P*(2N + 26)
-   * (read N bf16 grads, read+write fp32 master/m/v, write bf16 param) */
+  /* algorithmic HBM bytes of one fused step over all P elements: P*(2N + 26) (read N bf16
+   * grads, read+write fp32 master/m/v, write bf16 param); P*(4N + 26) for the Megatron
+   * stage, whose gradients are fp32 */
   uint64_t fused_step_bytes;
 } zero_layout;
 
@@ -176,6 +180,15 @@ ZERO_API int zero_adam_step(const zero_plan_t* plan, int rank, const float* g_sh
 ZERO_API int zero_fused_step(const zero_plan_t* plan, int rank, const zero_bf16* const grads[], float* master,
                     float* m, float* v, zero_bf16* param_out, const zero_adam* hp, int64_t step,
                     zero_stream_t stream);
+
+/* zero_fused_step with fp32 gradient contributions: grads[q] are fp32 (Megatron
+ * distributed optimizer, gradients accumulated and reduced in fp32 — [Interview] worked
+ * table, Megatron row and note). Same pointer conventions and arithmetic (the widening of
+ * the gradient is the identity); 4N + 26 bytes per parameter. Valid with any plan; the
+ * ZERO_STAGE_MEGATRON plan accounts its memory. */
+ZERO_API int zero_fused_step_fp32_grads(const zero_plan_t* plan, int rank, const float* const grads[], float* master,
+                                        float* m, float* v, zero_bf16* param_out, const zero_adam* hp, int64_t step,
+                                        zero_stream_t stream);
 
 /* As zero_fused_step, restricted to buckets [bucket_begin, bucket_end) of the shard(s):
  * the unit DDP / ZeRO reduce as soon as backward has produced a bucket ([Concepts] "Plain

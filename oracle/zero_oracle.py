@@ -128,15 +128,26 @@ def inv_n(n_ranks: int):
     return F32(1.0) / F32(n_ranks)
 
 
+def as_f32(x) -> np.ndarray:
+    """A gradient contribution as fp32: bf16 bit patterns (uint16) are widened exactly,
+    fp32 arrays (the Megatron distributed optimizer's fp32 gradients) are taken as they are."""
+    a = np.asarray(x)
+    if a.dtype == np.uint16:
+        return bf16_to_f32(a)
+    if a.dtype != np.float32:
+        raise TypeError(f"gradient contributions are bf16 bits or fp32, not {a.dtype}")
+    return a
+
+
 def reduce_sum_scale(grads, lo: int, hi: int) -> np.ndarray:
-    """The reduced gradient for flat indices [lo, hi): the N ranks' bf16 contributions
-    widened to fp32, added one rank at a time in rank order 0..N-1, then scaled by 1/N to
-    the average ([Wiring] DDP section: the GPUs average their gradients; [Concepts] "Plain
-    data parallel (DDP)" step 2)."""
+    """The reduced gradient for flat indices [lo, hi): the N ranks' contributions (bf16,
+    or fp32 for the Megatron distributed optimizer) in fp32, added one rank at a time in
+    rank order 0..N-1, then scaled by 1/N to the average ([Wiring] DDP section: the GPUs
+    average their gradients; [Concepts] "Plain data parallel (DDP)" step 2)."""
     n = len(grads)
-    acc = bf16_to_f32(grads[0][lo:hi]).copy()
+    acc = as_f32(grads[0][lo:hi]).copy()
     for q in range(1, n):
-        acc = acc + bf16_to_f32(grads[q][lo:hi])
+        acc = acc + as_f32(grads[q][lo:hi])
     return acc * inv_n(n)
 
 
@@ -353,6 +364,9 @@ def step_ranks(ranks, lay: Layout, local_grads, hp: AdamHyper, t: int):
     rank's full param buffer. ZeRO-2 keeps only its own slice of the gradient.
     ZeRO-3: as ZeRO-2, but each rank keeps only its own bf16 param slice; the full
     parameters exist only when `gather_params` assembles them for a unit.
+    Megatron distributed optimizer ([Interview] worked table, Megatron row and the note
+    beneath it): full bf16 params and full fp32 gradients (local_grads are fp32), fp32
+    master / m / v sharded; reduce-scatter, shard Adam and param all-gather as ZeRO-1.
     """
     stage = ranks[0].stage
     n = lay.n_ranks
@@ -372,7 +386,7 @@ def step_ranks(ranks, lay: Layout, local_grads, hp: AdamHyper, t: int):
         g_shard = reduce_scatter(lay, local_grads, r)
         b["master"], b["m"], b["v"] = adam_update(b["master"], b["m"], b["v"], g_shard, hp, t)
         new_shards.append(f32_to_bf16(b["master"]))
-    if stage in ("zero1", "zero2"):
+    if stage in ("zero1", "zero2", "megatron"):
         full = all_gather(new_shards)
         for st in ranks:
             st.buffers["param"] = full.copy()

@@ -141,6 +141,15 @@ def rank_grads(psi: int, psi_padded: int, rank: int, step: int, device="cpu", se
     return t
 
 
+def rank_grads_f32(psi: int, psi_padded: int, rank: int, step: int, device="cpu", seed_key=0, std=1e-3):
+    """One rank's fp32 local gradient (kept in fp32, as the Megatron distributed optimizer
+    accumulates it), length psi_padded, zero past psi."""
+    t = torch.zeros(psi_padded, dtype=torch.float32, device=device)
+    if psi:
+        _normal(psi, std, device, torch.float32, TID_GRAD, seed_key, rank, step, out=t[:psi])
+    return t
+
+
 def chunk_grads(n: int, n_ranks: int, step: int, device="cpu", seed_key=0, std=1e-3):
     """The n_ranks incoming bf16 gradient chunks (each n elements) that one rank receives
     for its own shard; returned as one [n_ranks, n] tensor, row q = rank q's chunk."""

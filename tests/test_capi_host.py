@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(z):
         assert hasattr(lib, name), name
 
 
-STAGES = ["ddp", "zero1", "zero2", "zero3"]
+STAGES = ["ddp", "zero1", "zero2", "zero3", "megatron"]
 
 
 @pytest.mark.parametrize("psi,n,bb", [(1, 1, 2), (7, 2, 4), (13, 3, 6), (1000, 8, 40), (1_000_003, 64, 1 << 20),
@@ -64,7 +64,8 @@ def test_plan_matches_oracle(z, psi, n, bb, stage):
     assert (L["comm_reduce_scatter"], L["comm_all_gather_fwd"], L["comm_all_gather_bwd"], L["comm_total"]) == \
         (c["reduce_scatter"], c["all_gather_fwd"], c["all_gather_bwd"], c["total"])
     assert L["ring_sent_elems"] == O.ring_sent_elements(c["total"], n)
-    assert L["fused_step_bytes"] == lay.psi_padded * (2 * n + 26)
+    grad_bytes = 4 if stage == "megatron" else 2
+    assert L["fused_step_bytes"] == lay.psi_padded * (grad_bytes * n + 26)
 
 
 @pytest.mark.parametrize("psi,n,bb", [(13, 3, 6), (1000, 8, 48), (4099, 5, 1 << 10)])
@@ -80,7 +81,7 @@ def test_bucket_ranges_match_oracle(z, psi, n, bb):
         z.zero_bucket_range(p, 0, lay.n_buckets)
 
 
-@pytest.mark.parametrize("args", [(0, 4, 2, 1 << 20), (10, 0, 2, 1 << 20), (10, 65, 2, 1 << 20), (10, 4, 4, 1 << 20),
+@pytest.mark.parametrize("args", [(0, 4, 2, 1 << 20), (10, 0, 2, 1 << 20), (10, 65, 2, 1 << 20), (10, 4, 5, 1 << 20),
                                   (10, 4, -1, 1 << 20), (10, 4, 2, 7)])
 def test_plan_rejects_bad_arguments(z, args):
     with pytest.raises(z.ZeroError) as e:

@@ -403,6 +403,39 @@ def test_fused_elements_equals_strategy_step():
     assert O.gather_params(ranks).tobytes() == p.tobytes()
 
 
+def test_megatron_fp32_grads_reduce_in_rank_order():
+    grads = [np.array([2.0 ** 24], np.float32), np.array([1.0], np.float32), np.array([1.0], np.float32),
+             np.array([0.0], np.float32)]
+    assert O.reduce_sum_scale(grads, 0, 1)[0] == np.float32(2.0 ** 22)
+    with pytest.raises(TypeError):
+        O.reduce_sum_scale([np.zeros(2, np.float64)], 0, 2)
+
+
+@pytest.mark.parametrize("psi,n", [(13, 3), (1000, 8), (1001, 64)])
+def test_megatron_equals_zero1_on_bf16_exact_grads(psi, n):
+    """Megatron's distributed optimizer is ZeRO-1-style ([Interview] worked table note):
+    with fp32 gradients that are exactly the widened bf16 ones it must give ZeRO-1's
+    parameters bit for bit; with general fp32 gradients it must match plain fp32 Adam."""
+    hp = O.AdamHyper()
+    master0, all_grads = make_case(psi, n, 3, psi + 7 * n)
+    lay = O.make_layout(psi, n, 2 * n * 5)
+    z1 = run_strategy("zero1", lay, master0, all_grads, hp)
+    mg = run_strategy("megatron", lay, master0, [[O.bf16_to_f32(g) for g in gs] for gs in all_grads], hp)
+    assert O.gather_params(mg).tobytes() == O.gather_params(z1).tobytes()
+    assert O.gather_master(mg, lay).tobytes() == O.gather_master(z1, lay).tobytes()
+    assert mg[0].buffers["grad"].dtype == np.float32 and mg[0].buffers["grad"].size == lay.psi_padded
+
+
+def test_megatron_single_rank_is_plain_adam_on_fp32_grads():
+    hp = O.AdamHyper()
+    rng = np.random.default_rng(12)
+    master0 = rng.normal(0, 0.02, 999).astype(np.float32)
+    grads = [[rng.normal(0, 1e-3, 999).astype(np.float32)] for _ in range(3)]
+    ranks = run_strategy("megatron", O.make_layout(999, 1, 1 << 20), master0, grads, hp)
+    tw, _, _ = run_torch_adam(master0, [g[0] for g in grads], hp, decoupled=False)
+    assert np.all(np.abs(ranks[0].buffers["master"] - tw) <= 3 * (np.abs(tw) * 2 * U32 + 16 * U32 * 1e-4))
+
+
 # ---------------------------------------------------------------------------------------
 # FSDP linear: brute force in exact rational arithmetic, orientation and shard order
 # ---------------------------------------------------------------------------------------

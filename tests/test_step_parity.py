@@ -290,6 +290,120 @@ def test_allgather_params_cast(z):
                           "all-gather cast")
 
 
+# ---------------------------------------------------------------------------------------
+# Megatron distributed optimizer: fp32 gradient contributions
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("psi,n,bb,misalign", [(1_048_576, 4, 25 * MIB, False), (100_003, 5, 1 << 12, False),
+                                               (20_001, 64, 1 << 10, False), (65_539, 16, 1 << 14, True),
+                                               (13, 3, 6, False)])
+def test_megatron_fp32_grads_bit_exact(z, psi, n, bb, misalign):
+    P = -(-psi // n) * n
+    master0 = synth.master_params(psi, P, seed_key=n)
+    m0, v0 = synth.adam_moments(P, seed_key=n)
+    m0[psi:] = 0
+    v0[psi:] = 0
+    steps = [[synth.rank_grads_f32(psi, P, r, t, seed_key=n) for r in range(n)] for t in (1, 2)]
+    lay = O.make_layout(psi, n, bb)
+    ranks = O.init_ranks("megatron", lay, master0.numpy())
+    for r, st in enumerate(ranks):
+        lo, hi = O.shard_range(lay, r)
+        st.buffers["m"][:] = m0.numpy()[lo:hi]
+        st.buffers["v"][:] = v0.numpy()[lo:hi]
+    for t, gs in enumerate(steps, start=1):
+        O.step_ranks(ranks, lay, [g.numpy() for g in gs], HP, t)
+    want = (O.gather_master(ranks, lay), np.concatenate([st.buffers["m"] for st in ranks]),
+            np.concatenate([st.buffers["v"] for st in ranks]), O.gather_params(ranks))
+    plan = z.zero_plan(psi, n, "megatron", bb)
+    assert plan.state_total_bytes == 6 * P + 12 * (P // n)
+    for mode in ("all", "ranks"):
+        S = plan.shard_elems
+        master, m, v = (offset_buf(P, torch.float32, misalign) for _ in range(3))
+        param = offset_buf(P, torch.bfloat16, misalign)
+        master.copy_(master0)
+        m.copy_(m0)
+        v.copy_(v0)
+        gbuf = [offset_buf(P, torch.float32, misalign) for _ in range(n)]
+        for t, gs in enumerate(steps, start=1):
+            for q in range(n):
+                gbuf[q].copy_(gs[q])
+            if mode == "all":
+                z.zero_fused_step_fp32_grads(plan, z.ZERO_ALL_RANKS, gbuf, master, m, v, param, HP, t)
+            else:
+                for r in range(n):
+                    sl = slice(r * S, (r + 1) * S)
+                    z.zero_fused_step_fp32_grads(plan, r, gbuf, master[sl], m[sl], v[sl], param, HP, t)
+        z.zero_device_status()
+        compare((f32(master), f32(m), f32(v), bits16(param)), want, f"megatron {mode}")
+
+
+def test_megatron_gpt2_small_n8_sampled(z):
+    """GPT-2-small list, N = 8, fp32 gradients (8 x 497 MB), 2 steps, every rank in one
+    launch, against the oracle on sampled indices."""
+    psi, n = synth.GPT2_SMALL_PSI, 8
+    plan = z.zero_plan(psi, n, "megatron", 25 * MIB)
+    P, S, C = plan.psi_padded, plan.shard_elems, plan.bucket_elems
+    master = synth.master_params(psi, P, device=DEV)
+    m = torch.zeros(P, device=DEV)
+    v = torch.zeros(P, device=DEV)
+    param = torch.empty(P, dtype=torch.bfloat16, device=DEV)
+    idx = sample_indices(P, S, C, n, seed=5)
+    idx_t = torch.from_numpy(idx).to(DEV)
+    w_s, m_s, v_s = f32(take(master, idx_t)), f32(take(m, idx_t)), f32(take(v, idx_t))
+    for t in (1, 2):
+        grads = [synth.rank_grads_f32(psi, P, r, t, device=DEV) for r in range(n)]
+        gs = [f32(take(g, idx_t)) for g in grads]
+        w_s, m_s, v_s, p_s = O.fused_step_elements(gs, w_s, m_s, v_s, HP, t)
+        z.zero_fused_step_fp32_grads(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, HP, t)
+        del grads
+    z.zero_device_status()
+    compare((f32(take(master, idx_t)), f32(take(m, idx_t)), f32(take(v, idx_t)), bits16(take(param, idx_t))),
+            (w_s, m_s, v_s, p_s), "megatron gpt2 sampled")
+
+
+def test_zero1_via_allreduce_equals_zero1(z):
+    """ZeRO-1 implemented with a full gradient all-reduce and a parameter all-gather (3 psi
+    of communication — [Interview] follow-up on ZeRO-1 vs ZeRO-2 communication) computes the
+    same parameters as the reduce-scatter form (2 psi), bit for bit."""
+    psi, n, bb = 100_003, 5, 1 << 12
+    master0, m0, v0, grads = make_inputs(psi, n, 2, seed=21, moments=True)
+    want = oracle_run("zero1", psi, n, bb, master0, m0, v0, grads)
+    plan = z.zero_plan(psi, n, "zero1", bb)
+    P, S = plan.psi_padded, plan.shard_elems
+    master, m, v = master0.to(DEV), m0.to(DEV), v0.to(DEV)
+    param = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    g_full = torch.empty(P, device=DEV)
+    for t, gs in enumerate(grads, start=1):
+        gd = [g.to(DEV) for g in gs]
+        z.ddp_allreduce(plan, gd, g_full)
+        for r in range(n):
+            sl = slice(r * S, (r + 1) * S)
+            z.zero_adam_step(plan, r, g_full[sl], master[sl], m[sl], v[sl], None, HP, t)
+        z.zero_allgather_params(plan, [master[r * S:(r + 1) * S] for r in range(n)], param)
+    z.zero_device_status()
+    compare((f32(master), f32(m), f32(v), bits16(param)), want, "zero1 via all-reduce")
+
+
+def test_buckets_in_gradient_ready_order(z):
+    """Backward produces gradients last layer first, so DDP reduces buckets in reverse
+    order of the flat buffer ([Concepts] "Plain data parallel (DDP)"); launching the
+    buckets from last to first must give the same bits as one launch."""
+    psi, n, bb = 262_147, 4, 1 << 12
+    master0, m0, v0, grads = make_inputs(psi, n, 2, seed=23, moments=True)
+    want = oracle_run("zero2", psi, n, bb, master0, m0, v0, grads)
+    plan = z.zero_plan(psi, n, "zero2", bb)
+    P, NB = plan.psi_padded, plan.n_buckets
+    assert NB > 50
+    master, m, v = master0.to(DEV), m0.to(DEV), v0.to(DEV)
+    param = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    for t, gs in enumerate(grads, start=1):
+        gd = [g.to(DEV) for g in gs]
+        for k in reversed(range(NB)):
+            z.zero_fused_step_buckets(plan, z.ZERO_ALL_RANKS, k, k + 1, gd, master, m, v, param, HP, t)
+    z.zero_device_status()
+    compare((f32(master), f32(m), f32(v), bits16(param)), want, "reverse-order buckets")
+
+
 def test_device_status_is_clean_after_all_kernels(z):
     z.zero_device_status()
 
