@@ -387,6 +387,19 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         res["roofline"] = {"bound": "tensor", "achieved": res["tflops"], "peak": tf_peak, "unit": "TFLOP/s",
                            "frac": res["tflops"] / tf_peak,
                            "peak_source": f"{peak_src} bf16_tflops (burst)" if peak_src == "measured" else "fallback"}
+        # backward of W_up for 8 ranks of 2048 tokens: W^T, dY^T, X^T layouts + 8 dX GEMMs +
+        # one rank-reduced dW GEMM
+        R, K, Mb = 14336, 4096, 2048
+        shards = synth.weight_shards(R, K, n, device=dev, seed_key=11)
+        A = [synth.activations(Mb, K, device=dev, seed_key=q) for q in range(n)]
+        dY = [synth.upstream_grad(Mb, R, device=dev, seed_key=q) for q in range(n)]
+        dX = [torch.empty(Mb, K, device=dev) for _ in range(n)]
+        dW = torch.empty(R, K, device=dev)
+        ws = torch.empty(z.fsdp_unit_backward_workspace(n, R, K, Mb), dtype=torch.uint8, device=dev)
+        ms = time_launches(lambda: z.fsdp_unit_backward(shards, A, dY, dX, dW, ws, stream=stream), 5, stream)
+        flop = 2.0 * (2.0 * n * Mb * R * K)
+        res["backward_up"] = {"ms": ms, "tflops": flop / ms / 1e9, "frac": flop / ms / 1e9 / tf_peak,
+                              "ranks": n, "tokens_per_rank": Mb, "launches": 3 + n + 1}
     except Exception as e:  # the GEMM leg must not hide the step's line
         res["error"] = str(e)[:300]
     return res

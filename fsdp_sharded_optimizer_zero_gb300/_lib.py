@@ -34,7 +34,7 @@ EXPORTS = (
     "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_fp32_grads",
     "zero_fused_step_buckets",
     "zero_allgather_params", "ddp_allreduce", "fsdp_gather_rows", "fsdp_unit_forward",
-    "fsdp_unit_forward_static_scratch", "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
+    "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_unit_forward_static_scratch", "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
 )
 
 
@@ -86,6 +86,8 @@ def _load():
         "fsdp_gather_rows": (I, [I, PP, I64, I64, VP, VP]),
         "fsdp_unit_forward": (I, [I, PP, I64, I64, VP, I64, VP, VP, VP, VP]),
         "fsdp_unit_forward_static_scratch": (I, [I, PP, I64, I64, VP, I64, VP, VP, VP]),
+        "fsdp_unit_backward_workspace": (I, [I, I64, I64, I64, C.POINTER(U64)]),
+        "fsdp_unit_backward": (I, [I, PP, I64, I64, PP, PP, I64, PP, VP, VP, U64, VP]),
         "zero_last_error": (C.c_char_p, []),
         "zero_device_status": (I, [VP]),
         "zero_set_fused_kernel": (I, [I]),
@@ -250,6 +252,25 @@ def fsdp_unit_forward(w_shards, A, Y, Y_bf16=None, scratch_w=None, stream=None):
                                   _dev(A, torch.bfloat16, "A"), m_tok, _dev(Y, torch.float32, "Y"),
                                   _dev(Y_bf16, torch.bfloat16, "Y_bf16"),
                                   _dev(scratch_w, torch.bfloat16, "scratch_w"), _stream(stream)))
+
+
+def fsdp_unit_backward_workspace(n_ranks: int, rows_out: int, k_in: int, m_tokens: int) -> int:
+    b = C.c_uint64()
+    _check(_lib.fsdp_unit_backward_workspace(n_ranks, rows_out, k_in, m_tokens, C.byref(b)))
+    return b.value
+
+
+def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace, stream=None):
+    """A, dY, dX: per-rank lists; dW: [rows_out, k_in] fp32; workspace: a uint8 CUDA tensor
+    of at least fsdp_unit_backward_workspace(...) bytes."""
+    n = len(w_shards)
+    rows = sum(int(s.shape[0]) for s in w_shards)
+    k = int(A[0].shape[1])
+    m_tok = int(A[0].shape[0])
+    _check(_lib.fsdp_unit_backward(
+        n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, k, _ptr_array(A, torch.bfloat16, "A"),
+        _ptr_array(dY, torch.bfloat16, "dY"), m_tok, _ptr_array(dX, torch.float32, "dX"),
+        _dev(dW, torch.float32, "dW"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
 
 
 def fsdp_unit_forward_static_scratch(w_shards, A, Y, Y_bf16=None, stream=None):

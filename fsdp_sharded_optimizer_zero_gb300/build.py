@@ -16,7 +16,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libzero_gb300.so"
-SOURCES = ["capi.cu", "step_kernels.cu", "fsdp_gemm.cu", "fsdp_static_scratch.cu"]
+SOURCES = ["capi.cu", "step_kernels.cu", "fsdp_gemm.cu", "fsdp_unit.cu", "fsdp_static_scratch.cu"]
 HEADERS = ["internal.h", "device_common.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = [

@@ -423,9 +423,9 @@ extern "C" int fsdp_unit_forward(int n_ranks, const zero_bf16* const w_shards[],
     int rc = fsdp_gather_rows(n_ranks, w_shards, rows_out, k_in, scratch_w, stream);
     if (rc) return rc;
     const uint16_t* w1[1] = {scratch_w};
-    return launch_fsdp_gemm(1, w1, rows_out, k_in, A, m_tokens, Y, Y_bf16, st);
+    return launch_fsdp_gemm(1, w1, rows_out, k_in, A, m_tokens, Y, Y_bf16, 1.0f, st);
   }
-  return launch_fsdp_gemm(n_ranks, w_shards, rows_out, k_in, A, m_tokens, Y, Y_bf16, st);
+  return launch_fsdp_gemm(n_ranks, w_shards, rows_out, k_in, A, m_tokens, Y, Y_bf16, 1.0f, st);
 }
 
 // ======================================================================================

@@ -51,6 +51,7 @@ struct GemmParams {
   CUtensorMap w[kMaxShards];     // shard s [shard_rows, K] bf16, box 64 x 256
   float* y;                      // [M, R] fp32
   uint16_t* yb;                  // [M, R] bf16 or null
+  float alpha;                   // output scale (1: none)
   int m, r, k, shard_rows, n_shards;
 };
 
@@ -62,7 +63,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return ok != 0;
 }
 
-__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, int col0, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, int col0, uint32_t (&r)[32]) {
+  if (p.alpha != 1.0f) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), p.alpha));
+  }
   float* yrow = p.y + static_cast<size_t>(row) * p.r;
   const bool full = col0 + 32 <= p.r;
   if (full && (p.r & 3) == 0) {
@@ -269,7 +274,7 @@ int encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
 }  // namespace
 
 int launch_fsdp_gemm(int n_shards, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
-                     const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, cudaStream_t st) {
+                     const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st) {
   if (m_tokens > INT32_MAX / 2 || rows_out > INT32_MAX / 2 || k_in > INT32_MAX / 2)
     return set_error(ZERO_ERR_INVALID_ARG, "fsdp_unit_forward: sizes must be below 2^30");
   const int64_t shard_rows = rows_out / n_shards;
@@ -287,6 +292,7 @@ int launch_fsdp_gemm(int n_shards, const uint16_t* const* w_shards, int64_t rows
     if ((rc = encode_2d(&p.w[s], w_shards[s], k_in, shard_rows, BK, BN))) return rc;
   p.y = Y;
   p.yb = Y_bf16;
+  p.alpha = alpha;
   p.m = static_cast<int>(m_tokens);
   p.r = static_cast<int>(rows_out);
   p.k = static_cast<int>(k_in);

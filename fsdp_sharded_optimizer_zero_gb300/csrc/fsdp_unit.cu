@@ -1,0 +1,113 @@
+// FSDP unit backward ([Interview] follow-up "手写 FSDP 的一层 linear": all-gather W again,
+// compute dX, compute the full-shape dW locally, reduce-scatter dW into each rank's 1/N of
+// the rows; [Concepts] "ZeRO and FSDP": gather before backward, then reduce-scatter).
+//
+// With the N ranks on one GPU the step is, for every rank q with local batch X_q [M, K] and
+// upstream gradient dY_q [M, R]:
+//   dX_q = dY_q W                                  (W [R, K] gathered from its row shards)
+//   dW   = (1/N) sum_q dY_q^T X_q                  (all ranks' contributions, reduced)
+// and rank r's reduce-scatter result is rows [r R/N, (r+1) R/N) of dW, a contiguous block.
+//
+// Both products run on the tcgen05 GEMM, which takes K-major operands. Three launches of
+// the transpose-and-concatenate kernel lay the operands out for it:
+//   W^T    [K, R]   = the N shards transposed side by side (the backward all-gather),
+//   dY^T   [R, N M] = the N ranks' dY transposed and concatenated,
+//   X^T    [K, N M] = the N ranks' X  transposed and concatenated,
+// so dW = (1/N) dY^T (X^T)^T is ONE GEMM whose reduction axis runs over every rank's
+// tokens: the sum over ranks happens inside the fp32 tensor-core accumulation, and the
+// 1/N scale is applied in the epilogue. dX_q = dY_q (W^T)^T is one GEMM per rank.
+#include <string.h>
+
+#include "internal.h"
+
+using namespace zgb;
+
+namespace {
+
+uint64_t align256(uint64_t b) { return (b + 255) & ~uint64_t(255); }
+
+struct BackwardWorkspace {
+  uint64_t wt, dyt, xt, total;  // byte offsets of W^T, dY^T, X^T and the total size
+};
+
+BackwardWorkspace backward_workspace(int n, int64_t rows_out, int64_t k_in, int64_t m_tokens) {
+  const uint64_t R = static_cast<uint64_t>(rows_out), K = static_cast<uint64_t>(k_in);
+  const uint64_t NM = static_cast<uint64_t>(n) * static_cast<uint64_t>(m_tokens);
+  BackwardWorkspace w;
+  w.wt = 0;
+  w.dyt = align256(2 * R * K);
+  w.xt = w.dyt + align256(2 * R * NM);
+  w.total = w.xt + align256(2 * K * NM);
+  return w;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t k_in, int64_t m_tokens,
+                                            uint64_t* bytes) {
+  if (!bytes) return set_error(ZERO_ERR_INVALID_ARG, "fsdp_unit_backward_workspace: bytes is NULL");
+  if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || rows_out < 1 || k_in < 1 || m_tokens < 1)
+    return set_error(ZERO_ERR_INVALID_ARG, "fsdp_unit_backward_workspace: bad sizes");
+  *bytes = backward_workspace(n_ranks, rows_out, k_in, m_tokens).total;
+  return ZERO_OK;
+}
+
+extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[], int64_t rows_out, int64_t k_in,
+                                  const zero_bf16* const A[], const zero_bf16* const dY[], int64_t m_tokens,
+                                  float* const dX[], float* dW, void* workspace, uint64_t workspace_bytes,
+                                  zero_stream_t stream) {
+  const char* who = "fsdp_unit_backward";
+  if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: n_ranks %d outside 1..%d", who, n_ranks, ZERO_MAX_RANKS);
+  if (rows_out < 1 || k_in < 1 || m_tokens < 1) return set_error(ZERO_ERR_INVALID_ARG, "%s: sizes must be >= 1", who);
+  if (rows_out % n_ranks != 0)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: rows_out %lld is not a multiple of n_ranks %d", who,
+                     (long long)rows_out, n_ranks);
+  const int64_t nm = static_cast<int64_t>(n_ranks) * m_tokens;
+  if (k_in % 8 || rows_out % 8 || nm % 8)
+    return set_error(ZERO_ERR_INVALID_ARG,
+                     "%s: k_in, rows_out and n_ranks * m_tokens must be multiples of 8 (16-byte GEMM rows)", who);
+  if (!w_shards || !A || !dY || !dX || !dW || !workspace)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: NULL argument", who);
+  const BackwardWorkspace ws = backward_workspace(n_ranks, rows_out, k_in, m_tokens);
+  if (workspace_bytes < ws.total)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: workspace of %llu bytes is below the %llu needed", who,
+                     (unsigned long long)workspace_bytes, (unsigned long long)ws.total);
+  if (!aligned16(dW) || !aligned16(workspace))
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: dW and workspace must be 16-byte aligned", who);
+  GradPtrs wp, ap, dyp;
+  memset(&wp, 0, sizeof(wp));
+  memset(&ap, 0, sizeof(ap));
+  memset(&dyp, 0, sizeof(dyp));
+  for (int q = 0; q < n_ranks; ++q) {
+    if (!w_shards[q] || !A[q] || !dY[q] || !dX[q])
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: a pointer of rank %d is NULL (missing rank)", who, q);
+    if (!aligned16(w_shards[q]) || !aligned16(A[q]) || !aligned16(dY[q]) || !aligned16(dX[q]))
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: buffers of rank %d must be 16-byte aligned", who, q);
+    wp.p[q] = w_shards[q];
+    ap.p[q] = A[q];
+    dyp.p[q] = dY[q];
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  uint16_t* wt = reinterpret_cast<uint16_t*>(base + ws.wt);
+  uint16_t* dyt = reinterpret_cast<uint16_t*>(base + ws.dyt);
+  uint16_t* xt = reinterpret_cast<uint16_t*>(base + ws.xt);
+
+  cudaError_t e = launch_transpose_cat(wp, n_ranks, rows_out / n_ranks, k_in, wt, st);
+  if (e == cudaSuccess) e = launch_transpose_cat(dyp, n_ranks, m_tokens, rows_out, dyt, st);
+  if (e == cudaSuccess) e = launch_transpose_cat(ap, n_ranks, m_tokens, k_in, xt, st);
+  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
+
+  // dX_q [M, K] = dY_q [M, R] * (W^T [K, R])^T
+  const uint16_t* wt1[1] = {wt};
+  for (int q = 0; q < n_ranks; ++q) {
+    int rc = launch_fsdp_gemm(1, wt1, k_in, rows_out, dY[q], m_tokens, dX[q], nullptr, 1.0f, st);
+    if (rc) return rc;
+  }
+  // dW [R, K] = (1/N) dY^T [R, NM] * (X^T [K, NM])^T
+  const uint16_t* xt1[1] = {xt};
+  return launch_fsdp_gemm(1, xt1, k_in, nm, dyt, rows_out, dW, nullptr, 1.0f / static_cast<float>(n_ranks), st);
+}

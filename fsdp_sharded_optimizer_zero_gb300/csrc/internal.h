@@ -51,12 +51,16 @@ cudaError_t launch_allgather(const MasterPtrs& mp, int n, uint64_t shard, uint16
 cudaError_t launch_gather_rows(const GradPtrs& shards, int n, uint64_t shard_elems, uint16_t* full, bool vec,
                                cudaStream_t st);
 unsigned int step_kernels_read_clear_error();
+// dst[c][q * rows + r] = srcs[q][r][c] for q < n: the N row-major [rows, cols] bf16 sources
+// transposed and concatenated into one row-major [cols, n * rows] buffer
+cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int64_t cols, uint16_t* dst,
+                                 cudaStream_t st);
 
 // ---- FSDP GEMM (fsdp_gemm.cu) ----
-// Y[M, R] = A[M, K] * W^T with W given as n_ranks row shards of R/n_ranks rows each
-// (n_ranks = 1 with the full W for the materialised path).
+// Y[M, R] = alpha * A[M, K] * W^T with W given as n_ranks row shards of R/n_ranks rows
+// each (n_ranks = 1 with the full W for the materialised path). Both operands K-major.
 int launch_fsdp_gemm(int n_ranks, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
-                     const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, cudaStream_t st);
+                     const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st);
 unsigned int fsdp_gemm_read_clear_error();
 
 // ---- errors (capi.cu) ----

@@ -434,6 +434,59 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(GradPtrs shards, 
   }
 }
 
+// ------------------------------------------------------------------------------------
+// FSDP backward operand layout: dst[c][q * rows + r] = srcs[q][r][c], i.e. the N row-major
+// [rows, cols] bf16 sources transposed and concatenated along the new column axis. It
+// produces W^T from W's row shards (the backward all-gather of W) and the rank-concatenated
+// dY^T and X^T whose product sums the ranks' weight gradients inside one GEMM. 64 x 64
+// tiles through shared memory; 16-byte loads and stores when rows and columns allow.
+// ------------------------------------------------------------------------------------
+constexpr int kTT = 64;
+
+__global__ void __launch_bounds__(256) transpose_cat_kernel(GradPtrs srcs, int64_t rows, int64_t cols,
+                                                            int64_t total_rows, uint16_t* __restrict__ dst, int vec) {
+  __shared__ uint16_t tile[kTT][kTT + 2];
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTT;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTT;
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int v = t + i * 256, rr = v >> 3, cv = (v & 7) * 8;
+    const int64_t gr = r0 + rr;
+    if (gr >= total_rows) continue;
+    const int64_t q = gr / rows, lr = gr - q * rows;
+    const uint16_t* src = srcs.p[q] + lr * cols + c0 + cv;
+    if (vec && c0 + cv + 8 <= cols) {
+      const uint4 u = __ldcs(reinterpret_cast<const uint4*>(src));
+      uint32_t* trow = reinterpret_cast<uint32_t*>(&tile[rr][cv]);
+      trow[0] = u.x;
+      trow[1] = u.y;
+      trow[2] = u.z;
+      trow[3] = u.w;
+    } else {
+      for (int j = 0; j < 8; ++j) tile[rr][cv + j] = (c0 + cv + j < cols) ? src[j] : uint16_t(0);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int v = t + i * 256, cc = v >> 3, rv = (v & 7) * 8;
+    const int64_t dc = c0 + cc;
+    if (dc >= cols) continue;
+    uint16_t* out = dst + dc * total_rows + r0 + rv;
+    if (vec && r0 + rv + 8 <= total_rows) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = static_cast<uint32_t>(tile[rv + 2 * j][cc]) | (static_cast<uint32_t>(tile[rv + 2 * j + 1][cc]) << 16);
+      __stcs(reinterpret_cast<uint4*>(out), make_uint4(w[0], w[1], w[2], w[3]));
+    } else {
+      for (int j = 0; j < 8; ++j)
+        if (r0 + rv + j < total_rows) out[j] = tile[rv + j][cc];
+    }
+  }
+}
+
 unsigned int grid_for(uint64_t work_items) {
   const uint64_t want = (work_items + kThreads - 1) / kThreads;
   const uint64_t cap = static_cast<uint64_t>(num_sms()) * 16u;
@@ -558,6 +611,19 @@ cudaError_t launch_gather_rows(const GradPtrs& shards, int n, uint64_t shard_ele
   if (total == 0) return cudaSuccess;
   gather_rows_kernel<<<grid_for(vec ? total / 8 : total), kThreads, 0, st>>>(shards, n, shard_elems, full,
                                                                              vec ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int64_t cols, uint16_t* dst,
+                                 cudaStream_t st) {
+  const int64_t total_rows = rows * n;
+  if (total_rows == 0 || cols == 0) return cudaSuccess;
+  bool vec = cols % 8 == 0 && total_rows % 8 == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
+  for (int q = 0; q < n; ++q) vec = vec && (reinterpret_cast<uintptr_t>(srcs.p[q]) & 15) == 0;
+  const int64_t gy = (total_rows + kTT - 1) / kTT, gx = (cols + kTT - 1) / kTT;
+  if (gy > 65535 || gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  transpose_cat_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(
+      srcs, rows, cols, total_rows, dst, vec ? 1 : 0);
   return cudaGetLastError();
 }
 

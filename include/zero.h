@@ -236,6 +236,30 @@ ZERO_API int fsdp_unit_forward(int n_ranks, const zero_bf16* const w_shards[], i
                       const zero_bf16* A, int64_t m_tokens, float* Y, zero_bf16* Y_bf16, zero_bf16* scratch_w,
                       zero_stream_t stream);
 
+/* Bytes of device workspace fsdp_unit_backward needs: W^T (2*R*K), dY^T (2*R*N*M) and
+ * X^T (2*K*N*M), each rounded up to 256 bytes. */
+ZERO_API int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t k_in, int64_t m_tokens,
+                                          uint64_t* bytes);
+
+/* Backward of the FSDP unit's linear for all N simulated ranks ([Interview] follow-up
+ * "手写 FSDP 的一层 linear": all-gather W again, dX, full-shape dW, reduce-scatter of dW into
+ * each rank's 1/N of the rows; [Concepts] "ZeRO and FSDP" full-shard steps 2-3).
+ * w_shards[r]: row-major [rows_out/N, k_in] bf16 (rank r's rows of W [R, K]);
+ * A[q]: rank q's local activations, row-major [m_tokens, k_in] bf16;
+ * dY[q]: rank q's upstream gradient, row-major [m_tokens, rows_out] bf16;
+ * dX[q]: out, row-major [m_tokens, k_in] fp32: dX_q = dY_q W;
+ * dW: out, row-major [rows_out, k_in] fp32: dW = (1/N) sum_q dY_q^T X_q; rank r's
+ *     reduce-scattered shard is rows [r*R/N, (r+1)*R/N).
+ * workspace: device buffer of fsdp_unit_backward_workspace() bytes (caller-owned scratch).
+ * Requires rows_out % N == 0 and k_in, rows_out, N*m_tokens multiples of 8; all buffers
+ * 16-byte aligned. fp32 accumulation on the tensor cores in an unspecified order: each dX
+ * entry is within (R+1) 2^-23 sum|dy w| and each dW entry within (N M + 1) 2^-23 (1/N)
+ * sum|dy x| (+ half an ulp for the 1/N scale) of the exact value. */
+ZERO_API int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[], int64_t rows_out, int64_t k_in,
+                                const zero_bf16* const A[], const zero_bf16* const dY[], int64_t m_tokens,
+                                float* const dX[], float* dW, void* workspace, uint64_t workspace_bytes,
+                                zero_stream_t stream);
+
 /* Allocation-free variant of fsdp_unit_forward, for callers that cannot allocate device
  * memory where they run the unit (e.g. a plug-in inside a framework that owns all device
  * memory through its own pool, or a latency-critical path that cannot take cudaMalloc's

@@ -156,3 +156,111 @@ def test_mistral_mlp_unit_sampled(z):
         bad = np.abs(got - exact) > bound
         assert not bad.any(), f"{name}: {bad.sum()} sampled outputs outside the bound"
         del shards, Y, w_full
+
+
+# ---------------------------------------------------------------------------------------
+# FSDP unit backward: dX_q = dY_q W for every rank, dW = (1/N) sum_q dY_q^T X_q
+# ---------------------------------------------------------------------------------------
+
+def run_backward(z, n, rows, k, m, key=0, ints=False):
+    if ints:
+        rng = np.random.default_rng(key)
+        mk = lambda shape: torch.from_numpy(O.f32_to_bf16(rng.integers(-2, 3, shape).astype(np.float32))
+                                            .view(np.int16)).view(torch.bfloat16).to(DEV)
+        shards = [mk((rows // n, k)) for _ in range(n)]
+        A = [mk((m, k)) for _ in range(n)]
+        dY = [mk((m, rows)) for _ in range(n)]
+    else:
+        shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=key)
+        A = [synth.activations(m, k, device=DEV, seed_key=100 * key + q) for q in range(n)]
+        dY = [synth.upstream_grad(m, rows, device=DEV, seed_key=100 * key + q) for q in range(n)]
+    dX = [torch.full((m, k), float("nan"), device=DEV) for _ in range(n)]
+    dW = torch.full((rows, k), float("nan"), device=DEV)
+    ws = torch.empty(z.fsdp_unit_backward_workspace(n, rows, k, m), dtype=torch.uint8, device=DEV)
+    z.fsdp_unit_backward(shards, A, dY, dX, dW, ws)
+    z.zero_device_status()
+    return shards, A, dY, dX, dW
+
+
+def test_backward_integer_values_exact(z):
+    n, rows, k, m = 4, 512, 256, 128
+    shards, A, dY, dX, dW = run_backward(z, n, rows, k, m, key=3, ints=True)
+    w = O.bf16_to_f32(O.gather_rows([bits16(s) for s in shards])).astype(np.float64)
+    acc = np.zeros((rows, k))
+    for q in range(n):
+        a = O.bf16_to_f32(bits16(A[q])).astype(np.float64)
+        dy = O.bf16_to_f32(bits16(dY[q])).astype(np.float64)
+        assert np.array_equal(f32(dX[q]).astype(np.float64), dy @ w)
+        acc += dy.T @ a
+    assert np.array_equal(f32(dW).astype(np.float64), acc / n)
+
+
+@pytest.mark.parametrize("n,rows,k,m", [(4, 512, 256, 128), (3, 120, 72, 40), (8, 2048, 512, 96), (1, 256, 64, 200)])
+def test_backward_vs_oracle(z, n, rows, k, m):
+    shards, A, dY, dX, dW = run_backward(z, n, rows, k, m, key=rows)
+    sb = [bits16(s) for s in shards]
+    w64 = O.bf16_to_f32(O.gather_rows(sb)).astype(np.float64)
+    exact_dw = np.zeros((rows, k))
+    bound_dw = np.zeros((rows, k))
+    for q in range(n):
+        dx64, dw64 = O.fsdp_linear_backward(bits16(A[q]), sb, bits16(dY[q]), n)
+        dy_abs = np.abs(O.bf16_to_f32(bits16(dY[q])).astype(np.float64))
+        a_abs = np.abs(O.bf16_to_f32(bits16(A[q])).astype(np.float64))
+        bound_dx = (rows + 1) * 2.0 ** -23 * (dy_abs @ np.abs(w64))
+        assert np.all(np.abs(f32(dX[q]) - dx64) <= bound_dx), f"dX of rank {q}"
+        exact_dw += dw64
+        bound_dw += dy_abs.T @ a_abs
+    exact_dw /= n
+    bound = (n * m + 1) * 2.0 ** -23 * bound_dw / n + 2.0 ** -24 * np.abs(exact_dw)
+    assert np.all(np.abs(f32(dW) - exact_dw) <= bound), "reduce-scattered dW"
+    # each rank's shard of the reduced gradient equals the oracle's per-rank reduce-scatter
+    # of the fp32 per-rank dW (both within the same bound of the exact sum)
+    rs = rows // n
+    dws32 = [O.fsdp_linear_backward(bits16(A[q]), sb, bits16(dY[q]), n)[1].astype(np.float32) for q in range(n)]
+    for r in range(n):
+        ref = O.reduce_rows(dws32, n, r).astype(np.float64)
+        assert np.all(np.abs(f32(dW)[r * rs:(r + 1) * rs] - ref) <= 2 * bound[r * rs:(r + 1) * rs] + 1e-30)
+
+
+def test_backward_mistral_up_sampled(z):
+    """W_up [14336, 4096] in 8 row shards, 2048 tokens per rank: sampled dX and dW entries
+    against float64 dot products under the bounds."""
+    n, rows, k, m = 8, 14336, 4096, 2048
+    shards, A, dY, dX, dW = run_backward(z, n, rows, k, m, key=7)
+    rng = np.random.default_rng(1)
+    w_full = torch.cat(shards, 0)
+    for q in (0, n - 1):
+        i = rng.integers(0, m, 512)
+        c = rng.integers(0, k, 512)
+        dy = O.bf16_to_f32(bits16(dY[q][torch.from_numpy(i).to(DEV)])).astype(np.float64)
+        wc = O.bf16_to_f32(bits16(w_full[:, torch.from_numpy(c).to(DEV)].t().contiguous())).astype(np.float64)
+        exact = np.einsum("ir,ir->i", dy, wc)
+        bound = (rows + 1) * 2.0 ** -23 * np.einsum("ir,ir->i", np.abs(dy), np.abs(wc))
+        got = f32(dX[q][torch.from_numpy(i).to(DEV), torch.from_numpy(c).to(DEV)]).astype(np.float64)
+        assert np.all(np.abs(got - exact) <= bound), f"dX rank {q}"
+    rr = rng.integers(0, rows, 256)
+    cc = rng.integers(0, k, 256)
+    ex = np.zeros(256)
+    bd = np.zeros(256)
+    for q in range(n):
+        dyc = O.bf16_to_f32(bits16(dY[q][:, torch.from_numpy(rr).to(DEV)].t().contiguous())).astype(np.float64)
+        ac = O.bf16_to_f32(bits16(A[q][:, torch.from_numpy(cc).to(DEV)].t().contiguous())).astype(np.float64)
+        ex += np.einsum("im,im->i", dyc, ac)
+        bd += np.einsum("im,im->i", np.abs(dyc), np.abs(ac))
+    ex /= n
+    bound = (n * m + 1) * 2.0 ** -23 * bd / n + 2.0 ** -24 * np.abs(ex)
+    got = f32(dW[torch.from_numpy(rr).to(DEV), torch.from_numpy(cc).to(DEV)]).astype(np.float64)
+    assert np.all(np.abs(got - ex) <= bound), "dW"
+
+
+def test_backward_rejects_small_workspace(z):
+    n, rows, k, m = 2, 512, 64, 64
+    shards = synth.weight_shards(rows, k, n, device=DEV)
+    A = [synth.activations(m, k, device=DEV) for _ in range(n)]
+    dY = [synth.upstream_grad(m, rows, device=DEV) for _ in range(n)]
+    dX = [torch.empty(m, k, device=DEV) for _ in range(n)]
+    dW = torch.empty(rows, k, device=DEV)
+    ws = torch.empty(z.fsdp_unit_backward_workspace(n, rows, k, m) - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(z.ZeroError) as e:
+        z.fsdp_unit_backward(shards, A, dY, dX, dW, ws)
+    assert e.value.code == -1
