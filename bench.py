@@ -387,6 +387,23 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         res["roofline"] = {"bound": "tensor", "achieved": res["tflops"], "peak": tf_peak, "unit": "TFLOP/s",
                            "frac": res["tflops"] / tf_peak,
                            "peak_source": f"{peak_src} bf16_tflops (burst)" if peak_src == "measured" else "fallback"}
+        # the full MLP unit: gate + up in one kernel with the SiLU-gate epilogue, then down
+        gs_ = synth.weight_shards(14336, 4096, n, device=dev, seed_key=12)
+        us_ = synth.weight_shards(14336, 4096, n, device=dev, seed_key=11)
+        ds_ = synth.weight_shards(4096, 14336, n, device=dev, seed_key=13)
+        Hb = torch.empty(M, 14336, dtype=torch.bfloat16, device=dev)
+        Ym = torch.empty(M, 4096, device=dev)
+        ms = time_launches(lambda: z.fsdp_mlp_forward(gs_, us_, ds_, X, Hb, Ym, stream=stream), 10, stream)
+        flop = 3 * 2.0 * M * 14336 * 4096
+        res["mlp_unit"] = {"ms": ms, "tflops": flop / ms / 1e9, "frac": flop / ms / 1e9 / tf_peak,
+                           "note": "gate+up GEMM with silu(gate)*up epilogue (bf16 H) + down GEMM, fused gathers"}
+        side = torch.cuda.Stream()
+        sd = torch.empty(4096, 14336, dtype=torch.bfloat16, device=dev)
+        ms2 = time_launches(lambda: z.fsdp_mlp_forward(gs_, us_, ds_, X, Hb, Ym, scratch_down=sd, stream=stream,
+                                                       prefetch_stream=side), 10, stream)
+        res["mlp_unit_prefetched_gather"] = {"ms": ms2, "tflops": flop / ms2 / 1e9,
+                                             "note": "W_down gathered into scratch on a second stream during gate+up"}
+        del gs_, us_, ds_, Hb, Ym, sd
         # backward of W_up for 8 ranks of 2048 tokens: W^T, dY^T, X^T layouts + 8 dX GEMMs +
         # one rank-reduced dW GEMM
         R, K, Mb = 14336, 4096, 2048

@@ -34,7 +34,7 @@ EXPORTS = (
     "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_fp32_grads",
     "zero_fused_step_buckets",
     "zero_allgather_params", "ddp_allreduce", "fsdp_gather_rows", "fsdp_unit_forward",
-    "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_unit_forward_static_scratch", "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
+    "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward", "fsdp_unit_forward_static_scratch", "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
 )
 
 
@@ -88,6 +88,7 @@ def _load():
         "fsdp_unit_forward_static_scratch": (I, [I, PP, I64, I64, VP, I64, VP, VP, VP]),
         "fsdp_unit_backward_workspace": (I, [I, I64, I64, I64, C.POINTER(U64)]),
         "fsdp_unit_backward": (I, [I, PP, I64, I64, PP, PP, I64, PP, VP, VP, U64, VP]),
+        "fsdp_mlp_forward": (I, [I, PP, PP, PP, I64, I64, VP, I64, VP, VP, VP, VP, VP]),
         "zero_last_error": (C.c_char_p, []),
         "zero_device_status": (I, [VP]),
         "zero_set_fused_kernel": (I, [I]),
@@ -271,6 +272,19 @@ def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace, stream=None):
         n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, k, _ptr_array(A, torch.bfloat16, "A"),
         _ptr_array(dY, torch.bfloat16, "dY"), m_tok, _ptr_array(dX, torch.float32, "dX"),
         _dev(dW, torch.float32, "dW"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def fsdp_mlp_forward(gate_shards, up_shards, down_shards, X, H, Y, scratch_down=None, stream=None,
+                     prefetch_stream=None):
+    n = len(gate_shards)
+    d_ff = sum(int(s.shape[0]) for s in gate_shards)
+    d_model = int(X.shape[1])
+    _check(_lib.fsdp_mlp_forward(
+        n, _ptr_array(gate_shards, torch.bfloat16, "gate_shards"), _ptr_array(up_shards, torch.bfloat16, "up_shards"),
+        _ptr_array(down_shards, torch.bfloat16, "down_shards"), d_model, d_ff, _dev(X, torch.bfloat16, "X"),
+        int(X.shape[0]), _dev(H, torch.bfloat16, "H"), _dev(Y, torch.float32, "Y"),
+        _dev(scratch_down, torch.bfloat16, "scratch_down"), _stream(stream),
+        _stream(prefetch_stream) if prefetch_stream is not None else None))
 
 
 def fsdp_unit_forward_static_scratch(w_shards, A, Y, Y_bf16=None, stream=None):

@@ -38,7 +38,6 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;  // two accumulators of BN fp32 columns
 constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t kSmemBytes = STAGES * STAGE_BYTES + 1024;  // + alignment slack
-constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 
 constexpr unsigned int kErrEmpty = (2u << 8) | 1u;  // producer waiting for a free stage
 constexpr unsigned int kErrFull = (2u << 8) | 2u;   // MMA waiting for a loaded stage
@@ -48,9 +47,10 @@ constexpr unsigned int kErrDrain = (2u << 8) | 5u;  // draining after an abort
 
 struct GemmParams {
   CUtensorMap a;                 // A [M, K] bf16, box 64 x 128
-  CUtensorMap w[kMaxShards];     // shard s [shard_rows, K] bf16, box 64 x 256
+  CUtensorMap w[kMaxShards];     // shard s [shard_rows, K] bf16, box 64 x (256, or 128 in gate-up mode)
+  CUtensorMap w2[kMaxShards];    // gate-up mode: the up projection's shards (w holds the gate's)
   float* y;                      // [M, R] fp32
-  uint16_t* yb;                  // [M, R] bf16 or null
+  uint16_t* yb;                  // [M, R] bf16 or null (gate-up mode: H = silu(gate) * up)
   float alpha;                   // output scale (1: none)
   int m, r, k, shard_rows, n_shards;
 };
@@ -97,7 +97,39 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, in
   }
 }
 
+// gate-up epilogue: h = silu(g) * u = g / (1 + exp(-g)) * u in fp32, stored as bf16 (RNE)
+__device__ __forceinline__ void store_gate_up_chunk(const GemmParams& p, int row, int col0, const uint32_t (&g)[32],
+                                                    const uint32_t (&u)[32]) {
+  float h[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float gj = __uint_as_float(g[j]);
+    const float silu = __fdiv_rn(gj, __fadd_rn(1.0f, expf(-gj)));
+    h[j] = __fmul_rn(silu, __uint_as_float(u[j]));
+  }
+  uint16_t* brow = p.yb + static_cast<size_t>(row) * p.r;
+  if (col0 + 32 <= p.r && (p.r & 7) == 0) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 8)
+      __stcs(reinterpret_cast<uint4*>(brow + col0 + j),
+             make_uint4(pack_bf16x2(h[j], h[j + 1]), pack_bf16x2(h[j + 2], h[j + 3]), pack_bf16x2(h[j + 4], h[j + 5]),
+                        pack_bf16x2(h[j + 6], h[j + 7])));
+  } else {
+    for (int j = 0; j < 32; ++j)
+      if (col0 + j < p.r) brow[col0 + j] = f32_to_bf16_bits(h[j]);
+  }
+}
+
+// GATE_UP = false: Y = alpha A W^T with 128 x 256 output tiles.
+// GATE_UP = true: two B operands (gate and up shards, 128-row tiles each) share every A
+// tile; their two 128-column accumulators sit side by side in one 256-column TMEM buffer
+// and the epilogue writes H = silu(gate) * up for a 128 x 128 tile.
+template <bool GATE_UP>
 __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int TN = GATE_UP ? 128 : BN;  // output tile columns
+  constexpr uint32_t BT_BYTES = TN * BK * 2;  // one B tile per stage (two in gate-up mode)
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, TN);
+  static_assert(A_BYTES + (GATE_UP ? 2 : 1) * BT_BYTES == STAGE_BYTES, "stage layout");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
@@ -111,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_m = (p.m + BM - 1) / BM;
-  const int num_n = (p.r + BN - 1) / BN;
+  const int num_n = (p.r + TN - 1) / TN;
   const int num_k = (p.k + BK - 1) / BK;
   const int tiles = num_m * num_n;
 
@@ -130,7 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&p.a);
-    for (int s = 0; s < p.n_shards; ++s) prefetch_tmap(&p.w[s]);
+    for (int s = 0; s < p.n_shards; ++s) {
+      prefetch_tmap(&p.w[s]);
+      if (GATE_UP) prefetch_tmap(&p.w2[s]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
@@ -150,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
       bool stop = false;
       for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x) {
         const int m0 = (tile % num_m) * BM;
-        const int n0 = (tile / num_m) * BN;
+        const int n0 = (tile / num_m) * TN;
         const int shard = n0 / p.shard_rows;
         const int nl = n0 - shard * p.shard_rows;
         const void* wmap = &p.w[shard];
@@ -166,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           tma_load_2d(smem_u32(sa), &p.a, kb * BK, m0, fb);
           tma_load_2d(smem_u32(sa + A_BYTES), wmap, kb * BK, nl, fb);
+          if (GATE_UP) tma_load_2d(smem_u32(sa + A_BYTES + BT_BYTES), &p.w2[shard], kb * BK, nl, fb);
           last_issue[s] = it;
         }
       }
@@ -197,9 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
           const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sa + A_BYTES);
+          const uint64_t bd2 = sw128_kmajor_desc(sa + A_BYTES + BT_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)  // K = 16 per MMA: +32 bytes = +2 in the address field
-            umma_bf16(d, ad + 2u * k, bd + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < BK / 16; ++k) {  // K = 16 per MMA: +32 bytes = +2 in the address field
+            umma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+            if (GATE_UP) umma_bf16(d + TN, ad + 2u * k, bd2 + 2u * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
           umma_commit(smem_u32(&empty_bar[s]));
           issued = true;
         }
@@ -221,14 +260,24 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
       if (!warp_wait(smem_u32(&accf_bar[a]), u & 1u, abort, kErrAccF)) break;
       tc_fence_after();
       const int m0 = (tile % num_m) * BM;
-      const int n0 = (tile / num_m) * BN;
+      const int n0 = (tile / num_m) * TN;
       const int row = m0 + row_in_tile;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
+      if constexpr (GATE_UP) {
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld_32cols(taddr + c, r);
-        if (row < p.m && n0 + c < p.r) store_row_chunk(p, row, n0 + c, r);
+        for (int c = 0; c < TN; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld_32cols(taddr + c, g);
+          tmem_ld_32cols(taddr + TN + c, u);
+          if (row < p.m && n0 + c < p.r) store_gate_up_chunk(p, row, n0 + c, g, u);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld_32cols(taddr + c, r);
+          if (row < p.m && n0 + c < p.r) store_row_chunk(p, row, n0 + c, r);
+        }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acce_bar[a]));
@@ -244,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
 // ---- host side ----
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-std::once_flag g_attr_once[64];
+std::once_flag g_attr_once[2][64];
 
 int get_encode() {
   std::call_once(g_encode_once, [] {
@@ -273,23 +322,30 @@ int encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
 
 }  // namespace
 
-int launch_fsdp_gemm(int n_shards, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
-                     const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st) {
+namespace {
+
+template <bool GATE_UP>
+int launch_impl(int n_shards, const uint16_t* const* w_shards, const uint16_t* const* w2_shards, int64_t rows_out,
+                int64_t k_in, const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha,
+                cudaStream_t st, const char* who) {
+  constexpr int TN = GATE_UP ? 128 : BN;
   if (m_tokens > INT32_MAX / 2 || rows_out > INT32_MAX / 2 || k_in > INT32_MAX / 2)
-    return set_error(ZERO_ERR_INVALID_ARG, "fsdp_unit_forward: sizes must be below 2^30");
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: sizes must be below 2^30", who);
   const int64_t shard_rows = rows_out / n_shards;
-  if (n_shards > 1 && (shard_rows % BN != 0 || n_shards > kMaxShards))
+  if (n_shards > 1 && (shard_rows % TN != 0 || n_shards > kMaxShards))
     return set_error(ZERO_ERR_UNSUPPORTED,
-                     "fsdp_unit_forward: the fused gather needs rows_out/n_ranks (%lld) to be a multiple of %d and "
-                     "n_ranks <= %d; pass scratch_w to gather first",
-                     (long long)shard_rows, BN, kMaxShards);
+                     "%s: the fused gather needs rows/n_ranks (%lld) to be a multiple of %d and n_ranks <= %d; "
+                     "pass a scratch buffer to gather first",
+                     who, (long long)shard_rows, TN, kMaxShards);
   int rc = get_encode();
   if (rc) return rc;
   GemmParams p;
   memset(&p, 0, sizeof(p));
   if ((rc = encode_2d(&p.a, A, k_in, m_tokens, BK, BM))) return rc;
-  for (int s = 0; s < n_shards; ++s)
-    if ((rc = encode_2d(&p.w[s], w_shards[s], k_in, shard_rows, BK, BN))) return rc;
+  for (int s = 0; s < n_shards; ++s) {
+    if ((rc = encode_2d(&p.w[s], w_shards[s], k_in, shard_rows, BK, TN))) return rc;
+    if (GATE_UP && (rc = encode_2d(&p.w2[s], w2_shards[s], k_in, shard_rows, BK, TN))) return rc;
+  }
   p.y = Y;
   p.yb = Y_bf16;
   p.alpha = alpha;
@@ -301,18 +357,33 @@ int launch_fsdp_gemm(int n_shards, const uint16_t* const* w_shards, int64_t rows
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "fsdp_unit_forward: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
   cudaError_t attr = cudaSuccess;
-  std::call_once(g_attr_once[dev & 63], [&] {
-    attr = cudaFuncSetAttribute(fsdp_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  std::call_once(g_attr_once[GATE_UP ? 1 : 0][dev & 63], [&] {
+    attr = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
-  if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "fsdp_unit_forward: %s", cudaGetErrorString(attr));
-  const int64_t tiles = ((m_tokens + BM - 1) / BM) * ((rows_out + BN - 1) / BN);
+  if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(attr));
+  const int64_t tiles = ((m_tokens + BM - 1) / BM) * ((rows_out + TN - 1) / TN);
   const unsigned int grid = static_cast<unsigned int>(std::min<int64_t>(tiles, num_sms()));
-  fsdp_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
+  fsdp_gemm_kernel<GATE_UP><<<grid, kThreads, kSmemBytes, st>>>(p);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "fsdp_unit_forward: launch: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
   return ZERO_OK;
+}
+
+}  // namespace
+
+int launch_fsdp_gemm(int n_shards, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
+                     const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st) {
+  return launch_impl<false>(n_shards, w_shards, nullptr, rows_out, k_in, A, m_tokens, Y, Y_bf16, alpha, st,
+                            "fsdp_unit_forward");
+}
+
+int launch_fsdp_gate_up(int n_shards, const uint16_t* const* gate_shards, const uint16_t* const* up_shards,
+                        int64_t d_ff, int64_t d_model, const uint16_t* X, int64_t m_tokens, uint16_t* H,
+                        cudaStream_t st) {
+  return launch_impl<true>(n_shards, gate_shards, up_shards, d_ff, d_model, X, m_tokens, nullptr, H, 1.0f, st,
+                           "fsdp_mlp_forward");
 }
 
 unsigned int fsdp_gemm_read_clear_error() {

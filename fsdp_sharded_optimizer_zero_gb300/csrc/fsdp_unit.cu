@@ -111,3 +111,96 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
   const uint16_t* xt1[1] = {xt};
   return launch_fsdp_gemm(1, xt1, k_in, nm, dyt, rows_out, dW, nullptr, 1.0f / static_cast<float>(n_ranks), st);
 }
+
+// ======================================================================================
+// The full MLP unit forward of a Mistral-style block under FSDP:
+//   H = silu(X W_gate^T) * (X W_up^T)      (one kernel: both projections share every X
+//                                           tile; the SiLU-gate product is the epilogue)
+//   Y = H W_down^T
+// Each weight is all-gathered from its row shards inside the GEMM's loads. When W_down's
+// shards do not tile the GEMM (or the caller prefers it), the caller passes scratch_down
+// and the gather of W_down into it runs on prefetch_stream while the gate-up GEMM runs on
+// `stream` — the overlap FSDP gets from issuing the next unit's all-gather on a separate
+// stream ([Interview] follow-up "FSDP 怎么把通信藏起来?"; [Concepts] full sharding:
+// prefetch the next layer's all-gather while the current layer computes).
+// ======================================================================================
+
+namespace {
+
+// per-thread, per-device pair of events ordering the prefetch stream (no timing)
+thread_local cudaEvent_t t_events[64][2] = {};
+
+int prefetch_events(cudaEvent_t* ev) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64)
+    return set_error(ZERO_ERR_CUDA, "fsdp_mlp_forward: cudaGetDevice failed");
+  for (int i = 0; i < 2; ++i) {
+    if (!t_events[dev][i]) {
+      e = cudaEventCreateWithFlags(&t_events[dev][i], cudaEventDisableTiming);
+      if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "fsdp_mlp_forward: cudaEventCreate: %s", cudaGetErrorString(e));
+    }
+    ev[i] = t_events[dev][i];
+  }
+  return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" int fsdp_mlp_forward(int n_ranks, const zero_bf16* const gate_shards[], const zero_bf16* const up_shards[],
+                                const zero_bf16* const down_shards[], int64_t d_model, int64_t d_ff,
+                                const zero_bf16* X, int64_t m_tokens, zero_bf16* H, float* Y, zero_bf16* scratch_down,
+                                zero_stream_t stream, zero_stream_t prefetch_stream) {
+  const char* who = "fsdp_mlp_forward";
+  if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: n_ranks %d outside 1..%d", who, n_ranks, ZERO_MAX_RANKS);
+  if (d_model < 1 || d_ff < 1 || m_tokens < 1) return set_error(ZERO_ERR_INVALID_ARG, "%s: sizes must be >= 1", who);
+  if (d_model % n_ranks || d_ff % n_ranks)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: d_model and d_ff must be multiples of n_ranks", who);
+  if (d_model % 8 || d_ff % 8)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: d_model and d_ff must be multiples of 8 (16-byte rows)", who);
+  if (!gate_shards || !up_shards || !down_shards || !X || !H || !Y)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: NULL argument", who);
+  if (!aligned16(X) || !aligned16(H) || !aligned16(Y) || (scratch_down && !aligned16(scratch_down)))
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: X, H, Y and scratch_down must be 16-byte aligned", who);
+  GradPtrs dp;
+  memset(&dp, 0, sizeof(dp));
+  for (int q = 0; q < n_ranks; ++q) {
+    if (!gate_shards[q] || !up_shards[q] || !down_shards[q])
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: a shard of rank %d is NULL (missing rank)", who, q);
+    if (!aligned16(gate_shards[q]) || !aligned16(up_shards[q]) || !aligned16(down_shards[q]))
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: shards of rank %d must be 16-byte aligned", who, q);
+    dp.p[q] = down_shards[q];
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t pf = prefetch_stream ? reinterpret_cast<cudaStream_t>(prefetch_stream) : st;
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  if (scratch_down) {
+    int rc = 0;
+    if (pf != st) {
+      if ((rc = prefetch_events(ev))) return rc;
+      // the gather must see everything the caller queued on `stream` before this call
+      cudaError_t e = cudaEventRecord(ev[0], st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(pf, ev[0], 0);
+      if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+    }
+    cudaError_t e = launch_gather_rows(dp, n_ranks, static_cast<uint64_t>(d_model / n_ranks) * d_ff, scratch_down,
+                                       true, pf);
+    if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: gather of W_down: %s", who, cudaGetErrorString(e));
+    if (pf != st) {
+      e = cudaEventRecord(ev[1], pf);
+      if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+    }
+  }
+  int rc = launch_fsdp_gate_up(n_ranks, gate_shards, up_shards, d_ff, d_model, X, m_tokens, H, st);
+  if (rc) return rc;
+  if (scratch_down) {
+    if (pf != st) {
+      cudaError_t e = cudaStreamWaitEvent(st, ev[1], 0);
+      if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+    }
+    const uint16_t* w1[1] = {scratch_down};
+    return launch_fsdp_gemm(1, w1, d_model, d_ff, H, m_tokens, Y, nullptr, 1.0f, st);
+  }
+  return launch_fsdp_gemm(n_ranks, down_shards, d_model, d_ff, H, m_tokens, Y, nullptr, 1.0f, st);
+}

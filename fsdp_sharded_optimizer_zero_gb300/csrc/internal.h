@@ -61,6 +61,11 @@ cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int6
 // each (n_ranks = 1 with the full W for the materialised path). Both operands K-major.
 int launch_fsdp_gemm(int n_ranks, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
                      const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st);
+// H[M, d_ff] (bf16) = silu(X W_gate^T) * (X W_up^T), gate and up given as n_ranks row
+// shards each (d_ff / n_ranks rows, a multiple of 128, or n_ranks = 1 with full weights).
+int launch_fsdp_gate_up(int n_ranks, const uint16_t* const* gate_shards, const uint16_t* const* up_shards,
+                        int64_t d_ff, int64_t d_model, const uint16_t* X, int64_t m_tokens, uint16_t* H,
+                        cudaStream_t st);
 unsigned int fsdp_gemm_read_clear_error();
 
 // ---- errors (capi.cu) ----

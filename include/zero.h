@@ -260,6 +260,24 @@ ZERO_API int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[], 
                                 float* const dX[], float* dW, void* workspace, uint64_t workspace_bytes,
                                 zero_stream_t stream);
 
+/* Forward of a full FSDP MLP unit (Mistral-style): H = silu(X W_gate^T) * (X W_up^T) and
+ * Y = H W_down^T, each weight all-gathered from its N row shards ([Interview] Fig. 2 and
+ * the follow-up on hiding FSDP communication; [Concepts] full sharding with prefetch).
+ * gate_shards[r], up_shards[r]: row-major [d_ff/N, d_model] bf16; down_shards[r]:
+ * row-major [d_model/N, d_ff] bf16; X: row-major [m_tokens, d_model] bf16.
+ * H: out, row-major [m_tokens, d_ff] bf16 (silu(g) u computed in fp32 from the fp32
+ * accumulators, one rounding to bf16); Y: out, row-major [m_tokens, d_model] fp32.
+ * The gate and up projections run in one kernel sharing every X tile, with the SiLU-gate
+ * product as its epilogue (needs d_ff/N % 128 == 0). W_down is gathered inside the loads
+ * when d_model/N % 256 == 0 and scratch_down is NULL; otherwise pass scratch_down
+ * ([d_model, d_ff] bf16): its gather then runs on prefetch_stream (NULL = `stream`)
+ * while the gate-up GEMM runs, and `stream` waits for it before the down projection.
+ * d_model, d_ff multiples of 8; all buffers 16-byte aligned. */
+ZERO_API int fsdp_mlp_forward(int n_ranks, const zero_bf16* const gate_shards[], const zero_bf16* const up_shards[],
+                              const zero_bf16* const down_shards[], int64_t d_model, int64_t d_ff, const zero_bf16* X,
+                              int64_t m_tokens, zero_bf16* H, float* Y, zero_bf16* scratch_down, zero_stream_t stream,
+                              zero_stream_t prefetch_stream);
+
 /* Allocation-free variant of fsdp_unit_forward, for callers that cannot allocate device
  * memory where they run the unit (e.g. a plug-in inside a framework that owns all device
  * memory through its own pool, or a latency-critical path that cannot take cudaMalloc's

@@ -456,3 +456,32 @@ def reduce_rows(dw_list, n_ranks: int, rank: int) -> np.ndarray:
     for q in range(1, len(dw_list)):
         acc = acc + np.asarray(dw_list[q][rank * rs:(rank + 1) * rs], dtype=np.float32)
     return acc * inv_n(len(dw_list))
+
+
+# ========================================================================================
+# full MLP unit (Mistral-style): gate / up projections, SiLU-gate product, down projection
+# ========================================================================================
+
+def silu(x):
+    """SiLU (swish): x * sigmoid(x) = x / (1 + exp(-x)), in float64."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def mlp_unit_forward(x_bf16, gate_shards, up_shards, down_shards=None, h_bf16=None):
+    """The MLP unit an FSDP wrap of a Mistral-style block computes on its local batch, each
+    weight gathered from its row shards first ([Interview] Fig. 2: gather, compute, free):
+        G = X W_gate^T,  U = X W_up^T,  H = silu(G) * U,  Y = H W_down^T.
+    Everything in float64. Returns (G, U, H, Y); Y is computed from `h_bf16` (the bf16 H a
+    kernel produced, an exact input to the next product) when given, else from H, and is
+    None without down_shards."""
+    x = bf16_to_f32(x_bf16).astype(np.float64)
+    g = x @ bf16_to_f32(gather_rows(gate_shards)).astype(np.float64).T
+    u = x @ bf16_to_f32(gather_rows(up_shards)).astype(np.float64).T
+    h = silu(g) * u
+    y = None
+    if down_shards is not None:
+        hin = h if h_bf16 is None else bf16_to_f32(h_bf16).astype(np.float64)
+        y = hin @ bf16_to_f32(gather_rows(down_shards)).astype(np.float64).T
+    return g, u, h, y

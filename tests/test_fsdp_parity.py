@@ -264,3 +264,84 @@ def test_backward_rejects_small_workspace(z):
     with pytest.raises(z.ZeroError) as e:
         z.fsdp_unit_backward(shards, A, dY, dX, dW, ws)
     assert e.value.code == -1
+
+
+# ---------------------------------------------------------------------------------------
+# full MLP unit: H = silu(X Wg^T) * (X Wu^T) in one kernel, then Y = H Wd^T
+# ---------------------------------------------------------------------------------------
+
+def h_bound(g64, u64, bg, bu, h_gpu):
+    """|H_gpu - H_exact| for H = silu(G) U from fp32 G, U within bg, bu of exact:
+    |silu'| <= 1.1, a few fp32 roundings in silu and the product, one bf16 rounding."""
+    sil = np.abs(O.silu(g64))
+    return (1.1 * bg * np.abs(u64) + sil * bu + 1.1 * bg * bu + 16 * 2.0 ** -24 * sil * np.abs(u64)
+            + 2.0 ** -8 * 1.01 * np.abs(h_gpu) + 1e-38)
+
+
+def make_mlp(n, d, f, m, key):
+    gate = synth.weight_shards(f, d, n, device=DEV, seed_key=10 * key + 1)
+    up = synth.weight_shards(f, d, n, device=DEV, seed_key=10 * key + 2)
+    down = synth.weight_shards(d, f, n, device=DEV, seed_key=10 * key + 3)
+    X = synth.activations(m, d, device=DEV, seed_key=key)
+    return gate, up, down, X
+
+
+@pytest.mark.parametrize("n,d,f,m,scratch", [(2, 512, 512, 200, False), (2, 256, 512, 200, True),
+                                             (4, 1024, 1024, 130, False), (8, 2048, 1024, 64, True),
+                                             (1, 256, 256, 1, False)])
+def test_mlp_unit_vs_oracle(z, n, d, f, m, scratch):
+    gate, up, down, X = make_mlp(n, d, f, m, key=d + f)
+    H = torch.zeros(m, f, dtype=torch.bfloat16, device=DEV)
+    Y = torch.full((m, d), float("nan"), device=DEV)
+    sd = torch.empty(d, f, dtype=torch.bfloat16, device=DEV) if scratch else None
+    side = torch.cuda.Stream() if scratch else None
+    z.fsdp_mlp_forward(gate, up, down, X, H, Y, scratch_down=sd, prefetch_stream=side)
+    z.zero_device_status()
+    gb, ub, db, xb = [bits16(s) for s in gate], [bits16(s) for s in up], [bits16(s) for s in down], bits16(X)
+    hb = bits16(H)
+    g64, u64, h64, y64 = O.mlp_unit_forward(xb, gb, ub, db, h_bf16=hb)
+    xa = np.abs(O.bf16_to_f32(xb).astype(np.float64))
+    bg = (d + 1) * 2.0 ** -23 * (xa @ np.abs(O.bf16_to_f32(O.gather_rows(gb)).astype(np.float64)).T)
+    bu = (d + 1) * 2.0 ** -23 * (xa @ np.abs(O.bf16_to_f32(O.gather_rows(ub)).astype(np.float64)).T)
+    h_gpu = O.bf16_to_f32(hb).astype(np.float64)
+    assert np.all(np.abs(h_gpu - h64) <= h_bound(g64, u64, bg, bu, h_gpu)), "H"
+    by = (f + 1) * 2.0 ** -23 * (np.abs(h_gpu) @ np.abs(O.bf16_to_f32(O.gather_rows(db)).astype(np.float64)).T)
+    assert np.all(np.abs(f32(Y) - y64) <= by + 1e-30), "Y"
+    if scratch:
+        assert_bf16_identical(bits16(sd), O.gather_rows(db), "W_down gathered into scratch")
+    if (d // n) % 256 == 0:
+        Y2 = torch.empty_like(Y)
+        H2 = torch.empty_like(H)
+        z.fsdp_mlp_forward(gate, up, down, X, H2, Y2,
+                           scratch_down=torch.empty(d, f, dtype=torch.bfloat16, device=DEV), prefetch_stream=None)
+        z.zero_device_status()
+        assert torch.equal(H2.view(torch.int16), H.view(torch.int16))
+        assert torch.equal(Y2.view(torch.int32), Y.view(torch.int32)), "fused and scratch W_down disagree"
+
+
+def test_mlp_unit_mistral_sampled(z):
+    """Mistral-7B MLP unit, N = 8 shards, 8192 tokens: 4096 sampled H entries against the
+    float64 oracle, 4096 sampled Y entries against float64 dot products of the kernel's H."""
+    n, d, f, m = 8, 4096, 14336, 8192
+    gate, up, down, X = make_mlp(n, d, f, m, key=5)
+    H = torch.empty(m, f, dtype=torch.bfloat16, device=DEV)
+    Y = torch.empty(m, d, device=DEV)
+    z.fsdp_mlp_forward(gate, up, down, X, H, Y)
+    z.zero_device_status()
+    rng = np.random.default_rng(3)
+    i = torch.from_numpy(rng.integers(0, m, 4096)).to(DEV)
+    j = torch.from_numpy(rng.integers(0, f, 4096)).to(DEV)
+    xi = O.bf16_to_f32(bits16(X[i])).astype(np.float64)
+    wg = O.bf16_to_f32(bits16(torch.cat(gate)[j])).astype(np.float64)
+    wu = O.bf16_to_f32(bits16(torch.cat(up)[j])).astype(np.float64)
+    g64, u64 = np.einsum("ik,ik->i", xi, wg), np.einsum("ik,ik->i", xi, wu)
+    bg = (d + 1) * 2.0 ** -23 * np.einsum("ik,ik->i", np.abs(xi), np.abs(wg))
+    bu = (d + 1) * 2.0 ** -23 * np.einsum("ik,ik->i", np.abs(xi), np.abs(wu))
+    h_gpu = O.bf16_to_f32(bits16(H[i, j])).astype(np.float64)
+    assert np.all(np.abs(h_gpu - O.silu(g64) * u64) <= h_bound(g64, u64, bg, bu, h_gpu)), "H"
+    c = torch.from_numpy(rng.integers(0, d, 4096)).to(DEV)
+    hi = O.bf16_to_f32(bits16(H[i])).astype(np.float64)
+    wd = O.bf16_to_f32(bits16(torch.cat(down)[c])).astype(np.float64)
+    ex = np.einsum("ik,ik->i", hi, wd)
+    by = (f + 1) * 2.0 ** -23 * np.einsum("ik,ik->i", np.abs(hi), np.abs(wd))
+    assert np.all(np.abs(f32(Y[i, c]).astype(np.float64) - ex) <= by + 1e-30), "Y"

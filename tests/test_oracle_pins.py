@@ -501,6 +501,37 @@ def test_reduce_rows_matches_elementwise_reduction():
         assert got.tobytes() == (acc * np.float32(0.25)).astype(np.float32).tobytes()
 
 
+def test_silu_matches_torch_and_identities():
+    x = np.concatenate([np.linspace(-60, 60, 2001), [0.0, -1e-300, 1e-300, -800.0, 800.0]])
+    ref = torch.nn.functional.silu(torch.tensor(x, dtype=torch.float64)).numpy()
+    assert np.allclose(O.silu(x), ref, rtol=1e-15, atol=1e-300)
+    assert O.silu(0.0) == 0.0
+    y = np.linspace(-30, 30, 601)
+    assert np.allclose(O.silu(y) - O.silu(-y), y, rtol=1e-14, atol=1e-14)  # silu(x) - silu(-x) = x
+
+
+def test_mlp_unit_forward_bruteforce():
+    rng = np.random.default_rng(31)
+    m, d, f, n = 3, 4, 6, 2
+    x = bf16_of(rng.normal(0, 1, (m, d)))
+    gate = [bf16_of(rng.normal(0, 0.5, (f // n, d))) for _ in range(n)]
+    up = [bf16_of(rng.normal(0, 0.5, (f // n, d))) for _ in range(n)]
+    down = [bf16_of(rng.normal(0, 0.5, (d // n, f))) for _ in range(n)]
+    g, u, h, y = O.mlp_unit_forward(x, gate, up, down)
+    xf = O.bf16_to_f32(x).astype(float)
+    wg = np.concatenate([O.bf16_to_f32(s) for s in gate]).astype(float)
+    wu = np.concatenate([O.bf16_to_f32(s) for s in up]).astype(float)
+    wd = np.concatenate([O.bf16_to_f32(s) for s in down]).astype(float)
+    for i in range(m):
+        for j in range(f):
+            gij = sum(xf[i, k] * wg[j, k] for k in range(d))
+            uij = sum(xf[i, k] * wu[j, k] for k in range(d))
+            assert g[i, j] == pytest.approx(gij, rel=1e-14, abs=1e-300)
+            assert h[i, j] == pytest.approx(gij / (1 + math.exp(-gij)) * uij, rel=1e-13, abs=1e-300)
+        for j in range(d):
+            assert y[i, j] == pytest.approx(sum(h[i, k] * wd[j, k] for k in range(f)), rel=1e-12, abs=1e-300)
+
+
 # ---------------------------------------------------------------------------------------
 # mutation tests: a planted mistake in the oracle must fail one of the pins above
 # ---------------------------------------------------------------------------------------
