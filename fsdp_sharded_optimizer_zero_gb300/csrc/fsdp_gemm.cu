@@ -32,12 +32,30 @@ ZGB_DECLARE_ERROR_WORD();
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+#ifndef ZGB_GEMM_BN
+#define ZGB_GEMM_BN 256
+#endif
+#ifndef ZGB_GEMM_STAGES
+#define ZGB_GEMM_STAGES 4
+#endif
+constexpr int BM = 128, BN = ZGB_GEMM_BN, BK = 64, STAGES = ZGB_GEMM_STAGES;
 constexpr int kMaxShards = 16;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;  // two accumulators of BN fp32 columns
-constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t kSmemBytes = STAGES * STAGE_BYTES + 1024;  // + alignment slack
+constexpr uint32_t A_BYTES = BM * BK * 2;
+
+// per mode: output tile columns, bytes of one B tile, bytes of one stage (A + one or two B
+// tiles), TMEM columns of one accumulator buffer (two buffers are allocated)
+template <bool GATE_UP> struct Mode {
+  static constexpr int TN = GATE_UP ? 128 : BN;
+  static constexpr uint32_t BT_BYTES = TN * BK * 2;
+  static constexpr uint32_t STAGE = A_BYTES + (GATE_UP ? 2u : 1u) * BT_BYTES;
+  static constexpr uint32_t ACC = GATE_UP ? 2 * TN : TN;
+  static constexpr uint32_t TMEM_COLS = 2 * ACC <= 32 ? 32 : (2 * ACC <= 64 ? 64 : (2 * ACC <= 128 ? 128 : (2 * ACC <= 256 ? 256 : 512)));
+  // plain mode: each epilogue warp stages 32 x 32 fp32 output chunks in two 4 KiB buffers
+  // for the TMA store (4 warps x 2 x 4 KiB)
+  static constexpr uint32_t EPI = GATE_UP ? 0u : 4u * 2u * 4096u;
+  static constexpr uint32_t SMEM = STAGES * STAGE + EPI + 1024;  // + alignment slack
+};
 
 constexpr unsigned int kErrEmpty = (2u << 8) | 1u;  // producer waiting for a free stage
 constexpr unsigned int kErrFull = (2u << 8) | 2u;   // MMA waiting for a loaded stage
@@ -51,8 +69,10 @@ struct GemmParams {
   CUtensorMap w2[kMaxShards];    // gate-up mode: the up projection's shards (w holds the gate's)
   float* y;                      // [M, R] fp32
   uint16_t* yb;                  // [M, R] bf16 or null (gate-up mode: H = silu(gate) * up)
+  CUtensorMap ymap;              // Y [M, R] fp32, box 32 x 32, 128-byte swizzle (when y_tma)
   float alpha;                   // output scale (1: none)
   int m, r, k, shard_rows, n_shards;
+  int y_tma;                     // write Y through shared memory and TMA stores
 };
 
 // warp-uniform bounded wait: lane 0 polls, the whole warp gets the verdict
@@ -63,14 +83,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return ok != 0;
 }
 
-__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, int col0, uint32_t (&r)[32]) {
-  if (p.alpha != 1.0f) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), p.alpha));
-  }
+// direct per-thread stores of one row's 32-column chunk (fp32 unless skipped, bf16 if asked)
+__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, int col0, const uint32_t (&r)[32],
+                                                bool write_f32) {
   float* yrow = p.y + static_cast<size_t>(row) * p.r;
   const bool full = col0 + 32 <= p.r;
-  if (full && (p.r & 3) == 0) {
+  if (!write_f32) {
+  } else if (full && (p.r & 3) == 0) {
 #pragma unroll
     for (int j = 0; j < 32; j += 4)
       __stcs(reinterpret_cast<float4*>(yrow + col0 + j),
@@ -126,10 +145,12 @@ __device__ __forceinline__ void store_gate_up_chunk(const GemmParams& p, int row
 // and the epilogue writes H = silu(gate) * up for a 128 x 128 tile.
 template <bool GATE_UP>
 __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_constant__ GemmParams p) {
-  constexpr int TN = GATE_UP ? 128 : BN;  // output tile columns
-  constexpr uint32_t BT_BYTES = TN * BK * 2;  // one B tile per stage (two in gate-up mode)
+  constexpr int TN = Mode<GATE_UP>::TN;                      // output tile columns
+  constexpr uint32_t BT_BYTES = Mode<GATE_UP>::BT_BYTES;    // one B tile (two in gate-up mode)
+  constexpr uint32_t STAGE_BYTES = Mode<GATE_UP>::STAGE;
+  constexpr uint32_t ACC = Mode<GATE_UP>::ACC;
+  constexpr uint32_t kTmemCols = Mode<GATE_UP>::TMEM_COLS;
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, TN);
-  static_assert(A_BYTES + (GATE_UP ? 2 : 1) * BT_BYTES == STAGE_BYTES, "stage layout");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
@@ -223,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
         if (u >= 1 && !mbar_wait_bounded(smem_u32(&acce_bar[a]), (u - 1) & 1u, abort, &g_zgb_dev_error, kErrAccE))
           break;
         tc_fence_after();
-        const uint32_t d = tmem_base + a * BN;
+        const uint32_t d = tmem_base + a * ACC;
         for (int kb = 0; kb < num_k; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, abort, &g_zgb_dev_error, kErrFull)) {
@@ -254,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
     // ---------------- epilogue (warps 2-5) ----------------
     const int q = warp & 3;  // a warp reads TMEM lanes [32q, 32q+32)
     const int row_in_tile = q * 32 + lane;
-    uint32_t i = 0;
+    uint32_t i = 0, epi_chunk = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
       const uint32_t a = i & 1u, u = i >> 1;
       if (!warp_wait(smem_u32(&accf_bar[a]), u & 1u, abort, kErrAccF)) break;
@@ -262,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
       const int m0 = (tile % num_m) * BM;
       const int n0 = (tile / num_m) * TN;
       const int row = m0 + row_in_tile;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * ACC;
+      uint8_t* epi = smem + STAGES * STAGE_BYTES + static_cast<uint32_t>(q) * 2u * 4096u;
       if constexpr (GATE_UP) {
 #pragma unroll 1
         for (int c = 0; c < TN; c += 32) {
@@ -276,12 +298,39 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
           tmem_ld_32cols(taddr + c, r);
-          if (row < p.m && n0 + c < p.r) store_row_chunk(p, row, n0 + c, r);
+          if (n0 + c >= p.r) continue;  // warp-uniform
+          if (p.alpha != 1.0f) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), p.alpha));
+          }
+          if (p.y_tma) {
+            // lane = row of a 32 x 32 chunk: 128-byte rows, 16-byte pieces placed with the
+            // 128-byte swizzle (piece j of row i at slot j ^ (i % 8)): conflict-free writes,
+            // and the layout the tensor map's swizzle reads back in order
+            uint8_t* buf = epi + (epi_chunk & 1u) * 4096u;
+            if (lane == 0 && epi_chunk >= 2) bulk_wait_group_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+                  make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.ymap, n0 + c, m0 + q * 32, smem_u32(buf));
+              bulk_commit_group();
+            }
+            ++epi_chunk;
+            if (p.yb && row < p.m) store_row_chunk(p, row, n0 + c, r, false);
+          } else if (row < p.m) {
+            store_row_chunk(p, row, n0 + c, r, true);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acce_bar[a]));
     }
+    if (lane == 0) bulk_wait_group_all();  // no store may still read this CTA's shared memory
   }
 
   tc_fence_before();
@@ -308,12 +357,13 @@ int get_encode() {
 }
 
 int encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-              uint32_t box_rows) {
+              uint32_t box_rows, bool fp32 = false) {
   const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint64_t strides[1] = {inner * (fp32 ? 4 : 2)};
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = g_encode(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(ZERO_ERR_CUDA, "fsdp_unit_forward: cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -346,6 +396,11 @@ int launch_impl(int n_shards, const uint16_t* const* w_shards, const uint16_t* c
     if ((rc = encode_2d(&p.w[s], w_shards[s], k_in, shard_rows, BK, TN))) return rc;
     if (GATE_UP && (rc = encode_2d(&p.w2[s], w2_shards[s], k_in, shard_rows, BK, TN))) return rc;
   }
+  // fp32 output through TMA stores when its rows are 16-byte multiples (R % 4 == 0)
+  if (!GATE_UP && Y && rows_out % 4 == 0 && (reinterpret_cast<uintptr_t>(Y) & 15) == 0) {
+    if ((rc = encode_2d(&p.ymap, Y, rows_out, m_tokens, 32, 32, true))) return rc;
+    p.y_tma = 1;
+  }
   p.y = Y;
   p.yb = Y_bf16;
   p.alpha = alpha;
@@ -360,12 +415,13 @@ int launch_impl(int n_shards, const uint16_t* const* w_shards, const uint16_t* c
   if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
   cudaError_t attr = cudaSuccess;
   std::call_once(g_attr_once[GATE_UP ? 1 : 0][dev & 63], [&] {
-    attr = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Mode<GATE_UP>::SMEM);
   });
   if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(attr));
   const int64_t tiles = ((m_tokens + BM - 1) / BM) * ((rows_out + TN - 1) / TN);
   const unsigned int grid = static_cast<unsigned int>(std::min<int64_t>(tiles, num_sms()));
-  fsdp_gemm_kernel<GATE_UP><<<grid, kThreads, kSmemBytes, st>>>(p);
+  fsdp_gemm_kernel<GATE_UP><<<grid, kThreads, Mode<GATE_UP>::SMEM, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
   return ZERO_OK;
