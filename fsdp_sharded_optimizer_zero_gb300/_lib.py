@@ -31,7 +31,7 @@ STAGE_IDS = {"ddp": 0, "zero1": 1, "zero2": 2, "zero3": 3, "megatron": 4}
 # every symbol declared in include/zero.h
 EXPORTS = (
     "zero_plan", "zero_plan_query", "zero_bucket_range", "zero_plan_destroy",
-    "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_fp32_grads",
+    "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_host", "zero_fused_step_fp32_grads",
     "zero_fused_step_buckets",
     "zero_allgather_params", "ddp_allreduce", "fsdp_gather_rows", "fsdp_unit_forward",
     "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward", "fsdp_unit_forward_static_scratch", "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
@@ -80,6 +80,7 @@ def _load():
         "zero_adam_step": (I, [P, I, VP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
         "zero_fused_step": (I, [P, I, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
         "zero_fused_step_fp32_grads": (I, [P, I, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
+        "zero_fused_step_host": (I, [P, I, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
         "zero_fused_step_buckets": (I, [P, I, U64, U64, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
         "zero_allgather_params": (I, [P, PP, VP, VP]),
         "ddp_allreduce": (I, [P, PP, VP, VP]),
@@ -207,6 +208,28 @@ def zero_fused_step(plan: Plan, rank: int, grads, master, m, v, param_out, hp, s
                                 _dev(master, torch.float32, "master"), _dev(m, torch.float32, "m"),
                                 _dev(v, torch.float32, "v"), _dev(param_out, torch.bfloat16, "param_out"),
                                 C.byref(a), step, _stream(stream)))
+
+
+def _host(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor in page-locked memory")
+    if t.dtype != dtype or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous {dtype} tensor")
+    if not t.is_pinned():
+        raise ValueError(f"{name} must be page-locked (tensor.pin_memory())")
+    return t.data_ptr()
+
+
+def zero_fused_step_host(plan: Plan, rank: int, host_grads, master, m, v, host_param_out, hp, step: int, stream=None):
+    """Fused step reading the ranks' gradients from page-locked host tensors and writing the
+    bf16 parameters to a page-locked host tensor; master / m / v are CUDA tensors."""
+    a = _adam(hp)
+    arr = (C.c_void_p * len(host_grads))(*[_host(g, torch.bfloat16, f"host_grads[{i}]")
+                                          for i, g in enumerate(host_grads)])
+    _check(_lib.zero_fused_step_host(plan.handle, rank, arr, _dev(master, torch.float32, "master"),
+                                     _dev(m, torch.float32, "m"), _dev(v, torch.float32, "v"),
+                                     _host(host_param_out, torch.bfloat16, "host_param_out"), C.byref(a), step,
+                                     _stream(stream)))
 
 
 def zero_fused_step_fp32_grads(plan: Plan, rank: int, grads, master, m, v, param_out, hp, step: int, stream=None):

@@ -332,6 +332,46 @@ extern "C" int zero_fused_step_fp32_grads(const zero_plan_t* plan, int rank, con
   return ZERO_OK;
 }
 
+// device address of a page-locked host buffer, or null (with the message set) when the
+// buffer is not page-locked host memory the device can address
+static const void* host_buffer_device_address(const void* p, const char* who, const char* what, int idx) {
+  if (!p) {
+    set_error(ZERO_ERR_INVALID_ARG, "%s: %s[%d] is NULL (missing rank)", who, what, idx);
+    return nullptr;
+  }
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_error(ZERO_ERR_INVALID_ARG, "%s: %s[%d]: cudaPointerGetAttributes: %s", who, what, idx, cudaGetErrorString(e));
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) {
+    set_error(ZERO_ERR_INVALID_ARG, "%s: %s[%d] is not page-locked host memory mapped for the device", who, what, idx);
+    return nullptr;
+  }
+  return a.devicePointer;
+}
+
+extern "C" int zero_fused_step_host(const zero_plan_t* plan, int rank, const zero_bf16* const host_grads[],
+                                    float* master, float* m, float* v, zero_bf16* host_param_out, const zero_adam* hp,
+                                    int64_t step, zero_stream_t stream) {
+  clear_error();
+  const char* who = "zero_fused_step_host";
+  CHECK_ARG(plan != nullptr, "%s: plan is NULL", who);
+  CHECK_ARG(host_grads != nullptr, "%s: host_grads array is NULL", who);
+  const zero_layout& L = plan->lay;
+  const zero_bf16* dev_grads[ZERO_MAX_RANKS];
+  for (int q = 0; q < L.n_ranks; ++q) {
+    dev_grads[q] = static_cast<const zero_bf16*>(host_buffer_device_address(host_grads[q], who, "host_grads", q));
+    if (!dev_grads[q]) return ZERO_ERR_INVALID_ARG;
+  }
+  zero_bf16* dev_param =
+      static_cast<zero_bf16*>(const_cast<void*>(host_buffer_device_address(host_param_out, who, "host_param_out", 0)));
+  if (!dev_param) return ZERO_ERR_INVALID_ARG;
+  return fused_impl(plan, rank, 0, L.n_buckets, dev_grads, master, m, v, dev_param, hp, step, stream, who);
+}
+
 extern "C" int zero_fused_step_buckets(const zero_plan_t* plan, int rank, uint64_t bucket_begin, uint64_t bucket_end,
                                        const zero_bf16* const grads[], float* master, float* m, float* v,
                                        zero_bf16* param_out, const zero_adam* hp, int64_t step, zero_stream_t stream) {

@@ -181,6 +181,19 @@ ZERO_API int zero_fused_step(const zero_plan_t* plan, int rank, const zero_bf16*
                     float* m, float* v, zero_bf16* param_out, const zero_adam* hp, int64_t step,
                     zero_stream_t stream);
 
+/* zero_fused_step with the gradients and the bf16 parameters in HOST memory: host_grads[q]
+ * and host_param_out must be page-locked (cudaHostAlloc / cudaMallocHost /
+ * cudaHostRegister) and mapped for the device; the kernel reads every rank's gradient
+ * straight from host memory and writes the parameters straight back over the host link
+ * (NVLink-C2C on Grace-Blackwell), so each byte crosses the link once and no device
+ * staging buffer exists. master / m / v stay in device memory. Pointer conventions and
+ * results as zero_fused_step; a buffer that is not page-locked host memory the device
+ * can address is rejected with ZERO_ERR_INVALID_ARG (checked with
+ * cudaPointerGetAttributes before anything is launched). */
+ZERO_API int zero_fused_step_host(const zero_plan_t* plan, int rank, const zero_bf16* const host_grads[],
+                                  float* master, float* m, float* v, zero_bf16* host_param_out, const zero_adam* hp,
+                                  int64_t step, zero_stream_t stream);
+
 /* zero_fused_step with fp32 gradient contributions: grads[q] are fp32 (Megatron
  * distributed optimizer, gradients accumulated and reduced in fp32 — [Interview] worked
  * table, Megatron row and note). Same pointer conventions and arithmetic (the widening of

@@ -113,3 +113,8 @@ def test_step_calls_reject_missing_rank_before_launch(z):
     assert lib.fsdp_unit_forward(4, good, 8, 12, 128, 4, 256, None, None, None) == -1   # k % 8
     assert lib.fsdp_gather_rows(4, grads, 8, 16, 256, None) == -1
     assert lib.zero_set_fused_kernel(3) == -1
+    # host-memory step: a buffer that is not page-locked host memory is rejected before launch
+    import numpy as np
+    buf = np.zeros(1024, np.uint16)
+    hosts = (C.c_void_p * 4)(*([buf.ctypes.data] * 4))
+    assert lib.zero_fused_step_host(p.handle, -2, hosts, 256, 512, 768, buf.ctypes.data, C.byref(adam), 1, None) == -1

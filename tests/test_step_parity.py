@@ -404,6 +404,48 @@ def test_buckets_in_gradient_ready_order(z):
     compare((f32(master), f32(m), f32(v), bits16(param)), want, "reverse-order buckets")
 
 
+# ---------------------------------------------------------------------------------------
+# gradients and parameters in page-locked host memory, read / written over the host link
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("psi,n,bb", [(1_048_576, 4, 25 * MIB), (100_003, 5, 1 << 12), (20_001, 64, 1 << 10)])
+def test_host_memory_step_bit_exact(z, psi, n, bb):
+    master0, m0, v0, grads = make_inputs(psi, n, 2, seed=41, moments=True)
+    want = oracle_run("zero2", psi, n, bb, master0, m0, v0, grads)
+    plan = z.zero_plan(psi, n, "zero2", bb)
+    P, S = plan.psi_padded, plan.shard_elems
+    for mode in ("all", "ranks"):
+        master, m, v = master0.to(DEV), m0.to(DEV), v0.to(DEV)
+        hparam = torch.zeros(P, dtype=torch.bfloat16).pin_memory()
+        for t, gs in enumerate(grads, start=1):
+            hg = [g.pin_memory() for g in gs]
+            if mode == "all":
+                z.zero_fused_step_host(plan, z.ZERO_ALL_RANKS, hg, master, m, v, hparam, HP, t)
+            else:
+                for r in range(n):
+                    sl = slice(r * S, (r + 1) * S)
+                    z.zero_fused_step_host(plan, r, hg, master[sl], m[sl], v[sl], hparam, HP, t)
+            torch.cuda.synchronize()
+        z.zero_device_status()
+        compare((f32(master), f32(m), f32(v), bits16(hparam)), want, f"host memory {mode}")
+
+
+def test_host_memory_step_rejects_pageable_buffers(z):
+    import ctypes as C
+    plan = z.zero_plan(4096, 2, "zero2", 1 << 12)
+    master = torch.zeros(4096, device=DEV)
+    pageable = [torch.zeros(4096, dtype=torch.bfloat16) for _ in range(2)]
+    hparam = torch.zeros(4096, dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(ValueError):
+        z.zero_fused_step_host(plan, z.ZERO_ALL_RANKS, pageable, master, master, master, hparam, HP, 1)
+    lib = z.library()
+    arr = (C.c_void_p * 2)(pageable[0].data_ptr(), pageable[1].data_ptr())
+    adam = z._lib.zero_adam(1e-4, 0.9, 0.999, 1e-8, 0.0)
+    rc = lib.zero_fused_step_host(plan.handle, z.ZERO_ALL_RANKS, arr, master.data_ptr(), master.data_ptr(),
+                                  master.data_ptr(), hparam.data_ptr(), C.byref(adam), 1, None)
+    assert rc == -1 and b"page-locked" in lib.zero_last_error()
+
+
 def test_device_status_is_clean_after_all_kernels(z):
     z.zero_device_status()
 
