@@ -32,9 +32,10 @@ STAGE_IDS = {"ddp": 0, "zero1": 1, "zero2": 2, "zero3": 3, "megatron": 4}
 EXPORTS = (
     "zero_plan", "zero_plan_query", "zero_bucket_range", "zero_plan_destroy",
     "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_host", "zero_fused_step_fp32_grads",
-    "zero_fused_step_buckets",
-    "zero_allgather_params", "ddp_allreduce", "fsdp_gather_rows", "fsdp_unit_forward",
-    "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward", "fsdp_unit_forward_static_scratch", "zero_last_error", "zero_device_status", "zero_set_fused_kernel", "zero_version",
+    "zero_fused_step_buckets", "zero_allgather_params", "ddp_allreduce",
+    "fsdp_gather_rows", "fsdp_unit_forward", "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward",
+    "fsdp_unit_forward_static_scratch",
+    "zero_last_error", "zero_device_status", "zero_selftest_bounded_wait", "zero_set_fused_kernel", "zero_version",
 )
 
 
@@ -92,6 +93,7 @@ def _load():
         "fsdp_mlp_forward": (I, [I, PP, PP, PP, I64, I64, VP, I64, VP, VP, VP, VP, VP]),
         "zero_last_error": (C.c_char_p, []),
         "zero_device_status": (I, [VP]),
+        "zero_selftest_bounded_wait": (I, [C.c_uint32, VP]),
         "zero_set_fused_kernel": (I, [I]),
         "zero_version": (I, []),
     }
@@ -322,6 +324,10 @@ def fsdp_unit_forward_static_scratch(w_shards, A, Y, Y_bf16=None, stream=None):
 
 def zero_device_status(stream=None):
     _check(_lib.zero_device_status(_stream(stream)))
+
+
+def zero_selftest_bounded_wait(timeout_ms: int, stream=None):
+    _check(_lib.zero_selftest_bounded_wait(timeout_ms, _stream(stream)))
 
 
 def zero_set_fused_kernel(which: int):

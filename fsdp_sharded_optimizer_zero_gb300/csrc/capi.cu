@@ -488,6 +488,15 @@ extern "C" int zero_device_status(zero_stream_t stream) {
   return ZERO_OK;
 }
 
+extern "C" int zero_selftest_bounded_wait(uint32_t timeout_ms, zero_stream_t stream) {
+  clear_error();
+  CHECK_ARG(timeout_ms >= 1 && timeout_ms <= 2000, "zero_selftest_bounded_wait: timeout_ms %u outside 1..2000",
+            timeout_ms);
+  CUDA_LAUNCH(launch_wait_selftest(static_cast<unsigned long long>(timeout_ms) * 1000000ull,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+  return ZERO_OK;
+}
+
 extern "C" int zero_set_fused_kernel(int which) {
   clear_error();
   CHECK_ARG(which >= 0 && which <= 2, "zero_set_fused_kernel: %d is not 0, 1 or 2", which);

@@ -130,13 +130,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // kWaitTimeoutNs or as soon as another thread of the CTA raised *abort; on a timeout it
 // records `code` in the error word and raises *abort. Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                  unsigned int* err_word, unsigned int code) {
+                                                  unsigned int* err_word, unsigned int code,
+                                                  unsigned long long timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if ((it & 15u) == 15u && globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > timeout_ns) {
       atomicCAS(err_word, 0u, code);
       *abort = 1;
       return false;

@@ -51,6 +51,7 @@ cudaError_t launch_allgather(const MasterPtrs& mp, int n, uint64_t shard, uint16
 cudaError_t launch_gather_rows(const GradPtrs& shards, int n, uint64_t shard_elems, uint16_t* full, bool vec,
                                cudaStream_t st);
 unsigned int step_kernels_read_clear_error();
+cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t st);
 // dst[c][q * rows + r] = srcs[q][r][c] for q < n: the N row-major [rows, cols] bf16 sources
 // transposed and concatenated into one row-major [cols, n * rows] buffer
 cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int64_t cols, uint16_t* dst,

@@ -26,6 +26,7 @@ constexpr int kThreads = 256;
 constexpr unsigned int kErrTmaEmpty = (1u << 8) | 1u;  // producer waiting for a free stage
 constexpr unsigned int kErrTmaFull = (1u << 8) | 2u;   // consumer waiting for a loaded stage
 constexpr unsigned int kErrTmaDrain = (1u << 8) | 3u;  // producer draining copies after an abort
+constexpr unsigned int kErrSelftest = (3u << 8) | 1u;  // the bounded-wait self-test
 
 // ------------------------------------------------------------------------------------
 // the reduced gradient: fp32 sum in rank order 0..N-1
@@ -487,6 +488,20 @@ __global__ void __launch_bounds__(256) transpose_cat_kernel(GradPtrs srcs, int64
   }
 }
 
+// One thread waits on an mbarrier that nothing arrives on, through the same bounded wait
+// the pipelined kernels use; after timeout_ns it records kErrSelftest and returns.
+__global__ void wait_selftest_kernel(unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, &g_zgb_dev_error, kErrSelftest, timeout_ns);
+}
+
 unsigned int grid_for(uint64_t work_items) {
   const uint64_t want = (work_items + kThreads - 1) / kThreads;
   const uint64_t cap = static_cast<uint64_t>(num_sms()) * 16u;
@@ -624,6 +639,11 @@ cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int6
   if (gy > 65535 || gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
   transpose_cat_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(
       srcs, rows, cols, total_rows, dst, vec ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(timeout_ns);
   return cudaGetLastError();
 }
 

@@ -319,6 +319,13 @@ ZERO_API const char* zero_last_error(void);
  * or ZERO_ERR_CUDA. */
 ZERO_API int zero_device_status(zero_stream_t stream);
 
+/* Check of the library's failure path, not part of the method: launches one thread that
+ * waits on an mbarrier nothing arrives on, through the same bounded wait the pipelined
+ * kernels use, with a limit of timeout_ms (1..2000). The wait runs out, records its code
+ * (0x301) in the device error word and the kernel returns; the next zero_device_status()
+ * reports ZERO_ERR_DEVICE and the context stays usable. Nothing traps or faults. */
+ZERO_API int zero_selftest_bounded_wait(uint32_t timeout_ms, zero_stream_t stream);
+
 /* Select the fused-step kernel: 0 = default (the register-streaming kernel), 1 = TMA
  * bulk-copy pipeline staging the N rank chunks in shared memory, 2 = register-streaming.
  * All give bit-identical results (misaligned buffers always take a scalar kernel). */

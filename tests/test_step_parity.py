@@ -590,3 +590,18 @@ def test_sweep_1p5b_sampled(z, n):
         z.zero_fused_step(plan, z.ZERO_RANK_VIEW, grads, master, m, v, param, HP, 1)
     z.zero_device_status()
     so.check(master, m, v, param, f"sweep N={n}")
+
+
+def test_bounded_wait_runs_out_and_reports(z):
+    """A wait that nothing satisfies gives up after its limit and reports through the
+    device error word; the context stays usable (a fused step afterwards is still exact)."""
+    z.zero_device_status()
+    z.zero_selftest_bounded_wait(200)
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_device_status()
+    assert e.value.code == -5 and "0x301" in str(e.value)
+    z.zero_device_status()  # the word was cleared
+    psi, n = 4099, 4
+    master0, m0, v0, grads = make_inputs(psi, n, 1, seed=2)
+    want = oracle_run("zero2", psi, n, 1 << 12, master0, m0, v0, grads)
+    compare(gpu_run(z, "zero2", "all", psi, n, 1 << 12, master0, m0, v0, grads), want, "after a timed-out wait")
