@@ -443,37 +443,47 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
 # the CPU oracle as baseline / reference arm
 # ---------------------------------------------------------------------------------------
 
-def oracle_rate(n_params: int, n_ranks: int = 8, reps: int = 1):
-    """Oracle params/s on the first n_params of the workload: N bf16 gradient slices,
-    fp32 master / m / v, one fused step (reduce, Adam, cast) in plain numpy."""
-    import numpy as np
-    import torch
+class OracleSample:
+    """The first n_params parameters of the bench workload (N = 8 bf16 gradient slices,
+    fp32 master / m / v), generated once; step() runs one fused oracle step (reduce, Adam,
+    cast in plain numpy) on the first `count` of them and returns its seconds."""
 
-    import synth
-    from oracle import zero_oracle as O
-    psi = synth.GPT2_SMALL_PSI
-    master = synth.master_params(n_params, n_params).numpy()
-    m = np.zeros(n_params, np.float32)
-    v = np.zeros(n_params, np.float32)
-    grads = [synth.rank_grads(n_params, n_params, r, 1).view(torch.int16).numpy().view(np.uint16)
-             for r in range(n_ranks)]
-    hp = O.AdamHyper()
-    t0 = time.perf_counter()
-    for t in range(1, reps + 1):
-        master, m, v, _ = O.fused_step_elements(grads, master, m, v, hp, t)
-    el = time.perf_counter() - t0
-    assert psi > n_params
-    return n_params * reps / el, el
+    def __init__(self, n_params: int, n_ranks: int = 8):
+        import numpy as np
+        import torch
+
+        import synth
+        from oracle import zero_oracle as O
+        self.O = O
+        self.n = n_params
+        self.master = synth.master_params(n_params, n_params).numpy()
+        self.m = np.zeros(n_params, np.float32)
+        self.v = np.zeros(n_params, np.float32)
+        self.grads = [synth.rank_grads(n_params, n_params, r, 1).view(torch.int16).numpy().view(np.uint16)
+                      for r in range(n_ranks)]
+        self.hp = O.AdamHyper()
+        self.t = 0
+
+    def step(self, count: int) -> float:
+        count = min(count, self.n)
+        self.t += 1
+        t0 = time.perf_counter()
+        w, m, v, _ = self.O.fused_step_elements([g[:count] for g in self.grads], self.master[:count],
+                                                self.m[:count], self.v[:count], self.hp, self.t)
+        el = time.perf_counter() - t0
+        self.master[:count], self.m[:count], self.v[:count] = w, m, v
+        return el
 
 
 def cpu_baseline(budget_s: float = 15.0):
     n_params = 4 * MIB
-    rate, el = oracle_rate(n_params)
+    s = OracleSample(n_params)
+    el = s.step(n_params)
     reps = max(1, int(budget_s / max(el, 1e-3)))
-    rate, el = oracle_rate(n_params, reps=reps)
-    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+    total = sum(s.step(n_params) for _ in range(reps))
+    return {"value": n_params * reps / total, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {n_params:,} of 124,356,864 GPT-2-small parameters, N=8 gradient slices, "
-                      f"{reps} fused steps ({el:.1f} s; numpy elementwise, single-threaded)"}
+                      f"{reps} fused steps ({total:.1f} s; numpy elementwise, single-threaded)"}
 
 
 def run_reference(args):
@@ -483,19 +493,18 @@ def run_reference(args):
         return
     import synth
     psi, n, stage, bb = synth.GPT2_SMALL_PSI, 8, "zero2", 25 * MIB
+    cap = 4 * MIB
+    s = OracleSample(cap)
+    rate = cap / s.step(cap)
     # size each step's sample so the whole run stays near args.ref_seconds
-    rate, _ = oracle_rate(1 << 18)
     per_step = args.ref_seconds / max(1, args.steps + args.warmup)
-    n_params = int(min(psi, max(4096, rate * per_step)))
+    count = int(min(cap, max(65536, rate * per_step)))
     for _ in range(args.warmup):
-        oracle_rate(n_params)
-    t_total = 0.0
-    for _ in range(args.steps):
-        _, el = oracle_rate(n_params)
-        t_total += el
-    value = n_params * args.steps / t_total
+        s.step(count)
+    t_total = sum(s.step(count) for _ in range(args.steps))
+    value = count * args.steps / t_total
     cb = {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-          "sample": f"{n_params:,} of {psi:,} parameters per step (N=8), numpy single-threaded"}
+          "sample": f"first {count:,} of {psi:,} parameters per step (N=8), numpy single-threaded"}
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": 1e3 * psi / value, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; GPT-2-small tensor shapes)",
@@ -613,7 +622,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
