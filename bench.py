@@ -117,7 +117,7 @@ class ClockSampler:
 
 def kernel_source_digest():
     h = hashlib.sha256()
-    for name in ("step_kernels.cu", "device_common.cuh"):
+    for name in ("fused_step.cu", "step_common.cuh", "device_common.cuh"):
         h.update((ROOT / "fsdp_sharded_optimizer_zero_gb300" / "csrc" / name).read_bytes())
     return h.hexdigest()[:16]
 

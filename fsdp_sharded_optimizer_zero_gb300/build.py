@@ -3,6 +3,7 @@ compiled in parallel, then one shared-library link. No CMake, no torch extension
 ABI carries no torch types). Rebuilds only when a source, header or flag changed."""
 from __future__ import annotations
 
+import fcntl
 import hashlib
 import os
 import shutil
@@ -16,8 +17,8 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libzero_gb300.so"
-SOURCES = ["capi.cu", "step_kernels.cu", "fsdp_gemm.cu", "fsdp_unit.cu", "fsdp_static_scratch.cu"]
-HEADERS = ["internal.h", "device_common.cuh", "tcgen05.cuh"]
+SOURCES = ["capi.cu", "fused_step.cu", "step_kernels.cu", "fsdp_gemm.cu", "fsdp_unit.cu", "fsdp_static_scratch.cu"]
+HEADERS = ["internal.h", "device_common.cuh", "step_common.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = [
     "-O3", "-std=c++17", "-lineinfo", *ARCH,
@@ -54,6 +55,18 @@ def build(verbose: bool = False, force: bool = False) -> Path:
     if not force and LIB.exists() and stamp.exists() and stamp.read_text() == digest:
         return LIB
     BUILD.mkdir(exist_ok=True)
+    # one builder at a time (several ranks of one job may call build() together)
+    with open(BUILD / "lock", "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and LIB.exists() and stamp.exists() and stamp.read_text() == digest:
+                return LIB
+            return _build_locked(digest, stamp, verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(digest: str, stamp: Path, verbose: bool) -> Path:
     cc = nvcc()
 
     def compile_one(src: str) -> Path:

@@ -478,13 +478,15 @@ extern "C" int zero_device_status(zero_stream_t stream) {
   clear_error();
   CUDA_LAUNCH(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
   const unsigned int a = step_kernels_read_clear_error();
+  const unsigned int f = fused_step_read_clear_error();
   const unsigned int b = fsdp_gemm_read_clear_error();
-  if (a == 0xffffffffu || b == 0xffffffffu) return set_error(ZERO_ERR_CUDA, "zero_device_status: cannot read the device error word");
-  if (a || b)
+  if (a == 0xffffffffu || f == 0xffffffffu || b == 0xffffffffu)
+    return set_error(ZERO_ERR_CUDA, "zero_device_status: cannot read the device error word");
+  if (a || f || b)
     return set_error(ZERO_ERR_DEVICE,
-                     "zero_device_status: a bounded wait gave up (step kernels code 0x%x, FSDP GEMM code 0x%x; "
-                     "high byte = kernel, low byte = wait)",
-                     a, b);
+                     "zero_device_status: a bounded wait gave up (step kernels code 0x%x, fused step code 0x%x, "
+                     "FSDP GEMM code 0x%x; high byte = kernel, low byte = wait)",
+                     a, f, b);
   return ZERO_OK;
 }
 

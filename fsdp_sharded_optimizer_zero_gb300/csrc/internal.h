@@ -35,7 +35,7 @@ struct Domain {
   uint64_t n_seg, seg_len, seg_stride;
 };
 
-// ---- launchers (step_kernels.cu) ----
+// ---- launchers (step_kernels.cu, fused_step.cu) ----
 cudaError_t launch_reduce(const GradPtrs& gp, int n, float* out, const Domain& d, float inv_n, bool vec,
                           cudaStream_t st);
 cudaError_t launch_adam(const float* g, float* master, float* m, float* v, uint16_t* param, const Domain& d,
@@ -51,6 +51,7 @@ cudaError_t launch_allgather(const MasterPtrs& mp, int n, uint64_t shard, uint16
 cudaError_t launch_gather_rows(const GradPtrs& shards, int n, uint64_t shard_elems, uint16_t* full, bool vec,
                                cudaStream_t st);
 unsigned int step_kernels_read_clear_error();
+unsigned int fused_step_read_clear_error();
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t st);
 // dst[c][q * rows + r] = srcs[q][r][c] for q < n: the N row-major [rows, cols] bf16 sources
 // transposed and concatenated into one row-major [cols, n * rows] buffer

@@ -605,3 +605,24 @@ def test_bounded_wait_runs_out_and_reports(z):
     master0, m0, v0, grads = make_inputs(psi, n, 1, seed=2)
     want = oracle_run("zero2", psi, n, 1 << 12, master0, m0, v0, grads)
     compare(gpu_run(z, "zero2", "all", psi, n, 1 << 12, master0, m0, v0, grads), want, "after a timed-out wait")
+
+
+def test_shard_above_2_pow_31_elements(z):
+    """One rank's view with S = 2^31 + 4099 elements (byte offsets far beyond 4 GiB, a
+    ragged tail): sampled against the oracle, including the last elements."""
+    n, S = 2, (1 << 31) + 4099
+    plan = z.zero_plan(S * n, n, "zero3", 64 * MIB)
+    assert plan.shard_elems == S
+    chunks = synth.chunk_grads(S, n, 1, device=DEV, seed_key=9)
+    rows = [chunks[q] for q in range(n)]
+    master = synth.master_params(S, S, device=DEV, seed_key=9)
+    m = torch.zeros(S, device=DEV)
+    v = torch.zeros(S, device=DEV)
+    p = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+    idx = np.unique(np.concatenate([sample_indices(S, S, plan.bucket_elems, 1, k=1 << 14, seed=3),
+                                    np.arange(S - 64, S), np.arange((1 << 31) - 32, (1 << 31) + 32)]))
+    so = SampledOracle(idx, master, m, v)
+    so.step(rows, 1)
+    z.zero_fused_step(plan, z.ZERO_RANK_VIEW, rows, master, m, v, p, HP, 1)
+    z.zero_device_status()
+    so.check(master, m, v, p, "S > 2^31")
