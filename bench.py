@@ -599,6 +599,32 @@ def run_case(args):
         ms = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1, stream),
                            4, stream)
         out.update(psi=psi, n_ranks=n, ms=ms, bytes=plan.fused_step_bytes, gbs=plan.fused_step_bytes / ms / 1e6)
+    elif args.case in ("tiny", "mistral_rank_view"):
+        # tiny: psi = 2^20, N = 4, every rank in one launch (35.7 MB: L2-resident, reported as
+        # such). mistral_rank_view: one rank's shard of the Mistral-7B list at N = 8
+        # (S = 905,216,512; its 8 incoming chunks, 14.5 GB), ZeRO-3, 50 MiB buckets.
+        hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+        hbm_peak = peaks()[0]
+        if args.case == "tiny":
+            psi, n = 1 << 20, 4
+            plan = z.zero_plan(psi, n, "zero2", 25 * MIB)
+            grads = [synth.rank_grads(psi, psi, r, 1, device=dev) for r in range(n)]
+            L, rank = psi, z.ZERO_ALL_RANKS
+        else:
+            psi, n = synth.MISTRAL_7B_PSI, 8
+            plan = z.zero_plan(psi, n, "zero3", 50 * MIB)
+            L, rank = plan.shard_elems, z.ZERO_RANK_VIEW
+            ch = synth.chunk_grads(L, n, 1, device=dev)
+            grads = [ch[q] for q in range(n)]
+        master = synth.master_params(L, L, device=dev)
+        m = torch.zeros(L, device=dev)
+        v = torch.zeros(L, device=dev)
+        param = torch.empty(L, dtype=torch.bfloat16, device=dev)
+        ms = time_launches(lambda: z.zero_fused_step(plan, rank, grads, master, m, v, param, hp, 1, stream), 20, stream)
+        byts = L * (2 * n + 26)
+        out.update(params_per_step=L, n_ranks=n, ms=ms, bytes=byts, gbs=byts / ms / 1e6,
+                   frac=byts / ms / 1e6 / hbm_peak, params_per_s=L / ms * 1e3,
+                   l2_resident=byts < 129e6)
     elif args.case == "gemm_small":
         M, R, K, n = 2048, 14336, 4096, 8
         X = synth.activations(M, K, device=dev)
@@ -614,7 +640,8 @@ def run_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", default=None, help="small profiling case: fused_small | gemm_small")
+    ap.add_argument("--case", default=None,
+                    help="one measured case: fused_small | gemm_small (ncu-sized) | tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
