@@ -64,14 +64,15 @@ constexpr unsigned int kErrAccF = (2u << 8) | 4u;   // epilogue waiting for a fi
 constexpr unsigned int kErrDrain = (2u << 8) | 5u;  // draining after an abort
 
 struct GemmParams {
-  CUtensorMap a;                 // A [M, K] bf16, box 64 x 128
+  CUtensorMap a[kMaxShards];     // A row shard s [a_shard_rows, K] bf16, box 64 x 128
   CUtensorMap w[kMaxShards];     // shard s [shard_rows, K] bf16, box 64 x (256, or 128 in gate-up mode)
   CUtensorMap w2[kMaxShards];    // gate-up mode: the up projection's shards (w holds the gate's)
   float* y;                      // [M, R] fp32
   uint16_t* yb;                  // [M, R] bf16 or null (gate-up mode: H = silu(gate) * up)
-  CUtensorMap ymap;              // Y [M, R] fp32, box 32 x 32, 128-byte swizzle (when y_tma)
+  CUtensorMap ymap[kMaxShards];  // Y row shard s [a_shard_rows, R] fp32, box 32 x 32, 128B swizzle (y_tma)
   float alpha;                   // output scale (1: none)
   int m, r, k, shard_rows, n_shards;
+  int a_shard_rows, a_shards;    // A and Y split by rows into a_shards pieces (1: not split)
   int y_tma;                     // write Y through shared memory and TMA stores
 };
 
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&p.a);
+    for (int s = 0; s < p.a_shards; ++s) prefetch_tmap(&p.a[s]);
     for (int s = 0; s < p.n_shards; ++s) {
       prefetch_tmap(&p.w[s]);
       if (GATE_UP) prefetch_tmap(&p.w2[s]);
@@ -210,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
         const int shard = n0 / p.shard_rows;
         const int nl = n0 - shard * p.shard_rows;
         const void* wmap = &p.w[shard];
+        const int ash = m0 / p.a_shard_rows;  // the A row shard holding this tile's rows
+        const int ml = m0 - ash * p.a_shard_rows;
         for (int kb = 0; kb < num_k; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (it >= STAGES &&
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
           const uint32_t fb = smem_u32(&full_bar[s]);
           uint8_t* sa = smem + s * STAGE_BYTES;
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          tma_load_2d(smem_u32(sa), &p.a, kb * BK, m0, fb);
+          tma_load_2d(smem_u32(sa), &p.a[ash], kb * BK, ml, fb);
           tma_load_2d(smem_u32(sa + A_BYTES), wmap, kb * BK, nl, fb);
           if (GATE_UP) tma_load_2d(smem_u32(sa + A_BYTES + BT_BYTES), &p.w2[shard], kb * BK, nl, fb);
           last_issue[s] = it;
@@ -283,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
       const int m0 = (tile % num_m) * BM;
       const int n0 = (tile / num_m) * TN;
       const int row = m0 + row_in_tile;
+      const int ash = m0 / p.a_shard_rows;
+      const int ml = m0 - ash * p.a_shard_rows;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * ACC;
       uint8_t* epi = smem + STAGES * STAGE_BYTES + static_cast<uint32_t>(q) * 2u * 4096u;
       if constexpr (GATE_UP) {
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&p.ymap, n0 + c, m0 + q * 32, smem_u32(buf));
+              tma_store_2d(&p.ymap[ash], n0 + c, ml + q * 32, smem_u32(buf));
               bulk_commit_group();
             }
             ++epi_chunk;
@@ -374,13 +379,20 @@ int encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
 
 namespace {
 
+// a_shards > 1: A and Y are given as a_shards row pieces of m_tokens / a_shards rows each
+// (a multiple of 128, so no output tile straddles two pieces); fp32 Y then goes through
+// TMA stores only and no bf16 copy is written.
 template <bool GATE_UP>
 int launch_impl(int n_shards, const uint16_t* const* w_shards, const uint16_t* const* w2_shards, int64_t rows_out,
-                int64_t k_in, const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha,
-                cudaStream_t st, const char* who) {
+                int64_t k_in, int a_shards, const uint16_t* const* A, int64_t m_tokens, float* const* Y,
+                uint16_t* Y_bf16, float alpha, cudaStream_t st, const char* who) {
   constexpr int TN = GATE_UP ? 128 : BN;
   if (m_tokens > INT32_MAX / 2 || rows_out > INT32_MAX / 2 || k_in > INT32_MAX / 2)
     return set_error(ZERO_ERR_INVALID_ARG, "%s: sizes must be below 2^30", who);
+  const int64_t a_rows = m_tokens / a_shards;
+  if (a_shards < 1 || a_shards > kMaxShards ||
+      (a_shards > 1 && (m_tokens % a_shards || a_rows % BM || GATE_UP || Y_bf16 || rows_out % 4)))
+    return set_error(ZERO_ERR_UNSUPPORTED, "%s: unsupported row split of A / Y into %d pieces", who, a_shards);
   const int64_t shard_rows = rows_out / n_shards;
   if (n_shards > 1 && (shard_rows % TN != 0 || n_shards > kMaxShards))
     return set_error(ZERO_ERR_UNSUPPORTED,
@@ -391,17 +403,25 @@ int launch_impl(int n_shards, const uint16_t* const* w_shards, const uint16_t* c
   if (rc) return rc;
   GemmParams p;
   memset(&p, 0, sizeof(p));
-  if ((rc = encode_2d(&p.a, A, k_in, m_tokens, BK, BM))) return rc;
+  for (int s = 0; s < a_shards; ++s)
+    if ((rc = encode_2d(&p.a[s], A[s], k_in, a_rows, BK, BM))) return rc;
   for (int s = 0; s < n_shards; ++s) {
     if ((rc = encode_2d(&p.w[s], w_shards[s], k_in, shard_rows, BK, TN))) return rc;
     if (GATE_UP && (rc = encode_2d(&p.w2[s], w2_shards[s], k_in, shard_rows, BK, TN))) return rc;
   }
   // fp32 output through TMA stores when its rows are 16-byte multiples (R % 4 == 0)
-  if (!GATE_UP && Y && rows_out % 4 == 0 && (reinterpret_cast<uintptr_t>(Y) & 15) == 0) {
-    if ((rc = encode_2d(&p.ymap, Y, rows_out, m_tokens, 32, 32, true))) return rc;
+  bool y_aligned = !GATE_UP && Y != nullptr && rows_out % 4 == 0;
+  for (int s = 0; y_aligned && s < a_shards; ++s) y_aligned = (reinterpret_cast<uintptr_t>(Y[s]) & 15) == 0;
+  if (y_aligned) {
+    for (int s = 0; s < a_shards; ++s)
+      if ((rc = encode_2d(&p.ymap[s], Y[s], rows_out, a_rows, 32, 32, true))) return rc;
     p.y_tma = 1;
+  } else if (a_shards > 1) {
+    return set_error(ZERO_ERR_UNSUPPORTED, "%s: row-split outputs must be 16-byte aligned", who);
   }
-  p.y = Y;
+  p.y = Y ? Y[0] : nullptr;
+  p.a_shard_rows = static_cast<int>(a_rows);
+  p.a_shards = a_shards;
   p.yb = Y_bf16;
   p.alpha = alpha;
   p.m = static_cast<int>(m_tokens);
@@ -431,14 +451,24 @@ int launch_impl(int n_shards, const uint16_t* const* w_shards, const uint16_t* c
 
 int launch_fsdp_gemm(int n_shards, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
                      const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st) {
-  return launch_impl<false>(n_shards, w_shards, nullptr, rows_out, k_in, A, m_tokens, Y, Y_bf16, alpha, st,
+  const uint16_t* a1[1] = {A};
+  float* y1[1] = {Y};
+  return launch_impl<false>(n_shards, w_shards, nullptr, rows_out, k_in, 1, a1, m_tokens, y1, Y_bf16, alpha, st,
                             "fsdp_unit_forward");
+}
+
+int launch_fsdp_gemm_row_split(int a_shards, const uint16_t* const* A, float* const* Y, int64_t rows_per_shard,
+                               const uint16_t* W, int64_t rows_out, int64_t k_in, float alpha, cudaStream_t st) {
+  const uint16_t* w1[1] = {W};
+  return launch_impl<false>(1, w1, nullptr, rows_out, k_in, a_shards, A, rows_per_shard * a_shards, Y, nullptr, alpha,
+                            st, "fsdp_unit_backward");
 }
 
 int launch_fsdp_gate_up(int n_shards, const uint16_t* const* gate_shards, const uint16_t* const* up_shards,
                         int64_t d_ff, int64_t d_model, const uint16_t* X, int64_t m_tokens, uint16_t* H,
                         cudaStream_t st) {
-  return launch_impl<true>(n_shards, gate_shards, up_shards, d_ff, d_model, X, m_tokens, nullptr, H, 1.0f, st,
+  const uint16_t* a1[1] = {X};
+  return launch_impl<true>(n_shards, gate_shards, up_shards, d_ff, d_model, 1, a1, m_tokens, nullptr, H, 1.0f, st,
                            "fsdp_mlp_forward");
 }
 

@@ -101,11 +101,18 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
   if (e == cudaSuccess) e = launch_transpose_cat(ap, n_ranks, m_tokens, k_in, xt, st);
   if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
 
-  // dX_q [M, K] = dY_q [M, R] * (W^T [K, R])^T
+  // dX_q [M, K] = dY_q [M, R] * (W^T [K, R])^T for every rank: one launch over all ranks'
+  // rows when each rank's M is a whole number of 128-row tiles, else one launch per rank
   const uint16_t* wt1[1] = {wt};
-  for (int q = 0; q < n_ranks; ++q) {
-    int rc = launch_fsdp_gemm(1, wt1, k_in, rows_out, dY[q], m_tokens, dX[q], nullptr, 1.0f, st);
+  if (m_tokens % 128 == 0 && n_ranks <= 16) {
+    int rc = launch_fsdp_gemm_row_split(n_ranks, reinterpret_cast<const uint16_t* const*>(dY), dX, m_tokens, wt,
+                                        k_in, rows_out, 1.0f, st);
     if (rc) return rc;
+  } else {
+    for (int q = 0; q < n_ranks; ++q) {
+      int rc = launch_fsdp_gemm(1, wt1, k_in, rows_out, dY[q], m_tokens, dX[q], nullptr, 1.0f, st);
+      if (rc) return rc;
+    }
   }
   // dW [R, K] = (1/N) dY^T [R, NM] * (X^T [K, NM])^T
   const uint16_t* xt1[1] = {xt};

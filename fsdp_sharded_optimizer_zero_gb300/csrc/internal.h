@@ -63,6 +63,10 @@ cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int6
 // each (n_ranks = 1 with the full W for the materialised path). Both operands K-major.
 int launch_fsdp_gemm(int n_ranks, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
                      const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st);
+// Y_s[rows_per_shard, R] = alpha * A_s W^T for s < a_shards in ONE persistent launch
+// (rows_per_shard % 128 == 0, a_shards <= 16, R % 4 == 0, 16-byte-aligned Y_s).
+int launch_fsdp_gemm_row_split(int a_shards, const uint16_t* const* A, float* const* Y, int64_t rows_per_shard,
+                               const uint16_t* W, int64_t rows_out, int64_t k_in, float alpha, cudaStream_t st);
 // H[M, d_ff] (bf16) = silu(X W_gate^T) * (X W_up^T), gate and up given as n_ranks row
 // shards each (d_ff / n_ranks rows, a multiple of 128, or n_ranks = 1 with full weights).
 int launch_fsdp_gate_up(int n_ranks, const uint16_t* const* gate_shards, const uint16_t* const* up_shards,

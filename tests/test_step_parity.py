@@ -165,7 +165,8 @@ def test_tiny_zero2_vs_ddp_workload(z):
 
 
 CASES = [(1, 1, 2), (7, 2, 4), (13, 3, 6), (1000, 8, 48), (100_003, 5, 1 << 12), (65_539, 16, 1 << 14),
-         (20_001, 64, 1 << 10), (262_147, 4, 1 << 16)]
+         (20_001, 64, 1 << 10), (262_147, 4, 1 << 16),
+         (5, 64, 128)]  # psi < N: 59 of the 64 one-element shards are padding
 
 
 @pytest.mark.parametrize("psi,n,bb", CASES)
