@@ -1,5 +1,6 @@
 // Device-side helpers shared by the library's kernels: bf16 widening / rounding, the
-// per-element Adam update, and thin PTX wrappers (mbarrier, bulk copies, timer).
+// per-element Adam update, and thin PTX wrappers (mbarrier, bulk copies, timer). Streaming
+// global accesses use the __ldcs / __stcs intrinsics (each byte is touched once per step).
 //
 // Every arithmetic step of the update uses an explicit round-to-nearest intrinsic
 // (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn): the compiler never contracts these into
@@ -63,34 +64,6 @@ __device__ __forceinline__ void adam_elem(float g, float& w, float& m, float& v,
   w = x;
   m = m1;
   v = v1;
-}
-
-// ------------------------------------------------------------------------------------
-// streaming global loads / stores (each byte is touched once per step)
-// ------------------------------------------------------------------------------------
-__device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.cs.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ float4 ld_stream_f4(const float* p) {
-  float4 r;
-  asm volatile("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
-  asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
-}
-__device__ __forceinline__ void st_stream_u2(void* p, uint2 v) {
-  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
-}
-__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
 // ------------------------------------------------------------------------------------

@@ -18,7 +18,7 @@ So the reduction and Adam run in float32 here, one IEEE-rounded numpy operation 
 arithmetic step, in the order written below (numpy never fuses a multiply into an add).
 The FSDP linear reference is computed in float64 and rounded once.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent (the same readings the CUDA library's header states):
   * reduced gradient = (((g_0 + g_1) + g_2) + ... + g_{N-1}) in fp32, rank order, then
     multiplied by f32(1/N); it stays fp32 (never rounded to bf16).
   * Adam = Kingma & Ba with bias correction, eps outside the square root, decoupled weight
