@@ -118,3 +118,38 @@ def test_step_calls_reject_missing_rank_before_launch(z):
     buf = np.zeros(1024, np.uint16)
     hosts = (C.c_void_p * 4)(*([buf.ctypes.data] * 4))
     assert lib.zero_fused_step_host(p.handle, -2, hosts, 256, 512, 768, buf.ctypes.data, C.byref(adam), 1, None) == -1
+
+
+def test_newer_entry_points_reject_bad_arguments_before_launch(z):
+    """fp32-gradient step, FSDP backward, MLP unit, static-scratch forward and the self-test:
+    argument errors come back as ZERO_ERR_INVALID_ARG with nothing launched."""
+    lib = z.library()
+    adam = z._lib.zero_adam(1e-4, 0.9, 0.999, 1e-8, 0.0)
+    p = z.zero_plan(1024, 4, "megatron", 1 << 20)
+    assert p.state_total_bytes == 6 * 1024 + 12 * 256
+    grads = (C.c_void_p * 4)(16, 32, None, 64)
+    assert lib.zero_fused_step_fp32_grads(p.handle, 0, grads, 256, 512, 768, 1024, C.byref(adam), 1, None) == -1
+    assert b"grads[2] is NULL" in lib.zero_last_error()
+    good = (C.c_void_p * 4)(16, 32, 48, 64)
+    assert lib.zero_fused_step_fp32_grads(p.handle, 4, good, 256, 512, 768, 1024, C.byref(adam), 1, None) == -1
+    # backward: rows % N, K % 8, workspace size, NULL rank pointer
+    ws = C.c_uint64()
+    assert lib.fsdp_unit_backward_workspace(4, 512, 256, 128, C.byref(ws)) == 0
+    assert ws.value == 2 * 512 * 256 + 2 * 512 * 512 + 2 * 256 * 512
+    assert lib.fsdp_unit_backward_workspace(0, 512, 256, 128, C.byref(ws)) == -1
+    args = lambda rows, k, m, wsb: (4, good, rows, k, good, good, m, good, 4096, 8192, wsb, None)
+    assert lib.fsdp_unit_backward(*args(510, 256, 128, 1 << 30)) == -1
+    assert lib.fsdp_unit_backward(*args(512, 252, 128, 1 << 30)) == -1
+    assert lib.fsdp_unit_backward(*args(512, 256, 128, 100)) == -1
+    assert b"workspace" in lib.zero_last_error()
+    assert lib.fsdp_unit_backward(4, grads, 512, 256, good, good, 128, good, 4096, 8192, 1 << 30, None) == -1
+    # MLP unit: d_model / d_ff multiples of N and of 8, aligned buffers
+    assert lib.fsdp_mlp_forward(4, good, good, good, 4096, 14330, 4096, 8, 4096, 4096, None, None, None) == -1
+    assert lib.fsdp_mlp_forward(4, good, good, grads, 4096, 14336, 4096, 8, 4096, 4096, None, None, None) == -1
+    assert lib.fsdp_mlp_forward(4, good, good, good, 4096, 14336, 4097, 8, 4096, 4096, None, None, None) == -1
+    # static scratch: weights above 8,388,608 elements
+    assert lib.fsdp_unit_forward_static_scratch(2, good, 4096, 4104, 4096, 128, 8192, None, None) == -1
+    assert b"static scratch" in lib.zero_last_error()
+    # self-test limit
+    assert lib.zero_selftest_bounded_wait(0, None) == -1
+    assert lib.zero_selftest_bounded_wait(5000, None) == -1
