@@ -626,13 +626,26 @@ def run_case(args):
         out.update(params_per_step=L, n_ranks=n, ms=ms, bytes=byts, gbs=byts / ms / 1e6,
                    frac=byts / ms / 1e6 / hbm_peak, params_per_s=L / ms * 1e3,
                    l2_resident=byts < 129e6)
-    elif args.case == "gemm_small":
-        M, R, K, n = 2048, 14336, 4096, 8
+    elif args.case in ("gemm_small", "gemm_w_up"):
+        # gemm_small: 2048 tokens; gemm_w_up: the full Mistral W_up shape, 8192 tokens
+        # (X 64 MB, W 117 MB in 8 row shards, Y 470 MB fp32: under 1 GB on the device)
+        M, R, K, n = (2048 if args.case == "gemm_small" else 8192), 14336, 4096, 8
         X = synth.activations(M, K, device=dev)
         shards = synth.weight_shards(R, K, n, device=dev)
         Y = torch.empty(M, R, device=dev)
         ms = time_launches(lambda: z.fsdp_unit_forward(shards, X, Y, stream=stream), 4, stream)
         out.update(M=M, R=R, K=K, ms=ms, tflops=2.0 * M * R * K / ms / 1e9)
+    elif args.case == "mlp_unit":
+        # Mistral MLP unit at 8192 tokens: gate-up kernel (silu epilogue) + down GEMM
+        M, n = 8192, 8
+        X = synth.activations(M, 4096, device=dev)
+        gs = synth.weight_shards(14336, 4096, n, device=dev, seed_key=1)
+        us = synth.weight_shards(14336, 4096, n, device=dev, seed_key=2)
+        ds = synth.weight_shards(4096, 14336, n, device=dev, seed_key=3)
+        H = torch.empty(M, 14336, dtype=torch.bfloat16, device=dev)
+        Y = torch.empty(M, 4096, device=dev)
+        ms = time_launches(lambda: z.fsdp_mlp_forward(gs, us, ds, X, H, Y, stream=stream), 4, stream)
+        out.update(M=M, ms=ms, tflops=3 * 2.0 * M * 14336 * 4096 / ms / 1e9)
     else:
         raise SystemExit(f"unknown case {args.case}")
     z.zero_device_status(stream)
@@ -642,7 +655,8 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="one measured case: fused_small | gemm_small (ncu-sized) | tiny | mistral_rank_view")
+                    help="one measured case: fused_small | gemm_small | gemm_w_up | mlp_unit (ncu-sized) | tiny | "
+                         "mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
