@@ -404,6 +404,18 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         res["roofline"] = {"bound": "tensor", "achieved": res["tflops"], "peak": tf_peak, "unit": "TFLOP/s",
                            "frac": res["tflops"] / tf_peak,
                            "peak_source": f"{peak_src} bf16_tflops (burst)" if peak_src == "measured" else "fallback"}
+        # row a6 on its own: the materialised all-gather of W_up's 8 row shards (4 B per
+        # element) and the backward's transpose of the same shards into W^T (4 B per element)
+        hbm = peaks()[0]
+        shards_up = synth.weight_shards(14336, 4096, n, device=dev, seed_key=11)
+        wfull = torch.empty(14336, 4096, dtype=torch.bfloat16, device=dev)
+        ms_g = time_launches(lambda: z.fsdp_gather_rows(shards_up, wfull, stream=stream), 20, stream)
+        ms_t = time_launches(lambda: z.fsdp_transpose_cat(shards_up, wfull.view(4096, 14336), stream=stream), 20,
+                             stream)
+        b_gt = 4.0 * 14336 * 4096
+        res["gather_rows_w_up"] = {"ms": ms_g, "gbs": b_gt / ms_g / 1e6, "frac": b_gt / ms_g / 1e6 / hbm}
+        res["transpose_cat_w_up"] = {"ms": ms_t, "gbs": b_gt / ms_t / 1e6, "frac": b_gt / ms_t / 1e6 / hbm}
+        del shards_up, wfull
         # the full MLP unit: gate + up in one kernel with the SiLU-gate epilogue, then down
         gs_ = synth.weight_shards(14336, 4096, n, device=dev, seed_key=12)
         us_ = synth.weight_shards(14336, 4096, n, device=dev, seed_key=11)

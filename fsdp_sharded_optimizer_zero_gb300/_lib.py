@@ -33,7 +33,7 @@ EXPORTS = (
     "zero_plan", "zero_plan_query", "zero_bucket_range", "zero_plan_destroy",
     "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_host", "zero_fused_step_fp32_grads",
     "zero_fused_step_buckets", "zero_allgather_params", "ddp_allreduce",
-    "fsdp_gather_rows", "fsdp_unit_forward", "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward",
+    "fsdp_gather_rows", "fsdp_unit_forward", "fsdp_transpose_cat", "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward",
     "fsdp_unit_forward_static_scratch",
     "zero_last_error", "zero_device_status", "zero_selftest_bounded_wait", "zero_set_fused_kernel", "zero_version",
 )
@@ -88,6 +88,7 @@ def _load():
         "fsdp_gather_rows": (I, [I, PP, I64, I64, VP, VP]),
         "fsdp_unit_forward": (I, [I, PP, I64, I64, VP, I64, VP, VP, VP, VP]),
         "fsdp_unit_forward_static_scratch": (I, [I, PP, I64, I64, VP, I64, VP, VP, VP]),
+        "fsdp_transpose_cat": (I, [I, PP, I64, I64, VP, VP]),
         "fsdp_unit_backward_workspace": (I, [I, I64, I64, I64, C.POINTER(U64)]),
         "fsdp_unit_backward": (I, [I, PP, I64, I64, PP, PP, I64, PP, VP, VP, U64, VP]),
         "fsdp_mlp_forward": (I, [I, PP, PP, PP, I64, I64, VP, I64, VP, VP, VP, VP, VP]),
@@ -278,6 +279,13 @@ def fsdp_unit_forward(w_shards, A, Y, Y_bf16=None, scratch_w=None, stream=None):
                                   _dev(A, torch.bfloat16, "A"), m_tok, _dev(Y, torch.float32, "Y"),
                                   _dev(Y_bf16, torch.bfloat16, "Y_bf16"),
                                   _dev(scratch_w, torch.bfloat16, "scratch_w"), _stream(stream)))
+
+
+def fsdp_transpose_cat(srcs, dst, stream=None):
+    """dst [cols, n*rows] = the n row-major [rows, cols] bf16 sources transposed side by side."""
+    rows, cols = int(srcs[0].shape[0]), int(srcs[0].shape[1])
+    _check(_lib.fsdp_transpose_cat(len(srcs), _ptr_array(srcs, torch.bfloat16, "srcs"), rows, cols,
+                                   _dev(dst, torch.bfloat16, "dst"), _stream(stream)))
 
 
 def fsdp_unit_backward_workspace(n_ranks: int, rows_out: int, k_in: int, m_tokens: int) -> int:

@@ -45,6 +45,24 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
+extern "C" int fsdp_transpose_cat(int n_srcs, const zero_bf16* const srcs[], int64_t rows, int64_t cols,
+                                  zero_bf16* dst, zero_stream_t stream) {
+  const char* who = "fsdp_transpose_cat";
+  if (n_srcs < 1 || n_srcs > ZERO_MAX_RANKS)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: n_srcs %d outside 1..%d", who, n_srcs, ZERO_MAX_RANKS);
+  if (rows < 1 || cols < 1) return set_error(ZERO_ERR_INVALID_ARG, "%s: rows and cols must be >= 1", who);
+  if (!srcs || !dst) return set_error(ZERO_ERR_INVALID_ARG, "%s: NULL argument", who);
+  GradPtrs sp;
+  memset(&sp, 0, sizeof(sp));
+  for (int q = 0; q < n_srcs; ++q) {
+    if (!srcs[q]) return set_error(ZERO_ERR_INVALID_ARG, "%s: srcs[%d] is NULL", who, q);
+    sp.p[q] = srcs[q];
+  }
+  cudaError_t e = launch_transpose_cat(sp, n_srcs, rows, cols, dst, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+  return ZERO_OK;
+}
+
 extern "C" int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t k_in, int64_t m_tokens,
                                             uint64_t* bytes) {
   if (!bytes) return set_error(ZERO_ERR_INVALID_ARG, "fsdp_unit_backward_workspace: bytes is NULL");

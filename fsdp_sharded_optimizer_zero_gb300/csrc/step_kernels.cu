@@ -125,11 +125,27 @@ __global__ void __launch_bounds__(kThreads) allgather_kernel(MasterPtrs mp, int 
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) gather_rows_kernel(GradPtrs shards, int n, uint64_t shard_elems,
                                                                uint16_t* __restrict__ full, int vec) {
-  if (vec) {  // shard_elems % 8 == 0 and 16-byte aligned: 16-byte units
+  if (vec) {  // shard_elems % 8 == 0 and 16-byte aligned: 16-byte units, 4 in flight per thread
     const uint64_t upr = shard_elems / 8, total = upr * static_cast<uint64_t>(n);
-    for (uint64_t u = blockIdx.x * (uint64_t)kThreads + threadIdx.x; u < total; u += (uint64_t)gridDim.x * kThreads) {
-      const uint64_t r = u / upr, i = (u - r * upr) * 8;
-      __stcs(reinterpret_cast<uint4*>(full + r * shard_elems + i), __ldcs(reinterpret_cast<const uint4*>(shards.p[r] + i)));
+    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+    for (uint64_t u0 = blockIdx.x * (uint64_t)kThreads + threadIdx.x; u0 < total; u0 += 4 * stride) {
+      uint4 x[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t u = u0 + k * stride;
+        if (u < total) {
+          const uint64_t r = u / upr, i = (u - r * upr) * 8;
+          x[k] = __ldcs(reinterpret_cast<const uint4*>(shards.p[r] + i));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t u = u0 + k * stride;
+        if (u < total) {
+          const uint64_t r = u / upr, i = (u - r * upr) * 8;
+          __stcs(reinterpret_cast<uint4*>(full + r * shard_elems + i), x[k]);
+        }
+      }
     }
   } else {
     const uint64_t total = shard_elems * static_cast<uint64_t>(n);
@@ -177,21 +193,27 @@ __global__ void __launch_bounds__(256) transpose_cat_kernel(GradPtrs srcs, int64
     }
   }
   __syncthreads();
+  {
+    // each thread builds two output rows (source columns cc, cc+1) x 8 output columns
+    // (source rows rv..rv+7): eight 32-bit reads of (tile[row][cc], tile[row][cc+1]),
+    // split into the two rows with byte permutes
+    const int cc = (t >> 3) * 2, rv = (t & 7) * 8;
+    uint32_t w[8];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int v = t + i * 256, cc = v >> 3, rv = (v & 7) * 8;
-    const int64_t dc = c0 + cc;
-    if (dc >= cols) continue;
-    uint16_t* out = dst + dc * total_rows + r0 + rv;
-    if (vec && r0 + rv + 8 <= total_rows) {
-      uint32_t w[4];
+    for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint32_t*>(&tile[rv + j][cc]);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        w[j] = static_cast<uint32_t>(tile[rv + 2 * j][cc]) | (static_cast<uint32_t>(tile[rv + 2 * j + 1][cc]) << 16);
-      __stcs(reinterpret_cast<uint4*>(out), make_uint4(w[0], w[1], w[2], w[3]));
-    } else {
-      for (int j = 0; j < 8; ++j)
-        if (r0 + rv + j < total_rows) out[j] = tile[rv + j][cc];
+    for (int h = 0; h < 2; ++h) {
+      const int64_t dc = c0 + cc + h;
+      if (dc >= cols) continue;
+      uint16_t* out = dst + dc * total_rows + r0 + rv;
+      const uint32_t sel = h ? 0x7632u : 0x5410u;  // high or low halves of two words
+      if (vec && r0 + rv + 8 <= total_rows) {
+        __stcs(reinterpret_cast<uint4*>(out), make_uint4(__byte_perm(w[0], w[1], sel), __byte_perm(w[2], w[3], sel),
+                                                         __byte_perm(w[4], w[5], sel), __byte_perm(w[6], w[7], sel)));
+      } else {
+        for (int j = 0; j < 8; ++j)
+          if (r0 + rv + j < total_rows) out[j] = static_cast<uint16_t>(h ? (w[j] >> 16) : (w[j] & 0xffffu));
+      }
     }
   }
   }

@@ -249,6 +249,15 @@ ZERO_API int fsdp_unit_forward(int n_ranks, const zero_bf16* const w_shards[], i
                       const zero_bf16* A, int64_t m_tokens, float* Y, zero_bf16* Y_bf16, zero_bf16* scratch_w,
                       zero_stream_t stream);
 
+/* The backward's operand layout step, as a call of its own: dst[c][q*rows + r] =
+ * srcs[q][r][c] for q < n_srcs — the n_srcs row-major [rows, cols] bf16 sources
+ * transposed and concatenated into one row-major [cols, n_srcs*rows] bf16 buffer (W^T
+ * from W's row shards is the backward all-gather of [Interview] follow-up "手写 FSDP 的一层
+ * linear"; the ranks' dY^T and X^T are the operands of the reduced dW). Any alignment;
+ * 16-byte-aligned buffers with cols and n_srcs*rows multiples of 8 take 16-byte accesses. */
+ZERO_API int fsdp_transpose_cat(int n_srcs, const zero_bf16* const srcs[], int64_t rows, int64_t cols, zero_bf16* dst,
+                                zero_stream_t stream);
+
 /* Bytes of device workspace fsdp_unit_backward needs: W^T (2*R*K), dY^T (2*R*N*M) and
  * X^T (2*K*N*M), each rounded up to 256 bytes. */
 ZERO_API int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t k_in, int64_t m_tokens,

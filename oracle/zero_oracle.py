@@ -485,3 +485,10 @@ def mlp_unit_forward(x_bf16, gate_shards, up_shards, down_shards=None, h_bf16=No
         hin = h if h_bf16 is None else bf16_to_f32(h_bf16).astype(np.float64)
         y = hin @ bf16_to_f32(gather_rows(down_shards)).astype(np.float64).T
     return g, u, h, y
+
+
+def transpose_cat(srcs) -> np.ndarray:
+    """The FSDP backward's operand layout: dst[c][q*rows + r] = srcs[q][r][c] — the sources
+    transposed and placed side by side (W^T from W's row shards is the backward all-gather,
+    [Interview] follow-up on a hand-written FSDP linear). A bit copy."""
+    return np.concatenate([np.asarray(s).T for s in srcs], axis=1)

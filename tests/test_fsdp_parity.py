@@ -158,6 +158,19 @@ def test_mistral_mlp_unit_sampled(z):
         del shards, Y, w_full
 
 
+@pytest.mark.parametrize("n,rows,cols,misalign", [(8, 1792, 512, False), (3, 70, 130, False), (2, 64, 64, True),
+                                                  (1, 1, 9, False), (4, 129, 8, False)])
+def test_transpose_cat_bit_exact(z, n, rows, cols, misalign):
+    srcs = synth.weight_shards(n * rows, cols, n, device=DEV, seed_key=rows)
+    if misalign:
+        dst = torch.zeros(cols * n * rows + 1, dtype=torch.bfloat16, device=DEV)[1:].view(cols, n * rows)
+    else:
+        dst = torch.zeros(cols, n * rows, dtype=torch.bfloat16, device=DEV)
+    z.fsdp_transpose_cat(srcs, dst)
+    z.zero_device_status()
+    assert_bf16_identical(bits16(dst), O.transpose_cat([bits16(s) for s in srcs]), "transpose_cat")
+
+
 # ---------------------------------------------------------------------------------------
 # FSDP unit backward: dX_q = dY_q W for every rank, dW = (1/N) sum_q dY_q^T X_q
 # ---------------------------------------------------------------------------------------

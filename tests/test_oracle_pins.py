@@ -489,6 +489,19 @@ def test_fsdp_linear_backward_bruteforce():
             assert dw[j, q] == pytest.approx(sum(float(dyf[i, j]) * float(af[i, q]) for i in range(m)), rel=1e-14)
 
 
+def test_transpose_cat_bruteforce():
+    rng = np.random.default_rng(17)
+    srcs = [rng.integers(0, 65535, (3, 5)).astype(np.uint16) for _ in range(4)]
+    dst = O.transpose_cat(srcs)
+    assert dst.shape == (5, 12)
+    for q in range(4):
+        for r in range(3):
+            for c in range(5):
+                assert dst[c, q * 3 + r] == srcs[q][r, c]
+    # W^T from row shards equals the transpose of the gathered W
+    assert np.array_equal(O.transpose_cat(srcs), O.gather_rows(srcs).T)
+
+
 def test_reduce_rows_matches_elementwise_reduction():
     rng = np.random.default_rng(8)
     n, rows, k = 4, 8, 5
