@@ -163,59 +163,70 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(GradPtrs shards, 
 // dY^T and X^T whose product sums the ranks' weight gradients inside one GEMM. 64 x 64
 // tiles through shared memory; 16-byte loads and stores when rows and columns allow.
 // ------------------------------------------------------------------------------------
-constexpr int kTT = 64;
+#ifndef ZGB_TT_R
+#define ZGB_TT_R 64
+#endif
+#ifndef ZGB_TT_C
+#define ZGB_TT_C 64
+#endif
+constexpr int kTR = ZGB_TT_R;  // tile rows (source rows = output columns)
+constexpr int kTC = ZGB_TT_C;  // tile columns (source columns = output rows)
+static_assert(kTR % 8 == 0 && kTC % 16 == 0, "tile shape");
 
 __global__ void __launch_bounds__(256) transpose_cat_kernel(GradPtrs srcs, int64_t rows, int64_t cols,
                                                             int64_t total_rows, uint16_t* __restrict__ dst, int vec) {
-  __shared__ uint16_t tile[kTT][kTT + 2];
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTT;
+  __shared__ uint16_t tile[kTR][kTC + 2];
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTC;
   const int t = threadIdx.x;
-  const int64_t row_tiles = (total_rows + kTT - 1) / kTT;
+  const int64_t row_tiles = (total_rows + kTR - 1) / kTR;
   for (int64_t ty = blockIdx.y; ty < row_tiles; ty += gridDim.y) {
-  const int64_t r0 = ty * kTT;
-  __syncthreads();  // the previous row tile's reads of `tile` are done
+    const int64_t r0 = ty * kTR;
+    __syncthreads();  // the previous row tile's reads of `tile` are done
+    // load: kTR rows of kTC columns, 16 bytes per thread-iteration
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int v = t + i * 256, rr = v >> 3, cv = (v & 7) * 8;
-    const int64_t gr = r0 + rr;
-    if (gr >= total_rows) continue;
-    const int64_t q = gr / rows, lr = gr - q * rows;
-    const uint16_t* src = srcs.p[q] + lr * cols + c0 + cv;
-    if (vec && c0 + cv + 8 <= cols) {
-      const uint4 u = __ldcs(reinterpret_cast<const uint4*>(src));
-      uint32_t* trow = reinterpret_cast<uint32_t*>(&tile[rr][cv]);
-      trow[0] = u.x;
-      trow[1] = u.y;
-      trow[2] = u.z;
-      trow[3] = u.w;
-    } else {
-      for (int j = 0; j < 8; ++j) tile[rr][cv + j] = (c0 + cv + j < cols) ? src[j] : uint16_t(0);
-    }
-  }
-  __syncthreads();
-  {
-    // each thread builds two output rows (source columns cc, cc+1) x 8 output columns
-    // (source rows rv..rv+7): eight 32-bit reads of (tile[row][cc], tile[row][cc+1]),
-    // split into the two rows with byte permutes
-    const int cc = (t >> 3) * 2, rv = (t & 7) * 8;
-    uint32_t w[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint32_t*>(&tile[rv + j][cc]);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t dc = c0 + cc + h;
-      if (dc >= cols) continue;
-      uint16_t* out = dst + dc * total_rows + r0 + rv;
-      const uint32_t sel = h ? 0x7632u : 0x5410u;  // high or low halves of two words
-      if (vec && r0 + rv + 8 <= total_rows) {
-        __stcs(reinterpret_cast<uint4*>(out), make_uint4(__byte_perm(w[0], w[1], sel), __byte_perm(w[2], w[3], sel),
-                                                         __byte_perm(w[4], w[5], sel), __byte_perm(w[6], w[7], sel)));
+    for (int v = t; v < kTR * kTC / 8; v += 256) {
+      const int rr = v / (kTC / 8), cv = (v % (kTC / 8)) * 8;
+      const int64_t gr = r0 + rr;
+      if (gr >= total_rows) continue;
+      const int64_t q = gr / rows, lr = gr - q * rows;
+      const uint16_t* src = srcs.p[q] + lr * cols + c0 + cv;
+      if (vec && c0 + cv + 8 <= cols) {
+        const uint4 u = __ldcs(reinterpret_cast<const uint4*>(src));
+        uint32_t* trow = reinterpret_cast<uint32_t*>(&tile[rr][cv]);
+        trow[0] = u.x;
+        trow[1] = u.y;
+        trow[2] = u.z;
+        trow[3] = u.w;
       } else {
-        for (int j = 0; j < 8; ++j)
-          if (r0 + rv + j < total_rows) out[j] = static_cast<uint16_t>(h ? (w[j] >> 16) : (w[j] & 0xffffu));
+        for (int j = 0; j < 8; ++j) tile[rr][cv + j] = (c0 + cv + j < cols) ? src[j] : uint16_t(0);
       }
     }
-  }
+    __syncthreads();
+    // store: each thread-iteration builds two output rows (source columns cc, cc+1) x 8
+    // output columns (source rows rv..rv+7) from eight 32-bit reads of (tile[row][cc],
+    // tile[row][cc+1]), split into the two rows with byte permutes
+#pragma unroll
+    for (int u = t; u < kTR * kTC / 16; u += 256) {
+      const int cc = (u / (kTR / 8)) * 2, rv = (u % (kTR / 8)) * 8;
+      uint32_t w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint32_t*>(&tile[rv + j][cc]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t dc = c0 + cc + h;
+        if (dc >= cols) continue;
+        uint16_t* out = dst + dc * total_rows + r0 + rv;
+        const uint32_t sel = h ? 0x7632u : 0x5410u;  // high or low halves of two words
+        if (vec && r0 + rv + 8 <= total_rows) {
+          __stcs(reinterpret_cast<uint4*>(out),
+                 make_uint4(__byte_perm(w[0], w[1], sel), __byte_perm(w[2], w[3], sel), __byte_perm(w[4], w[5], sel),
+                            __byte_perm(w[6], w[7], sel)));
+        } else {
+          for (int j = 0; j < 8; ++j)
+            if (r0 + rv + j < total_rows) out[j] = static_cast<uint16_t>(h ? (w[j] >> 16) : (w[j] & 0xffffu));
+        }
+      }
+    }
   }
 }
 
@@ -284,7 +295,7 @@ cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int6
   if (total_rows == 0 || cols == 0) return cudaSuccess;
   bool vec = cols % 8 == 0 && total_rows % 8 == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
   for (int q = 0; q < n; ++q) vec = vec && (reinterpret_cast<uintptr_t>(srcs.p[q]) & 15) == 0;
-  const int64_t gy = std::min<int64_t>((total_rows + kTT - 1) / kTT, 65535), gx = (cols + kTT - 1) / kTT;
+  const int64_t gy = std::min<int64_t>((total_rows + kTR - 1) / kTR, 65535), gx = (cols + kTC - 1) / kTC;
   if (gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
   transpose_cat_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(
       srcs, rows, cols, total_rows, dst, vec ? 1 : 0);
