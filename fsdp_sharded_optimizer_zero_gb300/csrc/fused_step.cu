@@ -30,7 +30,8 @@ __global__ void __launch_bounds__(kThreads) fused_vec_kernel(RankPtrs<G> gp, int
                                                              uint16_t* __restrict__ param, Domain d,
                                                              AdamScalars sc) {
   const uint64_t ups = (d.seg_len + 3) / 4, total = ups * d.n_seg;
-  for (uint64_t u = blockIdx.x * (uint64_t)kThreads + threadIdx.x; u < total; u += (uint64_t)gridDim.x * kThreads) {
+  const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+  for (uint64_t u = blockIdx.x * (uint64_t)kThreads + threadIdx.x; u < total; u += stride) {
     const UnitPos p = unit_pos(d, ups, u);
     if (p.count == 4) {
       const float4 w = __ldcs(reinterpret_cast<const float4*>(master + p.base));
@@ -44,6 +45,13 @@ __global__ void __launch_bounds__(kThreads) fused_vec_kernel(RankPtrs<G> gp, int
     }
   }
 }
+
+// Blocks per SM of the register-streaming kernel's grid on long launches. With 40
+// registers per thread six 256-thread blocks fit on an SM, but on GB300 four held the
+// highest share of the copy bandwidth for N = 1, 2, 8, 12, 16, 32, 64 and both gradient
+// types; one full wave (six per SM) or several waves of the full grid lost 2-8 %. N = 4
+// showed no grid that won on every domain shape, so it keeps the full grid.
+inline unsigned int fused_vec_blocks_per_sm(int n) { return n == 4 ? 16u : 4u; }
 
 // scalar variant for buffers whose alignment rules out vector accesses
 template <typename G>
@@ -234,7 +242,7 @@ cudaError_t launch_fused(const GradPtrs& gp, int n, float* master, float* m, flo
     return cudaGetLastError();
   }
   if (variant == 2) {
-    const unsigned int grid = grid_for((d.seg_len + 3) / 4 * d.n_seg);
+    const unsigned int grid = grid_streaming((d.seg_len + 3) / 4 * d.n_seg, fused_vec_blocks_per_sm(n));
     return dispatch_nr(n, [&](auto nr) {
       fused_vec_kernel<decltype(nr)::value, uint16_t><<<grid, kThreads, 0, st>>>(gp, n, master, m, v, param, d, sc);
       return cudaGetLastError();
@@ -249,7 +257,7 @@ cudaError_t launch_fused_f32g(const F32GradPtrs& gp, int n, float* master, float
   const uint64_t total = d.seg_len * d.n_seg;
   if (total == 0) return cudaSuccess;
   if (variant == 2) {
-    const unsigned int grid = grid_for((d.seg_len + 3) / 4 * d.n_seg);
+    const unsigned int grid = grid_streaming((d.seg_len + 3) / 4 * d.n_seg, fused_vec_blocks_per_sm(n));
     return dispatch_nr(n, [&](auto nr) {
       fused_vec_kernel<decltype(nr)::value, float><<<grid, kThreads, 0, st>>>(gp, n, master, m, v, param, d, sc);
       return cudaGetLastError();

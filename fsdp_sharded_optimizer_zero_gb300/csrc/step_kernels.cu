@@ -244,6 +244,15 @@ __global__ void wait_selftest_kernel(unsigned long long timeout_ns) {
   if (threadIdx.x == 0) mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, &g_zgb_dev_error, kErrSelftest, timeout_ns);
 }
 
+// Blocks per SM of the vector reduce and Adam grids on long launches, measured on GB300. A thread of the
+// reduce keeps 8 B of gradient loads per rank in flight (all N ranks for N = 1, 2, 4, 8,
+// 16; eight at a time otherwise): from 64 B (N >= 8) four blocks per SM held 0.96-1.00
+// of the copy bandwidth where the full grid held 0.89-0.96; at N = 4 (32 B) six did
+// best; with less in flight the full grid is needed to cover the latency. Adam keeps
+// 64 B in flight per thread: four per SM.
+inline unsigned int reduce_blocks_per_sm(int n) { return n >= 8 ? 4u : n >= 4 ? 6u : 16u; }
+constexpr unsigned int kAdamBlocksPerSm = 4;
+
 }  // namespace
 
 cudaError_t launch_reduce(const GradPtrs& gp, int n, float* out, const Domain& d, float inv_n, bool vec,
@@ -254,7 +263,7 @@ cudaError_t launch_reduce(const GradPtrs& gp, int n, float* out, const Domain& d
     reduce_scalar_kernel<<<grid_for(total), kThreads, 0, st>>>(gp, n, out, d, inv_n);
     return cudaGetLastError();
   }
-  const unsigned int grid = grid_for((d.seg_len + 3) / 4 * d.n_seg);
+  const unsigned int grid = grid_streaming((d.seg_len + 3) / 4 * d.n_seg, reduce_blocks_per_sm(n));
   return dispatch_nr(n, [&](auto nr) {
     reduce_vec_kernel<decltype(nr)::value><<<grid, kThreads, 0, st>>>(gp, n, out, d, inv_n);
     return cudaGetLastError();
@@ -266,7 +275,8 @@ cudaError_t launch_adam(const float* g, float* master, float* m, float* v, uint1
   const uint64_t total = d.seg_len * d.n_seg;
   if (total == 0) return cudaSuccess;
   if (vec)
-    adam_vec_kernel<<<grid_for((d.seg_len + 3) / 4 * d.n_seg), kThreads, 0, st>>>(g, master, m, v, param, d, sc);
+    adam_vec_kernel<<<grid_streaming((d.seg_len + 3) / 4 * d.n_seg, kAdamBlocksPerSm), kThreads, 0, st>>>(
+        g, master, m, v, param, d, sc);
   else
     adam_scalar_kernel<<<grid_for(total), kThreads, 0, st>>>(g, master, m, v, param, d, sc);
   return cudaGetLastError();
