@@ -294,9 +294,9 @@ def fsdp_unit_backward_workspace(n_ranks: int, rows_out: int, k_in: int, m_token
     return b.value
 
 
-def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace, stream=None):
+def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace=None, stream=None):
     """A, dY, dX: per-rank lists; dW: [rows_out, k_in] fp32; workspace: a uint8 CUDA tensor
-    of at least fsdp_unit_backward_workspace(...) bytes."""
+    of at least fsdp_unit_backward_workspace(...) bytes (None when that is 0)."""
     n = len(w_shards)
     rows = sum(int(s.shape[0]) for s in w_shards)
     k = int(A[0].shape[1])
@@ -304,7 +304,8 @@ def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace, stream=None):
     _check(_lib.fsdp_unit_backward(
         n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, k, _ptr_array(A, torch.bfloat16, "A"),
         _ptr_array(dY, torch.bfloat16, "dY"), m_tok, _ptr_array(dX, torch.float32, "dX"),
-        _dev(dW, torch.float32, "dW"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+        _dev(dW, torch.float32, "dW"), _dev(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
 def fsdp_mlp_forward(gate_shards, up_shards, down_shards, X, H, Y, scratch_down=None, stream=None,

@@ -39,7 +39,7 @@ namespace {
 #define ZGB_GEMM_STAGES 4
 #endif
 constexpr int BM = 128, BN = ZGB_GEMM_BN, BK = 64, STAGES = ZGB_GEMM_STAGES;
-constexpr int kMaxShards = 16;
+constexpr int kMaxShards = kGemmMaxPieces;
 constexpr int kThreads = 192;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 
@@ -63,18 +63,31 @@ constexpr unsigned int kErrAccE = (2u << 8) | 3u;   // MMA waiting for a drained
 constexpr unsigned int kErrAccF = (2u << 8) | 4u;   // epilogue waiting for a finished tile
 constexpr unsigned int kErrDrain = (2u << 8) | 5u;  // draining after an abort
 
+// Operand layouts. K-major (the default): A is [M, K] and B is [R, K] row-major, A split
+// by rows into a_shards pieces of a_shard_rows rows (Y split the same way), B into
+// n_shards row shards of shard_rows rows. MN-major (a_mn / b_mn): the operand is stored
+// as [K, M] (A) or [K, R] (B) row-major with M (R) a multiple of 64, split along K into
+// pieces of a_shard_rows / shard_rows K rows (multiples of BK); the MMA reads it
+// transposed, so A^T or B^T never has to be materialised. Its tensor map is 3-D, {64
+// columns, K rows, column chunks of 64} with a 128-byte chunk stride, so ONE box of
+// 64 x BK x (BM or TN)/64 lands a whole stage operand as 64-column chunks of BK rows x
+// 128 B, 8 KiB apart: the layout the MN-major descriptor reads. (One 2-D box per chunk
+// took 5-6 TMA operations per stage and left the tensor pipe waiting: 15-46 % slower.)
 struct GemmParams {
-  CUtensorMap a[kMaxShards];     // A row shard s [a_shard_rows, K] bf16, box 64 x 128
-  CUtensorMap w[kMaxShards];     // shard s [shard_rows, K] bf16, box 64 x (256, or 128 in gate-up mode)
+  CUtensorMap a[kMaxShards];     // A piece s: K-major [a_shard_rows, K] box 64 x 128; MN-major [a_shard_rows, M] box 64 x 64
+  CUtensorMap w[kMaxShards];     // B piece s: K-major [shard_rows, K] box 64 x (256, or 128 in gate-up mode); MN-major [shard_rows, R] box 64 x 64
   CUtensorMap w2[kMaxShards];    // gate-up mode: the up projection's shards (w holds the gate's)
   float* y;                      // [M, R] fp32
   uint16_t* yb;                  // [M, R] bf16 or null (gate-up mode: H = silu(gate) * up)
-  CUtensorMap ymap[kMaxShards];  // Y row shard s [a_shard_rows, R] fp32, box 32 x 32, 128B swizzle (y_tma)
+  CUtensorMap ymap[kMaxShards];  // Y row piece s [y_shard_rows, R] fp32, box 32 x 32, 128B swizzle (y_tma)
   float alpha;                   // output scale (1: none)
   int m, r, k, shard_rows, n_shards;
-  int a_shard_rows, a_shards;    // A and Y split by rows into a_shards pieces (1: not split)
+  int a_shard_rows, a_shards;    // pieces of A (rows for K-major, K rows for MN-major)
+  int y_shard_rows;              // Y split by rows into pieces of y_shard_rows rows
+  int a_mn, b_mn;                // operand stored MN-major
   int y_tma;                     // write Y through shared memory and TMA stores
 };
+constexpr uint32_t kMnChunk = 64 * BK * 2;  // one 64-column chunk of an MN-major stage operand: 8 KiB
 
 // Output tile order of the persistent walk: bands of GROUP_M row blocks; inside a band the
 // walk goes down the rows of one column of tiles, then to the next column. The 152 tiles
@@ -227,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
         tile_coords(tile, num_m, num_n, mb, nb);
         const int m0 = mb * BM;
         const int n0 = nb * TN;
-        const int shard = n0 / p.shard_rows;
+        const int shard = p.b_mn ? 0 : n0 / p.shard_rows;
         const int nl = n0 - shard * p.shard_rows;
         const void* wmap = &p.w[shard];
-        const int ash = m0 / p.a_shard_rows;  // the A row shard holding this tile's rows
+        const int ash = p.a_mn ? 0 : m0 / p.a_shard_rows;  // the A row shard holding this tile's rows
         const int ml = m0 - ash * p.a_shard_rows;
         for (int kb = 0; kb < num_k; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -242,8 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
           const uint32_t fb = smem_u32(&full_bar[s]);
           uint8_t* sa = smem + s * STAGE_BYTES;
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          tma_load_2d(smem_u32(sa), &p.a[ash], kb * BK, ml, fb);
-          tma_load_2d(smem_u32(sa + A_BYTES), wmap, kb * BK, nl, fb);
+          if (!GATE_UP && p.a_mn) {  // K rows kb*BK.. of the piece holding them, BM / 64 M chunks
+            const int ks = kb * BK / p.a_shard_rows, kl = kb * BK - ks * p.a_shard_rows;
+            tma_load_3d(smem_u32(sa), &p.a[ks], 0, kl, m0 / 64, fb);
+          } else {
+            tma_load_2d(smem_u32(sa), &p.a[ash], kb * BK, ml, fb);
+          }
+          if (!GATE_UP && p.b_mn) {  // the same for B: TN / 64 chunks of 64 columns
+            const int ks = kb * BK / p.shard_rows, kl = kb * BK - ks * p.shard_rows;
+            tma_load_3d(smem_u32(sa + A_BYTES), &p.w[ks], 0, kl, n0 / 64, fb);
+          } else {
+            tma_load_2d(smem_u32(sa + A_BYTES), wmap, kb * BK, nl, fb);
+          }
           if (GATE_UP) tma_load_2d(smem_u32(sa + A_BYTES + BT_BYTES), &p.w2[shard], kb * BK, nl, fb);
           last_issue[s] = it;
         }
@@ -259,6 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
+      // K-major: the next 16 K columns start 32 bytes further (+2 in the address field);
+      // MN-major: 16 K rows = two 8-row groups further, 2048 bytes (+128)
+      const bool a_mn = !GATE_UP && p.a_mn, b_mn = !GATE_UP && p.b_mn;
+      const uint32_t a_step = a_mn ? 128u : 2u, b_step = b_mn ? 128u : 2u;
+      const uint32_t idesc = idesc_bf16_f32(BM, TN, a_mn, b_mn);
       uint32_t it = 0, i = 0;
       bool stop = false, issued = false;
       for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x, ++i) {
@@ -275,11 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-          const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sa + A_BYTES);
+          const uint64_t ad = a_mn ? sw128_mnmajor_desc(sa, kMnChunk) : sw128_kmajor_desc(sa);
+          const uint64_t bd = b_mn ? sw128_mnmajor_desc(sa + A_BYTES, kMnChunk) : sw128_kmajor_desc(sa + A_BYTES);
           const uint64_t bd2 = sw128_kmajor_desc(sa + A_BYTES + BT_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {  // K = 16 per MMA: +32 bytes = +2 in the address field
-            umma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < BK / 16; ++k) {  // K = 16 per MMA
+            umma_bf16(d, ad + a_step * k, bd + b_step * k, idesc, (kb | k) != 0 ? 1u : 0u);
             if (GATE_UP) umma_bf16(d + TN, ad + 2u * k, bd2 + 2u * k, IDESC, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit(smem_u32(&empty_bar[s]));
@@ -307,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
       const int m0 = mb * BM;
       const int n0 = nb * TN;
       const int row = m0 + row_in_tile;
-      const int ash = m0 / p.a_shard_rows;
-      const int ml = m0 - ash * p.a_shard_rows;
+      const int ash = m0 / p.y_shard_rows;  // the Y row piece holding this tile's rows
+      const int ml = m0 - ash * p.y_shard_rows;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * ACC;
       uint8_t* epi = smem + STAGES * STAGE_BYTES + static_cast<uint32_t>(q) * 2u * 4096u;
       if constexpr (GATE_UP) {
@@ -396,60 +425,106 @@ int encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
   return ZERO_OK;
 }
 
+// MN-major operand [rows, cols] bf16 row-major (cols % 64 == 0) as the 3-D tensor
+// {64, rows, cols / 64}: element (x, y, z) at base + 2 x + y * 2 cols + z * 128 B; box
+// {64, BK, chunks}
+int encode_mn(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t chunks) {
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols * 2, 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BK), chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(ZERO_ERR_CUDA, "fsdp_unit_backward: cuTensorMapEncodeTiled (MN-major) failed (%d)", (int)r);
+  return ZERO_OK;
+}
+
 }  // namespace
 
 namespace {
 
-// a_shards > 1: A and Y are given as a_shards row pieces of m_tokens / a_shards rows each
-// (a multiple of 128, so no output tile straddles two pieces); fp32 Y then goes through
-// TMA stores only and no bf16 copy is written.
+// One GEMM operand given as pieces: K-major pieces split the M (A) or R (B) rows; MN-major
+// pieces ([K rows, M or R columns] row-major) split the K rows. piece_rows: rows of one
+// piece (every piece the same).
+struct Operand {
+  int pieces;
+  const uint16_t* const* ptr;
+  bool mn;
+  int64_t piece_rows;
+};
+
+// Y (y_pieces row pieces) = alpha * A * B^T, M x R, inner dimension K. GATE_UP: B and B2
+// are the gate and up shards (K-major) and Y_bf16 receives H = silu(gate) * up.
 template <bool GATE_UP>
-int launch_impl(int n_shards, const uint16_t* const* w_shards, const uint16_t* const* w2_shards, int64_t rows_out,
-                int64_t k_in, int a_shards, const uint16_t* const* A, int64_t m_tokens, float* const* Y,
-                uint16_t* Y_bf16, float alpha, cudaStream_t st, const char* who) {
+int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, int64_t m_tokens, int64_t rows_out,
+                int64_t k_in, float* const* Y, int y_pieces, uint16_t* Y_bf16, float alpha, cudaStream_t st,
+                const char* who) {
   constexpr int TN = GATE_UP ? 128 : BN;
   if (m_tokens > INT32_MAX / 2 || rows_out > INT32_MAX / 2 || k_in > INT32_MAX / 2)
     return set_error(ZERO_ERR_INVALID_ARG, "%s: sizes must be below 2^30", who);
-  const int64_t a_rows = m_tokens / a_shards;
-  if (a_shards < 1 || a_shards > kMaxShards ||
-      (a_shards > 1 && (m_tokens % a_shards || a_rows % BM || GATE_UP || Y_bf16 || rows_out % 4)))
-    return set_error(ZERO_ERR_UNSUPPORTED, "%s: unsupported row split of A / Y into %d pieces", who, a_shards);
-  const int64_t shard_rows = rows_out / n_shards;
-  if (n_shards > 1 && (shard_rows % TN != 0 || n_shards > kMaxShards))
+  if (A.pieces < 1 || A.pieces > kMaxShards || B.pieces < 1 || B.pieces > kMaxShards || y_pieces < 1 ||
+      y_pieces > kMaxShards)
+    return set_error(ZERO_ERR_UNSUPPORTED, "%s: at most %d pieces per operand", who, kMaxShards);
+  if (GATE_UP && (A.mn || B.mn)) return set_error(ZERO_ERR_UNSUPPORTED, "%s: gate-up mode is K-major only", who);
+  // A and Y pieces
+  if (A.mn) {
+    if (A.piece_rows * A.pieces != k_in || (A.pieces > 1 && A.piece_rows % BK) || m_tokens % 64 || y_pieces != 1)
+      return set_error(ZERO_ERR_UNSUPPORTED, "%s: unsupported split of the MN-major A operand", who);
+  } else {
+    if (A.piece_rows * A.pieces != m_tokens || y_pieces != A.pieces ||
+        (A.pieces > 1 && (A.piece_rows % BM || GATE_UP || Y_bf16 || rows_out % 4)))
+      return set_error(ZERO_ERR_UNSUPPORTED, "%s: unsupported row split of A / Y into %d pieces", who, A.pieces);
+  }
+  if (B.mn) {
+    if (B.piece_rows * B.pieces != k_in || (B.pieces > 1 && B.piece_rows % BK) || rows_out % 64)
+      return set_error(ZERO_ERR_UNSUPPORTED, "%s: unsupported split of the MN-major B operand", who);
+  } else if (B.piece_rows * B.pieces != rows_out || (B.pieces > 1 && B.piece_rows % TN != 0)) {
     return set_error(ZERO_ERR_UNSUPPORTED,
                      "%s: the fused gather needs rows/n_ranks (%lld) to be a multiple of %d and n_ranks <= %d; "
                      "pass a scratch buffer to gather first",
-                     who, (long long)shard_rows, TN, kMaxShards);
+                     who, (long long)B.piece_rows, TN, kMaxShards);
+  }
   int rc = get_encode();
   if (rc) return rc;
   GemmParams p;
   memset(&p, 0, sizeof(p));
-  for (int s = 0; s < a_shards; ++s)
-    if ((rc = encode_2d(&p.a[s], A[s], k_in, a_rows, BK, BM))) return rc;
-  for (int s = 0; s < n_shards; ++s) {
-    if ((rc = encode_2d(&p.w[s], w_shards[s], k_in, shard_rows, BK, TN))) return rc;
-    if (GATE_UP && (rc = encode_2d(&p.w2[s], w2_shards[s], k_in, shard_rows, BK, TN))) return rc;
+  for (int s = 0; s < A.pieces; ++s) {
+    rc = A.mn ? encode_mn(&p.a[s], A.ptr[s], m_tokens, A.piece_rows, BM / 64)
+              : encode_2d(&p.a[s], A.ptr[s], k_in, A.piece_rows, BK, BM);
+    if (rc) return rc;
   }
+  for (int s = 0; s < B.pieces; ++s) {
+    rc = B.mn ? encode_mn(&p.w[s], B.ptr[s], rows_out, B.piece_rows, TN / 64)
+              : encode_2d(&p.w[s], B.ptr[s], k_in, B.piece_rows, BK, TN);
+    if (rc) return rc;
+    if (GATE_UP && (rc = encode_2d(&p.w2[s], B2[s], k_in, B.piece_rows, BK, TN))) return rc;
+  }
+  const int64_t y_rows = m_tokens / y_pieces;
   // fp32 output through TMA stores when its rows are 16-byte multiples (R % 4 == 0)
   bool y_aligned = !GATE_UP && Y != nullptr && rows_out % 4 == 0;
-  for (int s = 0; y_aligned && s < a_shards; ++s) y_aligned = (reinterpret_cast<uintptr_t>(Y[s]) & 15) == 0;
+  for (int s = 0; y_aligned && s < y_pieces; ++s) y_aligned = (reinterpret_cast<uintptr_t>(Y[s]) & 15) == 0;
   if (y_aligned) {
-    for (int s = 0; s < a_shards; ++s)
-      if ((rc = encode_2d(&p.ymap[s], Y[s], rows_out, a_rows, 32, 32, true))) return rc;
+    for (int s = 0; s < y_pieces; ++s)
+      if ((rc = encode_2d(&p.ymap[s], Y[s], rows_out, y_rows, 32, 32, true))) return rc;
     p.y_tma = 1;
-  } else if (a_shards > 1) {
+  } else if (y_pieces > 1) {
     return set_error(ZERO_ERR_UNSUPPORTED, "%s: row-split outputs must be 16-byte aligned", who);
   }
   p.y = Y ? Y[0] : nullptr;
-  p.a_shard_rows = static_cast<int>(a_rows);
-  p.a_shards = a_shards;
+  p.a_shard_rows = static_cast<int>(A.piece_rows);
+  p.a_shards = A.pieces;
+  p.y_shard_rows = static_cast<int>(y_rows);
+  p.a_mn = A.mn ? 1 : 0;
+  p.b_mn = B.mn ? 1 : 0;
   p.yb = Y_bf16;
   p.alpha = alpha;
   p.m = static_cast<int>(m_tokens);
   p.r = static_cast<int>(rows_out);
   p.k = static_cast<int>(k_in);
-  p.shard_rows = static_cast<int>(shard_rows);
-  p.n_shards = n_shards;
+  p.shard_rows = static_cast<int>(B.piece_rows);
+  p.n_shards = B.pieces;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -474,23 +549,40 @@ int launch_fsdp_gemm(int n_shards, const uint16_t* const* w_shards, int64_t rows
                      const uint16_t* A, int64_t m_tokens, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st) {
   const uint16_t* a1[1] = {A};
   float* y1[1] = {Y};
-  return launch_impl<false>(n_shards, w_shards, nullptr, rows_out, k_in, 1, a1, m_tokens, y1, Y_bf16, alpha, st,
-                            "fsdp_unit_forward");
+  return launch_gemm<false>({1, a1, false, m_tokens}, {n_shards, w_shards, false, rows_out / n_shards}, nullptr,
+                            m_tokens, rows_out, k_in, y1, 1, Y_bf16, alpha, st, "fsdp_unit_forward");
 }
 
 int launch_fsdp_gemm_row_split(int a_shards, const uint16_t* const* A, float* const* Y, int64_t rows_per_shard,
                                const uint16_t* W, int64_t rows_out, int64_t k_in, float alpha, cudaStream_t st) {
   const uint16_t* w1[1] = {W};
-  return launch_impl<false>(1, w1, nullptr, rows_out, k_in, a_shards, A, rows_per_shard * a_shards, Y, nullptr, alpha,
-                            st, "fsdp_unit_backward");
+  return launch_gemm<false>({a_shards, A, false, rows_per_shard}, {1, w1, false, rows_out}, nullptr,
+                            rows_per_shard * a_shards, rows_out, k_in, Y, a_shards, nullptr, alpha, st,
+                            "fsdp_unit_backward");
 }
 
 int launch_fsdp_gate_up(int n_shards, const uint16_t* const* gate_shards, const uint16_t* const* up_shards,
                         int64_t d_ff, int64_t d_model, const uint16_t* X, int64_t m_tokens, uint16_t* H,
                         cudaStream_t st) {
   const uint16_t* a1[1] = {X};
-  return launch_impl<true>(n_shards, gate_shards, up_shards, d_ff, d_model, 1, a1, m_tokens, nullptr, H, 1.0f, st,
-                           "fsdp_mlp_forward");
+  return launch_gemm<true>({1, a1, false, m_tokens}, {n_shards, gate_shards, false, d_ff / n_shards}, up_shards,
+                           m_tokens, d_ff, d_model, nullptr, 1, H, 1.0f, st, "fsdp_mlp_forward");
+}
+
+int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces_rows, int dy_pieces,
+                       const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in, float* const* dX,
+                       cudaStream_t st) {
+  return launch_gemm<false>({dy_pieces, dY, false, dy_pieces_rows}, {n_ranks, w_shards, true, rows_out / n_ranks},
+                            nullptr, dy_pieces_rows * dy_pieces, k_in, rows_out, dX, dy_pieces, nullptr, 1.0f, st,
+                            "fsdp_unit_backward");
+}
+
+int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* const* X, int64_t m_tokens,
+                       int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st) {
+  float* y1[1] = {dW};
+  return launch_gemm<false>({n_ranks, dY, true, m_tokens}, {n_ranks, X, true, m_tokens}, nullptr, rows_out, k_in,
+                            m_tokens * n_ranks, y1, 1, nullptr, 1.0f / static_cast<float>(n_ranks), st,
+                            "fsdp_unit_backward");
 }
 
 unsigned int fsdp_gemm_read_clear_error() {

@@ -30,10 +30,19 @@ struct BackwardWorkspace {
   uint64_t wt, dyt, xt, total;  // byte offsets of W^T, dY^T, X^T and the total size
 };
 
+// The backward reads W, dY and X in place (MN-major GEMM operands, no transposes) when
+// every K piece is a whole number of 64-row K blocks (the W shards' R / N rows for dX, each
+// rank's m_tokens rows for dW) and the MN-major operands' rows are whole 64-column chunks
+// (k_in % 64 == 0; R % 64 follows from R / N).
+bool backward_in_place(int n, int64_t rows_out, int64_t k_in, int64_t m_tokens) {
+  return n <= kGemmMaxPieces && (rows_out / n) % 64 == 0 && m_tokens % 64 == 0 && k_in % 64 == 0;
+}
+
 BackwardWorkspace backward_workspace(int n, int64_t rows_out, int64_t k_in, int64_t m_tokens) {
+  BackwardWorkspace w{0, 0, 0, 0};
+  if (backward_in_place(n, rows_out, k_in, m_tokens)) return w;
   const uint64_t R = static_cast<uint64_t>(rows_out), K = static_cast<uint64_t>(k_in);
   const uint64_t NM = static_cast<uint64_t>(n) * static_cast<uint64_t>(m_tokens);
-  BackwardWorkspace w;
   w.wt = 0;
   w.dyt = align256(2 * R * K);
   w.xt = w.dyt + align256(2 * R * NM);
@@ -87,13 +96,12 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
   if (k_in % 8 || rows_out % 8 || nm % 8)
     return set_error(ZERO_ERR_INVALID_ARG,
                      "%s: k_in, rows_out and n_ranks * m_tokens must be multiples of 8 (16-byte GEMM rows)", who);
-  if (!w_shards || !A || !dY || !dX || !dW || !workspace)
-    return set_error(ZERO_ERR_INVALID_ARG, "%s: NULL argument", who);
+  if (!w_shards || !A || !dY || !dX || !dW) return set_error(ZERO_ERR_INVALID_ARG, "%s: NULL argument", who);
   const BackwardWorkspace ws = backward_workspace(n_ranks, rows_out, k_in, m_tokens);
-  if (workspace_bytes < ws.total)
+  if (ws.total > 0 && (!workspace || workspace_bytes < ws.total))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: workspace of %llu bytes is below the %llu needed", who,
-                     (unsigned long long)workspace_bytes, (unsigned long long)ws.total);
-  if (!aligned16(dW) || !aligned16(workspace))
+                     workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.total);
+  if (!aligned16(dW) || (ws.total > 0 && !aligned16(workspace)))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: dW and workspace must be 16-byte aligned", who);
   GradPtrs wp, ap, dyp;
   memset(&wp, 0, sizeof(wp));
@@ -109,6 +117,23 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
     dyp.p[q] = dY[q];
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (ws.total == 0) {
+    // dX_q = dY_q W with W read as its row shards: one launch over all ranks' rows when each
+    // rank's M is a whole number of 128-row tiles, else one launch per rank
+    const uint16_t* const* dy = reinterpret_cast<const uint16_t* const*>(dY);
+    const uint16_t* const* wsh = reinterpret_cast<const uint16_t* const*>(w_shards);
+    int rc;
+    if (m_tokens % 128 == 0) {
+      rc = launch_fsdp_bwd_dx(n_ranks, dy, m_tokens, n_ranks, wsh, rows_out, k_in, dX, st);
+      if (rc) return rc;
+    } else {
+      for (int q = 0; q < n_ranks; ++q)
+        if ((rc = launch_fsdp_bwd_dx(n_ranks, dy + q, m_tokens, 1, wsh, rows_out, k_in, dX + q, st))) return rc;
+    }
+    // dW = (1/N) sum_q dY_q^T X_q: the K loop runs over every rank's tokens in turn
+    return launch_fsdp_bwd_dw(n_ranks, dy, reinterpret_cast<const uint16_t* const*>(A), m_tokens, rows_out, k_in,
+                              dW, st);
+  }
   uint8_t* base = static_cast<uint8_t*>(workspace);
   uint16_t* wt = reinterpret_cast<uint16_t*>(base + ws.wt);
   uint16_t* dyt = reinterpret_cast<uint16_t*>(base + ws.dyt);

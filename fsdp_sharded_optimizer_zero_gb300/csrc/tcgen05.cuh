@@ -17,6 +17,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* tmap,
       : "memory");
 }
 
+// 3-D tiled TMA load of the box at coordinates (x, y, z) into shared memory, completing its
+// bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst_smem),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // 2-D tiled TMA store of a shared-memory box to global memory at (x, y), tracked in this
 // thread's bulk async-group; out-of-bounds parts of the box are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src_smem) {
@@ -65,11 +76,24 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
+// Shared-memory operand descriptor for an MN-major tile with the 128-byte swizzle: the
+// tile is stored as K rows of 64 contiguous M (or N) elements (128 B per row, 8-row groups
+// 1024 B apart), and further 64-element M/N chunks follow each other `chunk_bytes` apart.
+// For MN-major swizzled layouts the leading byte offset (bits 16-29) is the distance
+// between M/N chunks and the stride byte offset (bits 32-45) the distance between 8-row
+// K groups; fixed 0b001 at bits 46-48, base offset 0, swizzle mode 2 = 128-byte.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t chunk_bytes) {
+  return static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(chunk_bytes >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
-// M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+// (bits 7-9 = 1, 10-12 = 1), A / B major-ness at bits 15 / 16 (0 = K-major, 1 = MN-major),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn = false, bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
