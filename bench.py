@@ -434,7 +434,7 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
                                              "note": "W_down gathered into scratch on a second stream during gate+up"}
         del gs_, us_, ds_, Hb, Ym, sd
         # backward of W_up for 8 ranks of 2048 tokens: one dX GEMM over all ranks reading the
-        # W shards in place, one rank-reduced dW GEMM reading dY and X in place
+        # W shards in place, X^T laid out, one rank-reduced dW GEMM reading dY in place
         R, K, Mb = 14336, 4096, 2048
         shards = synth.weight_shards(R, K, n, device=dev, seed_key=11)
         A = [synth.activations(Mb, K, device=dev, seed_key=q) for q in range(n)]
@@ -442,13 +442,13 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         dX = [torch.empty(Mb, K, device=dev) for _ in range(n)]
         dW = torch.empty(R, K, device=dev)
         wsb = z.fsdp_unit_backward_workspace(n, R, K, Mb)
-        ws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
         ms = time_launches(lambda: z.fsdp_unit_backward(shards, A, dY, dX, dW, ws, stream=stream), 5, stream)
         flop = 2.0 * (2.0 * n * Mb * R * K)
         res["backward_up"] = {"ms": ms, "tflops": flop / ms / 1e9, "frac": flop / ms / 1e9 / tf_peak,
                               "ranks": n, "tokens_per_rank": Mb,
                               "launches": 5, "workspace_bytes": wsb,
-                              "note": "no transposes: W, dY and X read in place as MN-major operands; "
+                              "note": "W and dY read in place as MN-major operands, X^T transposed; "
                                       "one dX GEMM over all ranks, one dW GEMM"}
     except Exception as e:  # the GEMM leg must not hide the step's line
         res["error"] = str(e)[:300]

@@ -294,9 +294,9 @@ def fsdp_unit_backward_workspace(n_ranks: int, rows_out: int, k_in: int, m_token
     return b.value
 
 
-def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace=None, stream=None):
+def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace, stream=None):
     """A, dY, dX: per-rank lists; dW: [rows_out, k_in] fp32; workspace: a uint8 CUDA tensor
-    of at least fsdp_unit_backward_workspace(...) bytes (None when that is 0)."""
+    of at least fsdp_unit_backward_workspace(...) bytes."""
     n = len(w_shards)
     rows = sum(int(s.shape[0]) for s in w_shards)
     k = int(A[0].shape[1])

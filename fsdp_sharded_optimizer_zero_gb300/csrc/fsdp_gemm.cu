@@ -577,10 +577,11 @@ int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces
                             "fsdp_unit_backward");
 }
 
-int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* const* X, int64_t m_tokens,
+int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* Xt, int64_t m_tokens,
                        int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st) {
   float* y1[1] = {dW};
-  return launch_gemm<false>({n_ranks, dY, true, m_tokens}, {n_ranks, X, true, m_tokens}, nullptr, rows_out, k_in,
+  const uint16_t* xt1[1] = {Xt};
+  return launch_gemm<false>({n_ranks, dY, true, m_tokens}, {1, xt1, false, k_in}, nullptr, rows_out, k_in,
                             m_tokens * n_ranks, y1, 1, nullptr, 1.0f / static_cast<float>(n_ranks), st,
                             "fsdp_unit_backward");
 }

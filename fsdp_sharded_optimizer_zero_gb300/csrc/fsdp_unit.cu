@@ -30,19 +30,23 @@ struct BackwardWorkspace {
   uint64_t wt, dyt, xt, total;  // byte offsets of W^T, dY^T, X^T and the total size
 };
 
-// The backward reads W, dY and X in place (MN-major GEMM operands, no transposes) when
-// every K piece is a whole number of 64-row K blocks (the W shards' R / N rows for dX, each
-// rank's m_tokens rows for dW) and the MN-major operands' rows are whole 64-column chunks
-// (k_in % 64 == 0; R % 64 follows from R / N).
+// The backward reads W and dY in place (MN-major GEMM operands) when every K piece is a
+// whole number of 64-row K blocks (the W shards' R / N rows for dX, each rank's m_tokens
+// rows for dW) and the MN-major operands' rows are whole 64-column chunks (k_in % 64 == 0;
+// R % 64 follows from R / N). X is still transposed: each MN-major operand costs the GEMM
+// 8-14 % on GB300, and dW with both operands MN-major lost more than X^T's transpose.
 bool backward_in_place(int n, int64_t rows_out, int64_t k_in, int64_t m_tokens) {
   return n <= kGemmMaxPieces && (rows_out / n) % 64 == 0 && m_tokens % 64 == 0 && k_in % 64 == 0;
 }
 
 BackwardWorkspace backward_workspace(int n, int64_t rows_out, int64_t k_in, int64_t m_tokens) {
   BackwardWorkspace w{0, 0, 0, 0};
-  if (backward_in_place(n, rows_out, k_in, m_tokens)) return w;
   const uint64_t R = static_cast<uint64_t>(rows_out), K = static_cast<uint64_t>(k_in);
   const uint64_t NM = static_cast<uint64_t>(n) * static_cast<uint64_t>(m_tokens);
+  if (backward_in_place(n, rows_out, k_in, m_tokens)) {  // X^T only
+    w.total = align256(2 * K * NM);
+    return w;
+  }
   w.wt = 0;
   w.dyt = align256(2 * R * K);
   w.xt = w.dyt + align256(2 * R * NM);
@@ -98,10 +102,10 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
                      "%s: k_in, rows_out and n_ranks * m_tokens must be multiples of 8 (16-byte GEMM rows)", who);
   if (!w_shards || !A || !dY || !dX || !dW) return set_error(ZERO_ERR_INVALID_ARG, "%s: NULL argument", who);
   const BackwardWorkspace ws = backward_workspace(n_ranks, rows_out, k_in, m_tokens);
-  if (ws.total > 0 && (!workspace || workspace_bytes < ws.total))
+  if (!workspace || workspace_bytes < ws.total)
     return set_error(ZERO_ERR_INVALID_ARG, "%s: workspace of %llu bytes is below the %llu needed", who,
                      workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.total);
-  if (!aligned16(dW) || (ws.total > 0 && !aligned16(workspace)))
+  if (!aligned16(dW) || !aligned16(workspace))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: dW and workspace must be 16-byte aligned", who);
   GradPtrs wp, ap, dyp;
   memset(&wp, 0, sizeof(wp));
@@ -117,7 +121,7 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
     dyp.p[q] = dY[q];
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (ws.total == 0) {
+  if (backward_in_place(n_ranks, rows_out, k_in, m_tokens)) {
     // dX_q = dY_q W with W read as its row shards: one launch over all ranks' rows when each
     // rank's M is a whole number of 128-row tiles, else one launch per rank
     const uint16_t* const* dy = reinterpret_cast<const uint16_t* const*>(dY);
@@ -130,9 +134,12 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
       for (int q = 0; q < n_ranks; ++q)
         if ((rc = launch_fsdp_bwd_dx(n_ranks, dy + q, m_tokens, 1, wsh, rows_out, k_in, dX + q, st))) return rc;
     }
-    // dW = (1/N) sum_q dY_q^T X_q: the K loop runs over every rank's tokens in turn
-    return launch_fsdp_bwd_dw(n_ranks, dy, reinterpret_cast<const uint16_t* const*>(A), m_tokens, rows_out, k_in,
-                              dW, st);
+    // dW = (1/N) sum_q dY_q^T X_q: the K loop runs over every rank's tokens in turn, dY
+    // read in place, X from its rank-concatenated transpose
+    uint16_t* xt = static_cast<uint16_t*>(workspace);
+    cudaError_t e = launch_transpose_cat(ap, n_ranks, m_tokens, k_in, xt, st);
+    if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
+    return launch_fsdp_bwd_dw(n_ranks, dy, xt, m_tokens, rows_out, k_in, dW, st);
   }
   uint8_t* base = static_cast<uint8_t*>(workspace);
   uint16_t* wt = reinterpret_cast<uint16_t*>(base + ws.wt);

@@ -72,16 +72,17 @@ int launch_fsdp_gemm_row_split(int a_shards, const uint16_t* const* A, float* co
 int launch_fsdp_gate_up(int n_ranks, const uint16_t* const* gate_shards, const uint16_t* const* up_shards,
                         int64_t d_ff, int64_t d_model, const uint16_t* X, int64_t m_tokens, uint16_t* H,
                         cudaStream_t st);
-// Backward GEMMs reading W, dY and X in place as MN-major operands (no transposes):
+// Backward GEMMs reading operands in place as MN-major tiles:
 // dX_q[M, K] = dY_q W for the dy_pieces row pieces of dY / dX (dy_pieces = 1: one rank),
-// with W given as its n_ranks row shards (R / n_ranks a multiple of 64);
-// dW[R, K] = (1/n_ranks) sum_q dY_q^T X_q with every rank's m_tokens rows (a multiple of
-// 64) as one K piece. At most kGemmMaxPieces pieces per operand.
+// with W read in place from its n_ranks row shards (R / n_ranks a multiple of 64);
+// dW[R, K] = (1/n_ranks) sum_q dY_q^T X_q with dY read in place (every rank's m_tokens
+// rows, a multiple of 64, one K piece) and X as the rank-concatenated X^T [K, N M].
+// At most kGemmMaxPieces pieces per operand.
 constexpr int kGemmMaxPieces = 16;
 int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces_rows, int dy_pieces,
                        const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in, float* const* dX,
                        cudaStream_t st);
-int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* const* X, int64_t m_tokens,
+int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* Xt, int64_t m_tokens,
                        int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st);
 unsigned int fsdp_gemm_read_clear_error();
 

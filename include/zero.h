@@ -258,10 +258,10 @@ ZERO_API int fsdp_unit_forward(int n_ranks, const zero_bf16* const w_shards[], i
 ZERO_API int fsdp_transpose_cat(int n_srcs, const zero_bf16* const srcs[], int64_t rows, int64_t cols, zero_bf16* dst,
                                 zero_stream_t stream);
 
-/* Bytes of device workspace fsdp_unit_backward needs. 0 when R/N, k_in and m_tokens are
- * multiples of 64 and N <= 16: the GEMMs then read W's shards, dY and X in place (as
- * MN-major tensor-core operands). Otherwise W^T (2*R*K), dY^T (2*R*N*M) and X^T
- * (2*K*N*M), each rounded up to 256 bytes, for transposed copies. */
+/* Bytes of device workspace fsdp_unit_backward needs for transposed operand copies, each
+ * rounded up to 256 bytes. When R/N, k_in and m_tokens are multiples of 64 and N <= 16
+ * the GEMMs read W's shards and dY in place (as MN-major tensor-core operands) and only
+ * X^T (2*K*N*M) is needed; otherwise W^T (2*R*K), dY^T (2*R*N*M) and X^T. */
 ZERO_API int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t k_in, int64_t m_tokens,
                                           uint64_t* bytes);
 
@@ -274,8 +274,7 @@ ZERO_API int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t
  * dX[q]: out, row-major [m_tokens, k_in] fp32: dX_q = dY_q W;
  * dW: out, row-major [rows_out, k_in] fp32: dW = (1/N) sum_q dY_q^T X_q; rank r's
  *     reduce-scattered shard is rows [r*R/N, (r+1)*R/N).
- * workspace: device buffer of fsdp_unit_backward_workspace() bytes (caller-owned scratch;
- *     may be NULL when that size is 0).
+ * workspace: device buffer of fsdp_unit_backward_workspace() bytes (caller-owned scratch).
  * Requires rows_out % N == 0 and k_in, rows_out, N*m_tokens multiples of 8; all buffers
  * 16-byte aligned. fp32 accumulation on the tensor cores in an unspecified order: each dX
  * entry is within (R+1) 2^-23 sum|dy w| and each dW entry within (N M + 1) 2^-23 (1/N)

@@ -134,15 +134,17 @@ def test_newer_entry_points_reject_bad_arguments_before_launch(z):
     assert lib.zero_fused_step_fp32_grads(p.handle, 4, good, 256, 512, 768, 1024, C.byref(adam), 1, None) == -1
     # backward: rows % N, K % 8, workspace size, NULL rank pointer
     ws = C.c_uint64()
-    # in place (R/N, K and M multiples of 64): no workspace; otherwise W^T, dY^T and X^T
+    # W and dY in place (R/N, K and M multiples of 64): X^T only; otherwise W^T, dY^T, X^T
     assert lib.fsdp_unit_backward_workspace(4, 512, 256, 128, C.byref(ws)) == 0
-    assert ws.value == 0
+    assert ws.value == 2 * 256 * 512
     assert lib.fsdp_unit_backward_workspace(4, 512, 256, 40, C.byref(ws)) == 0
     assert ws.value == 2 * 512 * 256 + 2 * 512 * 160 + 2 * 256 * 160
     assert lib.fsdp_unit_backward_workspace(17, 17 * 64, 256, 128, C.byref(ws)) == 0
-    assert ws.value > 0  # more than 16 ranks: one GEMM operand cannot hold every piece
+    assert ws.value > 2 * 256 * 17 * 128  # more than 16 ranks: one GEMM operand cannot hold every piece
+    assert lib.fsdp_unit_backward_workspace(4, 512, 192, 128, C.byref(ws)) == 0
+    assert ws.value == 2 * 192 * 512
     assert lib.fsdp_unit_backward_workspace(4, 512, 200, 128, C.byref(ws)) == 0
-    assert ws.value > 0  # K not a multiple of 64
+    assert ws.value > 2 * 200 * 512  # K not a multiple of 64
     assert lib.fsdp_unit_backward_workspace(0, 512, 256, 128, C.byref(ws)) == -1
     args = lambda rows, k, m, wsb: (4, good, rows, k, good, good, m, good, 4096, 8192, wsb, None)
     assert lib.fsdp_unit_backward(*args(510, 256, 128, 1 << 30)) == -1

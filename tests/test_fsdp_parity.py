@@ -189,20 +189,20 @@ def run_backward(z, n, rows, k, m, key=0, ints=False):
         dY = [synth.upstream_grad(m, rows, device=DEV, seed_key=100 * key + q) for q in range(n)]
     dX = [torch.full((m, k), float("nan"), device=DEV) for _ in range(n)]
     dW = torch.full((rows, k), float("nan"), device=DEV)
-    wsb = z.fsdp_unit_backward_workspace(n, rows, k, m)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV) if wsb else None
+    ws = torch.empty(z.fsdp_unit_backward_workspace(n, rows, k, m), dtype=torch.uint8, device=DEV)
     z.fsdp_unit_backward(shards, A, dY, dX, dW, ws)
     z.zero_device_status()
     return shards, A, dY, dX, dW
 
 
-def test_backward_workspace_only_when_transposing(z):
-    # W, dY and X are read in place when R/N, M and K are multiples of 64 (and N <= 16)
-    assert z.fsdp_unit_backward_workspace(8, 14336, 4096, 2048) == 0
-    assert z.fsdp_unit_backward_workspace(5, 320, 192, 192) == 0
-    assert z.fsdp_unit_backward_workspace(5, 320, 200, 192) > 0
-    assert z.fsdp_unit_backward_workspace(4, 512, 256, 40) > 0
-    assert z.fsdp_unit_backward_workspace(8, 2048, 512, 96) > 0
+def test_backward_workspace_sizes(z):
+    # W and dY are read in place when R/N, M and K are multiples of 64 (and N <= 16): the
+    # workspace holds X^T alone; otherwise W^T, dY^T and X^T
+    assert z.fsdp_unit_backward_workspace(8, 14336, 4096, 2048) == 2 * 4096 * 8 * 2048
+    assert z.fsdp_unit_backward_workspace(5, 320, 192, 192) == 2 * 192 * 5 * 192
+    assert z.fsdp_unit_backward_workspace(5, 320, 200, 192) > 2 * 200 * 5 * 192
+    assert z.fsdp_unit_backward_workspace(4, 512, 256, 40) > 2 * 256 * 4 * 40
+    assert z.fsdp_unit_backward_workspace(8, 2048, 512, 96) > 2 * 512 * 8 * 96
 
 
 # in place: one dX launch over all ranks (M % 128 == 0), per-rank dX launches (M % 128 ==
