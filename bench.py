@@ -661,6 +661,20 @@ def run_case(args):
         Y = torch.empty(M, 4096, device=dev)
         ms = time_launches(lambda: z.fsdp_mlp_forward(gs, us, ds, X, H, Y, stream=stream), 4, stream)
         out.update(M=M, ms=ms, tflops=3 * 2.0 * M * 14336 * 4096 / ms / 1e9)
+    elif args.case == "backward_up":
+        # FSDP unit backward of W_up [14336, 4096] in 8 row shards, 2048 tokens per rank
+        # (dY 470 MB, X 134 MB, dX 268 MB, dW 235 MB, X^T workspace 134 MB): 3 launches
+        # (dX GEMM, X transpose, dW GEMM) per call, 4 calls
+        n, R, K, M = 8, 14336, 4096, 2048
+        shards = synth.weight_shards(R, K, n, device=dev, seed_key=11)
+        A = [synth.activations(M, K, device=dev, seed_key=q) for q in range(n)]
+        dY = [synth.upstream_grad(M, R, device=dev, seed_key=q) for q in range(n)]
+        dX = [torch.empty(M, K, device=dev) for _ in range(n)]
+        dW = torch.empty(R, K, device=dev)
+        ws = torch.empty(z.fsdp_unit_backward_workspace(n, R, K, M), dtype=torch.uint8, device=dev)
+        ms = time_launches(lambda: z.fsdp_unit_backward(shards, A, dY, dX, dW, ws, stream=stream), 3, stream)
+        out.update(n_ranks=n, R=R, K=K, M=M, ms=ms, tflops=4.0 * n * M * R * K / ms / 1e9,
+                   workspace_bytes=ws.numel())
     else:
         raise SystemExit(f"unknown case {args.case}")
     z.zero_device_status(stream)
@@ -670,8 +684,8 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="one measured case: fused_small | gemm_small | gemm_w_up | mlp_unit (ncu-sized) | tiny | "
-                         "mistral_rank_view")
+                    help="one measured case: fused_small | gemm_small | gemm_w_up | mlp_unit | backward_up (ncu-sized) | "
+                         "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
