@@ -284,6 +284,39 @@ def test_backward_mistral_up_sampled(z):
     assert np.all(np.abs(got - ex) <= bound), "dW"
 
 
+def test_backward_mistral_down_sampled(z):
+    """W_down [4096, 14336] in 8 row shards of 512 rows (read in place as the dX GEMM's
+    MN-major B), 1024 tokens per rank: sampled dX and dW entries against float64 dot
+    products under the bounds."""
+    n, rows, k, m = 8, 4096, 14336, 1024
+    assert z.fsdp_unit_backward_workspace(n, rows, k, m) == 2 * k * n * m  # the in-place path
+    shards, A, dY, dX, dW = run_backward(z, n, rows, k, m, key=9)
+    rng = np.random.default_rng(2)
+    w_full = torch.cat(shards, 0)
+    for q in (0, 3, n - 1):
+        i = torch.from_numpy(rng.integers(0, m, 384)).to(DEV)
+        c = torch.from_numpy(rng.integers(0, k, 384)).to(DEV)
+        dy = O.bf16_to_f32(bits16(dY[q][i])).astype(np.float64)
+        wc = O.bf16_to_f32(bits16(w_full[:, c].t().contiguous())).astype(np.float64)
+        exact = np.einsum("ir,ir->i", dy, wc)
+        bound = (rows + 1) * 2.0 ** -23 * np.einsum("ir,ir->i", np.abs(dy), np.abs(wc))
+        assert np.all(np.abs(f32(dX[q][i, c]).astype(np.float64) - exact) <= bound), f"dX rank {q}"
+    # dW rows on both sides of every shard seam, random columns
+    rr = np.concatenate([np.arange(1, n) * (rows // n) + d for d in (-1, 0)] + [rng.integers(0, rows, 128)])
+    cc = rng.integers(0, k, rr.size)
+    ex = np.zeros(rr.size)
+    bd = np.zeros(rr.size)
+    for q in range(n):
+        dyc = O.bf16_to_f32(bits16(dY[q][:, torch.from_numpy(rr).to(DEV)].t().contiguous())).astype(np.float64)
+        ac = O.bf16_to_f32(bits16(A[q][:, torch.from_numpy(cc).to(DEV)].t().contiguous())).astype(np.float64)
+        ex += np.einsum("im,im->i", dyc, ac)
+        bd += np.einsum("im,im->i", np.abs(dyc), np.abs(ac))
+    ex /= n
+    bound = (n * m + 1) * 2.0 ** -23 * bd / n + 2.0 ** -24 * np.abs(ex)
+    got = f32(dW[torch.from_numpy(rr).to(DEV), torch.from_numpy(cc).to(DEV)]).astype(np.float64)
+    assert np.all(np.abs(got - ex) <= bound), "dW"
+
+
 def test_backward_rejects_small_workspace(z):
     n, rows, k, m = 2, 512, 64, 40
     shards = synth.weight_shards(rows, k, n, device=DEV)
