@@ -661,6 +661,27 @@ def run_case(args):
         Y = torch.empty(M, 4096, device=dev)
         ms = time_launches(lambda: z.fsdp_mlp_forward(gs, us, ds, X, H, Y, stream=stream), 4, stream)
         out.update(M=M, ms=ms, tflops=3 * 2.0 * M * 14336 * 4096 / ms / 1e9)
+    elif args.case == "legs_small":
+        # the standalone step kernels on psi = 33,554,432 flat, N = 8, all ranks (1.1 GB of
+        # inputs): DDP all-reduce (reduce_vec_kernel<8>), Adam with the bf16 cast
+        # (adam_vec_kernel), the parameter all-gather (allgather_kernel); 3 launches each
+        psi, n = 1 << 25, 8
+        plan = z.zero_plan(psi, n, "ddp", 25 * MIB)
+        S = plan.shard_elems
+        grads = [synth.rank_grads(psi, psi, r, 1, device=dev) for r in range(n)]
+        g = torch.empty(psi, device=dev)
+        master = synth.master_params(psi, psi, device=dev)
+        m = torch.zeros(psi, device=dev)
+        v = torch.zeros(psi, device=dev)
+        param = torch.empty(psi, dtype=torch.bfloat16, device=dev)
+        hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+        ms_ar = time_launches(lambda: z.ddp_allreduce(plan, grads, g, stream), 2, stream)
+        ms_ad = time_launches(lambda: z.zero_adam_step(plan, z.ZERO_ALL_RANKS, g, master, m, v, param, hp, 1, stream),
+                              2, stream)
+        ms_ag = time_launches(lambda: z.zero_allgather_params(plan, [master[r * S:(r + 1) * S] for r in range(n)],
+                                                              param, stream), 2, stream)
+        out.update(psi=psi, n_ranks=n, allreduce_ms=ms_ar, adam_ms=ms_ad, allgather_ms=ms_ag,
+                   allreduce_bytes=psi * (2 * n + 4), adam_bytes=psi * 30, allgather_bytes=psi * 6)
     elif args.case == "backward_up":
         # FSDP unit backward of W_up [14336, 4096] in 8 row shards, 2048 tokens per rank
         # (dY 470 MB, X 134 MB, dX 268 MB, dW 235 MB, X^T workspace 134 MB): 3 launches
@@ -684,7 +705,8 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="one measured case: fused_small | gemm_small | gemm_w_up | mlp_unit | backward_up (ncu-sized) | "
+                    help="one measured case: fused_small | legs_small | gemm_small | gemm_w_up | mlp_unit | backward_up "
+                         "(ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)

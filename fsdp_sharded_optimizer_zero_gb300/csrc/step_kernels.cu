@@ -307,7 +307,8 @@ cudaError_t launch_allgather(const MasterPtrs& mp, int n, uint64_t shard, uint16
                              cudaStream_t st) {
   const uint64_t total = shard * static_cast<uint64_t>(n);
   if (total == 0) return cudaSuccess;
-  allgather_kernel<<<grid_for(vec ? total / 4 : total), kThreads, 0, st>>>(mp, n, shard, full, vec ? 1 : 0);
+  allgather_kernel<<<vec ? grid_for(total / 4, kAgBlocksPerSm) : grid_for(total), kThreads, 0, st>>>(mp, n, shard, full,
+                                                                                               vec ? 1 : 0);
   return cudaGetLastError();
 }
 
