@@ -158,8 +158,13 @@ def test_mistral_mlp_unit_sampled(z):
         del shards, Y, w_full
 
 
-@pytest.mark.parametrize("n,rows,cols,misalign", [(8, 1792, 512, False), (3, 70, 130, False), (2, 64, 64, True),
-                                                  (1, 1, 9, False), (4, 129, 8, False)])
+# aligned (16-byte rows, the pipelined kernel): whole tiles; tiles straddling ranks with
+# ragged edges in both dimensions (3 x 40 rows, 72 columns; 5 x 200, 136; 16 x 8, 8); many
+# tiles per persistent CTA (X^T of 8 ranks x 2048 tokens x 4096: 16384 tiles).
+# unaligned (the element kernel): odd columns, misaligned destination, tiny, rows % 8 != 0
+@pytest.mark.parametrize("n,rows,cols,misalign", [(8, 1792, 512, False), (3, 40, 72, False), (5, 200, 136, False),
+                                                  (16, 8, 8, False), (8, 2048, 4096, False), (3, 70, 130, False),
+                                                  (2, 64, 64, True), (1, 1, 9, False), (4, 129, 8, False)])
 def test_transpose_cat_bit_exact(z, n, rows, cols, misalign):
     srcs = synth.weight_shards(n * rows, cols, n, device=DEV, seed_key=rows)
     if misalign:
