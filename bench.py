@@ -536,8 +536,10 @@ def run_reference(args):
 def run_sweep(args):
     """psi = 1.5e9, N in {2,4,8,16,64}, buckets {1,5,25,100} MiB. For each point: one launch
     over all buckets, and one launch per bucket (as DDP reduces each bucket once backward
-    produced it) captured in a CUDA graph. N <= 16: all N ranks' shards (full simulation);
-    N = 64: one rank's view (its 64 incoming chunks), which bounds device memory."""
+    produced it) captured in a CUDA graph. All N ranks' shards (full simulation) whenever
+    the (2N + 14) P bytes of gradients, state and parameters fit in free device memory with
+    an 8 GiB margin (N = 64: 213 GB, which a GB300 holds); otherwise one rank's view (its N
+    incoming chunks)."""
     import torch
 
     import fsdp_sharded_optimizer_zero_gb300 as z
@@ -549,9 +551,10 @@ def run_sweep(args):
     psi = 1_500_000_000
     hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
     for n in (2, 4, 8, 16, 64):
-        full = n <= 16
         plan0 = z.zero_plan(psi, n, "zero2", MIB)
         P, S = plan0.psi_padded, plan0.shard_elems
+        torch.cuda.empty_cache()
+        full = (2 * n + 14) * P + (8 << 30) <= torch.cuda.mem_get_info()[0]
         L = P if full else S
         if full:
             grads = [synth.rank_grads(psi, P, r, 1, device=dev) for r in range(n)]
