@@ -543,7 +543,7 @@ def test_mistral7b_rank_view_n8_sampled(z):
     master = synth.master_params(S, S, device=DEV, seed_key=3)
     m = torch.zeros(S, device=DEV)
     v = torch.zeros(S, device=DEV)
-    so = SampledOracle(sample_indices(S, S, C, 1, seed=1), master, m, v)
+    so = SampledOracle(sample_indices(S, S, C, 1, k=1 << 20, seed=1), master, m, v)  # 2^20 random + every edge
     so.step(rows, 1)
     w2, m2, v2 = master.clone(), m.clone(), v.clone()
     p1 = torch.empty(S, dtype=torch.bfloat16, device=DEV)
@@ -554,6 +554,7 @@ def test_mistral7b_rank_view_n8_sampled(z):
     z.zero_device_status()
     so.check(master, m, v, p1, "mistral rank view")
     assert torch.equal(master.view(torch.int32), w2.view(torch.int32))
+    assert torch.equal(m.view(torch.int32), m2.view(torch.int32))
     assert torch.equal(v.view(torch.int32), v2.view(torch.int32))
     assert torch.equal(p1.view(torch.int16), p2.view(torch.int16))
 
