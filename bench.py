@@ -17,10 +17,16 @@ workload. --sweep prints one line per point of the 1.5B-parameter bandwidth swee
 """
 from __future__ import annotations
 
+import os
+
+# The oracle's numpy calls (cpu_baseline, the reference arm, the timings beside each leg)
+# run on one host thread, so the cores they report are exact: pin numpy's BLAS before
+# numpy is first imported.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+
 import argparse
 import hashlib
 import json
-import os
 import statistics
 import subprocess
 import sys
@@ -255,6 +261,8 @@ def run_ours(args):
         out["legs"] = extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+        if "legs" in out:
+            oracle_beside_legs(out["legs"])
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -352,10 +360,11 @@ def extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args):
                                                           stream), it, stream)
     b_ar, b_ad, b_ag = P * (2 * n + 4), P * 28, P * 6
     legs["ddp_allreduce"] = {"ms": ms_ar, "gbs": b_ar / ms_ar / 1e6, "frac": b_ar / ms_ar / 1e6 / hbm_peak,
-                             "bytes": b_ar}
-    legs["adam_step"] = {"ms": ms_ad, "gbs": b_ad / ms_ad / 1e6, "frac": b_ad / ms_ad / 1e6 / hbm_peak, "bytes": b_ad}
+                             "bytes": b_ar, "params_per_s": P / ms_ar * 1e3}
+    legs["adam_step"] = {"ms": ms_ad, "gbs": b_ad / ms_ad / 1e6, "frac": b_ad / ms_ad / 1e6 / hbm_peak, "bytes": b_ad,
+                         "params_per_s": P / ms_ad * 1e3}
     legs["allgather_params"] = {"ms": ms_ag, "gbs": b_ag / ms_ag / 1e6, "frac": b_ag / ms_ag / 1e6 / hbm_peak,
-                                "bytes": b_ag}
+                                "bytes": b_ag, "params_per_s": P / ms_ag * 1e3}
     legs["unfused_pipeline_ms"] = ms_ar + ms_ad + ms_ag
     z.zero_set_fused_kernel(1)
     ms_tma = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1,
@@ -489,6 +498,67 @@ class OracleSample:
         el = time.perf_counter() - t0
         self.master[:count], self.m[:count], self.v[:count] = w, m, v
         return el
+
+
+def _time_bounded(fn, budget_s: float):
+    """Seconds per call of fn, over as many calls as fit in budget_s (at least one)."""
+    fn()
+    t0, k = time.perf_counter(), 0
+    while True:
+        fn()
+        k += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return el / k, k
+
+
+def oracle_beside_legs(legs: dict, budget_s: float = 1.5):
+    """The oracle as it stands, timed on the host beside each GPU leg on a bounded sample of
+    that leg's workload; numpy with its BLAS pinned to one thread. Adds legs[k]["cpu_oracle"]."""
+    import numpy as np
+    import torch
+
+    import synth
+    from oracle import zero_oracle as O
+    n_params, n = 4 * MIB, 8
+    s = OracleSample(n_params)
+    g = O.reduce_sum_scale(s.grads, 0, n_params)
+    S = n_params // n
+    g32 = [synth.rank_grads_f32(n_params, n_params, r, 1).numpy() for r in range(n)]
+    elem = f"first {n_params:,} of the 124,356,864 GPT-2-small parameters, N = 8"
+
+    def put(key, per_call, calls, value, unit, sample):
+        if key in legs and isinstance(legs[key], dict):
+            legs[key]["cpu_oracle"] = {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                                       "sample": f"{sample}; {calls} calls, {per_call * 1e3:.1f} ms each"}
+
+    t, k = _time_bounded(lambda: O.reduce_sum_scale(s.grads, 0, n_params), budget_s)
+    put("ddp_allreduce", t, k, n_params / t, "params/s", elem + " bf16 gradient slices, rank-order fp32 sum x 1/N")
+    t, k = _time_bounded(lambda: O.adam_update(s.master, s.m, s.v, g, s.hp, 1), budget_s)
+    put("adam_step", t, k, n_params / t, "params/s", elem + ", Adam on fp32 master / m / v")
+    t, k = _time_bounded(lambda: O.f32_to_bf16(O.all_gather([s.master[i * S:(i + 1) * S] for i in range(n)])),
+                         budget_s)
+    put("allgather_params", t, k, n_params / t, "params/s", elem + ", bf16 cast and all-gather of 8 master shards")
+    t, k = _time_bounded(lambda: O.fused_step_elements(g32, s.master, s.m, s.v, s.hp, 1), budget_s)
+    put("megatron_fp32_grads", t, k, n_params / t, "params/s", elem + " fp32 gradient slices, fused step")
+    fl = legs.get("fsdp_unit_forward")
+    if isinstance(fl, dict):
+        R, K, rows = 14336, 4096, 16
+        shards = [x.view(torch.int16).numpy().view(np.uint16) for x in synth.weight_shards(R, K, n)]
+        a = synth.activations(rows, K).view(torch.int16).numpy().view(np.uint16)
+        dy = synth.upstream_grad(rows, R).view(torch.int16).numpy().view(np.uint16)
+        t, k = _time_bounded(lambda: O.fsdp_linear_forward(a, shards), budget_s)
+        for key in ("up", "gate"):
+            if isinstance(fl.get(key), dict):
+                fl[key]["cpu_oracle"] = {"value": 2.0 * rows * R * K / t / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                         "kind": "oracle", "sample": f"{rows} of 8192 token rows against the full "
+                                         f"14336 x 4096 weight from 8 shards (float64); {k} calls"}
+        if isinstance(fl.get("backward_up"), dict):
+            t, k = _time_bounded(lambda: O.fsdp_linear_backward(a, shards, dy, n), budget_s)
+            fl["backward_up"]["cpu_oracle"] = {
+                "value": 4.0 * rows * R * K / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                "sample": f"one rank's {rows} of 2048 tokens: dX and dW against the full 14336 x 4096 weight "
+                          f"(float64); {k} calls"}
 
 
 def cpu_baseline(budget_s: float = 15.0):
