@@ -755,6 +755,19 @@ def run_case(args):
                                                               param, stream), 2, stream)
         out.update(psi=psi, n_ranks=n, allreduce_ms=ms_ar, adam_ms=ms_ad, allgather_ms=ms_ag,
                    allreduce_bytes=psi * (2 * n + 4), adam_bytes=psi * 30, allgather_bytes=psi * 6)
+    elif args.case == "gather_w_up":
+        # W_up [14336, 4096] bf16 from 8 row shards: the materialised all-gather
+        # (fsdp_gather_rows) and the backward's transposed gather W^T (fsdp_transpose_cat);
+        # 235 MB moved per launch each, 3 launches each
+        n, R, K = 8, 14336, 4096
+        shards = synth.weight_shards(R, K, n, device=dev)
+        W = torch.empty(R, K, dtype=torch.bfloat16, device=dev)
+        Wt = torch.empty(K, R, dtype=torch.bfloat16, device=dev)
+        ms_g = time_launches(lambda: z.fsdp_gather_rows(shards, W, stream=stream), 2, stream)
+        ms_t = time_launches(lambda: z.fsdp_transpose_cat(shards, Wt, stream=stream), 2, stream)
+        byts = 4 * R * K
+        out.update(R=R, K=K, n_ranks=n, gather_ms=ms_g, transpose_ms=ms_t, bytes=byts,
+                   gather_gbs=byts / ms_g / 1e6, transpose_gbs=byts / ms_t / 1e6)
     elif args.case == "backward_up":
         # FSDP unit backward of W_up [14336, 4096] in 8 row shards, 2048 tokens per rank
         # (dY 470 MB, X 134 MB, dX 268 MB, dW 235 MB, X^T workspace 134 MB): 3 launches
@@ -778,8 +791,8 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="one measured case: fused_small | legs_small | gemm_small | gemm_w_up | mlp_unit | backward_up "
-                         "(ncu-sized) | "
+                    help="one measured case: fused_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
+                         "backward_up (ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
