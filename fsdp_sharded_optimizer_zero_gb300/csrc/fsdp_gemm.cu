@@ -171,9 +171,10 @@ __device__ __forceinline__ void store_gate_up_chunk(const GemmParams& p, int row
 }
 
 // GATE_UP = false: Y = alpha A W^T with 128 x 256 output tiles.
-// GATE_UP = true: two B operands (gate and up shards, 128-row tiles each) share every A
-// tile; their two 128-column accumulators sit side by side in one 256-column TMEM buffer
-// and the epilogue writes H = silu(gate) * up for a 128 x 128 tile.
+// GATE_UP = true: two B operands (gate and up shards, 128-row tiles each, back to back in
+// the stage) share every A tile through one N = 256 MMA per K step; their two 128-column
+// accumulators sit side by side in one 256-column TMEM buffer and the epilogue writes
+// H = silu(gate) * up for a 128 x 128 tile.
 template <bool GATE_UP>
 __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr int TN = Mode<GATE_UP>::TN;                      // output tile columns
@@ -181,7 +182,6 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
   constexpr uint32_t STAGE_BYTES = Mode<GATE_UP>::STAGE;
   constexpr uint32_t ACC = Mode<GATE_UP>::ACC;
   constexpr uint32_t kTmemCols = Mode<GATE_UP>::TMEM_COLS;
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, TN);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
@@ -286,7 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
       // MN-major: 16 K rows = two 8-row groups further, 2048 bytes (+128)
       const bool a_mn = !GATE_UP && p.a_mn, b_mn = !GATE_UP && p.b_mn;
       const uint32_t a_step = a_mn ? 128u : 2u, b_step = b_mn ? 128u : 2u;
-      const uint32_t idesc = idesc_bf16_f32(BM, TN, a_mn, b_mn);
+      // gate-up mode: the gate and up tiles sit back to back in the stage (128 rows each, the
+      // same 128-byte row pitch), so ONE N = 256 MMA over both reads the A tile once and
+      // fills the two side-by-side 128-column accumulators (gate, then up)
+      const uint32_t idesc = idesc_bf16_f32(BM, GATE_UP ? 2 * TN : TN, a_mn, b_mn);
       uint32_t it = 0, i = 0;
       bool stop = false, issued = false;
       for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x, ++i) {
@@ -305,12 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
           const uint64_t ad = a_mn ? sw128_mnmajor_desc(sa, kMnChunk) : sw128_kmajor_desc(sa);
           const uint64_t bd = b_mn ? sw128_mnmajor_desc(sa + A_BYTES, kMnChunk) : sw128_kmajor_desc(sa + A_BYTES);
-          const uint64_t bd2 = sw128_kmajor_desc(sa + A_BYTES + BT_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {  // K = 16 per MMA
+          for (int k = 0; k < BK / 16; ++k)  // K = 16 per MMA
             umma_bf16(d, ad + a_step * k, bd + b_step * k, idesc, (kb | k) != 0 ? 1u : 0u);
-            if (GATE_UP) umma_bf16(d + TN, ad + 2u * k, bd2 + 2u * k, IDESC, (kb | k) != 0 ? 1u : 0u);
-          }
           umma_commit(smem_u32(&empty_bar[s]));
           issued = true;
         }
