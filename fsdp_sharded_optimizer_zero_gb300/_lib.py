@@ -170,6 +170,50 @@ class Plan:
 
 
 # ---------------------------------------------------------------------------------------
+# buffer sizes: the C ABI takes raw pointers, so the binding checks every tensor's length
+# against the plan (or the FSDP shapes) before anything is launched; a short buffer would
+# otherwise be written past its end on the device
+# ---------------------------------------------------------------------------------------
+
+def _need(t, n: int, name: str):
+    if t is not None and t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements; this call needs at least {n}")
+
+
+def _step_sizes(plan: "Plan", rank: int):
+    """Elements of (each rank's gradient, g / master / m / v, param_out) for `rank`, from
+    the header's pointer conventions; zeros for a rank the library itself will reject."""
+    P, S = plan.psi_padded, plan.shard_elems
+    if rank == ZERO_ALL_RANKS:
+        return P, P, P
+    if rank == ZERO_RANK_VIEW:
+        return S, S, S
+    if 0 <= rank < plan.n_ranks:
+        return P, S, (S if plan.stage == STAGE_IDS["zero3"] else P)
+    return 0, 0, 0
+
+
+def _check_step(plan: "Plan", rank: int, grads=None, state=(), param_out=None):
+    ng, ns, npar = _step_sizes(plan, rank)
+    if grads is not None:
+        if len(grads) != plan.n_ranks:
+            raise ValueError(f"grads holds {len(grads)} rank buffers; the plan has {plan.n_ranks} ranks")
+        for i, g in enumerate(grads):
+            _need(g, ng, f"grads[{i}]")
+    for name, t in state:
+        _need(t, ns, name)
+    _need(param_out, npar, "param_out")
+
+
+def _shards_shape(shards, name: str):
+    """(rows of one shard, columns): every shard the same 2-D shape."""
+    shapes = {tuple(s.shape) for s in shards}
+    if len(shapes) != 1 or len(next(iter(shapes))) != 2:
+        raise ValueError(f"{name} must be 2-D tensors of one shape (got {sorted(shapes)})")
+    return next(iter(shapes))
+
+
+# ---------------------------------------------------------------------------------------
 # entry points
 # ---------------------------------------------------------------------------------------
 
@@ -193,11 +237,13 @@ def zero_bucket_range(plan: Plan, rank: int, bucket: int):
 
 
 def zero_reduce_scatter(plan: Plan, rank: int, grads, g_shard, stream=None):
+    _check_step(plan, rank, grads, [("g_shard", g_shard)])
     _check(_lib.zero_reduce_scatter(plan.handle, rank, _ptr_array(grads, torch.bfloat16, "grads"),
                                     _dev(g_shard, torch.float32, "g_shard"), _stream(stream)))
 
 
 def zero_adam_step(plan: Plan, rank: int, g_shard, master, m, v, param_out, hp, step: int, stream=None):
+    _check_step(plan, rank, None, [("g_shard", g_shard), ("master", master), ("m", m), ("v", v)], param_out)
     a = _adam(hp)
     _check(_lib.zero_adam_step(plan.handle, rank, _dev(g_shard, torch.float32, "g_shard"),
                                _dev(master, torch.float32, "master"), _dev(m, torch.float32, "m"),
@@ -206,6 +252,7 @@ def zero_adam_step(plan: Plan, rank: int, g_shard, master, m, v, param_out, hp, 
 
 
 def zero_fused_step(plan: Plan, rank: int, grads, master, m, v, param_out, hp, step: int, stream=None):
+    _check_step(plan, rank, grads, [("master", master), ("m", m), ("v", v)], param_out)
     a = _adam(hp)
     _check(_lib.zero_fused_step(plan.handle, rank, _ptr_array(grads, torch.bfloat16, "grads"),
                                 _dev(master, torch.float32, "master"), _dev(m, torch.float32, "m"),
@@ -226,6 +273,7 @@ def _host(t: torch.Tensor, dtype, name: str) -> int:
 def zero_fused_step_host(plan: Plan, rank: int, host_grads, master, m, v, host_param_out, hp, step: int, stream=None):
     """Fused step reading the ranks' gradients from page-locked host tensors and writing the
     bf16 parameters to a page-locked host tensor; master / m / v are CUDA tensors."""
+    _check_step(plan, rank, host_grads, [("master", master), ("m", m), ("v", v)], host_param_out)
     a = _adam(hp)
     arr = (C.c_void_p * len(host_grads))(*[_host(g, torch.bfloat16, f"host_grads[{i}]")
                                           for i, g in enumerate(host_grads)])
@@ -236,6 +284,7 @@ def zero_fused_step_host(plan: Plan, rank: int, host_grads, master, m, v, host_p
 
 
 def zero_fused_step_fp32_grads(plan: Plan, rank: int, grads, master, m, v, param_out, hp, step: int, stream=None):
+    _check_step(plan, rank, grads, [("master", master), ("m", m), ("v", v)], param_out)
     a = _adam(hp)
     _check(_lib.zero_fused_step_fp32_grads(plan.handle, rank, _ptr_array(grads, torch.float32, "grads"),
                                            _dev(master, torch.float32, "master"), _dev(m, torch.float32, "m"),
@@ -245,6 +294,7 @@ def zero_fused_step_fp32_grads(plan: Plan, rank: int, grads, master, m, v, param
 
 def zero_fused_step_buckets(plan: Plan, rank: int, bucket_begin: int, bucket_end: int, grads, master, m, v,
                             param_out, hp, step: int, stream=None):
+    _check_step(plan, rank, grads, [("master", master), ("m", m), ("v", v)], param_out)
     a = _adam(hp)
     _check(_lib.zero_fused_step_buckets(plan.handle, rank, bucket_begin, bucket_end,
                                         _ptr_array(grads, torch.bfloat16, "grads"),
@@ -254,27 +304,44 @@ def zero_fused_step_buckets(plan: Plan, rank: int, bucket_begin: int, bucket_end
 
 
 def zero_allgather_params(plan: Plan, masters, full_param, stream=None):
+    if len(masters) != plan.n_ranks:
+        raise ValueError(f"masters holds {len(masters)} shards; the plan has {plan.n_ranks} ranks")
+    for i, t in enumerate(masters):
+        _need(t, plan.shard_elems, f"masters[{i}]")
+    _need(full_param, plan.psi_padded, "full_param")
     _check(_lib.zero_allgather_params(plan.handle, _ptr_array(masters, torch.float32, "masters"),
                                       _dev(full_param, torch.bfloat16, "full_param"), _stream(stream)))
 
 
 def ddp_allreduce(plan: Plan, grads, g_full, stream=None):
+    _check_step(plan, ZERO_ALL_RANKS, grads, [("g_full", g_full)])
     _check(_lib.ddp_allreduce(plan.handle, _ptr_array(grads, torch.bfloat16, "grads"),
                               _dev(g_full, torch.float32, "g_full"), _stream(stream)))
 
 
 def fsdp_gather_rows(w_shards, w_full, stream=None):
     n = len(w_shards)
-    rows, k = w_full.shape
-    _check(_lib.fsdp_gather_rows(n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, k,
+    rs, k = _shards_shape(w_shards, "w_shards")
+    if w_full.dim() != 2 or tuple(w_full.shape) != (n * rs, k):
+        raise ValueError(f"w_full must be [{n * rs}, {k}] (got {tuple(w_full.shape)})")
+    _check(_lib.fsdp_gather_rows(n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), n * rs, k,
                                  _dev(w_full, torch.bfloat16, "w_full"), _stream(stream)))
 
 
-def fsdp_unit_forward(w_shards, A, Y, Y_bf16=None, scratch_w=None, stream=None):
+def _forward_shapes(w_shards, A, Y, Y_bf16, scratch_w):
     n = len(w_shards)
-    rows = sum(int(s.shape[0]) for s in w_shards)
-    k = int(A.shape[1])
-    m_tok = int(A.shape[0])
+    rs, k = _shards_shape(w_shards, "w_shards")
+    if A.dim() != 2 or int(A.shape[1]) != k:
+        raise ValueError(f"A must be [m_tokens, {k}] (got {tuple(A.shape)})")
+    rows, m_tok = n * rs, int(A.shape[0])
+    _need(Y, m_tok * rows, "Y")
+    _need(Y_bf16, m_tok * rows, "Y_bf16")
+    _need(scratch_w, rows * k, "scratch_w")
+    return n, rows, k, m_tok
+
+
+def fsdp_unit_forward(w_shards, A, Y, Y_bf16=None, scratch_w=None, stream=None):
+    n, rows, k, m_tok = _forward_shapes(w_shards, A, Y, Y_bf16, scratch_w)
     _check(_lib.fsdp_unit_forward(n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, k,
                                   _dev(A, torch.bfloat16, "A"), m_tok, _dev(Y, torch.float32, "Y"),
                                   _dev(Y_bf16, torch.bfloat16, "Y_bf16"),
@@ -283,7 +350,8 @@ def fsdp_unit_forward(w_shards, A, Y, Y_bf16=None, scratch_w=None, stream=None):
 
 def fsdp_transpose_cat(srcs, dst, stream=None):
     """dst [cols, n*rows] = the n row-major [rows, cols] bf16 sources transposed side by side."""
-    rows, cols = int(srcs[0].shape[0]), int(srcs[0].shape[1])
+    rows, cols = _shards_shape(srcs, "srcs")
+    _need(dst, len(srcs) * rows * cols, "dst")
     _check(_lib.fsdp_transpose_cat(len(srcs), _ptr_array(srcs, torch.bfloat16, "srcs"), rows, cols,
                                    _dev(dst, torch.bfloat16, "dst"), _stream(stream)))
 
@@ -298,9 +366,16 @@ def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace, stream=None):
     """A, dY, dX: per-rank lists; dW: [rows_out, k_in] fp32; workspace: a uint8 CUDA tensor
     of at least fsdp_unit_backward_workspace(...) bytes."""
     n = len(w_shards)
-    rows = sum(int(s.shape[0]) for s in w_shards)
-    k = int(A[0].shape[1])
-    m_tok = int(A[0].shape[0])
+    rs, k = _shards_shape(w_shards, "w_shards")
+    rows = n * rs
+    if not (len(A) == len(dY) == len(dX) == n):
+        raise ValueError(f"A, dY and dX must hold one tensor per rank ({n})")
+    m_tok, ka = _shards_shape(A, "A")
+    if ka != k or _shards_shape(dY, "dY") != (m_tok, rows):
+        raise ValueError(f"A must be [m_tokens, {k}] and dY [m_tokens, {rows}] per rank")
+    for i, t in enumerate(dX):
+        _need(t, m_tok * k, f"dX[{i}]")
+    _need(dW, rows * k, "dW")
     _check(_lib.fsdp_unit_backward(
         n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, k, _ptr_array(A, torch.bfloat16, "A"),
         _ptr_array(dY, torch.bfloat16, "dY"), m_tok, _ptr_array(dX, torch.float32, "dX"),
@@ -311,8 +386,18 @@ def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace, stream=None):
 def fsdp_mlp_forward(gate_shards, up_shards, down_shards, X, H, Y, scratch_down=None, stream=None,
                      prefetch_stream=None):
     n = len(gate_shards)
-    d_ff = sum(int(s.shape[0]) for s in gate_shards)
-    d_model = int(X.shape[1])
+    fs, d_model = _shards_shape(gate_shards, "gate_shards")
+    d_ff = n * fs
+    if len(up_shards) != n or _shards_shape(up_shards, "up_shards") != (fs, d_model):
+        raise ValueError("up_shards must match gate_shards")
+    ds, dff2 = _shards_shape(down_shards, "down_shards")
+    if len(down_shards) != n or dff2 != d_ff or n * ds != d_model:
+        raise ValueError(f"down_shards must be {n} shards of [{d_model // max(n, 1)}, {d_ff}]")
+    if X.dim() != 2 or int(X.shape[1]) != d_model:
+        raise ValueError(f"X must be [m_tokens, {d_model}] (got {tuple(X.shape)})")
+    _need(H, int(X.shape[0]) * d_ff, "H")
+    _need(Y, int(X.shape[0]) * d_model, "Y")
+    _need(scratch_down, d_model * d_ff, "scratch_down")
     _check(_lib.fsdp_mlp_forward(
         n, _ptr_array(gate_shards, torch.bfloat16, "gate_shards"), _ptr_array(up_shards, torch.bfloat16, "up_shards"),
         _ptr_array(down_shards, torch.bfloat16, "down_shards"), d_model, d_ff, _dev(X, torch.bfloat16, "X"),
@@ -324,11 +409,10 @@ def fsdp_mlp_forward(gate_shards, up_shards, down_shards, X, H, Y, scratch_down=
 def fsdp_unit_forward_static_scratch(w_shards, A, Y, Y_bf16=None, stream=None):
     """fsdp_unit_forward with the gathered W in the library's own 16 MiB device array
     (for callers that cannot allocate); no scratch argument."""
-    n = len(w_shards)
-    rows = sum(int(s.shape[0]) for s in w_shards)
+    n, rows, k, m_tok = _forward_shapes(w_shards, A, Y, Y_bf16, None)
     _check(_lib.fsdp_unit_forward_static_scratch(
-        n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, int(A.shape[1]), _dev(A, torch.bfloat16, "A"),
-        int(A.shape[0]), _dev(Y, torch.float32, "Y"), _dev(Y_bf16, torch.bfloat16, "Y_bf16"), _stream(stream)))
+        n, _ptr_array(w_shards, torch.bfloat16, "w_shards"), rows, k, _dev(A, torch.bfloat16, "A"),
+        m_tok, _dev(Y, torch.float32, "Y"), _dev(Y_bf16, torch.bfloat16, "Y_bf16"), _stream(stream)))
 
 
 def zero_device_status(stream=None):
