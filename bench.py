@@ -561,13 +561,28 @@ def oracle_beside_legs(legs: dict, budget_s: float = 1.5):
                           f"(float64); {k} calls"}
 
 
+def host_info() -> dict:
+    """The host the oracle was timed on: architecture, logical CPUs, CPU model if known."""
+    import platform
+    info = {"machine": platform.machine(), "nproc": os.cpu_count()}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.split(":")[0].strip() in ("model name", "CPU part", "Hardware"):
+                    info["cpu"] = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return info
+
+
 def cpu_baseline(budget_s: float = 15.0):
     n_params = 4 * MIB
     s = OracleSample(n_params)
     el = s.step(n_params)
     reps = max(1, int(budget_s / max(el, 1e-3)))
     total = sum(s.step(n_params) for _ in range(reps))
-    return {"value": n_params * reps / total, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": n_params * reps / total, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_info(),
             "sample": f"first {n_params:,} of 124,356,864 GPT-2-small parameters, N=8 gradient slices, "
                       f"{reps} fused steps ({total:.1f} s; numpy elementwise, single-threaded)"}
 
@@ -589,7 +604,7 @@ def run_reference(args):
         s.step(count)
     t_total = sum(s.step(count) for _ in range(args.steps))
     value = count * args.steps / t_total
-    cb = {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+    cb = {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_info(),
           "sample": f"first {count:,} of {psi:,} parameters per step (N=8), numpy single-threaded"}
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": 1e3 * psi / value, "higher_is_better": True, "scaling": "weak",
