@@ -17,9 +17,13 @@
  *   - Returns zero_status: ZERO_OK (0) or a negative error. On error nothing is launched
  *     and zero_last_error() returns a thread-local message describing the cause.
  *   - Tensor arguments are raw DEVICE pointers owned by the caller (e.g. allocated by
- *     PyTorch). bf16 tensors are passed as zero_bf16 (raw IEEE bfloat16 bits).
- *     Any alignment is accepted; 16-byte-aligned buffers take the vectorised / TMA path,
- *     others a scalar path with bit-identical results.
+ *     PyTorch); zero_fused_step_host alone takes page-locked host buffers. bf16 tensors
+ *     are passed as zero_bf16 (raw IEEE bfloat16 bits). No call is given buffer lengths:
+ *     each buffer must hold what the call's description states.
+ *   - The step calls accept any alignment: 16-byte-aligned buffers take the vectorised
+ *     path, others a scalar path with bit-identical results. The FSDP calls (whose GEMM
+ *     operands are TMA tensor maps) require 16-byte-aligned buffers and return
+ *     ZERO_ERR_INVALID_ARG otherwise.
  *   - Arrays of per-rank pointers (grads[], masters[], w_shards[]) are HOST arrays of
  *     n_ranks device pointers; they are copied into the kernel's parameters, so the host
  *     array may be reused as soon as the call returns.
