@@ -20,10 +20,11 @@
  *     PyTorch); zero_fused_step_host alone takes page-locked host buffers. bf16 tensors
  *     are passed as zero_bf16 (raw IEEE bfloat16 bits). No call is given buffer lengths:
  *     each buffer must hold what the call's description states.
- *   - The step calls accept any alignment: 16-byte-aligned buffers take the vectorised
- *     path, others a scalar path with bit-identical results. The FSDP calls (whose GEMM
- *     operands are TMA tensor maps) require 16-byte-aligned buffers and return
- *     ZERO_ERR_INVALID_ARG otherwise.
+ *   - The step calls, fsdp_gather_rows and fsdp_transpose_cat accept any alignment:
+ *     16-byte-aligned buffers take the vectorised path, others a scalar path with
+ *     bit-identical results. The GEMM-based FSDP calls (fsdp_unit_forward and its static-
+ *     scratch variant, fsdp_unit_backward, fsdp_mlp_forward), whose operands are TMA tensor
+ *     maps, require 16-byte-aligned buffers and return ZERO_ERR_INVALID_ARG otherwise.
  *   - Arrays of per-rank pointers (grads[], masters[], w_shards[]) are HOST arrays of
  *     n_ranks device pointers; they are copied into the kernel's parameters, so the host
  *     array may be reused as soon as the call returns.
