@@ -1,0 +1,62 @@
+"""Seeded random shapes for the FSDP unit: the forward with the gather fused into the GEMM's
+loads (shard rows a multiple of 256) or through a scratch buffer (any shard rows), the
+backward on both its in-place and its transposed path, and the MLP unit; each checked
+against the oracle by the same bounds as the fixed-shape tests."""
+import numpy as np
+import pytest
+
+import test_fsdp_parity as F  # the fixed-shape checks, called with random shapes
+from test_fsdp_parity import z  # noqa: F401  (fixture)
+
+pytestmark = pytest.mark.gpu
+
+
+def forward_case(i):
+    rng = np.random.default_rng(2000 + i)
+    n = int(rng.choice([1, 2, 3, 4, 8]))
+    k = 8 * int(rng.integers(1, 130))
+    m = int(rng.integers(1, 700))
+    if i % 2 == 0:  # fused gather: shard rows a multiple of 256
+        return "fused", m, n * 256 * int(rng.integers(1, 4)), k, n
+    return "scratch", m, n * int(rng.integers(1, 300)), k, n
+
+
+def backward_case(i):
+    rng = np.random.default_rng(3000 + i)
+    n = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+    if i % 2 == 0:  # in place: R / N, K and M multiples of 64
+        return n, n * 64 * int(rng.integers(1, 6)), 64 * int(rng.integers(1, 9)), 64 * int(rng.integers(1, 5))
+    rows = n * 8 * int(rng.integers(1, 40))
+    k = 8 * int(rng.integers(1, 70))
+    m = int(rng.integers(1, 300))
+    while (n * m) % 8:  # the GEMMs' 16-byte rows
+        m += 1
+    return n, rows, k, m
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_random_forward(z, i):
+    path, m, rows, k, n = forward_case(i)
+    if path == "fused":
+        F.test_gemm_fused_gather_vs_oracle(z, m, rows, k, n)
+    else:
+        F.test_gemm_scratch_gather_vs_oracle(z, m, rows, k, n)
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_random_backward(z, i):
+    n, rows, k, m = backward_case(i)
+    F.test_backward_vs_oracle(z, n, rows, k, m)
+    if rows * k <= 1 << 20 and n * m * max(rows, k) <= 1 << 22:
+        F.test_backward_integer_values_exact(z, n, rows, k, m)
+
+
+@pytest.mark.parametrize("i", range(4))
+def test_random_mlp_unit(z, i):
+    rng = np.random.default_rng(4000 + i)
+    n = int(rng.choice([1, 2, 4]))
+    scratch = bool(i % 2)
+    d = n * 256 * int(rng.integers(1, 3)) if not scratch else n * 8 * int(rng.integers(1, 64))
+    f = n * 128 * int(rng.integers(1, 4))
+    m = int(rng.integers(1, 400))
+    F.test_mlp_unit_vs_oracle(z, n, d, f, m, scratch)
