@@ -400,7 +400,7 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
     try:
         total_ms, total_flop = 0.0, 0.0
         for name, (R, K, A) in mats.items():
-            shards = synth.weight_shards(R, K, n, device=dev, seed_key=hash(name) % 1000)
+            shards = synth.weight_shards(R, K, n, device=dev, seed_key={"up": 11, "gate": 12, "down": 13}[name])
             Y = torch.empty(M, R, device=dev)
             ms = time_launches(lambda: z.fsdp_unit_forward(shards, A, Y, stream=stream), 10, stream)
             flop = 2.0 * M * R * K
@@ -413,6 +413,14 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         res["roofline"] = {"bound": "tensor", "achieved": res["tflops"], "peak": tf_peak, "unit": "TFLOP/s",
                            "frac": res["tflops"] / tf_peak,
                            "peak_source": f"{peak_src} bf16_tflops (burst)" if peak_src == "measured" else "fallback"}
+        # the same W_up GEMM with a bf16-only output (Y = NULL): half the output bytes
+        shards = synth.weight_shards(14336, 4096, n, device=dev, seed_key=11)
+        Yb = torch.empty(M, 14336, dtype=torch.bfloat16, device=dev)
+        ms = time_launches(lambda: z.fsdp_unit_forward(shards, X, None, Y_bf16=Yb, stream=stream), 10, stream)
+        res["up_bf16_output"] = {"ms": ms, "tflops": 2.0 * M * 14336 * 4096 / ms / 1e9,
+                                 "frac": 2.0 * M * 14336 * 4096 / ms / 1e9 / tf_peak,
+                                 "note": "Y_bf16 only (no fp32 Y); not part of the unit's fp32-output roofline"}
+        del shards, Yb
         # row a6 on its own: the materialised all-gather of W_up's 8 row shards (4 B per
         # element) and the backward's transpose of the same shards into W^T (4 B per element)
         hbm = peaks()[0]

@@ -450,7 +450,9 @@ extern "C" int fsdp_unit_forward(int n_ranks, const zero_bf16* const w_shards[],
   CHECK_ARG(rows_out % n_ranks == 0, "%s: rows_out %lld is not a multiple of n_ranks %d", who, (long long)rows_out,
             n_ranks);
   CHECK_ARG(k_in % 8 == 0, "%s: k_in %lld must be a multiple of 8 (16-byte rows)", who, (long long)k_in);
-  CHECK_ARG(A != nullptr && Y != nullptr && w_shards != nullptr, "%s: NULL argument", who);
+  CHECK_ARG(A != nullptr && w_shards != nullptr, "%s: NULL argument", who);
+  CHECK_ARG(Y != nullptr || Y_bf16 != nullptr, "%s: Y and Y_bf16 are both NULL", who);
+  CHECK_ARG(Y != nullptr || rows_out % 8 == 0, "%s: a bf16-only output needs rows_out %% 8 == 0", who);
   CHECK_ARG(aligned(A, 16) && aligned(Y, 16) && (!Y_bf16 || aligned(Y_bf16, 16)) &&
                 (!scratch_w || aligned(scratch_w, 16)),
             "%s: A, Y, Y_bf16 and scratch_w must be 16-byte aligned", who);

@@ -86,6 +86,8 @@ struct GemmParams {
   int y_shard_rows;              // Y split by rows into pieces of y_shard_rows rows
   int a_mn, b_mn;                // operand stored MN-major
   int y_tma;                     // write Y through shared memory and TMA stores
+  CUtensorMap ybmap;             // bf16-only output: Y_bf16 [M, R], box 64 x 32, 128B swizzle (yb_tma)
+  int yb_tma;                    // no fp32 Y: write bf16 Y through shared memory and TMA stores
 };
 constexpr uint32_t kMnChunk = 64 * BK * 2;  // one 64-column chunk of an MN-major stage operand: 8 KiB
 
@@ -348,6 +350,44 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
           tmem_ld_32cols(taddr + TN + c, u);
           if (row < p.m && n0 + c < p.r) store_gate_up_chunk(p, row, n0 + c, g, u);
         }
+      } else if (p.yb_tma) {
+        // bf16-only output: 64 columns per chunk (two 32-column TMEM loads), each row packed
+        // to 128 B of bf16 and placed with the 128-byte swizzle as in the fp32 path below
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 64) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32cols(taddr + c, r0);
+          tmem_ld_32cols(taddr + c + 32, r1);
+          if (n0 + c >= p.r) continue;  // warp-uniform
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float a0 = __uint_as_float(r0[2 * j]), a1 = __uint_as_float(r0[2 * j + 1]);
+            float b0 = __uint_as_float(r1[2 * j]), b1 = __uint_as_float(r1[2 * j + 1]);
+            if (p.alpha != 1.0f) {
+              a0 = __fmul_rn(a0, p.alpha);
+              a1 = __fmul_rn(a1, p.alpha);
+              b0 = __fmul_rn(b0, p.alpha);
+              b1 = __fmul_rn(b1, p.alpha);
+            }
+            w[j] = pack_bf16x2(a0, a1);
+            w[16 + j] = pack_bf16x2(b0, b1);
+          }
+          uint8_t* buf = epi + (epi_chunk & 1u) * 4096u;
+          if (lane == 0 && epi_chunk >= 2) bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.ybmap, n0 + c, m0 + q * 32, smem_u32(buf));
+            bulk_commit_group();
+          }
+          ++epi_chunk;
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -502,8 +542,16 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
     if (GATE_UP && (rc = encode_2d(&p.w2[s], B2[s], k_in, B.piece_rows, BK, TN))) return rc;
   }
   const int64_t y_rows = m_tokens / y_pieces;
+  const bool no_f32 = Y == nullptr || Y[0] == nullptr;
+  if (!GATE_UP && no_f32) {  // bf16-only output through TMA stores
+    if (!Y_bf16 || y_pieces != 1 || rows_out % 8 || (reinterpret_cast<uintptr_t>(Y_bf16) & 15))
+      return set_error(ZERO_ERR_UNSUPPORTED,
+                       "%s: a bf16-only output needs one 16-byte-aligned Y_bf16 with rows_out %% 8 == 0", who);
+    if ((rc = encode_2d(&p.ybmap, Y_bf16, rows_out, m_tokens, 64, 32))) return rc;
+    p.yb_tma = 1;
+  }
   // fp32 output through TMA stores when its rows are 16-byte multiples (R % 4 == 0)
-  bool y_aligned = !GATE_UP && Y != nullptr && rows_out % 4 == 0;
+  bool y_aligned = !GATE_UP && !no_f32 && rows_out % 4 == 0;
   for (int s = 0; y_aligned && s < y_pieces; ++s) y_aligned = (reinterpret_cast<uintptr_t>(Y[s]) & 15) == 0;
   if (y_aligned) {
     for (int s = 0; s < y_pieces; ++s)

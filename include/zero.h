@@ -243,6 +243,8 @@ ZERO_API int fsdp_gather_rows(int n_ranks, const zero_bf16* const w_shards[], in
  * (the [out, in] layout of a linear layer) assembled from its N row shards, fp32
  * accumulation on the tensor cores. A: row-major [m_tokens, k_in] bf16. Y: row-major
  * [m_tokens, rows_out] fp32. Y_bf16 (nullable): bf16 copy of Y (round-to-nearest-even).
+ * Y may be NULL when Y_bf16 is given (needs rows_out % 8 == 0): only the bf16 result is
+ * written, with the same bits as the bf16 copy, and half the output bytes.
  * scratch_w (nullable): a [rows_out, k_in] bf16 buffer; if given, the shards are first
  * gathered into it (fsdp_gather_rows) and the GEMM reads the gathered W, which the caller
  * frees after use; if NULL the gather is fused into the GEMM's loads (each tile is loaded

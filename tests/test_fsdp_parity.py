@@ -95,6 +95,22 @@ def test_gemm_scratch_gather_vs_oracle(z, m, rows, k, n):
         assert torch.equal(Y.view(torch.int32), Y2.view(torch.int32)), "fused and scratch gathers disagree"
 
 
+@pytest.mark.parametrize("m,rows,k,n,scratch", [(300, 2048, 264, 8, False), (129, 512, 72, 2, False),
+                                                 (200, 1000, 136, 5, True), (1, 256, 8, 1, False)])
+def test_gemm_bf16_only_output_equals_rounded_fp32(z, m, rows, k, n, scratch):
+    """With Y = NULL the kernel writes only bf16 Y (TMA stores of 64-column chunks); it must
+    equal, bit for bit, the round-to-nearest-even of the fp32 result of the same GEMM."""
+    shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=rows + k)
+    A = synth.activations(m, k, device=DEV, seed_key=m)
+    sw = (lambda: torch.empty(rows, k, dtype=torch.bfloat16, device=DEV)) if scratch else (lambda: None)
+    Y = torch.empty(m, rows, device=DEV)
+    z.fsdp_unit_forward(shards, A, Y, scratch_w=sw())
+    Yb = torch.full((m, rows), float("nan"), dtype=torch.bfloat16, device=DEV)
+    z.fsdp_unit_forward(shards, A, None, Y_bf16=Yb, scratch_w=sw())
+    z.zero_device_status()
+    assert_bf16_identical(bits16(Yb), O.f32_to_bf16(f32(Y)), "bf16-only output")
+
+
 def test_gemm_integer_values_exact(z):
     """Small integers: every product and partial sum is exact in fp32, so any summation
     order gives the exact result; checks orientation (Y = A W^T) and shard order."""
