@@ -12,9 +12,15 @@
 //   warp 1        allocates 512 TMEM columns, then one lane issues tcgen05.mma
 //                 (M=128, N=256, K=16; fp32 accumulators in TMEM, two 256-column buffers)
 //                 and tcgen05.commit frees each stage and publishes each finished tile;
-//   warps 2-5     epilogue: tcgen05.ld 32 columns at a time, fp32 (and optional bf16)
-//                 streaming stores to HBM, then release the accumulator buffer, so the
-//                 epilogue of tile i overlaps the main loop of tile i+1.
+//   warps 2-5     epilogue: tcgen05.ld 32 columns at a time into registers, each warp's
+//                 32 x 32 fp32 chunks staged in shared memory (128-byte swizzle) and
+//                 written by TMA stores (64-column bf16 chunks when only a bf16 Y is asked
+//                 for), then the accumulator buffer is released, so the epilogue of tile i
+//                 overlaps the main loop of tile i+1.
+// Other modes of the same kernel: gate-up (two B operands, one N = 256 MMA per K step,
+// SiLU-gate epilogue writing bf16 H), A split by rows into pieces with matching Y pieces
+// (the backward's dX for all ranks in one launch), and MN-major A / B operands split along
+// K (the backward reading W and dY in place; see GemmParams).
 // Every mbarrier wait is bounded (error word + CTA abort flag, no trap); after an abort
 // the producer drains its copies and the MMA warp its MMAs before TMEM is released.
 #include <cuda.h>
