@@ -19,9 +19,10 @@ from __future__ import annotations
 
 import os
 
-# The oracle's numpy calls (cpu_baseline, the reference arm, the timings beside each leg)
-# run on one host thread, so the cores they report are exact: pin numpy's BLAS before
-# numpy is first imported.
+# Each oracle call (cpu_baseline, the reference arm, the timings beside each leg) runs on
+# one host thread; cpu_baseline and the reference arm run one such call per core on
+# disjoint ranges. Pin numpy's BLAS before numpy is first imported, so the cores they
+# report are exact.
 os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
 
 import argparse
@@ -479,9 +480,12 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
 class OracleSample:
     """The first n_params parameters of the bench workload (N = 8 bf16 gradient slices,
     fp32 master / m / v), generated once; step() runs one fused oracle step (reduce, Adam,
-    cast in plain numpy) on the first `count` of them and returns its seconds."""
+    cast in plain numpy) on the first `count` of them and returns its seconds. With
+    threads > 1 the same oracle call runs on `threads` contiguous ranges at once: the step
+    is elementwise, so the split changes no result, and numpy releases the interpreter lock
+    inside its array operations."""
 
-    def __init__(self, n_params: int, n_ranks: int = 8):
+    def __init__(self, n_params: int, n_ranks: int = 8, threads: int = 1):
         import numpy as np
         import torch
 
@@ -496,16 +500,27 @@ class OracleSample:
                       for r in range(n_ranks)]
         self.hp = O.AdamHyper()
         self.t = 0
+        self.threads = max(1, int(threads))
+        self._pool = None
+        if self.threads > 1:
+            from concurrent.futures import ThreadPoolExecutor
+            self._pool = ThreadPoolExecutor(self.threads)
+
+    def _range(self, lo: int, hi: int) -> None:
+        w, m, v, _ = self.O.fused_step_elements([g[lo:hi] for g in self.grads], self.master[lo:hi],
+                                                self.m[lo:hi], self.v[lo:hi], self.hp, self.t)
+        self.master[lo:hi], self.m[lo:hi], self.v[lo:hi] = w, m, v
 
     def step(self, count: int) -> float:
         count = min(count, self.n)
         self.t += 1
+        cuts = [count * i // self.threads for i in range(self.threads + 1)]
         t0 = time.perf_counter()
-        w, m, v, _ = self.O.fused_step_elements([g[:count] for g in self.grads], self.master[:count],
-                                                self.m[:count], self.v[:count], self.hp, self.t)
-        el = time.perf_counter() - t0
-        self.master[:count], self.m[:count], self.v[:count] = w, m, v
-        return el
+        if self._pool is None:
+            self._range(0, count)
+        else:
+            list(self._pool.map(lambda i: self._range(cuts[i], cuts[i + 1]), range(self.threads)))
+        return time.perf_counter() - t0
 
 
 def _time_bounded(fn, budget_s: float):
@@ -584,15 +599,23 @@ def host_info() -> dict:
     return info
 
 
-def cpu_baseline(budget_s: float = 15.0):
-    n_params = 4 * MIB
-    s = OracleSample(n_params)
+def cpu_baseline(budget_s: float = 12.0, one_core_s: float = 4.0):
+    """The oracle on every host core (contiguous ranges of the sample, one thread each), and
+    for context the same oracle on one core."""
+    cores = os.cpu_count() or 1
+    n_params = 16 * MIB
+    s = OracleSample(n_params, threads=cores)
     el = s.step(n_params)
     reps = max(1, int(budget_s / max(el, 1e-3)))
     total = sum(s.step(n_params) for _ in range(reps))
-    return {"value": n_params * reps / total, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_info(),
+    one = OracleSample(4 * MIB)
+    one_el, one_reps = _time_bounded(lambda: one.step(4 * MIB), one_core_s)
+    return {"value": n_params * reps / total, "unit": UNIT, "cores": cores, "kind": "oracle", "host": host_info(),
+            "one_core_value": 4 * MIB / one_el,
             "sample": f"first {n_params:,} of 124,356,864 GPT-2-small parameters, N=8 gradient slices, "
-                      f"{reps} fused steps ({total:.1f} s; numpy elementwise, single-threaded)"}
+                      f"{reps} fused steps ({total:.1f} s), split into {cores} contiguous ranges run by "
+                      f"{cores} threads (numpy elementwise); one_core_value: the first {4 * MIB:,} on one "
+                      f"thread, {one_reps} steps"}
 
 
 def run_reference(args):
@@ -602,8 +625,10 @@ def run_reference(args):
         return
     import synth
     psi, n, stage, bb = synth.GPT2_SMALL_PSI, 8, "zero2", 25 * MIB
-    cap = 4 * MIB
-    s = OracleSample(cap)
+    cap = 16 * MIB
+    cores = os.cpu_count() or 1
+    s = OracleSample(cap, threads=cores)
+    s.step(cap)
     rate = cap / s.step(cap)
     # size each step's sample so the whole run stays near args.ref_seconds
     per_step = args.ref_seconds / max(1, args.steps + args.warmup)
@@ -612,8 +637,9 @@ def run_reference(args):
         s.step(count)
     t_total = sum(s.step(count) for _ in range(args.steps))
     value = count * args.steps / t_total
-    cb = {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_info(),
-          "sample": f"first {count:,} of {psi:,} parameters per step (N=8), numpy single-threaded"}
+    cb = {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "host": host_info(),
+          "sample": f"first {count:,} of {psi:,} parameters per step (N=8), numpy elementwise, split into "
+                    f"{cores} contiguous ranges run by {cores} threads"}
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": 1e3 * psi / value, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; GPT-2-small tensor shapes)",

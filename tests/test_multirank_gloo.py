@@ -61,3 +61,21 @@ def test_two_gloo_ranks_aggregate_like_the_bench():
         assert out[rank][1] == pytest.approx(2 * 1000 * 10 / 2.0)
     assert '"impl": "reference"' in out[0][2]
     assert out[1][2] == ""
+
+
+def test_oracle_split_across_threads_changes_no_bit():
+    """cpu_baseline and the reference arm run the oracle on every host core by splitting
+    the sample into contiguous ranges; the step is elementwise, so three steps of the split
+    run must leave master, m and v identical to three steps of one call over everything."""
+    sys.path.insert(0, str(ROOT))
+    import numpy as np
+
+    import bench
+    n = 100_003
+    one, split = bench.OracleSample(n), bench.OracleSample(n, threads=7)
+    for count in (n, n - 17, n):
+        one.step(count)
+        split.step(count)
+    for a, b in ((one.master, split.master), (one.m, split.m), (one.v, split.v)):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert one.t == split.t == 3
