@@ -35,7 +35,7 @@ EXPORTS = (
     "zero_fused_step_buckets", "zero_allgather_params", "ddp_allreduce",
     "fsdp_gather_rows", "fsdp_unit_forward", "fsdp_transpose_cat", "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward",
     "fsdp_unit_forward_static_scratch",
-    "zero_last_error", "zero_device_status", "zero_selftest_bounded_wait", "zero_set_fused_kernel", "zero_version",
+    "zero_last_error", "zero_device_status", "zero_selftest_bounded_wait", "zero_set_fused_kernel", "zero_set_gemm_kernel", "zero_version",
 )
 
 
@@ -96,6 +96,7 @@ def _load():
         "zero_device_status": (I, [VP]),
         "zero_selftest_bounded_wait": (I, [C.c_uint32, VP]),
         "zero_set_fused_kernel": (I, [I]),
+        "zero_set_gemm_kernel": (I, [I]),
         "zero_version": (I, []),
     }
     for name, (res, args) in sig.items():
@@ -425,6 +426,10 @@ def zero_selftest_bounded_wait(timeout_ms: int, stream=None):
 
 def zero_set_fused_kernel(which: int):
     _check(_lib.zero_set_fused_kernel(which))
+
+
+def zero_set_gemm_kernel(which: int):
+    _check(_lib.zero_set_gemm_kernel(which))
 
 
 def zero_version() -> int:

@@ -508,4 +508,11 @@ extern "C" int zero_set_fused_kernel(int which) {
   return ZERO_OK;
 }
 
+extern "C" int zero_set_gemm_kernel(int which) {
+  clear_error();
+  CHECK_ARG(which >= 0 && which <= 2, "zero_set_gemm_kernel: %d is not 0, 1 or 2", which);
+  set_gemm_kernel(which);
+  return ZERO_OK;
+}
+
 extern "C" int zero_version(void) { return 100; }

@@ -1,23 +1,31 @@
 // FSDP unit GEMM on the 5th-generation tensor cores: Y[M, R] = A[M, K] * W^T, where W
 // [R, K] (the [out, in] layout of a linear layer) is held as N dim-0 row shards.
 //
-// The all-gather of W is fused into the operand loads: each 256-row tile of W lies inside
-// one shard (shard rows are a multiple of 256), so the TMA producer picks that shard's
-// tensor map and loads the tile straight from the shard; the full W is never assembled.
-// (With a caller scratch buffer the host instead gathers W first and passes one map.)
+// The all-gather of W is fused into the operand loads: each W tile (or each CTA's half of
+// one) lies inside one shard, so the TMA producer picks that shard's tensor map and loads
+// the tile straight from the shard; the full W is never assembled. (With a caller scratch
+// buffer the host instead gathers W first and passes one map.)
 //
-// Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles):
+// Two kernels compute the same sums in the same order (bit-identical results):
+//   fsdp_gemm_pair_kernel  a cluster of two CTAs per 256-row tile, tcgen05.mma.cta_group::2
+//                          (M = 256, N = 256) over both CTAs' shared memory: each CTA loads
+//                          half of A and half of B, a third fewer operand bytes per flop.
+//                          The default for K-major operands.
+//   fsdp_gemm_kernel       one CTA per 128 x 256 tile, tcgen05.mma.cta_group::1. The
+//                          default where an operand is MN-major (the backward's in-place
+//                          GEMMs), where the pair measured no faster.
+// One-CTA kernel structure (one CTA per SM, persistent over its output tiles):
 //   warp 0        TMA producer: A tile 128x64 and W tile 256x64 (bf16, 128-byte swizzle)
 //                 per 64-wide K block into a 4-stage shared-memory ring;
 //   warp 1        allocates 512 TMEM columns, then one lane issues tcgen05.mma
 //                 (M=128, N=256, K=16; fp32 accumulators in TMEM, two 256-column buffers)
 //                 and tcgen05.commit frees each stage and publishes each finished tile;
-//   warps 2-5     epilogue: tcgen05.ld 32 columns at a time into registers, each warp's
-//                 32 x 32 fp32 chunks staged in shared memory (128-byte swizzle) and
-//                 written by TMA stores (64-column bf16 chunks when only a bf16 Y is asked
-//                 for), then the accumulator buffer is released, so the epilogue of tile i
-//                 overlaps the main loop of tile i+1.
-// Other modes of the same kernel: gate-up (two B operands, one N = 256 MMA per K step,
+//   warps 2-5     epilogue (epilogue_tile, shared with the pair kernel): tcgen05.ld 32
+//                 columns at a time into registers, each warp's 32 x 32 fp32 chunks staged
+//                 in shared memory (128-byte swizzle) and written by TMA stores (64-column
+//                 bf16 chunks when only a bf16 Y is asked for), then the accumulator buffer
+//                 is released, so the epilogue of tile i overlaps the main loop of tile i+1.
+// Other modes of both kernels: gate-up (two B operands, one N = 256 MMA per K step,
 // SiLU-gate epilogue writing bf16 H), A split by rows into pieces with matching Y pieces
 // (the backward's dX for all ranks in one launch), and MN-major A / B operands split along
 // K (the backward reading W and dY in place; see GemmParams).
@@ -27,6 +35,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -175,6 +184,97 @@ __device__ __forceinline__ void store_gate_up_chunk(const GemmParams& p, int row
   } else {
     for (int j = 0; j < 32; ++j)
       if (col0 + j < p.r) brow[col0 + j] = f32_to_bf16_bits(h[j]);
+  }
+}
+
+// Epilogue of one output tile, run by the four epilogue warps after the tile's accumulator
+// is complete: warp quarter q reads TMEM lanes [32q, 32q + 32) (tile rows 32q + lane) at
+// taddr, stages its chunks in its 8 KiB of shared memory at epi for TMA stores, and writes
+// rows m0 + 32q + lane, columns n0 .. n0 + TN of Y (row piece ash, local row ml) or of H.
+template <bool GATE_UP>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, uint8_t* epi, uint32_t& epi_chunk,
+                                              int m0, int n0, int ash, int ml, int q, int lane) {
+  constexpr int TN = Mode<GATE_UP>::TN;
+  const int row = m0 + q * 32 + lane;
+  if constexpr (GATE_UP) {
+#pragma unroll 1
+    for (int c = 0; c < TN; c += 32) {
+      uint32_t g[32], u[32];
+      tmem_ld_32cols(taddr + c, g);
+      tmem_ld_32cols(taddr + TN + c, u);
+      if (row < p.m && n0 + c < p.r) store_gate_up_chunk(p, row, n0 + c, g, u);
+    }
+  } else if (p.yb_tma) {
+    // bf16-only output: 64 columns per chunk (two 32-column TMEM loads), each row packed
+    // to 128 B of bf16 and placed with the 128-byte swizzle as in the fp32 path below
+#pragma unroll 1
+    for (int c = 0; c < TN; c += 64) {
+      uint32_t r0[32], r1[32];
+      tmem_ld_32cols(taddr + c, r0);
+      tmem_ld_32cols(taddr + c + 32, r1);
+      if (n0 + c >= p.r) continue;  // warp-uniform
+      uint32_t w[32];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float a0 = __uint_as_float(r0[2 * j]), a1 = __uint_as_float(r0[2 * j + 1]);
+        float b0 = __uint_as_float(r1[2 * j]), b1 = __uint_as_float(r1[2 * j + 1]);
+        if (p.alpha != 1.0f) {
+          a0 = __fmul_rn(a0, p.alpha);
+          a1 = __fmul_rn(a1, p.alpha);
+          b0 = __fmul_rn(b0, p.alpha);
+          b1 = __fmul_rn(b1, p.alpha);
+        }
+        w[j] = pack_bf16x2(a0, a1);
+        w[16 + j] = pack_bf16x2(b0, b1);
+      }
+      uint8_t* buf = epi + (epi_chunk & 1u) * 4096u;
+      if (lane == 0 && epi_chunk >= 2) bulk_wait_group_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.ybmap, n0 + c, m0 + q * 32, smem_u32(buf));
+        bulk_commit_group();
+      }
+      ++epi_chunk;
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < TN; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32cols(taddr + c, r);
+      if (n0 + c >= p.r) continue;  // warp-uniform
+      if (p.alpha != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), p.alpha));
+      }
+      if (p.y_tma) {
+        // lane = row of a 32 x 32 chunk: 128-byte rows, 16-byte pieces placed with the
+        // 128-byte swizzle (piece j of row i at slot j ^ (i % 8)): conflict-free writes,
+        // and the layout the tensor map's swizzle reads back in order
+        uint8_t* buf = epi + (epi_chunk & 1u) * 4096u;
+        if (lane == 0 && epi_chunk >= 2) bulk_wait_group_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+              make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.ymap[ash], n0 + c, ml + q * 32, smem_u32(buf));
+          bulk_commit_group();
+        }
+        ++epi_chunk;
+        if (p.yb && row < p.m) store_row_chunk(p, row, n0 + c, r, false);
+      } else if (row < p.m) {
+        store_row_chunk(p, row, n0 + c, r, true);
+      }
+    }
   }
 }
 
@@ -333,7 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
   } else {
     // ---------------- epilogue (warps 2-5) ----------------
     const int q = warp & 3;  // a warp reads TMEM lanes [32q, 32q+32)
-    const int row_in_tile = q * 32 + lane;
     uint32_t i = 0, epi_chunk = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
       const uint32_t a = i & 1u, u = i >> 1;
@@ -343,91 +442,11 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
       tile_coords(tile, num_m, num_n, mb, nb);
       const int m0 = mb * BM;
       const int n0 = nb * TN;
-      const int row = m0 + row_in_tile;
       const int ash = m0 / p.y_shard_rows;  // the Y row piece holding this tile's rows
       const int ml = m0 - ash * p.y_shard_rows;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * ACC;
       uint8_t* epi = smem + STAGES * STAGE_BYTES + static_cast<uint32_t>(q) * 2u * 4096u;
-      if constexpr (GATE_UP) {
-#pragma unroll 1
-        for (int c = 0; c < TN; c += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld_32cols(taddr + c, g);
-          tmem_ld_32cols(taddr + TN + c, u);
-          if (row < p.m && n0 + c < p.r) store_gate_up_chunk(p, row, n0 + c, g, u);
-        }
-      } else if (p.yb_tma) {
-        // bf16-only output: 64 columns per chunk (two 32-column TMEM loads), each row packed
-        // to 128 B of bf16 and placed with the 128-byte swizzle as in the fp32 path below
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 64) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32cols(taddr + c, r0);
-          tmem_ld_32cols(taddr + c + 32, r1);
-          if (n0 + c >= p.r) continue;  // warp-uniform
-          uint32_t w[32];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float a0 = __uint_as_float(r0[2 * j]), a1 = __uint_as_float(r0[2 * j + 1]);
-            float b0 = __uint_as_float(r1[2 * j]), b1 = __uint_as_float(r1[2 * j + 1]);
-            if (p.alpha != 1.0f) {
-              a0 = __fmul_rn(a0, p.alpha);
-              a1 = __fmul_rn(a1, p.alpha);
-              b0 = __fmul_rn(b0, p.alpha);
-              b1 = __fmul_rn(b1, p.alpha);
-            }
-            w[j] = pack_bf16x2(a0, a1);
-            w[16 + j] = pack_bf16x2(b0, b1);
-          }
-          uint8_t* buf = epi + (epi_chunk & 1u) * 4096u;
-          if (lane == 0 && epi_chunk >= 2) bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
-                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&p.ybmap, n0 + c, m0 + q * 32, smem_u32(buf));
-            bulk_commit_group();
-          }
-          ++epi_chunk;
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld_32cols(taddr + c, r);
-          if (n0 + c >= p.r) continue;  // warp-uniform
-          if (p.alpha != 1.0f) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), p.alpha));
-          }
-          if (p.y_tma) {
-            // lane = row of a 32 x 32 chunk: 128-byte rows, 16-byte pieces placed with the
-            // 128-byte swizzle (piece j of row i at slot j ^ (i % 8)): conflict-free writes,
-            // and the layout the tensor map's swizzle reads back in order
-            uint8_t* buf = epi + (epi_chunk & 1u) * 4096u;
-            if (lane == 0 && epi_chunk >= 2) bulk_wait_group_read<1>();
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
-                  make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&p.ymap[ash], n0 + c, ml + q * 32, smem_u32(buf));
-              bulk_commit_group();
-            }
-            ++epi_chunk;
-            if (p.yb && row < p.m) store_row_chunk(p, row, n0 + c, r, false);
-          } else if (row < p.m) {
-            store_row_chunk(p, row, n0 + c, r, true);
-          }
-        }
-      }
+      epilogue_tile<GATE_UP>(p, taddr, epi, epi_chunk, m0, n0, ash, ml, q, lane);
       tc_fence_before();
       mbar_arrive(smem_u32(&acce_bar[a]));
     }
@@ -440,7 +459,223 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// ---- CTA-pair form ----
+// The same GEMM on the two-CTA tensor-core form: a cluster of two CTAs on two SMs computes
+// a 256-row output tile with tcgen05.mma.cta_group::2 (M = 256, N = 256). Each CTA loads
+// only its 128 A rows and 128 of the 256 B rows, and the MMA reads both CTAs' shared
+// memory, so every SM moves a third fewer operand bytes per flop than in the one-CTA form
+// (Mistral MLP shapes: 1.50-1.66 -> 1.65-1.81 PFLOP/s). Plain mode: CTA r loads W rows
+// n0 + 128 r of a 256-column tile. Gate-up mode: the B operand of the N = 256 MMA is the
+// gate tile followed by the up tile, so the even CTA loads the gate's 128 rows and the odd
+// CTA the up projection's, and the accumulator holds gate | up exactly as in the one-CTA
+// kernel. The other modes carry over: A and Y row pieces (each CTA's 128 rows lie in one
+// piece, as pieces are multiples of 128 rows) and MN-major operands (each CTA's half is two
+// 64-column chunks, one 3-D box).
+//   both CTAs  warp 0: TMA producer; its copies complete on the EVEN CTA's full barrier,
+//              which expects the stage bytes of both;
+//   even CTA   warp 1: issues the MMAs; tcgen05.commit multicasts to both CTAs' empty
+//              barriers (a stage is free in both) and accumulator barriers;
+//   both CTAs  warps 2-5: epilogue of the CTA's own 128 rows from its own TMEM; each warp
+//              then arrives on the even CTA's accumulator-empty barrier (8 arrivals).
+// Before leaving, each producer waits until the MMAs released every stage it filled, and
+// the two CTAs meet at a cluster barrier, so neither CTA's shared memory or barriers are
+// still targeted by the other; every mbarrier wait is bounded as in the one-CTA kernel.
+constexpr int PAIR_STAGES = 6;
+constexpr uint32_t PAIR_HALF = 128 * BK * 2;      // one CTA's 128 A rows, and its 128 B rows
+constexpr uint32_t PAIR_STAGE = 2 * PAIR_HALF;
+constexpr uint32_t PAIR_ACC = 256;                // TMEM columns of one accumulator (N = 256)
+constexpr uint32_t PAIR_EPI = 4u * 2u * 4096u;
+constexpr uint32_t PAIR_SMEM = PAIR_STAGES * PAIR_STAGE + PAIR_EPI + 1024;
+
+constexpr unsigned int kErrPairEmpty = (4u << 8) | 1u;  // producer waiting for a free stage
+constexpr unsigned int kErrPairFull = (4u << 8) | 2u;   // MMA waiting for both CTAs' copies
+constexpr unsigned int kErrPairAccE = (4u << 8) | 3u;   // MMA waiting for both CTAs' epilogues
+constexpr unsigned int kErrPairAccF = (4u << 8) | 4u;   // epilogue waiting for a finished tile
+constexpr unsigned int kErrPairDrain = (4u << 8) | 5u;  // releasing stages / draining after an abort
+
+// the walk of tile_coords over 256-row blocks (bands of 12 = the one-CTA kernel's 24 x 128 rows)
+__device__ __forceinline__ void pair_tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
+  const int g = ZGB_GEMM_GROUP_M > 0 ? (ZGB_GEMM_GROUP_M + 1) / 2 : 0;
+  const int band_rows = g > 0 && g < num_m ? g : num_m;
+  const int band = tile / (band_rows * num_n), in_band = tile - band * band_rows * num_n;
+  const int rows = min(band_rows, num_m - band * band_rows);
+  mb = band * band_rows + in_band % rows;
+  nb = in_band / rows;
+}
+
+template <bool GATE_UP>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    fsdp_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int TN = Mode<GATE_UP>::TN;  // output tile columns: 256, or 128 of H in gate-up mode
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[PAIR_STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[PAIR_STAGES];
+  __shared__ __align__(8) uint64_t accf_bar[2];
+  __shared__ __align__(8) uint64_t acce_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  volatile int* abort = &abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: the even CTA, which issues the MMAs
+  const int pair = static_cast<int>(blockIdx.x >> 1), pairs = static_cast<int>(gridDim.x >> 1);
+  const int num_m = (p.m + 255) / 256;
+  const int num_n = (p.r + TN - 1) / TN;
+  const int num_k = (p.k + BK - 1) / BK;
+  const int tiles = num_m * num_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&accf_bar[a]), 1);
+      mbar_init(smem_u32(&acce_bar[a]), 8);  // 4 epilogue warps in each CTA
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < p.a_shards; ++s) prefetch_tmap(&p.a[s]);
+    for (int s = 0; s < p.n_shards; ++s) prefetch_tmap(GATE_UP && rank ? &p.w2[s] : &p.w[s]);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&tmem_base_sh), 2 * PAIR_ACC);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated before any copy
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool stop = false;
+      for (int tile = pair; tile < tiles && !stop; tile += pairs) {
+        int mb, nb;
+        pair_tile_coords(tile, num_m, num_n, mb, nb);
+        const int m0 = mb * 256 + static_cast<int>(rank) * 128;
+        const int nrow = nb * TN + (GATE_UP ? 0 : static_cast<int>(rank) * 128);
+        // K-major pieces holding this CTA's rows; a half past the last row (M or R % 256 ==
+        // 128) starts beyond the last piece and reads zeros
+        const int ash = p.a_mn ? 0 : min(m0 / p.a_shard_rows, p.a_shards - 1);
+        const int ml = m0 - ash * p.a_shard_rows;
+        const int shard = p.b_mn ? 0 : min(nrow / p.shard_rows, p.n_shards - 1);
+        const int nl = nrow - shard * p.shard_rows;
+        const void* bmap = GATE_UP && rank ? &p.w2[shard] : &p.w[shard];
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
+          const uint32_t s = it % PAIR_STAGES, ph = (it / PAIR_STAGES) & 1u;
+          if (it >= PAIR_STAGES &&
+              !mbar_wait_bounded(smem_u32(&empty_bar[s]), ph ^ 1u, abort, &g_zgb_dev_error, kErrPairEmpty)) {
+            stop = true;
+            break;
+          }
+          const uint32_t fb = mapa_shared(smem_u32(&full_bar[s]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * PAIR_STAGE);
+          uint8_t* sa = smem + s * PAIR_STAGE;
+          if (!GATE_UP && p.a_mn) {  // K rows kb*BK.. of the piece holding them, this CTA's two M chunks
+            const int ks = kb * BK / p.a_shard_rows, kl = kb * BK - ks * p.a_shard_rows;
+            tma_load_3d_pair(smem_u32(sa), &p.a[ks], 0, kl, m0 / 64, fb);
+          } else {
+            tma_load_2d_pair(smem_u32(sa), &p.a[ash], kb * BK, ml, fb);
+          }
+          if (!GATE_UP && p.b_mn) {  // the same for B: this CTA's two chunks of 64 columns
+            const int ks = kb * BK / p.shard_rows, kl = kb * BK - ks * p.shard_rows;
+            tma_load_3d_pair(smem_u32(sa + PAIR_HALF), &p.w[ks], 0, kl, nrow / 64, fb);
+          } else {
+            tma_load_2d_pair(smem_u32(sa + PAIR_HALF), bmap, kb * BK, nl, fb);
+          }
+        }
+      }
+      // every stage this CTA filled is read by the even CTA's MMAs: wait until they released it
+      int never = 0;
+      const uint32_t first = it > static_cast<uint32_t>(PAIR_STAGES) ? it - PAIR_STAGES : 0u;
+      for (uint32_t j = first; j < it; ++j)
+        mbar_wait_bounded(smem_u32(&empty_bar[j % PAIR_STAGES]), (j / PAIR_STAGES) & 1u, &never, &g_zgb_dev_error,
+                          kErrPairDrain);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (even CTA) ----------------
+    if (rank == 0 && lane == 0) {
+      // K steps of 16 as in the one-CTA kernel: +32 B (K-major) or +2048 B (MN-major)
+      const bool a_mn = !GATE_UP && p.a_mn, b_mn = !GATE_UP && p.b_mn;
+      const uint32_t a_step = a_mn ? 128u : 2u, b_step = b_mn ? 128u : 2u;
+      const uint32_t idesc = idesc_bf16_f32(256, 256, a_mn, b_mn);
+      uint32_t it = 0, i = 0;
+      bool stop = false, issued = false;
+      for (int tile = pair; tile < tiles && !stop; tile += pairs, ++i) {
+        const uint32_t a = i & 1u, u = i >> 1;
+        if (u >= 1 && !mbar_wait_cluster_bounded(smem_u32(&acce_bar[a]), (u - 1) & 1u, abort, &g_zgb_dev_error,
+                                                 kErrPairAccE))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + a * PAIR_ACC;
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
+          const uint32_t s = it % PAIR_STAGES, ph = (it / PAIR_STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, abort, &g_zgb_dev_error, kErrPairFull)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * PAIR_STAGE);
+          const uint64_t ad = a_mn ? sw128_mnmajor_desc(sa, kMnChunk) : sw128_kmajor_desc(sa);
+          const uint64_t bd = b_mn ? sw128_mnmajor_desc(sa + PAIR_HALF, kMnChunk) : sw128_kmajor_desc(sa + PAIR_HALF);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16_pair(d, ad + a_step * k, bd + b_step * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit_pair(smem_u32(&empty_bar[s]), 0x3);
+          issued = true;
+        }
+        if (!stop) umma_commit_pair(smem_u32(&accf_bar[a]), 0x3);
+      }
+      if (*abort && issued) {
+        int never = 0;
+        umma_commit_pair(smem_u32(&drain_bar), 0x1);
+        mbar_wait_bounded(smem_u32(&drain_bar), 0, &never, &g_zgb_dev_error, kErrPairDrain);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2-5, both CTAs) ----------------
+    const int q = warp & 3;
+    const int y_pieces = p.m / p.y_shard_rows;
+    uint32_t i = 0, epi_chunk = 0;
+    for (int tile = pair; tile < tiles; tile += pairs, ++i) {
+      const uint32_t a = i & 1u, u = i >> 1;
+      if (!warp_wait(smem_u32(&accf_bar[a]), u & 1u, abort, kErrPairAccF)) break;
+      tc_fence_after();
+      int mb, nb;
+      pair_tile_coords(tile, num_m, num_n, mb, nb);
+      const int m0 = mb * 256 + static_cast<int>(rank) * 128;
+      const int ash = min(m0 / p.y_shard_rows, y_pieces - 1);  // the Y row piece (rows past M: clipped)
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * PAIR_ACC;
+      uint8_t* epi = smem + PAIR_STAGES * PAIR_STAGE + static_cast<uint32_t>(q) * 2u * 4096u;
+      epilogue_tile<GATE_UP>(p, taddr, epi, epi_chunk, m0, nb * TN, ash, m0 - ash * p.y_shard_rows, q, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acce_bar[a]), 0));
+    }
+    if (lane == 0) bulk_wait_group_all();
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // neither CTA's copies, MMAs or arrivals still target the other
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, 2 * PAIR_ACC);
+  }
+}
+
 // ---- host side ----
+// 0: CTA-pair kernel for K-major operands, one-CTA kernel otherwise; 1: one-CTA kernel
+// everywhere; 2: CTA-pair kernel everywhere
+std::atomic<int> g_gemm_kernel{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 std::once_flag g_attr_once[2][64];
@@ -514,6 +749,13 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
       y_pieces > kMaxShards)
     return set_error(ZERO_ERR_UNSUPPORTED, "%s: at most %d pieces per operand", who, kMaxShards);
   if (GATE_UP && (A.mn || B.mn)) return set_error(ZERO_ERR_UNSUPPORTED, "%s: gate-up mode is K-major only", who);
+  // Kernel choice: the CTA-pair kernel runs every mode, but by default only K-major
+  // operands take it; with an MN-major operand (the backward's in-place GEMMs) the pair
+  // form measured no faster, and 2-4 % slower over a whole backward call, than the one-CTA
+  // kernel. Pair CTAs load 128-row halves of a K-major B, so B pieces need a multiple of
+  // 128 rows; the one-CTA kernel loads whole TN-row tiles.
+  const int choice = g_gemm_kernel.load();
+  const bool pair = choice == 2 || (choice == 0 && !A.mn && !B.mn);
   // A and Y pieces
   if (A.mn) {
     if (A.piece_rows * A.pieces != k_in || (A.pieces > 1 && A.piece_rows % BK) || m_tokens % 64 || y_pieces != 1)
@@ -526,11 +768,11 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
   if (B.mn) {
     if (B.piece_rows * B.pieces != k_in || (B.pieces > 1 && B.piece_rows % BK) || rows_out % 64)
       return set_error(ZERO_ERR_UNSUPPORTED, "%s: unsupported split of the MN-major B operand", who);
-  } else if (B.piece_rows * B.pieces != rows_out || (B.pieces > 1 && B.piece_rows % TN != 0)) {
+  } else if (B.piece_rows * B.pieces != rows_out || (B.pieces > 1 && B.piece_rows % (pair ? 128 : TN) != 0)) {
     return set_error(ZERO_ERR_UNSUPPORTED,
                      "%s: the fused gather needs rows/n_ranks (%lld) to be a multiple of %d and n_ranks <= %d; "
                      "pass a scratch buffer to gather first",
-                     who, (long long)B.piece_rows, TN, kMaxShards);
+                     who, (long long)B.piece_rows, pair ? 128 : TN, kMaxShards);
   }
   int rc = get_encode();
   if (rc) return rc;
@@ -542,8 +784,8 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
     if (rc) return rc;
   }
   for (int s = 0; s < B.pieces; ++s) {
-    rc = B.mn ? encode_mn(&p.w[s], B.ptr[s], rows_out, B.piece_rows, TN / 64)
-              : encode_2d(&p.w[s], B.ptr[s], k_in, B.piece_rows, BK, TN);
+    rc = B.mn ? encode_mn(&p.w[s], B.ptr[s], rows_out, B.piece_rows, pair ? 2 : TN / 64)
+              : encode_2d(&p.w[s], B.ptr[s], k_in, B.piece_rows, BK, pair ? 128 : TN);
     if (rc) return rc;
     if (GATE_UP && (rc = encode_2d(&p.w2[s], B2[s], k_in, B.piece_rows, BK, TN))) return rc;
   }
@@ -587,8 +829,20 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
   std::call_once(g_attr_once[GATE_UP ? 1 : 0][dev & 63], [&] {
     attr = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Mode<GATE_UP>::SMEM);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(fsdp_gemm_pair_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  PAIR_SMEM);
   });
   if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(attr));
+  if (pair) {
+    // one 256-row tile per CTA pair at a time; one pair per two SMs
+    const int64_t tiles = ((m_tokens + 255) / 256) * ((rows_out + TN - 1) / TN);
+    const unsigned int pairs = static_cast<unsigned int>(std::min<int64_t>(tiles, std::max(1, num_sms() / 2)));
+    fsdp_gemm_pair_kernel<GATE_UP><<<2 * pairs, kThreads, PAIR_SMEM, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
+    return ZERO_OK;
+  }
   const int64_t tiles = ((m_tokens + BM - 1) / BM) * ((rows_out + TN - 1) / TN);
   const unsigned int grid = static_cast<unsigned int>(std::min<int64_t>(tiles, num_sms()));
   fsdp_gemm_kernel<GATE_UP><<<grid, kThreads, Mode<GATE_UP>::SMEM, st>>>(p);
@@ -638,6 +892,12 @@ int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* X
   return launch_gemm<false>({n_ranks, dY, true, m_tokens}, {1, xt1, false, k_in}, nullptr, rows_out, k_in,
                             m_tokens * n_ranks, y1, 1, nullptr, 1.0f / static_cast<float>(n_ranks), st,
                             "fsdp_unit_backward");
+}
+
+int set_gemm_kernel(int which) {
+  if (which < 0 || which > 2) return -1;
+  g_gemm_kernel.store(which);
+  return 0;
 }
 
 unsigned int fsdp_gemm_read_clear_error() {

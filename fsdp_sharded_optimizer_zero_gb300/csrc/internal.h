@@ -85,6 +85,7 @@ int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces
 int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* Xt, int64_t m_tokens,
                        int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st);
 unsigned int fsdp_gemm_read_clear_error();
+int set_gemm_kernel(int which);  // 0 = default, 1 = one-CTA kernel everywhere, 2 = CTA-pair kernel everywhere
 
 // ---- errors (capi.cu) ----
 int set_error(int code, const char* fmt, ...);

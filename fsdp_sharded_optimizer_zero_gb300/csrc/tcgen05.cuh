@@ -28,6 +28,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void* tmap,
       : "memory");
 }
 
+// The same load issued by either CTA of a CTA pair (cluster of two) whose tcgen05.mma runs
+// with cta_group::2: the box lands in this CTA's shared memory and its bytes complete on
+// `bar_cluster`, a shared::cluster address that may name the barrier in the peer CTA.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst_smem, const void* tmap, int32_t x, int32_t y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst_smem),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
+// 3-D form of tma_load_2d_pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst_smem, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(dst_smem),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      : "memory");
+}
+
 // 2-D tiled TMA store of a shared-memory box to global memory at (x, y), tracked in this
 // thread's bulk async-group; out-of-bounds parts of the box are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src_smem) {
@@ -60,6 +82,18 @@ __device__ __forceinline__ void tmem_relinquish() {
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// CTA-pair forms (cta_group::2): executed by one warp in EACH CTA of the pair, which get the
+// same columns in both CTAs' TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -105,6 +139,29 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (+)= A * B^T across a CTA pair, issued by one thread of the even CTA: M = 256 rows, the
+// first 128 of A (and of D, in TMEM) in the even CTA and the other 128 in the odd one; the
+// N rows of B likewise split in halves, the first in the even CTA. The descriptors give
+// shared-memory offsets that hold in both CTAs.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at shared-memory offset `bar` of every CTA of the pair set in
+// `mask` (bit r = cluster rank r) when the pair operations this thread issued completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
       : "memory");
 }
 

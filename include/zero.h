@@ -248,7 +248,8 @@ ZERO_API int fsdp_gather_rows(int n_ranks, const zero_bf16* const w_shards[], in
  * scratch_w (nullable): a [rows_out, k_in] bf16 buffer; if given, the shards are first
  * gathered into it (fsdp_gather_rows) and the GEMM reads the gathered W, which the caller
  * frees after use; if NULL the gather is fused into the GEMM's loads (each tile is loaded
- * straight from its shard), which needs (rows_out/n_ranks) % 256 == 0.
+ * straight from its shard), which needs (rows_out/n_ranks) % 128 == 0 (% 256 under
+ * zero_set_gemm_kernel(1)).
  * Requires k_in % 8 == 0 (16-byte rows for the tensor-memory copies), and 16-byte-aligned
  * A, shards and scratch_w. Results are fp32 sums of exact bf16 products in an unspecified
  * order: within K * 2^-23 * sum|a*w| of the exact value. */
@@ -300,7 +301,8 @@ ZERO_API int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[], 
  * accumulators, one rounding to bf16); Y: out, row-major [m_tokens, d_model] fp32.
  * The gate and up projections run in one kernel sharing every X tile, with the SiLU-gate
  * product as its epilogue (needs d_ff/N % 128 == 0). W_down is gathered inside the loads
- * when d_model/N % 256 == 0 and scratch_down is NULL; otherwise pass scratch_down
+ * when d_model/N % 128 == 0 (% 256 under zero_set_gemm_kernel(1)) and scratch_down is
+ * NULL; otherwise pass scratch_down
  * ([d_model, d_ff] bf16): its gather then runs on prefetch_stream (NULL = `stream`)
  * while the gate-up GEMM runs, and `stream` waits for it before the down projection.
  * d_model, d_ff multiples of 8; all buffers 16-byte aligned. */
@@ -348,6 +350,16 @@ ZERO_API int zero_selftest_bounded_wait(uint32_t timeout_ms, zero_stream_t strea
  * bulk-copy pipeline staging the N rank chunks in shared memory, 2 = register-streaming.
  * All give bit-identical results (misaligned buffers always take a scalar kernel). */
 ZERO_API int zero_set_fused_kernel(int which);
+
+/* Select the tensor-core GEMM kernel of the FSDP calls. 0 = default: the CTA-pair kernel
+ * (tcgen05.mma.cta_group::2, a cluster of two CTAs on two SMs per 256-row tile) wherever
+ * both operands are K-major (every forward, the MLP unit, the backward's transposed path),
+ * the one-CTA kernel where an operand is MN-major (the backward's in-place GEMMs). 1 = the
+ * one-CTA kernel everywhere; 2 = the CTA-pair kernel everywhere. All give bit-identical
+ * results (each output sums the same products in the same order). The fused gather needs
+ * rows_out / n_ranks to be a multiple of 128 on the pair kernel, of 256 on the one-CTA
+ * kernel. Process-wide; affects calls made after it returns. */
+ZERO_API int zero_set_gemm_kernel(int which);
 
 /* Library version, e.g. 100 for 0.1.0. */
 ZERO_API int zero_version(void);

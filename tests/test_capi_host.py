@@ -113,6 +113,8 @@ def test_step_calls_reject_missing_rank_before_launch(z):
     assert lib.fsdp_unit_forward(4, good, 8, 12, 128, 4, 256, None, None, None) == -1   # k % 8
     assert lib.fsdp_gather_rows(4, grads, 8, 16, 256, None) == -1
     assert lib.zero_set_fused_kernel(3) == -1
+    assert lib.zero_set_gemm_kernel(3) == -1 and lib.zero_set_gemm_kernel(-1) == -1
+    assert lib.zero_set_gemm_kernel(2) == 0 and lib.zero_set_gemm_kernel(1) == 0 and lib.zero_set_gemm_kernel(0) == 0
     # host-memory step: a buffer that is not page-locked host memory is rejected before launch
     import numpy as np
     buf = np.zeros(1024, np.uint16)

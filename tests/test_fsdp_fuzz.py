@@ -1,5 +1,5 @@
 """Seeded random shapes for the FSDP unit: the forward with the gather fused into the GEMM's
-loads (shard rows a multiple of 256) or through a scratch buffer (any shard rows), the
+loads (shard rows a multiple of 128) or through a scratch buffer (any shard rows), the
 backward on both its in-place and its transposed path, and the MLP unit; each checked
 against the oracle by the same bounds as the fixed-shape tests."""
 import numpy as np
@@ -16,8 +16,8 @@ def forward_case(i):
     n = int(rng.choice([1, 2, 3, 4, 8]))
     k = 8 * int(rng.integers(1, 130))
     m = int(rng.integers(1, 700))
-    if i % 2 == 0:  # fused gather: shard rows a multiple of 256
-        return "fused", m, n * 256 * int(rng.integers(1, 4)), k, n
+    if i % 2 == 0:  # fused gather: shard rows a multiple of 128
+        return "fused", m, n * 128 * int(rng.integers(1, 6)), k, n
     return "scratch", m, n * int(rng.integers(1, 300)), k, n
 
 
@@ -56,7 +56,7 @@ def test_random_mlp_unit(z, i):
     rng = np.random.default_rng(4000 + i)
     n = int(rng.choice([1, 2, 4]))
     scratch = bool(i % 2)
-    d = n * 256 * int(rng.integers(1, 3)) if not scratch else n * 8 * int(rng.integers(1, 64))
+    d = n * 128 * int(rng.integers(1, 5)) if not scratch else n * 8 * int(rng.integers(1, 64))
     f = n * 128 * int(rng.integers(1, 4))
     m = int(rng.integers(1, 400))
     F.test_mlp_unit_vs_oracle(z, n, d, f, m, scratch)

@@ -28,7 +28,15 @@ def z():
     import __graft_entry__ as g
     g.build()
     import fsdp_sharded_optimizer_zero_gb300 as z
-    return z
+    yield z
+    z.zero_set_gemm_kernel(0)
+
+
+@pytest.fixture(autouse=True)
+def _default_gemm_kernel(z):
+    z.zero_set_gemm_kernel(0)
+    yield
+    z.zero_set_gemm_kernel(0)
 
 
 def gemm_bound(a64, w64, K):
@@ -65,7 +73,9 @@ def test_gather_rows_misaligned_scalar_path(z):
 
 
 @pytest.mark.parametrize("m,rows,k,n", [(128, 256, 64, 1), (256, 2048, 512, 8), (200, 2048, 520, 8),
-                                        (384, 512, 1024, 2), (1, 256, 8, 1), (130, 4096, 136, 16)])
+                                        (384, 512, 1024, 2), (1, 256, 8, 1), (130, 4096, 136, 16),
+                                        # shard rows a multiple of 128 but not of 256: the CTA pair's halves
+                                        (300, 384, 136, 3), (257, 1152, 72, 9), (1, 128, 8, 1), (513, 640, 200, 5)])
 def test_gemm_fused_gather_vs_oracle(z, m, rows, k, n):
     shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=m)
     A = synth.activations(m, k, device=DEV, seed_key=k)
@@ -88,7 +98,7 @@ def test_gemm_scratch_gather_vs_oracle(z, m, rows, k, n):
     z.zero_device_status()
     check_gemm(f32(Y), bits16(A), [bits16(s) for s in shards], f"scratch m={m} rows={rows} k={k}")
     assert_bf16_identical(bits16(scratch), O.gather_rows([bits16(s) for s in shards]), "scratch holds gathered W")
-    if (rows // n) % 256 == 0:
+    if (rows // n) % 128 == 0:
         Y2 = torch.empty_like(Y)
         z.fsdp_unit_forward(shards, A, Y2)
         z.zero_device_status()
@@ -128,13 +138,50 @@ def test_gemm_integer_values_exact(z):
     assert np.array_equal(f32(Y), a @ w.T)
 
 
-def test_gemm_needs_scratch_when_shards_do_not_tile(z):
-    shards = synth.weight_shards(8 * 128, 64, 8, device=DEV)
+@pytest.mark.parametrize("shard_rows,kernel,ok", [(192, 0, False), (192, 1, False), (128, 0, True), (128, 1, False),
+                                                   (256, 1, True)])
+def test_gemm_needs_scratch_when_shards_do_not_tile(z, shard_rows, kernel, ok):
+    """Without a scratch buffer the fused gather needs each B tile to lie in one shard: shard
+    rows a multiple of 128 for the CTA-pair kernel (128-row halves), of 256 for the one-CTA
+    kernel (whole 256-row tiles); otherwise the call is ZERO_ERR_UNSUPPORTED (-4)."""
+    z.zero_set_gemm_kernel(kernel)
+    shards = synth.weight_shards(8 * shard_rows, 64, 8, device=DEV)
     A = synth.activations(128, 64, device=DEV)
-    Y = torch.empty(128, 1024, device=DEV)
+    Y = torch.empty(128, 8 * shard_rows, device=DEV)
+    if ok:
+        z.fsdp_unit_forward(shards, A, Y)
+        z.zero_device_status()
+        check_gemm(f32(Y), bits16(A), [bits16(s) for s in shards], f"shard rows {shard_rows}")
+        return
     with pytest.raises(z.ZeroError) as e:
         z.fsdp_unit_forward(shards, A, Y)
     assert e.value.code == -4
+
+
+@pytest.mark.parametrize("m,rows,k,n,mode", [(128, 256, 64, 1, "fused"), (300, 2048, 520, 8, "fused"),
+                                             (1, 256, 8, 1, "fused"), (257, 512, 136, 2, "fused"),
+                                             (640, 4096, 1024, 16, "fused"), (300, 1024, 264, 8, "scratch"),
+                                             (129, 300, 72, 3, "scratch"), (200, 2048, 72, 4, "bf16"),
+                                             (130, 1000, 136, 5, "bf16_scratch")])
+def test_pair_and_one_cta_kernels_bit_identical(z, m, rows, k, n, mode):
+    """The CTA-pair kernel (the default) and the one-CTA kernel feed each output the same
+    K = 16 products in the same order, so they must give the same bits; with the pair
+    kernel checked against the oracle above, this carries the check to the other one."""
+    shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=rows + m)
+    A = synth.activations(m, k, device=DEV, seed_key=k + m)
+    outs = []
+    for kernel in (0, 1):
+        z.zero_set_gemm_kernel(kernel)
+        sw = torch.empty(rows, k, dtype=torch.bfloat16, device=DEV) if mode.endswith("scratch") else None
+        if mode.startswith("bf16"):
+            out = torch.full((m, rows), float("nan"), dtype=torch.bfloat16, device=DEV)
+            z.fsdp_unit_forward(shards, A, None, Y_bf16=out, scratch_w=sw)
+        else:
+            out = torch.full((m, rows), float("nan"), device=DEV)
+            z.fsdp_unit_forward(shards, A, out, scratch_w=sw)
+        z.zero_device_status()
+        outs.append(out.view(torch.int16 if mode.startswith("bf16") else torch.int32).clone())
+    assert torch.equal(outs[0], outs[1]), f"pair and one-CTA kernels differ: {mode} m={m} rows={rows} k={k} n={n}"
 
 
 def test_mistral_mlp_unit_sampled(z):
@@ -373,7 +420,7 @@ def make_mlp(n, d, f, m, key):
 
 @pytest.mark.parametrize("n,d,f,m,scratch", [(2, 512, 512, 200, False), (2, 256, 512, 200, True),
                                              (4, 1024, 1024, 130, False), (8, 2048, 1024, 64, True),
-                                             (1, 256, 256, 1, False)])
+                                             (1, 256, 256, 1, False), (3, 384, 384, 100, False)])
 def test_mlp_unit_vs_oracle(z, n, d, f, m, scratch):
     gate, up, down, X = make_mlp(n, d, f, m, key=d + f)
     H = torch.zeros(m, f, dtype=torch.bfloat16, device=DEV)
@@ -394,7 +441,7 @@ def test_mlp_unit_vs_oracle(z, n, d, f, m, scratch):
     assert np.all(np.abs(f32(Y) - y64) <= by + 1e-30), "Y"
     if scratch:
         assert_bf16_identical(bits16(sd), O.gather_rows(db), "W_down gathered into scratch")
-    if (d // n) % 256 == 0:
+    if (d // n) % 128 == 0:
         Y2 = torch.empty_like(Y)
         H2 = torch.empty_like(H)
         z.fsdp_mlp_forward(gate, up, down, X, H2, Y2,
@@ -430,3 +477,40 @@ def test_mlp_unit_mistral_sampled(z):
     ex = np.einsum("ik,ik->i", hi, wd)
     by = (f + 1) * 2.0 ** -23 * np.einsum("ik,ik->i", np.abs(hi), np.abs(wd))
     assert np.all(np.abs(f32(Y[i, c]).astype(np.float64) - ex) <= by + 1e-30), "Y"
+
+
+@pytest.mark.parametrize("n,d,f,m,scratch", [(2, 512, 512, 200, False), (4, 1024, 1024, 130, True),
+                                             (1, 256, 384, 257, False)])
+def test_mlp_unit_pair_and_one_cta_kernels_bit_identical(z, n, d, f, m, scratch):
+    """Gate-up and down projections on the CTA-pair kernels (the default) and on the one-CTA
+    kernels: H and Y bit for bit the same."""
+    gate, up, down, X = make_mlp(n, d, f, m, key=3 * d + f)
+    outs = []
+    for kernel in (0, 1):
+        z.zero_set_gemm_kernel(kernel)
+        H = torch.zeros(m, f, dtype=torch.bfloat16, device=DEV)
+        Y = torch.full((m, d), float("nan"), device=DEV)
+        sd = torch.empty(d, f, dtype=torch.bfloat16, device=DEV) if scratch else None
+        z.fsdp_mlp_forward(gate, up, down, X, H, Y, scratch_down=sd, prefetch_stream=None)
+        z.zero_device_status()
+        outs.append((H.view(torch.int16).clone(), Y.view(torch.int32).clone()))
+    assert torch.equal(outs[0][0], outs[1][0]), "H"
+    assert torch.equal(outs[0][1], outs[1][1]), "Y"
+
+
+@pytest.mark.parametrize("n,rows,k,m", [(3, 120, 72, 40), (5, 320, 200, 192), (4, 512, 256, 128), (8, 2048, 512, 96),
+                                        (16, 1024, 192, 128), (1, 128, 64, 64)])
+def test_backward_pair_and_one_cta_kernels_bit_identical(z, n, rows, k, m):
+    """The backward under the default choice, on the one-CTA kernels everywhere and on the
+    CTA-pair kernels everywhere (selectors 0, 1, 2) gives the same dX and dW bits: the
+    transposed path (K-major operands) and the in-place path (MN-major W and dY; dX over all
+    ranks' row pieces when M % 128 == 0, else per rank)."""
+    outs = []
+    for kernel in (0, 1, 2):
+        z.zero_set_gemm_kernel(kernel)
+        _, _, _, dX, dW = run_backward(z, n, rows, k, m, key=rows + 1)
+        outs.append(([x.view(torch.int32).clone() for x in dX], dW.view(torch.int32).clone()))
+    for sel in (1, 2):
+        for q in range(n):
+            assert torch.equal(outs[0][0][q], outs[sel][0][q]), f"dX of rank {q}, selector {sel}"
+        assert torch.equal(outs[0][1], outs[sel][1]), f"dW, selector {sel}"
