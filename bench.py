@@ -652,10 +652,33 @@ def run_reference(args):
 # the 1.5B-parameter bandwidth sweep
 # ---------------------------------------------------------------------------------------
 
+def bucket_graph(z, plan, rank, args, n_streams):
+    """A CUDA graph of one fused-step launch per bucket, bucket k on stream k % n_streams,
+    captured on the current stream. The buckets are disjoint index ranges, so launches on
+    different streams may overlap: the next bucket's ramp-up runs during this one's drain."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = [torch.cuda.Stream() for _ in range(n_streams - 1)]
+    with torch.cuda.graph(g, stream=torch.cuda.current_stream()):
+        cur = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        for s in side:
+            s.wait_event(fork)
+        streams = [cur] + side
+        for k in range(plan.n_buckets):
+            z.zero_fused_step_buckets(plan, rank, k, k + 1, *args, streams[k % n_streams])
+        for s in side:
+            join = torch.cuda.Event()
+            join.record(s)
+            cur.wait_event(join)
+    return g
+
+
 def run_sweep(args):
     """psi = 1.5e9, N in {2,4,8,16,64}, buckets {1,5,25,100} MiB. For each point: one launch
     over all buckets, and one launch per bucket (as DDP reduces each bucket once backward
-    produced it) captured in a CUDA graph. All N ranks' shards (full simulation) whenever
+    produced it) captured in a CUDA graph, on one stream and round-robin on four. All N ranks' shards (full simulation) whenever
     the (2N + 14) P bytes of gradients, state and parameters fit in free device memory with
     an 8 GiB margin (N = 64: 213 GB, which a GB300 holds); otherwise one rank's view (its N
     incoming chunks)."""
@@ -692,11 +715,11 @@ def run_sweep(args):
             with torch.cuda.stream(stream):
                 one = time_launches(lambda: z.zero_fused_step(plan, rank, grads, master, m, v, param, hp, 1, stream),
                                     10, stream)
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    for k in range(NB):
-                        z.zero_fused_step_buckets(plan, rank, k, k + 1, grads, master, m, v, param, hp, 1, stream)
+                g = bucket_graph(z, plan, rank, (grads, master, m, v, param, hp, 1), 1)
                 per_bucket = time_launches(lambda: g.replay(), 10, stream)
+                del g
+                g = bucket_graph(z, plan, rank, (grads, master, m, v, param, hp, 1), 4)
+                per_bucket_4 = time_launches(lambda: g.replay(), 10, stream)
             z.zero_device_status(stream)
             line = {"sweep": "fused step", "psi": psi, "n_ranks": n, "bucket_mib": bmib, "n_buckets": NB,
                     "mode": "all ranks" if full else "rank view", "bytes_per_step": byts,
@@ -704,6 +727,9 @@ def run_sweep(args):
                     "single_launch_frac": byts / one / 1e6 / hbm_peak,
                     "per_bucket_graph_ms": per_bucket, "per_bucket_graph_gbs": byts / per_bucket / 1e6,
                     "per_bucket_graph_frac": byts / per_bucket / 1e6 / hbm_peak,
+                    "per_bucket_graph_4streams_ms": per_bucket_4,
+                    "per_bucket_graph_4streams_gbs": byts / per_bucket_4 / 1e6,
+                    "per_bucket_graph_4streams_frac": byts / per_bucket_4 / 1e6 / hbm_peak,
                     "state_bytes_per_rank": {s: z.zero_plan(psi, n, s, bmib * MIB).state_total_bytes
                                              for s in ("ddp", "zero1", "zero2", "zero3")},
                     "peak": hbm_peak, "peak_source": peak_src}

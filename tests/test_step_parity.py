@@ -405,6 +405,38 @@ def test_buckets_in_gradient_ready_order(z):
     compare((f32(master), f32(m), f32(v), bits16(param)), want, "reverse-order buckets")
 
 
+def test_buckets_on_four_streams_equal_the_oracle(z):
+    """Buckets are disjoint, so a caller may launch them on several streams at once (DDP
+    overlapping the per-bucket steps): bucket k on stream k % 4, forked from and joined to
+    the default stream, over two steps, must match the oracle bit for bit."""
+    psi, n, bb = 300_007, 8, 1 << 13
+    master0, m0, v0, grads = make_inputs(psi, n, 2, seed=29, moments=True)
+    want = oracle_run("zero2", psi, n, bb, master0, m0, v0, grads)
+    plan = z.zero_plan(psi, n, "zero2", bb)
+    P, NB = plan.psi_padded, plan.n_buckets
+    assert NB > 50
+    master, m, v = master0.to(DEV), m0.to(DEV), v0.to(DEV)
+    param = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    main = torch.cuda.current_stream()
+    side = [torch.cuda.Stream() for _ in range(3)]
+    for t, gs in enumerate(grads, start=1):
+        gd = [g.to(DEV) for g in gs]
+        fork = torch.cuda.Event()
+        fork.record(main)
+        for s in side:
+            s.wait_event(fork)
+        streams = [main] + side
+        for k in range(NB):
+            z.zero_fused_step_buckets(plan, z.ZERO_ALL_RANKS, k, k + 1, gd, master, m, v, param, HP, t,
+                                      streams[k % 4])
+        for s in side:
+            join = torch.cuda.Event()
+            join.record(s)
+            main.wait_event(join)
+    z.zero_device_status()
+    compare((f32(master), f32(m), f32(v), bits16(param)), want, "buckets on four streams")
+
+
 # ---------------------------------------------------------------------------------------
 # gradients and parameters in page-locked host memory, read / written over the host link
 # ---------------------------------------------------------------------------------------
