@@ -49,9 +49,10 @@ __global__ void __launch_bounds__(kThreads) fused_vec_kernel(RankPtrs<G> gp, int
 // Blocks per SM of the register-streaming kernel's grid on long launches. With 40
 // registers per thread six 256-thread blocks fit on an SM, but on GB300 four held the
 // highest share of the copy bandwidth for N = 1, 2, 8, 12, 16, 32, 64 and both gradient
-// types; one full wave (six per SM) or several waves of the full grid lost 2-8 %. N = 4
-// showed no grid that won on every domain shape, so it keeps the full grid.
-inline unsigned int fused_vec_blocks_per_sm(int n) { return n == 4 ? 16u : 4u; }
+// types; one full wave (six per SM) or several waves of the full grid lost 2-8 %. For
+// N = 3..7 (fewer bytes in flight per thread) the full grid held 0.5-2 % more (N = 4 showed
+// no grid that won on every domain shape).
+inline unsigned int fused_vec_blocks_per_sm(int n) { return n >= 3 && n <= 7 ? 16u : 4u; }
 
 // scalar variant for buffers whose alignment rules out vector accesses
 template <typename G>

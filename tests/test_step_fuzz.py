@@ -1,8 +1,8 @@
 """Seeded random cases of the step, every element compared bit for bit with the oracle:
 psi, N (1..64), stage, bucket size, rank mode, misaligned buffers, steps and starting
-moments drawn from a fixed generator, plus three long launches (tens of millions of
-elements, odd psi, N = 2, 3, 5) that take the 4-CTA-per-SM grid and, for N = 3 and 5, the
-generic-N load groups."""
+moments drawn from a fixed generator, plus four long launches (tens of millions of
+elements, odd psi): N = 2 and 17 on the 4-CTA-per-SM grid (N = 17 through the generic-N
+load groups, which serve N > 16), N = 3 and 5 on the full grid."""
 import numpy as np
 import pytest
 
@@ -40,7 +40,7 @@ def test_random_step_bit_exact(z, i):
     compare(got, want, str(c))
 
 
-@pytest.mark.parametrize("psi,n", [(20_000_001, 2), (21_000_003, 3), (19_999_997, 5)])
+@pytest.mark.parametrize("psi,n", [(20_000_001, 2), (21_000_003, 3), (19_999_997, 5), (20_000_017, 17)])
 def test_long_launch_bit_exact(z, psi, n):
     master0, m0, v0, grads = make_inputs(psi, n, 1, seed=psi % 97)
     want = oracle_run("zero2", psi, n, 25 << 20, master0, m0, v0, grads)
