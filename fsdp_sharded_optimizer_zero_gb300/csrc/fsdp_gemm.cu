@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
 // a 256-row output tile with tcgen05.mma.cta_group::2 (M = 256, N = 256). Each CTA loads
 // only its 128 A rows and 128 of the 256 B rows, and the MMA reads both CTAs' shared
 // memory, so every SM moves a third fewer operand bytes per flop than in the one-CTA form
-// (Mistral MLP shapes: 1.50-1.66 -> 1.65-1.81 PFLOP/s). Plain mode: CTA r loads W rows
+// (Mistral MLP GEMMs, live: 1.63-1.68 -> 1.74-1.79 PFLOP/s). Plain mode: CTA r loads W rows
 // n0 + 128 r of a 256-column tile. Gate-up mode: the B operand of the N = 256 MMA is the
 // gate tile followed by the up tile, so the even CTA loads the gate's 128 rows and the odd
 // CTA the up projection's, and the accumulator holds gate | up exactly as in the one-CTA

@@ -294,7 +294,9 @@ def test_backward_integer_values_exact(z, n, rows, k, m):
 
 @pytest.mark.parametrize("n,rows,k,m", [(4, 512, 256, 128), (3, 120, 72, 40), (8, 2048, 512, 96), (1, 256, 64, 200),
                                         (2, 256, 64, 64), (5, 320, 192, 192), (1, 128, 64, 64), (16, 1024, 192, 128),
-                                        (5, 320, 200, 192)])
+                                        (5, 320, 200, 192),
+                                        # transposed path with M % 128 == 0: dX as one row-split GEMM
+                                        (2, 200, 72, 128), (3, 192, 40, 256)])
 def test_backward_vs_oracle(z, n, rows, k, m):
     shards, A, dY, dX, dW = run_backward(z, n, rows, k, m, key=rows)
     sb = [bits16(s) for s in shards]
@@ -499,7 +501,7 @@ def test_mlp_unit_pair_and_one_cta_kernels_bit_identical(z, n, d, f, m, scratch)
 
 
 @pytest.mark.parametrize("n,rows,k,m", [(3, 120, 72, 40), (5, 320, 200, 192), (4, 512, 256, 128), (8, 2048, 512, 96),
-                                        (16, 1024, 192, 128), (1, 128, 64, 64)])
+                                        (16, 1024, 192, 128), (1, 128, 64, 64), (2, 200, 72, 128), (3, 192, 40, 256)])
 def test_backward_pair_and_one_cta_kernels_bit_identical(z, n, rows, k, m):
     """The backward under the default choice, on the one-CTA kernels everywhere and on the
     CTA-pair kernels everywhere (selectors 0, 1, 2) gives the same dX and dW bits: the
