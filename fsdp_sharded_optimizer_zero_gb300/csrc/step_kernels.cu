@@ -347,8 +347,8 @@ __global__ void wait_selftest_kernel(unsigned long long timeout_ns) {
 }
 
 // Blocks per SM of the vector reduce and Adam grids on long launches, measured on GB300. A thread of the
-// reduce keeps 8 B of gradient loads per rank in flight (all N ranks for N = 1, 2, 4, 8,
-// 16; eight at a time otherwise): from 64 B (N >= 8) four blocks per SM held 0.96-1.00
+// reduce keeps 8 B of gradient loads per rank in flight (all N ranks for N <= 16, eight
+// at a time above): from 64 B (N >= 8) four blocks per SM held 0.96-1.00
 // of the copy bandwidth where the full grid held 0.89-0.96; at N = 4 (32 B) six did
 // best; with less in flight the full grid is needed to cover the latency. Adam keeps
 // 64 B in flight per thread: four per SM.
