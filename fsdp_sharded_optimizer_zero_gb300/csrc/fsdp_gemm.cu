@@ -507,6 +507,7 @@ template <bool GATE_UP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fsdp_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   constexpr int TN = Mode<GATE_UP>::TN;  // output tile columns: 256, or 128 of H in gate-up mode
+  static_assert(TN == (GATE_UP ? 128 : 256), "the pair MMA is N = 256: 256-column tiles, or gate | up halves");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[PAIR_STAGES];
   __shared__ __align__(8) uint64_t empty_bar[PAIR_STAGES];
