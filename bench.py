@@ -763,6 +763,20 @@ def run_case(args):
         ms = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1, stream),
                            4, stream)
         out.update(psi=psi, n_ranks=n, ms=ms, bytes=plan.fused_step_bytes, gbs=plan.fused_step_bytes / ms / 1e6)
+    elif args.case == "megatron_small":
+        # the Megatron distributed optimizer's step: psi = 33,554,432, N = 8, fp32 gradients
+        # (4N + 26 = 58 B per parameter, 1.95 GB per launch), 5 launches
+        psi, n = 1 << 25, 8
+        plan = z.zero_plan(psi, n, "megatron", 25 * MIB)
+        grads = [synth.rank_grads_f32(psi, psi, r, 1, device=dev) for r in range(n)]
+        master = synth.master_params(psi, psi, device=dev)
+        m = torch.zeros(psi, device=dev)
+        v = torch.zeros(psi, device=dev)
+        param = torch.empty(psi, dtype=torch.bfloat16, device=dev)
+        hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+        ms = time_launches(lambda: z.zero_fused_step_fp32_grads(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp,
+                                                                1, stream), 4, stream)
+        out.update(psi=psi, n_ranks=n, ms=ms, bytes=plan.fused_step_bytes, gbs=plan.fused_step_bytes / ms / 1e6)
     elif args.case in ("tiny", "mistral_rank_view"):
         # tiny: psi = 2^20, N = 4, every rank in one launch (35.7 MB: L2-resident, reported as
         # such). mistral_rank_view: one rank's shard of the Mistral-7B list at N = 8
@@ -866,7 +880,7 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="one measured case: fused_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
+                    help="one measured case: fused_small | megatron_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
                          "backward_up (ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
