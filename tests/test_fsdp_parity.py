@@ -516,3 +516,55 @@ def test_backward_pair_and_one_cta_kernels_bit_identical(z, n, rows, k, m):
         for q in range(n):
             assert torch.equal(outs[0][0][q], outs[sel][0][q]), f"dX of rank {q}, selector {sel}"
         assert torch.equal(outs[0][1], outs[sel][1]), f"dW, selector {sel}"
+
+
+def test_fsdp_calls_replay_from_a_cuda_graph(z):
+    """The FSDP calls are plain stream work (host-encoded tensor maps passed by value, no
+    allocation, the MLP unit's prefetch stream forked and joined through events), so they
+    can be captured once in a CUDA graph and replayed: the forward with its fused gather, the
+    MLP unit with W_down gathered on a prefetch stream, and the backward give the same bits
+    as eager calls."""
+    n, R, K, M = 4, 1024, 256, 256
+    shards = synth.weight_shards(R, K, n, device=DEV, seed_key=91)
+    X = synth.activations(M, K, device=DEV, seed_key=92)
+    gate, up, down, Xm = make_mlp(2, 512, 512, 200, key=93)
+    Hm_e = torch.empty(200, 512, dtype=torch.bfloat16, device=DEV)
+    Ym_e = torch.empty(200, 512, device=DEV)
+    sd = torch.empty(512, 512, dtype=torch.bfloat16, device=DEV)
+    A = [synth.activations(64, K, device=DEV, seed_key=94 + q) for q in range(n)]
+    dY = [synth.upstream_grad(64, R, device=DEV, seed_key=94 + q) for q in range(n)]
+    ws = torch.empty(z.fsdp_unit_backward_workspace(n, R, K, 64), dtype=torch.uint8, device=DEV)
+
+    def run(Y, Hm, Ym, dX, dW, stream, side):
+        z.fsdp_unit_forward(shards, X, Y, stream=stream)
+        z.fsdp_mlp_forward(gate, up, down, Xm, Hm, Ym, scratch_down=sd, stream=stream, prefetch_stream=side)
+        z.fsdp_unit_backward(shards, A, dY, dX, dW, ws, stream=stream)
+
+    def fresh():
+        return (torch.full((M, R), float("nan"), device=DEV),
+                torch.zeros(200, 512, dtype=torch.bfloat16, device=DEV),
+                torch.full((200, 512), float("nan"), device=DEV),
+                [torch.full((64, K), float("nan"), device=DEV) for _ in range(n)],
+                torch.full((R, K), float("nan"), device=DEV))
+
+    eager = fresh()
+    side = torch.cuda.Stream()
+    run(*eager, torch.cuda.current_stream(), side)
+    z.zero_device_status()
+    got = fresh()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            run(*got, cap, side)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    z.zero_device_status()
+    assert torch.equal(eager[0].view(torch.int32), got[0].view(torch.int32)), "forward"
+    assert torch.equal(eager[1].view(torch.int16), got[1].view(torch.int16)), "MLP H"
+    assert torch.equal(eager[2].view(torch.int32), got[2].view(torch.int32)), "MLP Y"
+    for q in range(n):
+        assert torch.equal(eager[3][q].view(torch.int32), got[3][q].view(torch.int32)), f"dX of rank {q}"
+    assert torch.equal(eager[4].view(torch.int32), got[4].view(torch.int32)), "dW"
