@@ -128,6 +128,9 @@ def _dev(t: torch.Tensor, dtype, name: str) -> int:
         raise TypeError(f"{name} must be a torch tensor")
     if t.device.type != "cuda":
         raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.device.index is not None and t.device.index != torch.cuda.current_device():
+        # the kernels run on the current device: another device's pointer would fault there
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
     if not t.is_contiguous():
