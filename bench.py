@@ -692,9 +692,20 @@ def run_sweep(args):
     hbm_peak, _, _, peak_src = peaks()
     psi = 1_500_000_000
     hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+    cores = os.cpu_count() or 1
     for n in (2, 4, 8, 16, 64):
         plan0 = z.zero_plan(psi, n, "zero2", MIB)
         P, S = plan0.psi_padded, plan0.shard_elems
+        # the oracle on every host core over a 2^22-parameter sample of this N, extrapolated
+        # to the sweep's 1.5e9 parameters (the step is elementwise: time grows in proportion)
+        ns = 1 << 22
+        sample = OracleSample(ns, n_ranks=n, threads=cores)
+        t_or, reps_or = _time_bounded(lambda: sample.step(ns), 3.0)
+        cpu_or = {"value": ns / t_or, "unit": UNIT, "cores": cores, "kind": "oracle", "extrapolated": True,
+                  "ms_per_step_extrapolated": psi / (ns / t_or) * 1e3,
+                  "sample": f"first {ns:,} parameters, N={n} gradient slices, {reps_or} fused steps on "
+                            f"{cores} threads; extrapolated to {psi:,} parameters"}
+        del sample
         torch.cuda.empty_cache()
         full = (2 * n + 14) * P + (8 << 30) <= torch.cuda.mem_get_info()[0]
         L = P if full else S
@@ -732,7 +743,7 @@ def run_sweep(args):
                     "per_bucket_graph_4streams_frac": byts / per_bucket_4 / 1e6 / hbm_peak,
                     "state_bytes_per_rank": {s: z.zero_plan(psi, n, s, bmib * MIB).state_total_bytes
                                              for s in ("ddp", "zero1", "zero2", "zero3")},
-                    "peak": hbm_peak, "peak_source": peak_src}
+                    "peak": hbm_peak, "peak_source": peak_src, "cpu_oracle": cpu_or}
             print(json.dumps(line), flush=True)
             del g
         del grads, master, m, v, param
