@@ -568,3 +568,37 @@ def test_fsdp_calls_replay_from_a_cuda_graph(z):
     for q in range(n):
         assert torch.equal(eager[3][q].view(torch.int32), got[3][q].view(torch.int32)), f"dX of rank {q}"
     assert torch.equal(eager[4].view(torch.int32), got[4].view(torch.int32)), "dW"
+
+
+@pytest.mark.parametrize("n,R,K,M", [(4, 512, 256, 200), (8, 1024, 136, 130)])
+def test_zero3_step_feeds_the_fsdp_unit(z, n, R, K, M):
+    """The ZeRO-3 / FSDP cycle of one linear layer: its weight W [R, K] is the flat parameter
+    (psi = R K), so a rank's ZeRO-3 shard [rS, (r+1)S) is exactly W's row shard r. Two fused
+    optimizer steps (every rank, bf16 parameter shards out) must equal the oracle's ZeRO-3
+    ranks bit for bit, and the next forward, gathering those shards inside the GEMM's loads,
+    must stay within the fp32 bound of the oracle's float64 product with the oracle's W."""
+    psi, bb = R * K, 1 << 16
+    plan = z.zero_plan(psi, n, "zero3", bb)
+    assert plan.psi_padded == psi and (R // n) * K == plan.shard_elems
+    lay = O.make_layout(psi, n, bb)
+    hp = O.AdamHyper()
+    master0 = synth.master_params(psi, psi, seed_key=R)
+    ranks = O.init_ranks("zero3", lay, master0.numpy())
+    master = master0.to(DEV)
+    m, v = torch.zeros(psi, device=DEV), torch.zeros(psi, device=DEV)
+    param = torch.zeros(psi, dtype=torch.bfloat16, device=DEV)
+    for t in (1, 2):
+        grads = [synth.rank_grads(psi, psi, r, t, seed_key=R) for r in range(n)]
+        z.zero_fused_step(plan, z.ZERO_ALL_RANKS, [g.to(DEV) for g in grads], master, m, v, param, hp, t)
+        O.step_ranks(ranks, lay, [bits16(g) for g in grads], hp, t)
+    z.zero_device_status()
+    assert_bf16_identical(bits16(param), O.gather_params(ranks), "ZeRO-3 parameter shards")
+    S = plan.shard_elems
+    shards = [param[r * S:(r + 1) * S].view(R // n, K) for r in range(n)]
+    X = synth.activations(M, K, device=DEV, seed_key=K)
+    Y = torch.full((M, R), float("nan"), device=DEV)
+    z.fsdp_unit_forward(shards, X, Y)
+    z.zero_device_status()
+    w_or = O.gather_params(ranks).reshape(R, K)
+    check_gemm(f32(Y), bits16(X), [w_or[r * (R // n):(r + 1) * (R // n)] for r in range(n)],
+               f"ZeRO-3 shards into the FSDP unit, n={n} R={R} K={K} M={M}")
