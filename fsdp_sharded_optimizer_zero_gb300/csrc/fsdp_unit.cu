@@ -8,14 +8,20 @@
 //   dW   = (1/N) sum_q dY_q^T X_q                  (all ranks' contributions, reduced)
 // and rank r's reduce-scatter result is rows [r R/N, (r+1) R/N) of dW, a contiguous block.
 //
-// Both products run on the tcgen05 GEMM, which takes K-major operands. Three launches of
-// the transpose-and-concatenate kernel lay the operands out for it:
-//   W^T    [K, R]   = the N shards transposed side by side (the backward all-gather),
-//   dY^T   [R, N M] = the N ranks' dY transposed and concatenated,
-//   X^T    [K, N M] = the N ranks' X  transposed and concatenated,
-// so dW = (1/N) dY^T (X^T)^T is ONE GEMM whose reduction axis runs over every rank's
-// tokens: the sum over ranks happens inside the fp32 tensor-core accumulation, and the
-// 1/N scale is applied in the epilogue. dX_q = dY_q (W^T)^T is one GEMM per rank.
+// Both products run on the tcgen05 GEMM. When R / N, K and M are multiples of 64 (and
+// N <= 16) the operands are read where they lie (the in-place path):
+//   dX_q = dY_q W   with dY_q a K-major A and W's row shards an MN-major B, the shard picked
+//                   by K block (the backward all-gather fused into the loads); one launch
+//                   over all ranks' row pieces when M % 128 == 0, else one per rank;
+//   dW = (1/N) sum_q dY_q^T X_q   with dY_q an MN-major A, the K loop over every rank's
+//                   tokens, and X^T [K, N M] laid out by one transpose-and-concatenate
+//                   launch into the workspace (a second MN-major operand costs more than
+//                   that transpose);
+// so the sum over ranks happens inside the fp32 tensor-core accumulation, and the 1/N scale
+// is applied in the epilogue. These MN-major GEMMs run on the one-CTA kernel, where the
+// CTA-pair form measured no faster. Other shapes take the transposed path: W^T [K, R],
+// dY^T [R, N M] and X^T [K, N M] in the workspace, then K-major GEMMs (on the CTA-pair
+// kernel). Both paths give the same bits.
 #include <string.h>
 
 #include "internal.h"
