@@ -836,9 +836,25 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
   });
   if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(attr));
   if (pair) {
-    // one 256-row tile per CTA pair at a time; one pair per two SMs
+    // one 256-row tile per CTA pair at a time, as many pairs as can be resident at once: a
+    // persistent grid larger than that runs its last clusters as a second wave (a 4-CTA
+    // variant with 38 clusters where 36 fit ran at half speed). On GB300 all 76 pairs fit.
+    static int max_pairs[2][64];
+    static std::once_flag pairs_once[2][64];
+    std::call_once(pairs_once[GATE_UP ? 1 : 0][dev & 63], [&] {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * std::max(1, num_sms() / 2), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = PAIR_SMEM;
+      int nc = 0;
+      if (cudaOccupancyMaxActiveClusters(&nc, fsdp_gemm_pair_kernel<GATE_UP>, &cfg) != cudaSuccess || nc < 1) {
+        (void)cudaGetLastError();
+        nc = std::max(1, num_sms() / 2);
+      }
+      max_pairs[GATE_UP ? 1 : 0][dev & 63] = std::min(nc, std::max(1, num_sms() / 2));
+    });
     const int64_t tiles = ((m_tokens + 255) / 256) * ((rows_out + TN - 1) / TN);
-    const unsigned int pairs = static_cast<unsigned int>(std::min<int64_t>(tiles, std::max(1, num_sms() / 2)));
+    const unsigned int pairs = static_cast<unsigned int>(std::min<int64_t>(tiles, max_pairs[GATE_UP ? 1 : 0][dev & 63]));
     fsdp_gemm_pair_kernel<GATE_UP><<<2 * pairs, kThreads, PAIR_SMEM, st>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
