@@ -465,7 +465,7 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         flop = 2.0 * (2.0 * n * Mb * R * K)
         res["backward_up"] = {"ms": ms, "tflops": flop / ms / 1e9, "frac": flop / ms / 1e9 / tf_peak,
                               "ranks": n, "tokens_per_rank": Mb,
-                              "launches": 5, "workspace_bytes": wsb,
+                              "launches": 3, "workspace_bytes": wsb,
                               "note": "W and dY read in place as MN-major operands, X^T transposed; "
                                       "one dX GEMM over all ranks, one dW GEMM"}
     except Exception as e:  # the GEMM leg must not hide the step's line
