@@ -411,8 +411,8 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
             del shards, Y
         res["total_ms"] = total_ms
         res["tflops"] = total_flop / total_ms / 1e9
-        res["roofline"] = {"bound": "tensor", "achieved": res["tflops"], "peak": tf_peak, "unit": "TFLOP/s",
-                           "frac": res["tflops"] / tf_peak,
+        res["roofline"] = {"bound": "tensor", "kernel": "fsdp_gemm_pair_kernel<false>", "achieved": res["tflops"],
+                           "peak": tf_peak, "unit": "TFLOP/s", "frac": res["tflops"] / tf_peak,
                            "peak_source": f"{peak_src} bf16_tflops (burst)" if peak_src == "measured" else "fallback"}
         # the same W_up GEMM with a bf16-only output (Y = NULL): half the output bytes
         shards = synth.weight_shards(14336, 4096, n, device=dev, seed_key=11)
@@ -421,7 +421,17 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         res["up_bf16_output"] = {"ms": ms, "tflops": 2.0 * M * 14336 * 4096 / ms / 1e9,
                                  "frac": 2.0 * M * 14336 * 4096 / ms / 1e9 / tf_peak,
                                  "note": "Y_bf16 only (no fp32 Y); not part of the unit's fp32-output roofline"}
-        del shards, Yb
+        # the same W_up GEMM on the one-CTA kernel (zero_set_gemm_kernel(1)), same bits
+        Y = torch.empty(M, 14336, device=dev)
+        z.zero_set_gemm_kernel(1)
+        try:
+            ms = time_launches(lambda: z.fsdp_unit_forward(shards, X, Y, stream=stream), 10, stream)
+        finally:
+            z.zero_set_gemm_kernel(0)
+        res["up_one_cta_kernel"] = {"ms": ms, "tflops": 2.0 * M * 14336 * 4096 / ms / 1e9,
+                                    "frac": 2.0 * M * 14336 * 4096 / ms / 1e9 / tf_peak,
+                                    "note": "fsdp_gemm_kernel<false>: one CTA per 128 x 256 tile, for comparison"}
+        del shards, Yb, Y
         # row a6 on its own: the materialised all-gather of W_up's 8 row shards (4 B per
         # element) and the backward's transpose of the same shards into W^T (4 B per element)
         hbm = peaks()[0]
