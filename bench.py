@@ -772,7 +772,8 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     out = {"case": args.case}
-    if args.case == "fused_small":
+    if args.case in ("fused_small", "fused_tma_small"):
+        # fused_tma_small: the same step on the TMA bulk-copy pipeline (zero_set_fused_kernel(1))
         psi, n = 1 << 25, 8
         plan = z.zero_plan(psi, n, "zero2", 25 * MIB)
         grads = [synth.rank_grads(psi, psi, r, 1, device=dev) for r in range(n)]
@@ -781,8 +782,12 @@ def run_case(args):
         v = torch.zeros(psi, device=dev)
         param = torch.empty(psi, dtype=torch.bfloat16, device=dev)
         hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
-        ms = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1, stream),
-                           4, stream)
+        z.zero_set_fused_kernel(1 if args.case == "fused_tma_small" else 0)
+        try:
+            ms = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1,
+                                                         stream), 4, stream)
+        finally:
+            z.zero_set_fused_kernel(0)
         out.update(psi=psi, n_ranks=n, ms=ms, bytes=plan.fused_step_bytes, gbs=plan.fused_step_bytes / ms / 1e6)
     elif args.case == "megatron_small":
         # the Megatron distributed optimizer's step: psi = 33,554,432, N = 8, fp32 gradients
@@ -901,7 +906,7 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="one measured case: fused_small | megatron_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
+                    help="one measured case: fused_small | fused_tma_small | megatron_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
                          "backward_up (ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
