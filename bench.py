@@ -789,6 +789,21 @@ def run_case(args):
         finally:
             z.zero_set_fused_kernel(0)
         out.update(psi=psi, n_ranks=n, ms=ms, bytes=plan.fused_step_bytes, gbs=plan.fused_step_bytes / ms / 1e6)
+    elif args.case == "e2e_small":
+        # the e2e kernel: psi = 33,554,432, N = 8, gradients and parameters in page-locked
+        # host memory (537 MB in, 67 MB out over the host link), master / m / v on the device
+        psi, n = 1 << 25, 8
+        plan = z.zero_plan(psi, n, "zero2", 25 * MIB)
+        host_grads = [synth.rank_grads(psi, psi, r, 1).pin_memory() for r in range(n)]
+        host_param = torch.empty(psi, dtype=torch.bfloat16).pin_memory()
+        master = synth.master_params(psi, psi, device=dev)
+        m = torch.zeros(psi, device=dev)
+        v = torch.zeros(psi, device=dev)
+        hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+        ms = time_launches(lambda: z.zero_fused_step_host(plan, z.ZERO_ALL_RANKS, host_grads, master, m, v, host_param,
+                                                          hp, 1, stream), 4, stream)
+        link = psi * (2 * n + 2)
+        out.update(psi=psi, n_ranks=n, ms=ms, host_link_bytes=link, host_link_gbs=link / ms / 1e6)
     elif args.case == "megatron_small":
         # the Megatron distributed optimizer's step: psi = 33,554,432, N = 8, fp32 gradients
         # (4N + 26 = 58 B per parameter, 1.95 GB per launch), 5 launches
@@ -906,7 +921,7 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="one measured case: fused_small | fused_tma_small | megatron_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
+                    help="one measured case: fused_small | fused_tma_small | megatron_small | e2e_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
                          "backward_up (ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
