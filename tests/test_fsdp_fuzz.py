@@ -4,6 +4,7 @@ backward on both its in-place and its transposed path, and the MLP unit; each ch
 against the oracle by the same bounds as the fixed-shape tests."""
 import numpy as np
 import pytest
+import torch
 
 import test_fsdp_parity as F  # the fixed-shape checks, called with random shapes
 from test_fsdp_parity import z  # noqa: F401  (fixture)
@@ -60,3 +61,21 @@ def test_random_mlp_unit(z, i):
     f = n * 128 * int(rng.integers(1, 4))
     m = int(rng.integers(1, 400))
     F.test_mlp_unit_vs_oracle(z, n, d, f, m, scratch)
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_random_backward_pair_kernel_everywhere_bit_identical(z, i):
+    """Random backward shapes under zero_set_gemm_kernel(2), where the CTA-pair kernel also
+    runs the MN-major GEMMs of the in-place path, against the default choice: the same bits."""
+    n, rows, k, m = backward_case(100 + i)
+    outs = []
+    try:
+        for kernel in (0, 2):
+            z.zero_set_gemm_kernel(kernel)
+            _, _, _, dX, dW = F.run_backward(z, n, rows, k, m, key=rows + 7 * i)
+            outs.append(([x.view(torch.int32).clone() for x in dX], dW.view(torch.int32).clone()))
+    finally:
+        z.zero_set_gemm_kernel(0)
+    for q in range(n):
+        assert torch.equal(outs[0][0][q], outs[1][0][q]), f"dX of rank {q}: n={n} rows={rows} k={k} m={m}"
+    assert torch.equal(outs[0][1], outs[1][1]), f"dW: n={n} rows={rows} k={k} m={m}"
