@@ -211,7 +211,9 @@ ZERO_API int zero_fused_step_fp32_grads(const zero_plan_t* plan, int rank, const
 /* As zero_fused_step, restricted to buckets [bucket_begin, bucket_end) of the shard(s):
  * the unit DDP / ZeRO reduce as soon as backward has produced a bucket ([Concepts] "Plain
  * data parallel (DDP)"). Pointers follow the same convention (whole-shard / whole-buffer
- * bases); the call offsets them to the buckets. */
+ * bases); the call offsets them to the buckets. Calls on disjoint bucket ranges touch
+ * disjoint memory, so a caller may issue them on different streams and let them overlap
+ * (one launch's ramp-up runs during another's drain; the results are the same bits). */
 ZERO_API int zero_fused_step_buckets(const zero_plan_t* plan, int rank, uint64_t bucket_begin, uint64_t bucket_end,
                             const zero_bf16* const grads[], float* master, float* m, float* v,
                             zero_bf16* param_out, const zero_adam* hp, int64_t step, zero_stream_t stream);
