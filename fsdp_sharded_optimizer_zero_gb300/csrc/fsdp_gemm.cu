@@ -123,7 +123,7 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
   nb = in_band / rows;
 }
 
-// warp-uniform bounded wait: lane 0 polls, the whole warp gets the verdict
+// warp-uniform bounded wait: lane 0 polls, the whole warp gets the result
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int code) {
   int ok = 0;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, &g_zgb_dev_error, code) ? 1 : 0;
