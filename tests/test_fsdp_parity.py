@@ -602,3 +602,17 @@ def test_zero3_step_feeds_the_fsdp_unit(z, n, R, K, M):
     w_or = O.gather_params(ranks).reshape(R, K)
     check_gemm(f32(Y), bits16(X), [w_or[r * (R // n):(r + 1) * (R // n)] for r in range(n)],
                f"ZeRO-3 shards into the FSDP unit, n={n} R={R} K={K} M={M}")
+
+
+@pytest.mark.parametrize("m,rows,k,n", [(255, 128, 8, 1), (257, 384, 56, 3), (1, 1152, 16, 9), (512, 256, 4104, 2),
+                                        (256, 640, 64, 5), (129, 128, 200, 1)])
+def test_pair_kernel_edge_shapes_vs_oracle(z, m, rows, k, n):
+    """Edges of the CTA-pair tiling against the oracle: K shorter than one 64-wide block or
+    ending in a ragged one, M just under / over a 256-row pair tile (the odd CTA's rows
+    past M), R with a 128-row half past the last shard row, one to nine shards."""
+    shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=m + k)
+    A = synth.activations(m, k, device=DEV, seed_key=rows)
+    Y = torch.full((m, rows), float("nan"), device=DEV)
+    z.fsdp_unit_forward(shards, A, Y)
+    z.zero_device_status()
+    check_gemm(f32(Y), bits16(A), [bits16(s) for s in shards], f"pair edge m={m} rows={rows} k={k} n={n}")
