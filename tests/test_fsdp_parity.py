@@ -422,7 +422,10 @@ def make_mlp(n, d, f, m, key):
 
 @pytest.mark.parametrize("n,d,f,m,scratch", [(2, 512, 512, 200, False), (2, 256, 512, 200, True),
                                              (4, 1024, 1024, 130, False), (8, 2048, 1024, 64, True),
-                                             (1, 256, 256, 1, False), (3, 384, 384, 100, False)])
+                                             (1, 256, 256, 1, False), (3, 384, 384, 100, False),
+                                             # pair-tile edges: M around 256, ragged d_model via scratch
+                                             (2, 256, 256, 257, False), (1, 136, 128, 255, True),
+                                             (4, 512, 512, 1, False)])
 def test_mlp_unit_vs_oracle(z, n, d, f, m, scratch):
     gate, up, down, X = make_mlp(n, d, f, m, key=d + f)
     H = torch.zeros(m, f, dtype=torch.bfloat16, device=DEV)
