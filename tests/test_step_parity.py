@@ -385,16 +385,18 @@ def test_zero1_via_allreduce_equals_zero1(z):
     compare((f32(master), f32(m), f32(v), bits16(param)), want, "zero1 via all-reduce")
 
 
+@pytest.mark.parametrize("mode", ["all", "unfused", "ddp"])
 @pytest.mark.parametrize("n", range(1, 18))
-def test_every_rank_count_bit_exact(z, n):
+def test_every_rank_count_bit_exact(z, n, mode):
     """Every rank count with its own kernel instance (N = 1..16) and the first one on the
-    generic path (17): the fused step over all ranks, two steps, bit for bit against the
-    oracle, on an odd psi so the padding and the scalar tail are exercised too."""
+    generic path (17), for the fused step, the standalone reduce-scatter + Adam, and the DDP
+    all-reduce + Adam: two steps over all ranks, bit for bit against the oracle, on an odd
+    psi so the padding and the scalar tail are exercised too."""
     psi, bb = 120_001, 1 << 14
     master0, m0, v0, grads = make_inputs(psi, n, 2, seed=40 + n, moments=True)
     want = oracle_run("zero2", psi, n, bb, master0, m0, v0, grads)
-    got = gpu_run(z, "zero2", "all", psi, n, bb, master0, m0, v0, grads)
-    compare(got, want, f"N={n}")
+    got = gpu_run(z, "zero2", mode, psi, n, bb, master0, m0, v0, grads)
+    compare(got, want, f"N={n} mode={mode}")
 
 
 def test_buckets_in_gradient_ready_order(z):
