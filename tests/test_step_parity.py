@@ -297,7 +297,9 @@ def test_allgather_params_cast(z):
 
 @pytest.mark.parametrize("psi,n,bb,misalign", [(1_048_576, 4, 25 * MIB, False), (100_003, 5, 1 << 12, False),
                                                (20_001, 64, 1 << 10, False), (65_539, 16, 1 << 14, True),
-                                               (13, 3, 6, False)])
+                                               (13, 3, 6, False)]
+                         # every rank count with its own fp32-gradient instance, and 17 (generic)
+                         + [(40_009, n, 1 << 14, False) for n in (1, 2, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 17)])
 def test_megatron_fp32_grads_bit_exact(z, psi, n, bb, misalign):
     P = -(-psi // n) * n
     master0 = synth.master_params(psi, P, seed_key=n)
