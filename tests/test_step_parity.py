@@ -237,7 +237,8 @@ def test_special_values(z):
     master0 = torch.from_numpy(w0)
     m0 = torch.zeros(psi)
     v0 = torch.zeros(psi)
-    want = oracle_run("zero2", psi, n, 1 << 12, master0, m0, v0, [gs])
+    with np.errstate(over="ignore", invalid="ignore"):  # inf and NaN inputs are the point here
+        want = oracle_run("zero2", psi, n, 1 << 12, master0, m0, v0, [gs])
     for variant in (1, 2):
         z.zero_set_fused_kernel(variant)
         compare(gpu_run(z, "zero2", "all", psi, n, 1 << 12, master0, m0, v0, [gs]), want, f"specials v{variant}")
