@@ -258,7 +258,9 @@ def run_ours(args):
     }
     # end to end through the public API: grads from pinned host memory, params back
     out["e2e"] = e2e_leg(z, synth, plan, psi, n, dev, hp, world, args)
-    if not args.no_legs:
+    # the other rows, reported by rank 0 only (they hold no collective, so the other ranks
+    # need not run them)
+    if not args.no_legs and rank == 0:
         out["legs"] = extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
