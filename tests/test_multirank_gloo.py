@@ -61,6 +61,18 @@ def test_two_gloo_ranks_aggregate_like_the_bench():
         assert out[rank][1] == pytest.approx(2 * 1000 * 10 / 2.0)
     assert '"impl": "reference"' in out[0][2]
     assert out[1][2] == ""
+    # the reference arm's line carries the contract's keys: its own metric and unit, the
+    # oracle as cpu_baseline (cores it used), and an e2e object with no host transfers
+    import json
+    line = json.loads(out[0][2].strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["unit"] == line["unit"]
 
 
 def test_oracle_split_across_threads_changes_no_bit():
