@@ -30,7 +30,7 @@ STAGE_IDS = {"ddp": 0, "zero1": 1, "zero2": 2, "zero3": 3, "megatron": 4}
 
 # every symbol declared in include/zero.h
 EXPORTS = (
-    "zero_plan", "zero_plan_query", "zero_bucket_range", "zero_plan_destroy",
+    "zero_plan", "zero_plan_query", "zero_bucket_range", "zero_plan_destroy", "zero_plan_check_memory",
     "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_host", "zero_fused_step_fp32_grads",
     "zero_fused_step_buckets", "zero_allgather_params", "ddp_allreduce",
     "fsdp_gather_rows", "fsdp_unit_forward", "fsdp_transpose_cat", "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward",
@@ -77,6 +77,7 @@ def _load():
         "zero_plan_query": (I, [P, C.POINTER(zero_layout)]),
         "zero_bucket_range": (I, [P, I, U64, C.POINTER(U64), C.POINTER(U64)]),
         "zero_plan_destroy": (I, [P]),
+        "zero_plan_check_memory": (I, [P, I, U64, C.POINTER(U64), C.POINTER(U64)]),
         "zero_reduce_scatter": (I, [P, I, PP, VP, VP]),
         "zero_adam_step": (I, [P, I, VP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
         "zero_fused_step": (I, [P, I, PP, VP, VP, VP, VP, C.POINTER(zero_adam), I64, VP]),
@@ -232,6 +233,15 @@ def zero_plan_query(plan: Plan) -> dict:
     lay = zero_layout()
     _check(_lib.zero_plan_query(plan.handle, C.byref(lay)))
     return {name: getattr(lay, name) for name, _ in zero_layout._fields_}
+
+
+def zero_plan_check_memory(plan: Plan, rank: int, budget_bytes: int = 0):
+    """(need, budget) in bytes for one step call of the plan in rank mode `rank`; raises
+    ZeroError with code ZERO_ERR_OOM when need > budget (budget 0 = the device's free
+    memory)."""
+    need, budget = C.c_uint64(), C.c_uint64()
+    _check(_lib.zero_plan_check_memory(plan.handle, rank, budget_bytes, C.byref(need), C.byref(budget)))
+    return need.value, budget.value
 
 
 def zero_bucket_range(plan: Plan, rank: int, bucket: int):

@@ -139,6 +139,39 @@ extern "C" int zero_plan_destroy(zero_plan_t* plan) {
   return ZERO_OK;
 }
 
+extern "C" int zero_plan_check_memory(const zero_plan_t* plan, int rank, uint64_t budget_bytes, uint64_t* need_bytes,
+                                      uint64_t* budget_out) {
+  clear_error();
+  const char* who = "zero_plan_check_memory";
+  CHECK_ARG(plan != nullptr, "%s: plan is NULL", who);
+  const zero_layout& L = plan->lay;
+  CHECK_ARG(rank == ZERO_RANK_VIEW || rank == ZERO_ALL_RANKS || (rank >= 0 && rank < L.n_ranks),
+            "%s: rank %d is not 0..%d, ZERO_RANK_VIEW or ZERO_ALL_RANKS", who, rank, L.n_ranks - 1);
+  const uint64_t P = L.psi_padded, S = L.shard_elems, n = static_cast<uint64_t>(L.n_ranks);
+  // the buffers one step call addresses in this rank mode: n gradient buffers (bf16, fp32
+  // for a Megatron plan), fp32 master / m / v, the bf16 parameter output
+  const uint64_t grad_elems = rank == ZERO_RANK_VIEW ? S : P;
+  const uint64_t state_elems = rank == ZERO_ALL_RANKS ? P : S;
+  const uint64_t param_elems = rank == ZERO_RANK_VIEW ? S : (rank >= 0 && L.stage == ZERO_STAGE_3 ? S : P);
+  const uint64_t gsz = L.stage == ZERO_STAGE_MEGATRON ? 4 : 2;
+  const uint64_t need = n * grad_elems * gsz + 12 * state_elems + 2 * param_elems;
+  if (need_bytes) *need_bytes = need;
+  uint64_t budget = budget_bytes;
+  if (budget == 0) {
+    size_t free_b = 0, total_b = 0;
+    CUDA_LAUNCH(cudaMemGetInfo(&free_b, &total_b));
+    budget = static_cast<uint64_t>(free_b);
+  }
+  if (budget_out) *budget_out = budget;
+  if (need > budget)
+    return set_error(ZERO_ERR_OOM,
+                     "%s: one step of this plan (psi %llu, N %d, stage %d, rank mode %d) addresses %llu bytes of "
+                     "device buffers; %s is %llu bytes",
+                     who, (unsigned long long)L.psi, L.n_ranks, L.stage, rank, (unsigned long long)need,
+                     budget_bytes ? "the caller's budget" : "this device's free memory", (unsigned long long)budget);
+  return ZERO_OK;
+}
+
 // ======================================================================================
 // the step
 // ======================================================================================

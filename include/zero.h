@@ -70,7 +70,8 @@ typedef uint16_t zero_bf16;                /* raw bfloat16 bits */
 typedef enum {
   ZERO_OK = 0,
   ZERO_ERR_INVALID_ARG = -1, /* a bad argument; nothing launched */
-  ZERO_ERR_OOM = -2,         /* host allocation failed (plan object) */
+  ZERO_ERR_OOM = -2,         /* host allocation failed (plan object), or a plan's buffers do not fit
+                                the device memory (zero_plan_check_memory) */
   ZERO_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed; message has the code */
   ZERO_ERR_UNSUPPORTED = -4, /* valid request this build / device cannot run */
   ZERO_ERR_DEVICE = -5       /* a kernel's device-side check fired (see zero_device_status) */
@@ -148,6 +149,23 @@ ZERO_API int zero_bucket_range(const zero_plan_t* plan, int rank, uint64_t bucke
 
 /* Free a plan (NULL is accepted). */
 ZERO_API int zero_plan_destroy(zero_plan_t* plan);
+
+/* Memory check before any buffer is allocated ([Wiring] "Fully Sharded Data Parallel
+ * (FSDP)": Mistral-7B ran out of memory under DDP, where every GPU holds the whole model
+ * state; the sharded stages exist so that it fits). *need_bytes receives the bytes of the
+ * device buffers one step call addresses in rank mode `rank` (the pointer conventions
+ * below), with G = 2 bytes per gradient element (4 for a ZERO_STAGE_MEGATRON plan):
+ *   rank = r:              N * P * G (every rank's gradient buffer) + 12 S (master, m, v)
+ *                          + 2 P (bf16 parameters; 2 S for ZeRO-3);
+ *   ZERO_RANK_VIEW:        N * S * G + 12 S + 2 S;
+ *   ZERO_ALL_RANKS:        N * P * G + 12 P + 2 P.
+ * budget_bytes: the memory the caller can give the step; 0 = this device's free memory
+ * (cudaMemGetInfo on the current device). *budget_out (nullable) receives the budget used.
+ * Returns ZERO_OK when need <= budget, ZERO_ERR_OOM when it is not (the message states both
+ * figures), ZERO_ERR_CUDA if the free memory cannot be read. Launches and allocates
+ * nothing. */
+ZERO_API int zero_plan_check_memory(const zero_plan_t* plan, int rank, uint64_t budget_bytes, uint64_t* need_bytes,
+                                    uint64_t* budget_out);
 
 /* ------------------------------------------------------------------------------------ */
 /* the step                                                                              */
@@ -317,13 +335,17 @@ ZERO_API int fsdp_mlp_forward(int n_ranks, const zero_bf16* const gate_shards[],
  * memory where they run the unit (e.g. a plug-in inside a framework that owns all device
  * memory through its own pool, or a latency-critical path that cannot take cudaMalloc's
  * device-wide synchronisation). The pages have no counterpart to this call.
- * Arguments as fsdp_unit_forward without scratch_w: it always gathers W first, into a
- * 16 MiB array inside this library (8,388,608 bf16 elements; rows_out * k_in above that
- * returns ZERO_ERR_INVALID_ARG), then runs the same GEMM. It allocates nothing. Every GPU
- * that loads the library holds the array until the process exits. The first call on a
- * device (with that device current) looks up the array's address: make it before any
- * stream capture. All calls share the array and it keeps the last call's W; calls that
- * overlap on the GPU race on it. */
+ * Arguments as fsdp_unit_forward without scratch_w. When the shards tile the GEMM (the
+ * fused gather of fsdp_unit_forward applies: n_ranks <= 16 and rows_out/n_ranks a multiple
+ * of 128, of 256 under zero_set_gemm_kernel(1)), W is read straight from its shards and no
+ * scratch is used. Otherwise W is gathered first into a 16 MiB array inside this library
+ * (8,388,608 bf16 elements; rows_out * k_in above that returns ZERO_ERR_INVALID_ARG), then
+ * the same GEMM runs. It allocates nothing. Every GPU that loads the library holds the
+ * array until the process exits. Each call outside stream capture looks up the array's
+ * address in the current device's current context; a call during capture reuses the
+ * address found in that same context, so make the first call on a device (and the first
+ * after a cudaDeviceReset) before any stream capture. All calls share the array and it
+ * keeps the last call's W; calls that overlap on the GPU race on it. */
 ZERO_API int fsdp_unit_forward_static_scratch(int n_ranks, const zero_bf16* const w_shards[], int64_t rows_out,
                                               int64_t k_in, const zero_bf16* A, int64_t m_tokens, float* Y,
                                               zero_bf16* Y_bf16, zero_stream_t stream);

@@ -160,9 +160,64 @@ def test_newer_entry_points_reject_bad_arguments_before_launch(z):
     assert lib.fsdp_mlp_forward(4, good, good, good, 4096, 14330, 4096, 8, 4096, 4096, None, None, None) == -1
     assert lib.fsdp_mlp_forward(4, good, good, grads, 4096, 14336, 4096, 8, 4096, 4096, None, None, None) == -1
     assert lib.fsdp_mlp_forward(4, good, good, good, 4096, 14336, 4097, 8, 4096, 4096, None, None, None) == -1
-    # static scratch: weights above 8,388,608 elements
-    assert lib.fsdp_unit_forward_static_scratch(2, good, 4096, 4104, 4096, 128, 8192, None, None) == -1
+    # static scratch: weights above 8,388,608 elements whose shards (2 x 2056 rows) do not
+    # tile the GEMM, so they would need the array
+    assert lib.fsdp_unit_forward_static_scratch(2, good, 4112, 4104, 4096, 128, 8192, None, None) == -1
     assert b"static scratch" in lib.zero_last_error()
     # self-test limit
     assert lib.zero_selftest_bounded_wait(0, None) == -1
     assert lib.zero_selftest_bounded_wait(5000, None) == -1
+
+
+def buffer_bytes(plan, rank):
+    """Bytes of the buffers one step call addresses, summed from the pointer conventions of
+    include/zero.h buffer by buffer (gradients, master, m, v, parameters)."""
+    P, S, n = plan.psi_padded, plan.shard_elems, plan.n_ranks
+    gbytes = 4 if plan.stage == 4 else 2
+    if rank == z_ALL:
+        bufs = [(P, gbytes)] * n + [(P, 4)] * 3 + [(P, 2)]
+    elif rank == z_VIEW:
+        bufs = [(S, gbytes)] * n + [(S, 4)] * 3 + [(S, 2)]
+    else:
+        bufs = [(P, gbytes)] * n + [(S, 4)] * 3 + [(S if plan.stage == 3 else P, 2)]
+    return sum(e * b for e, b in bufs)
+
+
+z_ALL, z_VIEW = -2, -1
+
+
+@pytest.mark.parametrize("psi,n,stage", [(1000, 8, "zero2"), (7, 3, "zero3"), (1_500_000_000, 64, "zero2"),
+                                         (7_241_732_096, 8, "zero3"), (124_356_864, 8, "megatron"),
+                                         (124_356_864, 8, "ddp")])
+def test_memory_check_counts_the_step_buffers(z, psi, n, stage):
+    plan = z.zero_plan(psi, n, stage, 1 << 20)
+    for rank in (z_ALL, z_VIEW, 0, n - 1):
+        want = buffer_bytes(plan, rank)
+        need, budget = z.zero_plan_check_memory(plan, rank, want)
+        assert (need, budget) == (want, want)
+        with pytest.raises(z.ZeroError) as e:
+            z.zero_plan_check_memory(plan, rank, want - 1)
+        assert e.value.code == -2 and str(want) in str(e.value)
+
+
+def test_memory_check_mistral_ddp_does_not_fit_an_80gb_gpu(z):
+    # [Wiring] "Fully Sharded Data Parallel (FSDP)": Mistral-7B ran out of memory under DDP
+    # on 80 GB GPUs. A DDP rank holds the whole model state, 16 bytes per parameter (one
+    # rank of a one-rank plan addresses exactly that), while a ZeRO-3 rank's view at N = 4
+    # (its shard plus the 4 incoming gradient chunks) fits.
+    budget = 80 * 10**9
+    ddp = z.zero_plan(7_241_732_096, 1, "ddp", 50 << 20)
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_plan_check_memory(ddp, 0, budget)
+    assert e.value.code == -2
+    assert buffer_bytes(ddp, 0) == 16 * 7_241_732_096 == ddp.state_total_bytes
+    z3 = z.zero_plan(7_241_732_096, 4, "zero3", 50 << 20)
+    need, _ = z.zero_plan_check_memory(z3, z_VIEW, budget)
+    assert need == (2 * 4 + 14) * z3.shard_elems < budget
+
+
+def test_memory_check_rejects_bad_rank(z):
+    plan = z.zero_plan(1000, 4, "zero2", 1 << 20)
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_plan_check_memory(plan, 4, 1 << 30)
+    assert e.value.code == -1

@@ -623,8 +623,17 @@ def test_sweep_1p5b_sampled(z, n, mode):
         assert z.zero_plan(psi, n, stage, bb).state_total_bytes == total
     if mode == "full":
         torch.cuda.empty_cache()
-        if (2 * n + 14) * P + (8 << 30) > torch.cuda.mem_get_info()[0]:
+        # the library states the step's need before anything is allocated: (2N + 14) P
+        # bytes of gradients, state and parameters, against the free memory less 8 GiB
+        free = torch.cuda.mem_get_info()[0]
+        try:
+            need, budget = z.zero_plan_check_memory(plan, z.ZERO_ALL_RANKS, max(1, free - (8 << 30)))
+        except z.ZeroError as e:
+            assert e.code == -2 and str((2 * n + 14) * P) in str(e)
             pytest.skip(f"{(2 * n + 14) * P / 1e9:.0f} GB of buffers do not fit in free device memory")
+        assert need == (2 * n + 14) * P
+        need0, free0 = z.zero_plan_check_memory(plan, z.ZERO_ALL_RANKS)
+        assert need0 == need and free0 == free
         grads = [synth.rank_grads(psi, P, r, 1, device=DEV) for r in range(n)]
         master = synth.master_params(psi, P, device=DEV)
         m = torch.zeros(P, device=DEV)
