@@ -679,7 +679,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 std::atomic<int> g_gemm_kernel{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-std::once_flag g_attr_once[2][64];
+OncePerDevice g_attr_once[2];
 
 int get_encode() {
   std::call_once(g_encode_once, [] {
@@ -826,13 +826,13 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
-  cudaError_t attr = cudaSuccess;
-  std::call_once(g_attr_once[GATE_UP ? 1 : 0][dev & 63], [&] {
-    attr = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Mode<GATE_UP>::SMEM);
-    if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(fsdp_gemm_pair_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  PAIR_SMEM);
+  const cudaError_t attr = g_attr_once[GATE_UP ? 1 : 0].run(dev, [] {
+    cudaError_t a = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Mode<GATE_UP>::SMEM);
+    if (a == cudaSuccess)
+      a = cudaFuncSetAttribute(fsdp_gemm_pair_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PAIR_SMEM);
+    return a;
   });
   if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(attr));
   if (pair) {
@@ -909,6 +909,13 @@ int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* X
   return launch_gemm<false>({n_ranks, dY, true, m_tokens}, {1, xt1, false, k_in}, nullptr, rows_out, k_in,
                             m_tokens * n_ranks, y1, 1, nullptr, 1.0f / static_cast<float>(n_ranks), st,
                             "fsdp_unit_backward");
+}
+
+bool fsdp_fused_gather_ok(int n_ranks, int64_t rows_out) {
+  if (n_ranks < 1 || n_ranks > kMaxShards || rows_out < 1 || rows_out % n_ranks) return false;
+  // K-major forward: the pair kernel loads 128-row halves of each W tile, the one-CTA
+  // kernel whole TN-row tiles, and each load must lie inside one shard
+  return n_ranks == 1 || (rows_out / n_ranks) % (g_gemm_kernel.load() == 1 ? BN : 128) == 0;
 }
 
 int set_gemm_kernel(int which) {

@@ -218,7 +218,7 @@ TmaConfig tma_config(int n) {
   return {tile, stages, stages * stage_bytes};
 }
 
-std::once_flag g_tma_attr_once[64];
+OncePerDevice g_tma_attr_once;
 }  // namespace
 
 cudaError_t launch_fused(const GradPtrs& gp, int n, float* master, float* m, float* v, uint16_t* param,
@@ -229,10 +229,9 @@ cudaError_t launch_fused(const GradPtrs& gp, int n, float* master, float* m, flo
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    cudaError_t attr_err = cudaSuccess;
-    std::call_once(g_tma_attr_once[dev & 63], [&] {
-      attr_err = cudaFuncSetAttribute(fused_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kTmaSmemBudget));
+    const cudaError_t attr_err = g_tma_attr_once.run(dev, [] {
+      return cudaFuncSetAttribute(fused_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kTmaSmemBudget));
     });
     if (attr_err != cudaSuccess) return attr_err;
     const TmaConfig c = tma_config(n);

@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/zero.h"
 
 struct zero_plan {
@@ -86,6 +89,32 @@ int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* X
                        int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st);
 unsigned int fsdp_gemm_read_clear_error();
 int set_gemm_kernel(int which);  // 0 = default, 1 = one-CTA kernel everywhere, 2 = CTA-pair kernel everywhere
+
+// Runs a set-up step (a kernel attribute) once per device until it succeeds. Unlike
+// std::call_once, a failed attempt (say, under an error left pending by an earlier launch)
+// leaves the device's flag clear, so the next call tries again instead of launching with
+// the attribute unset.
+class OncePerDevice {
+ public:
+  template <class F>
+  cudaError_t run(int dev, F&& setup) {
+    std::atomic<bool>& flag = done_[dev & 63];
+    if (flag.load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (flag.load(std::memory_order_relaxed)) return cudaSuccess;
+    const cudaError_t e = setup();
+    if (e == cudaSuccess) flag.store(true, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::atomic<bool> done_[64] = {};
+  std::mutex mu_;
+};
+
+// True when fsdp_unit_forward can read W straight from its n_ranks row shards (the fused
+// gather, no scratch) under the current zero_set_gemm_kernel choice.
+bool fsdp_fused_gather_ok(int n_ranks, int64_t rows_out);
 
 // ---- errors (capi.cu) ----
 int set_error(int code, const char* fmt, ...);
