@@ -1,11 +1,12 @@
 """Benchmark of the fused ZeRO optimizer step on GB300.
 
-Default workload: the GPT-2-small parameter list (124,356,864 parameters, flattened) with
-N = 8 simulated data-parallel ranks, ZeRO-2, 25 MiB buckets. One step = one launch of the
-fused reduce-scatter + Adam + bf16 all-gather kernel over every rank's shard: it reads the
-8 ranks' bf16 gradients and the fp32 master / m / v and writes master / m / v and the full
-bf16 parameter buffer: P * (2N + 26) = 5.22 GB of HBM traffic per step, far above the
-129 MB L2, so no flush is needed between steps.
+Default workload: one rank's view of the Mistral-7B parameter list (7,241,732,096
+parameters) at N = 8 simulated data-parallel ranks, ZeRO-3, 50 MiB buckets. The rank owns
+a 905,216,512-element shard; it holds the shard's fp32 master / m / v and receives the 8
+ranks' bf16 gradient chunks for it. One step = one launch of the fused reduce-scatter +
+Adam + bf16 cast over the whole shard (all 277 buckets): it reads the 8 chunks and master /
+m / v and writes master / m / v and the bf16 shard, S * (2N + 26) = 38.02 GB of HBM traffic
+per step, ~300x the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
 
@@ -52,15 +53,29 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def workload_config(psi, n, stage, bb):
+HP = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+
+
+def workload_config(psi, n, stage, bb, shard):
+    """The bench line's workload: one rank's view of the Mistral-7B list (its shard of
+    `shard` elements and the n incoming gradient chunks for it)."""
+    return {
+        "workload": f"Mistral-7B parameter list ({psi:,} params), one rank's view at N={n} simulated data-parallel "
+                    f"ranks, {stage.upper()}: fused reduce-scatter + Adam + bf16 cast over the rank's {shard:,}-element "
+                    f"shard from the {n} incoming bf16 gradient chunks, {bb // MIB} MiB buckets, all buckets in one "
+                    "launch per step",
+        "psi": psi, "n_ranks": n, "stage": stage, "bucket_bytes": bb, "shard_elems": shard,
+        "adam": HP, "grads": "bf16 N(0,1e-3) per incoming chunk", "master": "fp32 N(0,0.02)",
+        "l2": f"inputs larger than L2 ({shard * (2 * n + 26) / 1e9:.2f} GB per step vs 129 MB L2): no flush",
+    }
+
+
+def gpt2_config(psi, n, stage, bb):
     return {
         "workload": f"GPT-2-small parameter list ({psi:,} params) flattened, N={n} simulated data-parallel ranks, "
                     f"{stage.upper()} fused reduce-scatter + Adam + bf16 param all-gather, {bb // MIB} MiB buckets, "
                     "every rank's shard in one launch per step",
         "psi": psi, "n_ranks": n, "stage": stage, "bucket_bytes": bb,
-        "adam": {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0},
-        "grads": "bf16 N(0,1e-3) per rank", "master": "fp32 N(0,0.02)",
-        "l2": "inputs larger than L2 (5.22 GB per step vs 129 MB L2): no flush",
     }
 
 
@@ -129,9 +144,10 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, bytes_per_unit_launch: float):
-    """dram read + write bytes per launch of `kernel` from profiles/ncu_traffic.txt, scaled
-    to this launch by units processed, or None when absent or taken on other source."""
+def ncu_traffic(kernel: str, units: float, mode: str = "all_ranks"):
+    """dram read + write bytes per launch of `kernel` in rank mode `mode` from
+    profiles/ncu_traffic.txt, scaled to this launch by the units (parameters) it processes,
+    or None when absent or taken on other source."""
     p = ROOT / "profiles" / "ncu_traffic.txt"
     if not p.exists():
         return None
@@ -139,8 +155,9 @@ def ncu_traffic(kernel: str, bytes_per_unit_launch: float):
         if line.startswith("#") or not line.strip():
             continue
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-        if f.get("kernel") == kernel and f.get("source") == kernel_source_digest():
-            return float(f["dram_bytes_per_unit"]) * bytes_per_unit_launch
+        if (f.get("kernel") == kernel and f.get("mode", "all_ranks") == mode
+                and f.get("source") == kernel_source_digest()):
+            return float(f["dram_bytes_per_unit"]) * units
     return None
 
 
@@ -187,6 +204,21 @@ def barrier(world):
         dist.barrier()
 
 
+def mistral_rank_view(z, synth, dev):
+    """The bench workload on the device: the plan, the 8 incoming bf16 chunks for the
+    rank's shard, fp32 master / m / v and the bf16 shard out (27.2 GB)."""
+    import torch
+    psi, n, stage, bb = synth.MISTRAL_7B_PSI, 8, "zero3", 50 * MIB
+    plan = z.zero_plan(psi, n, stage, bb)
+    S = plan.shard_elems
+    ch = synth.chunk_grads(S, n, 1, device=dev)
+    st = {"plan": plan, "psi": psi, "n": n, "stage": stage, "bb": bb, "S": S, "chunks": ch,
+          "grads": [ch[q] for q in range(n)], "master": synth.master_params(S, S, device=dev),
+          "m": torch.zeros(S, device=dev), "v": torch.zeros(S, device=dev),
+          "param": torch.empty(S, dtype=torch.bfloat16, device=dev)}
+    return st
+
+
 def run_ours(args):
     import torch
 
@@ -196,23 +228,17 @@ def run_ours(args):
     world, rank, local = init_dist(args)
     dev = torch.device("cuda", torch.cuda.current_device())
     hbm_peak, tf_burst, tf_sust, peak_src = peaks()
-    psi, n, stage, bb = synth.GPT2_SMALL_PSI, 8, "zero2", 25 * MIB
-    plan = z.zero_plan(psi, n, stage, bb)
-    P = plan.psi_padded
-    bytes_per_step = plan.fused_step_bytes
-    grads = [synth.rank_grads(psi, P, r, 1, device=dev) for r in range(n)]
-    master = synth.master_params(psi, P, device=dev)
-    m = torch.zeros(P, device=dev)
-    v = torch.zeros(P, device=dev)
-    param = torch.empty(P, dtype=torch.bfloat16, device=dev)
-    hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+    w = mistral_rank_view(z, synth, dev)
+    plan, n, S = w["plan"], w["n"], w["S"]
+    bytes_per_step = S * (2 * n + 26)
     stream = torch.cuda.current_stream()
     step_no = 0
 
     def step():
         nonlocal step_no
         step_no += 1
-        z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, step_no, stream)
+        z.zero_fused_step(plan, z.ZERO_RANK_VIEW, w["grads"], w["master"], w["m"], w["v"], w["param"], HP, step_no,
+                          stream)
 
     for _ in range(args.warmup):
         step()
@@ -237,31 +263,44 @@ def run_ours(args):
     ms_total = max_over_ranks(t0.elapsed_time(t1), world)
     ms_step = ms_total / K
     launch_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    value = job_throughput(psi, K, world, ms_total / 1e3)
+    value = job_throughput(S, K, world, ms_total / 1e3)
     achieved = bytes_per_step / (launch_ms / 1e3) / 1e9
     clocks = clk.summary()
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded; GPT-2-small tensor shapes, random values; no dataset, no weights)",
-        "config": workload_config(psi, n, stage, bb),
+        "data": "synthetic (seeded; Mistral-7B parameter count and shard layout, random values; no dataset, no "
+                "weights)",
+        "config": workload_config(w["psi"], n, w["stage"], w["bb"], S),
         "hbm_gbs": bytes_per_step * K * world / (ms_total / 1e3) / 1e9,
         "hbm_pct_of_peak": 100.0 * (bytes_per_step * K / (ms_total / 1e3) / 1e9) / hbm_peak,
         "roofline": {"bound": "hbm", "kernel": "fused_vec_kernel<8>", "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "traffic": ncu_traffic("fused_vec_kernel", P),
-                     "algorithmic_bytes_per_launch": bytes_per_step, "launch_ms": launch_ms},
+                     "traffic": ncu_traffic("fused_vec_kernel", S, mode="rank_view"),
+                     "traffic_note": "dram read + write bytes per parameter from an ncu capture of the same kernel "
+                                     "in the same rank-view mode on 33,554,432-element chunks, times the shard's "
+                                     "parameters (the kernel is a pure stream)",
+                     "algorithmic_bytes_per_launch": bytes_per_step, "bytes_per_param": 2 * n + 26,
+                     "launch_ms": launch_ms},
         "clocks": clocks,
         "gpu_launches": K,
     }
-    # end to end through the public API: grads from pinned host memory, params back
-    out["e2e"] = e2e_leg(z, synth, plan, psi, n, dev, hp, world, args)
+    # the same step as one launch per 50 MiB bucket (277 launches, replayed from a CUDA graph)
+    bucket_leg = None
+    if not args.no_legs and rank == 0:
+        bucket_leg = per_bucket_leg(z, w, hbm_peak, stream)
+    # end to end through the public API: the incoming chunks from page-locked host memory,
+    # the bf16 shard back to it
+    out["e2e"] = e2e_leg(z, w, world, args)
+    del w
+    torch.cuda.empty_cache()
     # the other rows, reported by rank 0 only (they hold no collective, so the other ranks
     # need not run them)
     if not args.no_legs and rank == 0:
         out["legs"] = extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args)
+        out["legs"]["mistral_rank_view_per_bucket"] = bucket_leg
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
         if "legs" in out:
@@ -273,19 +312,69 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def e2e_leg(z, synth, plan, psi, n, dev, hp, world, args):
-    """The same metric end to end through the public API with HOST buffers: every step the 8
-    ranks' bf16 gradients (1.99 GB) come from page-locked host memory and the bf16
-    parameters (249 MB) go back to it. zero_fused_step_host reads the gradients and writes
-    the parameters straight over the host link inside the kernel (each byte crosses once);
-    the staged variant copies them with cudaMemcpyAsync around zero_fused_step instead."""
+def per_bucket_leg(z, w, hbm_peak, stream):
+    """The headline step as DDP / ZeRO issue it, one launch per 50 MiB bucket as backward
+    produces it: 277 launches captured in a CUDA graph, on one stream and round-robin on
+    four (the buckets are disjoint, so launches on different streams may overlap). Same
+    bits as the one launch (tested)."""
     import torch
-    P = plan.psi_padded
-    host_grads = [synth.rank_grads(psi, P, r, 2).pin_memory() for r in range(n)]
-    master = synth.master_params(psi, P, device=dev)
-    m = torch.zeros(P, device=dev)
-    v = torch.zeros(P, device=dev)
-    host_param = torch.empty(P, dtype=torch.bfloat16).pin_memory()
+    plan, n, S = w["plan"], w["n"], w["S"]
+    byts = S * (2 * n + 26)
+    a = (w["grads"], w["master"], w["m"], w["v"], w["param"], HP, 1)
+    res = {"n_buckets": plan.n_buckets, "bucket_elems": plan.bucket_elems, "bytes": byts}
+    for ns in (1, 4):
+        g = bucket_graph(z, plan, z.ZERO_RANK_VIEW, a, ns)
+        ms = time_launches(lambda: g.replay(), 10, stream)
+        res[f"streams_{ns}"] = {"ms": ms, "gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm_peak,
+                                "launches_per_step": plan.n_buckets}
+        del g
+    z.zero_device_status(stream)
+    return res
+
+
+def host_mem_available() -> int:
+    """MemAvailable of this host in bytes (0 if unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def e2e_elems(S: int, n: int, world: int, avail: int, bucket: int) -> int:
+    """Shard elements the e2e leg moves through host memory per step: the whole shard when
+    every rank's page-locked buffers ((2n + 2) bytes per element, rounded up to powers of two
+    by the pinned allocator) fit in half of the host's available memory, otherwise the
+    largest whole number of buckets that does (at least one)."""
+    def pinned(L):
+        return (n + 1) * (1 << (2 * L - 1).bit_length())
+    if avail <= 0 or world * pinned(S) <= avail // 2:
+        return S
+    L = S
+    while L > bucket and world * pinned(L) > avail // 2:
+        L = max(bucket, (L // 2) // bucket * bucket)
+    return L
+
+
+def e2e_leg(z, w, world, args):
+    """The same metric end to end through the public API with HOST buffers: every step the 8
+    incoming bf16 gradient chunks come from page-locked host memory and the bf16 shard goes
+    back to it. zero_fused_step_host reads the chunks and writes the shard straight over
+    the host link inside the kernel (each byte crosses once); the staged variant copies
+    them with cudaMemcpyAsync around zero_fused_step instead. When the host cannot pin the
+    whole shard's buffers for every rank, a stated prefix of whole buckets is moved."""
+    import torch
+    n, S = w["n"], w["S"]
+    L = e2e_elems(S, n, world, host_mem_available(), w["plan"].bucket_elems)
+    plan = w["plan"] if L == S else z.zero_plan(n * L, n, w["stage"], w["bb"])
+    host_chunks = [torch.empty(L, dtype=torch.bfloat16, pin_memory=True) for _ in range(n)]
+    for q in range(n):
+        host_chunks[q].copy_(w["grads"][q][:L])
+    host_param = torch.empty(L, dtype=torch.bfloat16, pin_memory=True)
+    master, m, v = w["master"][:L], w["m"][:L], w["v"][:L]
     stream = torch.cuda.current_stream()
     steps = max(3, args.e2e_steps)
 
@@ -303,26 +392,30 @@ def e2e_leg(z, synth, plan, psi, n, dev, hp, world, args):
         return el
 
     def direct(t):
-        z.zero_fused_step_host(plan, z.ZERO_ALL_RANKS, host_grads, master, m, v, host_param, hp, t, stream)
+        z.zero_fused_step_host(plan, z.ZERO_RANK_VIEW, host_chunks, master, m, v, host_param, HP, t, stream)
 
     el = run(direct, 1)
-    dgrads = [torch.empty(P, dtype=torch.bfloat16, device=dev) for _ in range(n)]
-    param = torch.empty(P, dtype=torch.bfloat16, device=dev)
+    dgrads = [w["grads"][q][:L] for q in range(n)]
+    param = w["param"][:L]
 
     def staged(t):
         for q in range(n):
-            dgrads[q].copy_(host_grads[q], non_blocking=True)
-        z.zero_fused_step(plan, z.ZERO_ALL_RANKS, dgrads, master, m, v, param, hp, t, stream)
+            dgrads[q].copy_(host_chunks[q], non_blocking=True)
+        z.zero_fused_step(plan, z.ZERO_RANK_VIEW, dgrads, master, m, v, param, HP, t, stream)
         host_param.copy_(param, non_blocking=True)
 
     el_staged = run(staged, 100)
-    return {"value": job_throughput(psi, steps, world, el), "unit": UNIT, "h2d_bytes_per_step": 2 * P * n,
-            "d2h_bytes_per_step": 2 * P, "steps": steps, "ms_per_step": 1e3 * el / steps,
-            "how": "zero_fused_step_host: the kernel reads the 8 ranks' bf16 gradients from page-locked host memory "
-                   "and writes the bf16 parameters back to it over the host link; wall clock over the steps",
-            "staged_copies": {"value": job_throughput(psi, steps, world, el_staged), "ms_per_step": 1e3 * el_staged / steps,
-                              "how": "cudaMemcpyAsync host->device of the gradients, zero_fused_step, device->host "
-                                     "copy of the parameters"}}
+    del host_chunks, host_param
+    return {"value": job_throughput(L, steps, world, el), "unit": UNIT, "h2d_bytes_per_step": 2 * L * n,
+            "d2h_bytes_per_step": 2 * L, "steps": steps, "ms_per_step": 1e3 * el / steps,
+            "elems_per_step": L, "whole_shard": L == S,
+            "how": "zero_fused_step_host: the kernel reads the 8 incoming bf16 gradient chunks from page-locked host "
+                   "memory and writes the bf16 shard back to it over the host link; wall clock over the steps"
+                   + ("" if L == S else f"; the first {L:,} of the {S:,} shard elements (whole 50 MiB buckets), as "
+                                        "the host could not pin the whole shard's buffers for every rank"),
+            "staged_copies": {"value": job_throughput(L, steps, world, el_staged), "ms_per_step": 1e3 * el_staged / steps,
+                              "how": "cudaMemcpyAsync host->device of the chunks, zero_fused_step, device->host "
+                                     "copy of the shard"}}
 
 
 def time_launches(fn, iters, stream):
@@ -369,11 +462,18 @@ def extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args):
     legs["allgather_params"] = {"ms": ms_ag, "gbs": b_ag / ms_ag / 1e6, "frac": b_ag / ms_ag / 1e6 / hbm_peak,
                                 "bytes": b_ag, "params_per_s": P / ms_ag * 1e3}
     legs["unfused_pipeline_ms"] = ms_ar + ms_ad + ms_ag
+    # the same list at N = 8, ZeRO-2, every rank's shard in one fused launch (5.22 GB)
+    plan2 = z.zero_plan(psi, n, "zero2", 25 * MIB)
+    ms_f = time_launches(lambda: z.zero_fused_step(plan2, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1, stream),
+                         200, stream)
+    b_f = P * (2 * n + 26)
+    legs["gpt2_small_fused_step"] = {"config": gpt2_config(psi, n, "zero2", 25 * MIB), "ms": ms_f,
+                                     "gbs": b_f / ms_f / 1e6, "frac": b_f / ms_f / 1e6 / hbm_peak, "bytes": b_f,
+                                     "params_per_s": psi / ms_f * 1e3, "kernel": "fused_vec_kernel<8>"}
     z.zero_set_fused_kernel(1)
     ms_tma = time_launches(lambda: z.zero_fused_step(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp, 1,
                                                      stream), it, stream)
     z.zero_set_fused_kernel(0)
-    b_f = P * (2 * n + 26)
     legs["fused_tma_pipeline_variant"] = {"ms": ms_tma, "gbs": b_f / ms_tma / 1e6, "frac": b_f / ms_tma / 1e6 / hbm_peak}
     del grads, g
     # Megatron distributed optimizer: the same fused step on fp32 gradients, 4N + 26 B/param
@@ -490,14 +590,16 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
 # ---------------------------------------------------------------------------------------
 
 class OracleSample:
-    """The first n_params parameters of the bench workload (N = 8 bf16 gradient slices,
-    fp32 master / m / v), generated once; step() runs one fused oracle step (reduce, Adam,
-    cast in plain numpy) on the first `count` of them and returns its seconds. With
-    threads > 1 the same oracle call runs on `threads` contiguous ranges at once: the step
-    is elementwise, so the split changes no result, and numpy releases the interpreter lock
-    inside its array operations."""
+    """A bounded sample of a fused-step workload, generated once: n_params parameters with
+    n_ranks bf16 gradient slices and fp32 master / m / v. chunks=True draws the slices as
+    one rank's incoming chunks (the Mistral-7B rank view, synth.chunk_grads), otherwise as
+    the ranks' flat gradient buffers (synth.rank_grads); both are the same distributions.
+    step() runs one fused oracle step (reduce, Adam, cast in plain numpy) on the first
+    `count` parameters and returns its seconds. With threads > 1 the same oracle call runs
+    on `threads` contiguous ranges at once: the step is elementwise, so the split changes
+    no result, and numpy releases the interpreter lock inside its array operations."""
 
-    def __init__(self, n_params: int, n_ranks: int = 8, threads: int = 1):
+    def __init__(self, n_params: int, n_ranks: int = 8, threads: int = 1, chunks: bool = False):
         import numpy as np
         import torch
 
@@ -508,8 +610,12 @@ class OracleSample:
         self.master = synth.master_params(n_params, n_params).numpy()
         self.m = np.zeros(n_params, np.float32)
         self.v = np.zeros(n_params, np.float32)
-        self.grads = [synth.rank_grads(n_params, n_params, r, 1).view(torch.int16).numpy().view(np.uint16)
-                      for r in range(n_ranks)]
+        if chunks:
+            ch = synth.chunk_grads(n_params, n_ranks, 1).view(torch.int16).numpy().view(np.uint16)
+            self.grads = [ch[q] for q in range(n_ranks)]
+        else:
+            self.grads = [synth.rank_grads(n_params, n_params, r, 1).view(torch.int16).numpy().view(np.uint16)
+                          for r in range(n_ranks)]
         self.hp = O.AdamHyper()
         self.t = 0
         self.threads = max(1, int(threads))
@@ -611,23 +717,27 @@ def host_info() -> dict:
     return info
 
 
+MISTRAL_SHARD = 905_216_512
+
+
 def cpu_baseline(budget_s: float = 12.0, one_core_s: float = 4.0):
     """The oracle on every host core (contiguous ranges of the sample, one thread each), and
-    for context the same oracle on one core."""
+    for context the same oracle on one core, on a sample of the bench workload: the first
+    elements of the Mistral-7B rank's shard with its 8 incoming gradient chunks."""
     cores = os.cpu_count() or 1
     n_params = 16 * MIB
-    s = OracleSample(n_params, threads=cores)
+    s = OracleSample(n_params, threads=cores, chunks=True)
     el = s.step(n_params)
     reps = max(1, int(budget_s / max(el, 1e-3)))
     total = sum(s.step(n_params) for _ in range(reps))
-    one = OracleSample(4 * MIB)
+    one = OracleSample(4 * MIB, chunks=True)
     one_el, one_reps = _time_bounded(lambda: one.step(4 * MIB), one_core_s)
     return {"value": n_params * reps / total, "unit": UNIT, "cores": cores, "kind": "oracle", "host": host_info(),
             "one_core_value": 4 * MIB / one_el,
-            "sample": f"first {n_params:,} of 124,356,864 GPT-2-small parameters, N=8 gradient slices, "
-                      f"{reps} fused steps ({total:.1f} s), split into {cores} contiguous ranges run by "
-                      f"{cores} threads (numpy elementwise); one_core_value: the first {4 * MIB:,} on one "
-                      f"thread, {one_reps} steps"}
+            "sample": f"{n_params:,} of the {MISTRAL_SHARD:,} elements of the Mistral-7B rank's shard (N=8, ZeRO-3) "
+                      f"with their 8 incoming bf16 gradient chunks, {reps} fused steps ({total:.1f} s), split into "
+                      f"{cores} contiguous ranges run by {cores} threads (numpy elementwise); one_core_value: "
+                      f"{4 * MIB:,} elements on one thread, {one_reps} steps"}
 
 
 def run_reference(args):
@@ -636,10 +746,10 @@ def run_reference(args):
     if rank != 0:
         return
     import synth
-    psi, n, stage, bb = synth.GPT2_SMALL_PSI, 8, "zero2", 25 * MIB
+    psi, n, stage, bb, S = synth.MISTRAL_7B_PSI, 8, "zero3", 50 * MIB, MISTRAL_SHARD
     cap = 16 * MIB
     cores = os.cpu_count() or 1
-    s = OracleSample(cap, threads=cores)
+    s = OracleSample(cap, threads=cores, chunks=True)
     s.step(cap)
     rate = cap / s.step(cap)
     # size each step's sample so the whole run stays near args.ref_seconds
@@ -650,12 +760,13 @@ def run_reference(args):
     t_total = sum(s.step(count) for _ in range(args.steps))
     value = count * args.steps / t_total
     cb = {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "host": host_info(),
-          "sample": f"first {count:,} of {psi:,} parameters per step (N=8), numpy elementwise, split into "
-                    f"{cores} contiguous ranges run by {cores} threads"}
+          "sample": f"{count:,} of the {S:,} elements of the Mistral-7B rank's shard per step (N=8 incoming chunks), "
+                    f"numpy elementwise, split into {cores} contiguous ranges run by {cores} threads"}
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-           "warmup": args.warmup, "ms_per_step": 1e3 * psi / value, "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; GPT-2-small tensor shapes)",
-           "config": workload_config(psi, n, stage, bb), "impl": "reference", "cpu_baseline": cb,
+           "warmup": args.warmup, "ms_per_step": 1e3 * S / value, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; Mistral-7B parameter count and shard "
+                                                        "layout)",
+           "config": workload_config(psi, n, stage, bb, S), "impl": "reference", "cpu_baseline": cb,
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -719,7 +830,13 @@ def run_sweep(args):
                             f"{cores} threads; extrapolated to {psi:,} parameters"}
         del sample
         torch.cuda.empty_cache()
-        full = (2 * n + 14) * P + (8 << 30) <= torch.cuda.mem_get_info()[0]
+        # all ranks when the step's buffers ((2N + 14) P bytes, as the library counts them)
+        # fit in free device memory less an 8 GiB margin
+        try:
+            z.zero_plan_check_memory(plan0, z.ZERO_ALL_RANKS, max(1, torch.cuda.mem_get_info()[0] - (8 << 30)))
+            full = True
+        except z.ZeroError:
+            full = False
         L = P if full else S
         if full:
             grads = [synth.rank_grads(psi, P, r, 1, device=dev) for r in range(n)]
@@ -820,10 +937,12 @@ def run_case(args):
         ms = time_launches(lambda: z.zero_fused_step_fp32_grads(plan, z.ZERO_ALL_RANKS, grads, master, m, v, param, hp,
                                                                 1, stream), 4, stream)
         out.update(psi=psi, n_ranks=n, ms=ms, bytes=plan.fused_step_bytes, gbs=plan.fused_step_bytes / ms / 1e6)
-    elif args.case in ("tiny", "mistral_rank_view"):
+    elif args.case in ("tiny", "mistral_rank_view", "rank_view_small"):
         # tiny: psi = 2^20, N = 4, every rank in one launch (35.7 MB: L2-resident, reported as
         # such). mistral_rank_view: one rank's shard of the Mistral-7B list at N = 8
         # (S = 905,216,512; its 8 incoming chunks, 14.5 GB), ZeRO-3, 50 MiB buckets.
+        # rank_view_small: the same rank-view launch on 33,554,432-element chunks (1.41 GB
+        # per launch, 11x the L2), sized for an ncu capture.
         hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
         hbm_peak = peaks()[0]
         if args.case == "tiny":
@@ -832,7 +951,7 @@ def run_case(args):
             grads = [synth.rank_grads(psi, psi, r, 1, device=dev) for r in range(n)]
             L, rank = psi, z.ZERO_ALL_RANKS
         else:
-            psi, n = synth.MISTRAL_7B_PSI, 8
+            psi, n = (synth.MISTRAL_7B_PSI if args.case == "mistral_rank_view" else 8 << 25), 8
             plan = z.zero_plan(psi, n, "zero3", 50 * MIB)
             L, rank = plan.shard_elems, z.ZERO_RANK_VIEW
             ch = synth.chunk_grads(L, n, 1, device=dev)
@@ -841,7 +960,8 @@ def run_case(args):
         m = torch.zeros(L, device=dev)
         v = torch.zeros(L, device=dev)
         param = torch.empty(L, dtype=torch.bfloat16, device=dev)
-        ms = time_launches(lambda: z.zero_fused_step(plan, rank, grads, master, m, v, param, hp, 1, stream), 20, stream)
+        ms = time_launches(lambda: z.zero_fused_step(plan, rank, grads, master, m, v, param, hp, 1, stream),
+                           4 if args.case == "rank_view_small" else 20, stream)
         byts = L * (2 * n + 26)
         out.update(params_per_step=L, n_ranks=n, ms=ms, bytes=byts, gbs=byts / ms / 1e6,
                    frac=byts / ms / 1e6 / hbm_peak, params_per_s=L / ms * 1e3,
@@ -924,7 +1044,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="one measured case: fused_small | fused_tma_small | megatron_small | e2e_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
-                         "backward_up (ncu-sized) | "
+                         "backward_up | rank_view_small (ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)

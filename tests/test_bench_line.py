@@ -27,8 +27,14 @@ def test_bench_prints_one_complete_line():
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
-    assert rf["algorithmic_bytes_per_launch"] == 124_356_864 * (2 * 8 + 26)
+    # the Mistral-7B rank view at N = 8: a 905,216,512-element shard, 2N + 26 bytes each
+    S = 905_216_512
+    assert d["config"]["shard_elems"] == S and d["config"]["n_ranks"] == 8 and d["config"]["stage"] == "zero3"
+    assert rf["algorithmic_bytes_per_launch"] == S * (2 * 8 + 26)
+    assert d["ms_per_step"] * 1e-3 * d["value"] == pytest.approx(S, rel=1e-9)
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     e2e = d["e2e"]
     assert e2e["unit"] == d["unit"] and e2e["value"] > 0
-    assert e2e["h2d_bytes_per_step"] == 8 * 124_356_864 * 2 and e2e["d2h_bytes_per_step"] == 124_356_864 * 2
+    L = e2e["elems_per_step"]
+    assert 0 < L <= S and e2e["whole_shard"] == (L == S)
+    assert e2e["h2d_bytes_per_step"] == 8 * L * 2 and e2e["d2h_bytes_per_step"] == L * 2
