@@ -322,13 +322,17 @@ def per_bucket_leg(z, w, hbm_peak, stream):
     byts = S * (2 * n + 26)
     a = (w["grads"], w["master"], w["m"], w["v"], w["param"], HP, 1)
     res = {"n_buckets": plan.n_buckets, "bucket_elems": plan.bucket_elems, "bytes": byts}
-    for ns in (1, 4):
-        g = bucket_graph(z, plan, z.ZERO_RANK_VIEW, a, ns)
-        ms = time_launches(lambda: g.replay(), 10, stream)
-        res[f"streams_{ns}"] = {"ms": ms, "gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm_peak,
-                                "launches_per_step": plan.n_buckets}
-        del g
-    z.zero_device_status(stream)
+    side = torch.cuda.Stream()  # graphs are captured on a stream other than the default one
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for ns in (1, 4):
+            g = bucket_graph(z, plan, z.ZERO_RANK_VIEW, a, ns)
+            ms = time_launches(lambda: g.replay(), 10, side)
+            res[f"streams_{ns}"] = {"ms": ms, "gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm_peak,
+                                    "launches_per_step": plan.n_buckets}
+            del g
+    stream.wait_stream(side)
+    z.zero_device_status(side)
     return res
 
 
@@ -487,7 +491,75 @@ def extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args):
     del grads32, master, m, v, param
     torch.cuda.empty_cache()
     legs["fsdp_unit_forward"] = fsdp_leg(z, synth, dev, tf_burst, peak_src, stream)
+    torch.cuda.empty_cache()
+    legs["fsdp_zero3_step"] = zero3_leg(z, synth, dev, tf_burst, hbm_peak, stream)
     return legs
+
+
+ZERO3_SHAPES = [(14336, 4096), (4096, 14336), (14336, 4096), (4096, 14336)]
+
+
+def zero3_units(z, synth, dev, n, m, shapes=ZERO3_SHAPES):
+    """A stack of FSDP units with the Mistral-7B MLP shapes (alternating 14336 x 4096 and
+    4096 x 14336, each in n row shards), ZeRO-3 state, n ranks of m tokens."""
+    import torch
+    units = []
+    nm = n * m
+    for i, (R, K) in enumerate(shapes):
+        w = torch.cat(synth.weight_shards(R, K, n, device=dev, seed_key=20 + i), 0).contiguous()
+        units.append({"plan": z.zero_plan(R * K, n, "zero3", 50 * MIB), "w": w, "master": w.float().reshape(-1),
+                      "m": torch.zeros(R * K, device=dev), "v": torch.zeros(R * K, device=dev),
+                      "x": torch.empty(nm, K, dtype=torch.bfloat16, device=dev),
+                      "dy": torch.empty(nm, R, dtype=torch.bfloat16, device=dev),
+                      "dw": torch.empty(R, K, device=dev)})
+    units[0]["x"].copy_(synth.activations(nm, shapes[0][1], device=dev))
+    units[-1]["dy"].copy_(synth.upstream_grad(nm, shapes[-1][0], device=dev))
+    return units
+
+
+def zero3_leg(z, synth, dev, tf_peak, hbm_peak, stream):
+    """One ZeRO-3 training step over 4 FSDP units with the Mistral-7B MLP shapes, N = 8
+    ranks of 1024 tokens (8192 in all): forward, backward in reverse with each rank's Adam
+    on its shard after the unit's backward. Timed serial and with the next unit's gather /
+    X^T layout prefetched on a second stream, with the gather fused into the GEMM loads and
+    materialised into a workspace slot."""
+    import torch
+    n, m = 8, 1024
+    res = {"units": [list(s) for s in ZERO3_SHAPES], "n_ranks": n, "tokens_per_rank": m}
+    try:
+        units = zero3_units(z, synth, dev, n, m)
+        nm = n * m
+        y = torch.empty(nm, ZERO3_SHAPES[-1][0], dtype=torch.bfloat16, device=dev)
+        dx = torch.empty(nm, ZERO3_SHAPES[0][1], dtype=torch.bfloat16, device=dev)
+        side = torch.cuda.Stream()
+        flop = sum(6.0 * nm * R * K for R, K in ZERO3_SHAPES)
+        adam_bytes = sum(30 * R * K for R, K in ZERO3_SHAPES)
+        res["gemm_flop_per_step"] = flop
+        res["adam_bytes_per_step"] = adam_bytes
+        for name, flags, pf in (("serial", 0, None), ("prefetch", z.FSDP_BACKWARD_PREFETCH, side),
+                                ("materialized_serial", z.FSDP_GATHER_MATERIALIZE, None),
+                                ("materialized_prefetch", z.FSDP_GATHER_MATERIALIZE | z.FSDP_BACKWARD_PREFETCH, side)):
+            ws = torch.empty(z.fsdp_zero3_step_workspace(n, ZERO3_SHAPES, m, flags), dtype=torch.uint8, device=dev)
+            t = [0]
+
+            def step():
+                t[0] += 1
+                z.fsdp_zero3_step(units, m, HP, t[0], y_out=y, dx_out=dx, flags=flags, workspace=ws, stream=stream,
+                                  prefetch_stream=pf)
+
+            ms = time_launches(step, 10, stream)
+            res[name] = {"ms": ms, "tflops": flop / ms / 1e9, "frac_of_bf16_peak": flop / ms / 1e9 / tf_peak,
+                         "workspace_bytes": ws.numel()}
+            del ws
+        z.zero_device_status(stream)
+        res["prefetch_gain"] = res["serial"]["ms"] / res["prefetch"]["ms"] - 1.0
+        res["materialized_prefetch_gain"] = (res["materialized_serial"]["ms"] / res["materialized_prefetch"]["ms"]
+                                             - 1.0)
+        res["note"] = ("tflops counts the 12 GEMMs' flops (6 N M R K per unit) over the whole step, which also holds "
+                       "4 Adam launches (30 B per parameter) and 4 X^T layouts")
+    except Exception as e:  # the leg must not hide the step's line
+        res["error"] = str(e)[:300]
+    return res
 
 
 def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
@@ -1020,6 +1092,21 @@ def run_case(args):
         byts = 4 * R * K
         out.update(R=R, K=K, n_ranks=n, gather_ms=ms_g, transpose_ms=ms_t, bytes=byts,
                    gather_gbs=byts / ms_g / 1e6, transpose_gbs=byts / ms_t / 1e6)
+    elif args.case == "zero3_step":
+        # one ZeRO-3 step over the 4 Mistral-shaped units, N = 8 ranks x 1024 tokens, with the
+        # prefetch stream (about 7 GB on the device), 3 steps
+        n, m = 8, 1024
+        units = zero3_units(z, synth, dev, n, m)
+        flags = z.FSDP_BACKWARD_PREFETCH
+        ws = torch.empty(z.fsdp_zero3_step_workspace(n, ZERO3_SHAPES, m, flags), dtype=torch.uint8, device=dev)
+        y = torch.empty(n * m, ZERO3_SHAPES[-1][0], dtype=torch.bfloat16, device=dev)
+        dx = torch.empty(n * m, ZERO3_SHAPES[0][1], dtype=torch.bfloat16, device=dev)
+        side = torch.cuda.Stream()
+        hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+        ms = time_launches(lambda: z.fsdp_zero3_step(units, m, hp, 1, y_out=y, dx_out=dx, flags=flags, workspace=ws,
+                                                     stream=stream, prefetch_stream=side), 2, stream)
+        flop = sum(6.0 * n * m * R * K for R, K in ZERO3_SHAPES)
+        out.update(n_ranks=n, tokens_per_rank=m, ms=ms, tflops=flop / ms / 1e9)
     elif args.case == "backward_up":
         # FSDP unit backward of W_up [14336, 4096] in 8 row shards, 2048 tokens per rank
         # (dY 470 MB, X 134 MB, dX 268 MB, dW 235 MB, X^T workspace 134 MB): 3 launches
@@ -1044,7 +1131,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="one measured case: fused_small | fused_tma_small | megatron_small | e2e_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
-                         "backward_up | rank_view_small (ncu-sized) | "
+                         "backward_up | rank_view_small | zero3_step (ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)

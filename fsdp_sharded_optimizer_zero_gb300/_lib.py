@@ -34,7 +34,7 @@ EXPORTS = (
     "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_host", "zero_fused_step_fp32_grads",
     "zero_fused_step_buckets", "zero_allgather_params", "ddp_allreduce",
     "fsdp_gather_rows", "fsdp_unit_forward", "fsdp_transpose_cat", "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward",
-    "fsdp_unit_forward_static_scratch",
+    "fsdp_zero3_step_workspace", "fsdp_zero3_step", "fsdp_unit_forward_static_scratch",
     "zero_last_error", "zero_device_status", "zero_selftest_bounded_wait", "zero_set_fused_kernel", "zero_set_gemm_kernel", "zero_version",
 )
 
@@ -57,6 +57,16 @@ class zero_layout(C.Structure):
         ("comm_all_gather_bwd", C.c_uint64), ("comm_total", C.c_uint64),
         ("ring_sent_elems", C.c_uint64), ("fused_step_bytes", C.c_uint64),
     ]
+
+
+class fsdp_unit_state(C.Structure):
+    _fields_ = [("rows_out", C.c_int64), ("k_in", C.c_int64), ("plan", C.c_void_p), ("w", C.c_void_p),
+                ("master", C.c_void_p), ("m", C.c_void_p), ("v", C.c_void_p), ("x", C.c_void_p), ("dy", C.c_void_p),
+                ("dw", C.c_void_p)]
+
+
+FSDP_GATHER_MATERIALIZE = 1
+FSDP_BACKWARD_PREFETCH = 2
 
 
 class zero_adam(C.Structure):
@@ -97,6 +107,9 @@ def _load():
         "zero_device_status": (I, [VP]),
         "zero_selftest_bounded_wait": (I, [C.c_uint32, VP]),
         "zero_set_fused_kernel": (I, [I]),
+        "fsdp_zero3_step_workspace": (I, [I, I, C.POINTER(fsdp_unit_state), I64, I, C.POINTER(U64)]),
+        "fsdp_zero3_step": (I, [I, I, C.POINTER(fsdp_unit_state), I64, VP, VP, C.POINTER(zero_adam), I64, I, VP, U64,
+                                VP, VP]),
         "zero_set_gemm_kernel": (I, [I]),
         "zero_version": (I, []),
     }
@@ -395,6 +408,60 @@ def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace, stream=None):
         _ptr_array(dY, torch.bfloat16, "dY"), m_tok, _ptr_array(dX, torch.float32, "dX"),
         _dev(dW, torch.float32, "dW"), _dev(workspace, torch.uint8, "workspace"),
         0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def _unit_array(units, shapes_only=False):
+    arr = (fsdp_unit_state * len(units))()
+    for i, u in enumerate(units):
+        rows, k = (int(u["w"].shape[0]), int(u["w"].shape[1])) if "w" in u else (int(u["rows_out"]), int(u["k_in"]))
+        arr[i].rows_out, arr[i].k_in = rows, k
+        if shapes_only:
+            continue
+        plan = u["plan"]
+        arr[i].plan = plan.handle
+        arr[i].w = _dev(u["w"], torch.bfloat16, f"units[{i}].w")
+        for name in ("master", "m", "v"):
+            _need(u[name], rows * k, f"units[{i}].{name}")
+            setattr(arr[i], name, _dev(u[name], torch.float32, f"units[{i}].{name}"))
+        nm = int(u["x"].shape[0]) if u["x"].dim() == 2 else -1
+        if u["x"].dim() != 2 or int(u["x"].shape[1]) != k:
+            raise ValueError(f"units[{i}].x must be [N*M, {k}] (got {tuple(u['x'].shape)})")
+        if u["dy"].dim() != 2 or tuple(u["dy"].shape) != (nm, rows):
+            raise ValueError(f"units[{i}].dy must be [{nm}, {rows}] (got {tuple(u['dy'].shape)})")
+        _need(u["dw"], rows * k, f"units[{i}].dw")
+        arr[i].x = _dev(u["x"], torch.bfloat16, f"units[{i}].x")
+        arr[i].dy = _dev(u["dy"], torch.bfloat16, f"units[{i}].dy")
+        arr[i].dw = _dev(u["dw"], torch.float32, f"units[{i}].dw")
+    return arr
+
+
+def fsdp_zero3_step_workspace(n_ranks: int, shapes, m_tokens: int, flags: int = 0) -> int:
+    """Workspace bytes of fsdp_zero3_step for units of the given (rows_out, k_in) shapes."""
+    arr = _unit_array([{"rows_out": r, "k_in": k} for r, k in shapes], shapes_only=True)
+    b = C.c_uint64()
+    _check(_lib.fsdp_zero3_step_workspace(n_ranks, len(arr), arr, m_tokens, flags, C.byref(b)))
+    return b.value
+
+
+def fsdp_zero3_step(units, m_tokens: int, hp, step: int, y_out=None, dx_out=None, flags: int = 0, workspace=None,
+                    stream=None, prefetch_stream=None):
+    """units: one dict per FSDP unit with plan, w [R, K] bf16 (the N row shards back to
+    back), master / m / v fp32 [R*K], x [N*M, K] bf16, dy [N*M, R] bf16, dw [R, K] fp32."""
+    if not units:
+        raise ValueError("units is empty")
+    n = units[0]["plan"].n_ranks
+    arr = _unit_array(units)
+    nm = n * m_tokens
+    if int(units[0]["x"].shape[0]) != nm:
+        raise ValueError(f"units[0].x must have N*M = {nm} rows")
+    _need(y_out, nm * int(units[-1]["w"].shape[0]), "y_out")
+    _need(dx_out, nm * int(units[0]["w"].shape[1]), "dx_out")
+    a = _adam(hp)
+    _check(_lib.fsdp_zero3_step(
+        n, len(arr), arr, m_tokens, _dev(y_out, torch.bfloat16, "y_out"), _dev(dx_out, torch.bfloat16, "dx_out"),
+        C.byref(a), step, flags, _dev(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _stream(stream),
+        None if prefetch_stream is None else _stream(prefetch_stream)))
 
 
 def fsdp_mlp_forward(gate_shards, up_shards, down_shards, X, H, Y, scratch_down=None, stream=None,

@@ -17,7 +17,8 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libzero_gb300.so"
-SOURCES = ["capi.cu", "fused_step.cu", "step_kernels.cu", "fsdp_gemm.cu", "fsdp_unit.cu", "fsdp_static_scratch.cu"]
+SOURCES = ["capi.cu", "fused_step.cu", "step_kernels.cu", "fsdp_gemm.cu", "fsdp_unit.cu", "fsdp_zero3.cu",
+           "fsdp_static_scratch.cu"]
 HEADERS = ["internal.h", "device_common.cuh", "step_common.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = [

@@ -233,6 +233,16 @@ int make_scalars(const zero_adam* hp, int64_t step, int n, const char* who, Adam
   return ZERO_OK;
 }
 
+}  // namespace
+
+// hp and step checked as every Adam call checks them (nothing launched)
+int zgb::check_adam_args(const zero_adam* hp, int64_t step, const char* who) {
+  AdamScalars sc;
+  return make_scalars(hp, step, 1, who, &sc);
+}
+
+namespace {
+
 int load_grads(const zero_bf16* const grads[], int n, uint64_t off, const char* who, GradPtrs* gp) {
   CHECK_ARG(grads != nullptr, "%s: grads array is NULL", who);
   memset(gp, 0, sizeof(*gp));

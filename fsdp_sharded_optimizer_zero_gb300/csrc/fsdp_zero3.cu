@@ -1,0 +1,244 @@
+// One ZeRO-3 / FSDP training step over a stack of FSDP units, for all N simulated ranks.
+//
+// A unit's life on a card ([Interview] Fig. 2; [Concepts] "ZeRO and FSDP", full-shard
+// steps 1-3): only its 1/N row shard is kept between uses; the full W exists only while
+// the unit computes (gathered before the forward, freed, gathered again before the
+// backward); after the backward the weight gradient is reduce-scattered so each rank keeps
+// the rows of its own shard, and each rank's Adam updates that shard alone.
+//
+// Here every "gather" reads the N shards where they lie: either inside the GEMM's operand
+// loads (the default: no copy of W exists at all), or, with FSDP_GATHER_MATERIALIZE, by a
+// gather kernel into a workspace slot that plays the all-gather's receive buffer. The
+// reduce of the reduce-scatter happens inside the dW GEMM's fp32 accumulation (its K loop
+// runs over every rank's tokens), so rank r's reduce-scattered gradient is simply rows
+// [r R/N, (r+1) R/N) of dW, contiguous with its flat-parameter shard.
+//
+// Overlap ([Interview] follow-up "FSDP 怎么把通信藏起来?": the all-gather on its own CUDA
+// stream, the backward prefetching the next unit's): with FSDP_BACKWARD_PREFETCH and a
+// prefetch stream, unit i-1's gather and its X^T layout (the dW GEMM's operand) are issued
+// on the prefetch stream as soon as unit i's backward starts, into the other of two slots;
+// events order each slot's reuse and each unit's start. Forward prefetch stays off (the
+// pages' default).
+//
+// Ordering inside a unit's backward: dX (reads W_i) and dW, then Adam writes the new W_i
+// shards. Unit i's W is not read again in this step (unit i-1's backward reads W_{i-1} and
+// the dY that unit i produced from the old W_i), so the update can follow each unit.
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "internal.h"
+
+using namespace zgb;
+
+namespace {
+
+const char* const kWho = "fsdp_zero3_step";
+
+uint64_t align256(uint64_t b) { return (b + 255) & ~uint64_t(255); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+struct Zero3Workspace {
+  int slots;                // 2 with backward prefetch, else 1
+  uint64_t xt_off[2];       // X^T [k_in, N M] bf16 of the unit in the slot
+  uint64_t w_off[2];        // gathered W [rows_out, k_in] bf16 (FSDP_GATHER_MATERIALIZE)
+  uint64_t total;
+};
+
+Zero3Workspace zero3_workspace(int n, int n_units, const fsdp_unit_state* u, int64_t m, int flags) {
+  Zero3Workspace w;
+  memset(&w, 0, sizeof(w));
+  uint64_t kmax = 0, wmax = 0;
+  for (int i = 0; i < n_units; ++i) {
+    kmax = std::max<uint64_t>(kmax, static_cast<uint64_t>(u[i].k_in));
+    wmax = std::max<uint64_t>(wmax, static_cast<uint64_t>(u[i].rows_out) * static_cast<uint64_t>(u[i].k_in));
+  }
+  w.slots = (flags & FSDP_BACKWARD_PREFETCH) ? 2 : 1;
+  const uint64_t xt = align256(2 * kmax * static_cast<uint64_t>(n) * static_cast<uint64_t>(m));
+  const uint64_t ww = (flags & FSDP_GATHER_MATERIALIZE) ? align256(2 * wmax) : 0;
+  uint64_t off = 0;
+  for (int s = 0; s < w.slots; ++s) {
+    w.xt_off[s] = off;
+    off += xt;
+    w.w_off[s] = off;
+    off += ww;
+  }
+  w.total = off;
+  return w;
+}
+
+// per-thread, per-device events ordering the prefetch stream (no timing)
+thread_local std::vector<cudaEvent_t> t_events[64];
+
+int get_events(size_t count, cudaEvent_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return set_error(ZERO_ERR_CUDA, "%s: cudaGetDevice failed", kWho);
+  std::vector<cudaEvent_t>& v = t_events[dev];
+  while (v.size() < count) {
+    cudaEvent_t ev = nullptr;
+    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: cudaEventCreate: %s", kWho, cudaGetErrorString(e));
+    v.push_back(ev);
+  }
+  *out = v.data();
+  return ZERO_OK;
+}
+
+int check_units(int n, int n_units, const fsdp_unit_state* u, int64_t m, int flags, bool buffers) {
+  if (n < 1 || n > kGemmMaxPieces)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: n_ranks %d outside 1..%d", kWho, n, kGemmMaxPieces);
+  if (n_units < 1 || n_units > 64) return set_error(ZERO_ERR_INVALID_ARG, "%s: n_units %d outside 1..64", kWho, n_units);
+  if (!u) return set_error(ZERO_ERR_INVALID_ARG, "%s: units is NULL", kWho);
+  if (m < 1 || (static_cast<int64_t>(n) * m) % 8)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: n_ranks * m_tokens must be a positive multiple of 8", kWho);
+  if (flags & ~(FSDP_GATHER_MATERIALIZE | FSDP_BACKWARD_PREFETCH))
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: unknown flags 0x%x", kWho, flags);
+  for (int i = 0; i < n_units; ++i) {
+    const fsdp_unit_state& s = u[i];
+    if (s.rows_out < 1 || s.k_in < 1 || s.rows_out > (1 << 30) || s.k_in > (1 << 30))
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: sizes outside 1..2^30", kWho, i);
+    if (s.rows_out % n || (s.rows_out / n) % 64 || s.k_in % 64)
+      return set_error(ZERO_ERR_INVALID_ARG,
+                       "%s: unit %d: needs rows_out / n_ranks and k_in multiples of 64 (got %lld / %d, %lld)", kWho, i,
+                       (long long)s.rows_out, n, (long long)s.k_in);
+    if (!(flags & FSDP_GATHER_MATERIALIZE) && !fsdp_fused_gather_ok(n, s.rows_out))
+      return set_error(ZERO_ERR_INVALID_ARG,
+                       "%s: unit %d: shards of %lld rows do not tile the GEMM for the fused gather; pass "
+                       "FSDP_GATHER_MATERIALIZE",
+                       kWho, i, (long long)(s.rows_out / n));
+    if (i + 1 < n_units && u[i + 1].k_in != s.rows_out)
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d's k_in %lld is not unit %d's rows_out %lld", kWho, i + 1,
+                       (long long)u[i + 1].k_in, i, (long long)s.rows_out);
+    if (!buffers) continue;
+    if (!s.plan) return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: plan is NULL", kWho, i);
+    zero_layout L;
+    zero_plan_query(s.plan, &L);
+    if (L.psi != static_cast<uint64_t>(s.rows_out) * static_cast<uint64_t>(s.k_in) || L.n_ranks != n ||
+        L.stage != ZERO_STAGE_3)
+      return set_error(ZERO_ERR_INVALID_ARG,
+                       "%s: unit %d: the plan must be zero_plan(rows_out * k_in, n_ranks, ZERO_STAGE_3, ...)", kWho, i);
+    if (!s.w || !s.master || !s.m || !s.v || !s.x || !s.dy || !s.dw)
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: a buffer is NULL", kWho, i);
+    if (!aligned16(s.w) || !aligned16(s.master) || !aligned16(s.m) || !aligned16(s.v) || !aligned16(s.x) ||
+        !aligned16(s.dy) || !aligned16(s.dw))
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: buffers must be 16-byte aligned", kWho, i);
+  }
+  return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit_state* units, int64_t m_tokens,
+                                         int flags, uint64_t* bytes) {
+  if (!bytes) return set_error(ZERO_ERR_INVALID_ARG, "fsdp_zero3_step_workspace: bytes is NULL");
+  int rc = check_units(n_ranks, n_units, units, m_tokens, flags, false);
+  if (rc) return rc;
+  *bytes = zero3_workspace(n_ranks, n_units, units, m_tokens, flags).total;
+  return ZERO_OK;
+}
+
+extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* units, int64_t m_tokens,
+                               zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step, int flags,
+                               void* workspace, uint64_t workspace_bytes, zero_stream_t stream,
+                               zero_stream_t prefetch_stream) {
+  const int n = n_ranks, L = n_units;
+  int rc = check_units(n, L, units, m_tokens, flags, true);
+  if (rc) return rc;
+  if ((rc = check_adam_args(hp, step, kWho))) return rc;
+  if ((y_out && !aligned16(y_out)) || (dx_out && !aligned16(dx_out)))
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: y_out and dx_out must be 16-byte aligned", kWho);
+  const Zero3Workspace ws = zero3_workspace(n, L, units, m_tokens, flags);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < ws.total)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: workspace of %llu bytes (16-byte aligned) is below the %llu needed",
+                     kWho, workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.total);
+  const bool materialize = (flags & FSDP_GATHER_MATERIALIZE) != 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t pf = ((flags & FSDP_BACKWARD_PREFETCH) && prefetch_stream)
+                        ? reinterpret_cast<cudaStream_t>(prefetch_stream)
+                        : st;
+  const bool overlap = pf != st;
+  const int64_t nm = static_cast<int64_t>(n) * m_tokens;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  auto xt_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.xt_off[i % ws.slots]); };
+  auto w_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.w_off[i % ws.slots]); };
+  // events: [0] forward done, [1 + i] unit i's operands ready, [1 + L + i] unit i's backward done
+  cudaEvent_t* ev = nullptr;
+  if (overlap && (rc = get_events(static_cast<size_t>(2 * L + 1), &ev))) return rc;
+  const auto ev_ready = [&](int i) { return ev[1 + i]; };
+  const auto ev_done = [&](int i) { return ev[1 + L + i]; };
+
+  // the N row shards of unit i (rank r's rows at r R/N), or its gathered copy
+  const uint16_t* shard_ptrs[kGemmMaxPieces];
+  auto shards_of = [&](int i) {
+    const fsdp_unit_state& s = units[i];
+    const int64_t per = (s.rows_out / n) * s.k_in;
+    for (int r = 0; r < n; ++r) shard_ptrs[r] = s.w + r * per;
+    return static_cast<const uint16_t* const*>(shard_ptrs);
+  };
+  auto gather = [&](int i, cudaStream_t s) {
+    return fsdp_gather_rows(n, shards_of(i), units[i].rows_out, units[i].k_in, w_slot(i),
+                            reinterpret_cast<zero_stream_t>(s));
+  };
+  auto wait = [&](cudaStream_t s, cudaEvent_t e) {
+    const cudaError_t err = cudaStreamWaitEvent(s, e, 0);
+    return err == cudaSuccess ? ZERO_OK : set_error(ZERO_ERR_CUDA, "%s: %s", kWho, cudaGetErrorString(err));
+  };
+  auto record = [&](cudaEvent_t e, cudaStream_t s) {
+    const cudaError_t err = cudaEventRecord(e, s);
+    return err == cudaSuccess ? ZERO_OK : set_error(ZERO_ERR_CUDA, "%s: %s", kWho, cudaGetErrorString(err));
+  };
+
+  // ---- forward, unit 0 -> last: gather, X_{i+1} = bf16(X_i W_i^T), free ----
+  for (int i = 0; i < L; ++i) {
+    const fsdp_unit_state& s = units[i];
+    zero_bf16* out = i + 1 < L ? units[i + 1].x : y_out;
+    if (!out) continue;
+    if (materialize) {
+      if ((rc = gather(i, st))) return rc;
+      const uint16_t* w1[1] = {w_slot(i)};
+      rc = launch_fsdp_gemm(1, w1, s.rows_out, s.k_in, s.x, nm, nullptr, out, 1.0f, st);
+    } else {
+      rc = launch_fsdp_gemm(n, shards_of(i), s.rows_out, s.k_in, s.x, nm, nullptr, out, 1.0f, st);
+    }
+    if (rc) return rc;
+  }
+
+  // ---- backward, last -> unit 0 ----
+  // unit i's operands: its gathered W (materialised mode) and X_i^T [k_in, N M]
+  auto prepare = [&](int i, cudaStream_t s) {
+    int r = ZERO_OK;
+    if (overlap && i + ws.slots < L && (r = wait(s, ev_done(i + ws.slots)))) return r;  // slot reuse
+    if (materialize && (r = gather(i, s))) return r;
+    const zero_bf16* x1[1] = {units[i].x};
+    if ((r = fsdp_transpose_cat(1, x1, nm, units[i].k_in, xt_slot(i), reinterpret_cast<zero_stream_t>(s)))) return r;
+    return overlap ? record(ev_ready(i), s) : ZERO_OK;
+  };
+  if (overlap) {
+    // the prefetch stream starts once the forward (which writes every unit's input) is done
+    if ((rc = record(ev[0], st)) || (rc = wait(pf, ev[0])) || (rc = prepare(L - 1, pf))) return rc;
+  }
+  for (int i = L - 1; i >= 0; --i) {
+    const fsdp_unit_state& s = units[i];
+    if (overlap) {
+      if ((rc = wait(st, ev_ready(i)))) return rc;
+      if (i > 0 && (rc = prepare(i - 1, pf))) return rc;  // overlaps this unit's GEMMs
+    } else if ((rc = prepare(i, st))) {
+      return rc;
+    }
+    const uint16_t* w1[1] = {w_slot(i)};
+    const uint16_t* const* wp = materialize ? w1 : shards_of(i);
+    const int pieces = materialize ? 1 : n;
+    zero_bf16* dx = i > 0 ? units[i - 1].dy : dx_out;
+    if (dx && (rc = launch_fsdp_bwd_dx_bf16(pieces, wp, s.rows_out, s.k_in, s.dy, nm, dx, st))) return rc;
+    if ((rc = launch_fsdp_bwd_dw_alpha(s.dy, nm, xt_slot(i), s.rows_out, s.k_in, s.dw,
+                                       1.0f / static_cast<float>(n), st)))
+      return rc;
+    // each rank's Adam on its shard (rows r R/N .. of dW): every rank's shard in one launch
+    if ((rc = zero_adam_step(s.plan, ZERO_ALL_RANKS, s.dw, s.master, s.m, s.v, s.w, hp, step, stream))) return rc;
+    if (overlap && (rc = record(ev_done(i), st))) return rc;
+  }
+  // every prefetch-stream launch was awaited by `stream` (unit 0's operands were the last)
+  return ZERO_OK;
+}

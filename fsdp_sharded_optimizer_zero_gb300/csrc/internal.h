@@ -87,6 +87,14 @@ int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces
                        cudaStream_t st);
 int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* Xt, int64_t m_tokens,
                        int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st);
+// The same two products over one contiguous operand for all ranks (rank q's rows at q M):
+// dX [NM, K] = dY [NM, R] W written as bf16 only (W read in place from w_pieces MN-major
+// pieces along K, or as one gathered W); dW [R, K] = alpha dY^T [R, NM] (X^T [K, NM])^T
+// with dY read in place as one MN-major piece. Bit-identical to the per-rank forms above.
+int launch_fsdp_bwd_dx_bf16(int w_pieces, const uint16_t* const* w, int64_t rows_out, int64_t k_in,
+                            const uint16_t* dY, int64_t nm, uint16_t* dX_bf16, cudaStream_t st);
+int launch_fsdp_bwd_dw_alpha(const uint16_t* dY, int64_t nm, const uint16_t* Xt, int64_t rows_out, int64_t k_in,
+                             float* dW, float alpha, cudaStream_t st);
 unsigned int fsdp_gemm_read_clear_error();
 int set_gemm_kernel(int which);  // 0 = default, 1 = one-CTA kernel everywhere, 2 = CTA-pair kernel everywhere
 
@@ -118,6 +126,8 @@ bool fsdp_fused_gather_ok(int n_ranks, int64_t rows_out);
 
 // ---- errors (capi.cu) ----
 int set_error(int code, const char* fmt, ...);
+// Adam hyper-parameters and step validated as the step calls do (ZERO_ERR_INVALID_ARG)
+int check_adam_args(const zero_adam* hp, int64_t step, const char* who);
 int num_sms();
 
 }  // namespace zgb

@@ -331,6 +331,70 @@ ZERO_API int fsdp_mlp_forward(int n_ranks, const zero_bf16* const gate_shards[],
                               int64_t m_tokens, zero_bf16* H, float* Y, zero_bf16* scratch_down, zero_stream_t stream,
                               zero_stream_t prefetch_stream);
 
+/* ------------------------------------------------------------------------------------ */
+/* ZeRO-3 / FSDP training step over a stack of units ([Interview] Fig. 2 and the follow-up */
+/* "FSDP 怎么把通信藏起来?"; [Concepts] "ZeRO and FSDP", full-shard steps 1-3)             */
+/* ------------------------------------------------------------------------------------ */
+
+/* One FSDP unit: a linear layer Y = X W^T whose weight W [rows_out, k_in] is held as N
+ * dim-0 row shards, its ZeRO-3 state, and the activations of every simulated rank. With
+ * M tokens per rank, rank q's rows of the [N*M, .] buffers are [q*M, (q+1)*M). */
+typedef struct {
+  int64_t rows_out, k_in;  /* W [rows_out, k_in]; rows_out % N == 0; unit i+1's k_in == unit i's rows_out */
+  const zero_plan_t* plan; /* zero_plan(rows_out * k_in, N, ZERO_STAGE_3, any bucket): rank r's shard = rows
+                              [r*R/N, (r+1)*R/N) of W, flat elements [r*S, (r+1)*S) */
+  zero_bf16* w;            /* [rows_out, k_in] bf16, the N shards back to back; the step writes the new shards */
+  float *master, *m, *v;   /* [rows_out * k_in] fp32 each, rank r's shard at r*S; updated in place */
+  zero_bf16* x;            /* [N*M, k_in] bf16: the unit's input. Unit 0: the caller's batch (read); unit i > 0:
+                              written by the forward (unit i-1's output) and kept for the backward */
+  zero_bf16* dy;           /* [N*M, rows_out] bf16: the gradient of the unit's output. Last unit: the caller's
+                              loss gradient (read); unit i < last: written by unit i+1's backward (its dX) */
+  float* dw;               /* out, [rows_out, k_in] fp32: dW = (1/N) sum_q dY_q^T X_q; rank r's reduce-scattered
+                              gradient = rows [r*R/N, (r+1)*R/N), which its Adam consumes */
+} fsdp_unit_state;
+
+/* flags of fsdp_zero3_step */
+#define FSDP_GATHER_MATERIALIZE 1 /* gather each unit's W into a workspace slot (the all-gather's receive
+                                     buffer: sharded model + the unit in use), reused after the unit; without
+                                     it the GEMMs read every tile straight from its shard */
+#define FSDP_BACKWARD_PREFETCH 2  /* issue unit i-1's gather and X^T layout on prefetch_stream while unit i's
+                                     backward GEMMs run on `stream` */
+
+/* Bytes of device workspace fsdp_zero3_step needs for these units, M tokens per rank and
+ * flags: X^T [k_in, N*M] bf16 of the largest unit (two slots with FSDP_BACKWARD_PREFETCH),
+ * plus the gathered W [rows_out, k_in] bf16 of the largest unit (two slots with prefetch)
+ * under FSDP_GATHER_MATERIALIZE; each slot rounded up to 256 bytes. Only the units' sizes
+ * are read. */
+ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit_state* units, int64_t m_tokens,
+                                       int flags, uint64_t* bytes);
+
+/* One training step of a stack of n_units FSDP units under ZeRO-3, for all N simulated
+ * ranks (M = m_tokens each), following a unit's life on a card ([Interview] Fig. 2):
+ *   forward, unit 0 -> last: gather W_i (fused into the GEMM's loads, or into a workspace
+ *     slot), X_{i+1} = bf16(X_i W_i^T) for every rank (the last unit's output goes to y_out;
+ *     with y_out NULL that product is skipped), W_i freed;
+ *   backward, last -> unit 0: gather W_i again, dY_{i-1} = bf16(dY_i W_i) (unit 0: into
+ *     dx_out, skipped when NULL), dW_i = (1/N) sum_q dY_{i,q}^T X_{i,q} (the reduce of the
+ *     reduce-scatter inside the fp32 tensor-core accumulation, rank r keeping its rows),
+ *     then each rank's Adam on its shard (zero_adam_step, ZERO_ALL_RANKS: every rank's
+ *     shard in one launch) writing the new bf16 shards of W_i — after W_i's last use;
+ *   with FSDP_BACKWARD_PREFETCH, unit i-1's gather and X^T layout run on prefetch_stream
+ *     while unit i computes ([Interview] follow-up "FSDP 怎么把通信藏起来?": the all-gather
+ *     on its own stream, the backward prefetching the next unit's).
+ * All work is ordered on `stream` by the time the call returns (prefetch_stream joins it).
+ * Results do not depend on the flags (same bits). dX / dY products are fp32 sums of exact
+ * bf16 products in an unspecified order (bounds as fsdp_unit_backward), rounded once to
+ * bf16; Adam is bit-exact as zero_adam_step.
+ * Requires 1 <= N <= 16, 1 <= n_units <= 64, N*M % 8 == 0; per unit k_in % 64 == 0,
+ * (rows_out / N) % 64 == 0, and without FSDP_GATHER_MATERIALIZE the fused gather's shard
+ * rule ((rows_out / N) % 128 == 0; 256 under zero_set_gemm_kernel(1)); 16-byte-aligned
+ * buffers; workspace of fsdp_zero3_step_workspace() bytes. prefetch_stream may be NULL
+ * (then everything runs on `stream`). */
+ZERO_API int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* units, int64_t m_tokens,
+                             zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step, int flags,
+                             void* workspace, uint64_t workspace_bytes, zero_stream_t stream,
+                             zero_stream_t prefetch_stream);
+
 /* Allocation-free variant of fsdp_unit_forward, for callers that cannot allocate device
  * memory where they run the unit (e.g. a plug-in inside a framework that owns all device
  * memory through its own pool, or a latency-critical path that cannot take cudaMalloc's

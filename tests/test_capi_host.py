@@ -221,3 +221,59 @@ def test_memory_check_rejects_bad_rank(z):
     with pytest.raises(z.ZeroError) as e:
         z.zero_plan_check_memory(plan, 4, 1 << 30)
     assert e.value.code == -1
+
+
+def test_zero3_step_rejects_bad_arguments_before_launch(z):
+    """fsdp_zero3_step validates every unit, the chain, the plans, the flags, the Adam
+    arguments and the workspace before anything is launched (fake device addresses)."""
+    lib = z.library()
+    S = z._lib.fsdp_unit_state
+    adam = z._lib.zero_adam(1e-4, 0.9, 0.999, 1e-8, 0.0)
+    n, m = 4, 64
+
+    def units(shapes, plans=None, fill=0x10000):
+        arr = (S * len(shapes))()
+        for i, (r, k) in enumerate(shapes):
+            arr[i].rows_out, arr[i].k_in = r, k
+            arr[i].plan = plans[i].handle if plans else None
+            for j, name in enumerate(("w", "master", "m", "v", "x", "dy", "dw")):
+                setattr(arr[i], name, fill + 0x1000 * (8 * i + j))
+        return arr
+
+    good = [(512, 256), (1024, 512)]
+    plans = [z.zero_plan(r * k, n, "zero3", 1 << 20) for r, k in good]
+    ws = C.c_uint64()
+    assert lib.fsdp_zero3_step_workspace(n, 2, units(good), m, 0, C.byref(ws)) == 0
+    assert ws.value == 2 * 512 * n * m
+    assert lib.fsdp_zero3_step_workspace(n, 2, units(good), m, 3, C.byref(ws)) == 0
+    assert ws.value == 2 * (2 * 512 * n * m + 2 * 1024 * 512)
+
+    def call(arr, nu=2, flags=0, wsb=1 << 30, step=1, hp=adam, mm=m, nr=n):
+        return lib.fsdp_zero3_step(nr, nu, arr, mm, None, None, C.byref(hp), step, flags, 0x100000, wsb, None, None)
+
+    # chain: unit 1's k_in must be unit 0's rows_out
+    assert call(units([(512, 256), (1024, 256)], plans)) == -1
+    assert b"is not unit 0's rows_out" in lib.zero_last_error()
+    # shard rows a multiple of 64, k_in a multiple of 64
+    assert call(units([(512, 200), (1024, 512)], plans)) == -1
+    assert call(units([(4 * 96, 256)], plans[:1]), nu=1) == -1
+    # shards of 64 rows do not tile the fused gather: FSDP_GATHER_MATERIALIZE needed
+    p64 = [z.zero_plan(256 * 256, n, "zero3", 1 << 20)]  # kept alive: destroying a plan clears the message
+    assert call(units([(256, 256)], p64), nu=1) == -1
+    assert b"FSDP_GATHER_MATERIALIZE" in lib.zero_last_error()
+    # plan must describe the unit: psi = R K, N ranks, ZeRO-3
+    assert call(units(good, [plans[1], plans[0]])) == -1
+    assert b"plan" in lib.zero_last_error()
+    p2 = [z.zero_plan(512 * 256, n, "zero2", 1 << 20), plans[1]]
+    assert call(units(good, p2)) == -1
+    assert call(units(good)) == -1                               # no plans
+    assert call(units(good, plans, fill=0x10008)) == -1          # misaligned buffers
+    assert call(units(good, plans), flags=8) == -1               # unknown flag
+    assert call(units(good, plans), step=0) == -1                # Adam step counts from 1
+    bad = z._lib.zero_adam(1e-4, 1.0, 0.999, 1e-8, 0.0)
+    assert call(units(good, plans), hp=bad) == -1                # beta1 outside [0, 1)
+    assert call(units(good, plans), wsb=100) == -1               # workspace too small
+    assert b"workspace" in lib.zero_last_error()
+    assert call(units(good, plans), nr=17) == -1                 # at most 16 ranks
+    assert call(units(good, plans), mm=3) == -1                  # N M a multiple of 8
+    assert call(units(good, plans), nu=0) == -1
