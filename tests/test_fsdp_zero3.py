@@ -194,29 +194,30 @@ def test_zero3_step_units_equal_standalone_calls(z):
     """One unit's part of the step equals the standalone calls: the forward output equals
     fsdp_unit_forward's bf16 output, dX equals RNE of fsdp_unit_backward's fp32 dX, dW is
     identical, and the update equals zero_adam_step on that dW."""
-    n, R, K, m = 4, 1024, 256, 128
-    units = make_units(z, n, [(R, K), (K, R)], m, key=3)
-    before = [clone_units([u])[0] for u in units]
+    n, m = 4, 128
+    (R0, K0), (R1, K1) = shapes = [(1024, 256), (512, 1024)]
+    units = make_units(z, n, shapes, m, key=3)
+    before = clone_units(units)
     run_step(z, units, m, 1, z.FSDP_BACKWARD_PREFETCH)
-    u0, b0 = units[0], before[0]
-    sh = list(b0["w"].view(n, R // n, K).unbind(0))
-    yb = torch.empty(n * m, R, dtype=torch.bfloat16, device=DEV)
-    z.fsdp_unit_forward([s.contiguous() for s in sh], b0["x"], None, Y_bf16=yb)
+    b0 = before[0]
+    sh0 = [s.contiguous() for s in b0["w"].view(n, R0 // n, K0).unbind(0)]
+    yb = torch.empty(n * m, R0, dtype=torch.bfloat16, device=DEV)
+    z.fsdp_unit_forward(sh0, b0["x"], None, Y_bf16=yb)
     assert torch.equal(yb.view(torch.int16), units[1]["x"].view(torch.int16))
-    # unit 1's backward (W [K, R] in 4 shards) gives unit 0's dY
+    # unit 1's backward (W_1 [R1, K1] in 4 shards) gives unit 0's dY
     b1 = before[1]
-    sh1 = [s.contiguous() for s in b1["w"].view(n, K // n, R).unbind(0)]
+    sh1 = [s.contiguous() for s in b1["w"].view(n, R1 // n, K1).unbind(0)]
     A = [units[1]["x"][q * m:(q + 1) * m].contiguous() for q in range(n)]
     dY = [b1["dy"][q * m:(q + 1) * m].contiguous() for q in range(n)]
-    dX = [torch.empty(m, R, device=DEV) for _ in range(n)]
-    dW = torch.empty(K, R, device=DEV)
-    ws = torch.empty(z.fsdp_unit_backward_workspace(n, K, R, m), dtype=torch.uint8, device=DEV)
+    dX = [torch.empty(m, K1, device=DEV) for _ in range(n)]
+    dW = torch.empty(R1, K1, device=DEV)
+    ws = torch.empty(z.fsdp_unit_backward_workspace(n, R1, K1, m), dtype=torch.uint8, device=DEV)
     z.fsdp_unit_backward(sh1, A, dY, dX, dW, ws)
     z.zero_device_status()
-    assert torch.equal(torch.cat(dX, 0).to(torch.bfloat16).view(torch.int16), u0["dy"].view(torch.int16))
+    assert torch.equal(torch.cat(dX, 0).to(torch.bfloat16).view(torch.int16), units[0]["dy"].view(torch.int16))
     assert torch.equal(dW.view(torch.int32), units[1]["dw"].view(torch.int32))
     master, mm, vv = b1["master"].clone(), b1["m"].clone(), b1["v"].clone()
-    w = torch.empty(K * R, dtype=torch.bfloat16, device=DEV)
+    w = torch.empty(R1 * K1, dtype=torch.bfloat16, device=DEV)
     z.zero_adam_step(b1["plan"], z.ZERO_ALL_RANKS, dW.view(-1), master, mm, vv, w, HP, 1)
     z.zero_device_status()
     assert torch.equal(master.view(torch.int32), units[1]["master"].view(torch.int32))
