@@ -635,8 +635,9 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         res["mlp_unit_prefetched_gather"] = {"ms": ms2, "tflops": flop / ms2 / 1e9,
                                              "note": "W_down gathered into scratch on a second stream during gate+up"}
         del gs_, us_, ds_, Hb, Ym, sd
-        # backward of W_up for 8 ranks of 2048 tokens: one dX GEMM over all ranks reading the
-        # W shards in place, X^T laid out, one rank-reduced dW GEMM reading dY in place
+        # backward of W_up for 8 ranks of 2048 tokens: W^T (the backward gather, transposed)
+        # and X^T laid out in one launch, one dX GEMM over all ranks on the CTA-pair kernel,
+        # one rank-reduced dW GEMM reading dY in place
         R, K, Mb = 14336, 4096, 2048
         shards = synth.weight_shards(R, K, n, device=dev, seed_key=11)
         A = [synth.activations(Mb, K, device=dev, seed_key=q) for q in range(n)]
@@ -650,8 +651,15 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         res["backward_up"] = {"ms": ms, "tflops": flop / ms / 1e9, "frac": flop / ms / 1e9 / tf_peak,
                               "ranks": n, "tokens_per_rank": Mb,
                               "launches": 3, "workspace_bytes": wsb,
-                              "note": "W and dY read in place as MN-major operands, X^T transposed; "
-                                      "one dX GEMM over all ranks, one dW GEMM"}
+                              "note": "W^T and X^T laid out by one transpose launch; dX over all ranks with "
+                                      "both operands K-major (CTA-pair kernel); dW reads dY in place (MN-major)"}
+        # the same call with a workspace that holds X^T alone: W read in place (MN-major)
+        ws_x = torch.empty((2 * K * n * Mb + 255) // 256 * 256, dtype=torch.uint8, device=dev)
+        ms_x = time_launches(lambda: z.fsdp_unit_backward(shards, A, dY, dX, dW, ws_x, stream=stream), 5, stream)
+        res["backward_up_w_in_place"] = {"ms": ms_x, "tflops": flop / ms_x / 1e9, "frac": flop / ms_x / 1e9 / tf_peak,
+                                         "workspace_bytes": ws_x.numel(),
+                                         "note": "workspace of X^T alone: W's shards read in place as an MN-major "
+                                                 "operand of the dX GEMM (one-CTA kernel)"}
     except Exception as e:  # the GEMM leg must not hide the step's line
         res["error"] = str(e)[:300]
     return res

@@ -918,14 +918,6 @@ bool fsdp_fused_gather_ok(int n_ranks, int64_t rows_out) {
   return n_ranks == 1 || (rows_out / n_ranks) % (g_gemm_kernel.load() == 1 ? BN : 128) == 0;
 }
 
-int launch_fsdp_bwd_dx_bf16(int w_pieces, const uint16_t* const* w, int64_t rows_out, int64_t k_in,
-                            const uint16_t* dY, int64_t nm, uint16_t* dX_bf16, cudaStream_t st) {
-  const uint16_t* dy1[1] = {dY};
-  float* y1[1] = {nullptr};
-  return launch_gemm<false>({1, dy1, false, nm}, {w_pieces, w, true, rows_out / w_pieces}, nullptr, nm, k_in,
-                            rows_out, y1, 1, dX_bf16, 1.0f, st, "fsdp_zero3_step");
-}
-
 int launch_fsdp_bwd_dw_alpha(const uint16_t* dY, int64_t nm, const uint16_t* Xt, int64_t rows_out, int64_t k_in,
                              float* dW, float alpha, cudaStream_t st) {
   const uint16_t* dy1[1] = {dY};

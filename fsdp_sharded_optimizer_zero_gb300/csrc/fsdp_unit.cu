@@ -9,19 +9,24 @@
 // and rank r's reduce-scatter result is rows [r R/N, (r+1) R/N) of dW, a contiguous block.
 //
 // Both products run on the tcgen05 GEMM. When R / N, K and M are multiples of 64 (and
-// N <= 16) the operands are read where they lie (the in-place path):
-//   dX_q = dY_q W   with dY_q a K-major A and W's row shards an MN-major B, the shard picked
-//                   by K block (the backward all-gather fused into the loads); one launch
-//                   over all ranks' row pieces when M % 128 == 0, else one per rank;
+// N <= 16) dY is read where it lies:
+//   dX_q = dY_q W   with dY_q a K-major A. W comes from its row shards either as W^T [K, R]
+//                   laid out in the workspace by the backward all-gather (a transposing
+//                   gather), a K-major B that the CTA-pair kernel runs (the default when the
+//                   workspace holds it), or read in place as an MN-major B with the shard
+//                   picked by K block (when the workspace holds only X^T). One launch over
+//                   all ranks' row pieces when M % 128 == 0, else one per rank;
 //   dW = (1/N) sum_q dY_q^T X_q   with dY_q an MN-major A, the K loop over every rank's
-//                   tokens, and X^T [K, N M] laid out by one transpose-and-concatenate
-//                   launch into the workspace (a second MN-major operand costs more than
-//                   that transpose);
+//                   tokens, and X^T [K, N M] laid out in the workspace (a second MN-major
+//                   operand costs more than that transpose). W^T and X^T are laid out by
+//                   ONE launch of the transpose kernel;
 // so the sum over ranks happens inside the fp32 tensor-core accumulation, and the 1/N scale
-// is applied in the epilogue. These MN-major GEMMs run on the one-CTA kernel, where the
-// CTA-pair form measured no faster. Other shapes take the transposed path: W^T [K, R],
-// dY^T [R, N M] and X^T [K, N M] in the workspace, then K-major GEMMs (on the CTA-pair
-// kernel). Both paths give the same bits.
+// is applied in the epilogue. On GB300 each MN-major operand costs its GEMM 5-14 %, so
+// W^T's 44 us transpose (W_up) buys back more than it costs: 2.534 against 2.652 ms per
+// call on W_up, 8 ranks x 2048 tokens (median of 8 interleaved rounds, same bits). The
+// MN-major dW stays on the one-CTA kernel. Other shapes take the transposed path: W^T
+// [K, R], dY^T [R, N M] and X^T [K, N M] in the workspace, then K-major GEMMs (on the
+// CTA-pair kernel). Every path gives the same bits.
 #include <string.h>
 
 #include "internal.h"
@@ -34,6 +39,7 @@ uint64_t align256(uint64_t b) { return (b + 255) & ~uint64_t(255); }
 
 struct BackwardWorkspace {
   uint64_t wt, dyt, xt, total;  // byte offsets of W^T, dY^T, X^T and the total size
+  uint64_t min_total;           // the smallest workspace the call accepts
 };
 
 // The backward reads W and dY in place (MN-major GEMM operands) when every K piece is a
@@ -46,17 +52,20 @@ bool backward_in_place(int n, int64_t rows_out, int64_t k_in, int64_t m_tokens) 
 }
 
 BackwardWorkspace backward_workspace(int n, int64_t rows_out, int64_t k_in, int64_t m_tokens) {
-  BackwardWorkspace w{0, 0, 0, 0};
+  BackwardWorkspace w{0, 0, 0, 0, 0};
   const uint64_t R = static_cast<uint64_t>(rows_out), K = static_cast<uint64_t>(k_in);
   const uint64_t NM = static_cast<uint64_t>(n) * static_cast<uint64_t>(m_tokens);
-  if (backward_in_place(n, rows_out, k_in, m_tokens)) {  // X^T only
-    w.total = align256(2 * K * NM);
+  if (backward_in_place(n, rows_out, k_in, m_tokens)) {  // X^T, then W^T (or W in place)
+    w.xt = 0;
+    w.wt = align256(2 * K * NM);
+    w.min_total = w.wt;
+    w.total = w.wt + align256(2 * R * K);
     return w;
   }
   w.wt = 0;
   w.dyt = align256(2 * R * K);
   w.xt = w.dyt + align256(2 * R * NM);
-  w.total = w.xt + align256(2 * K * NM);
+  w.total = w.min_total = w.xt + align256(2 * K * NM);
   return w;
 }
 
@@ -108,9 +117,9 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
                      "%s: k_in, rows_out and n_ranks * m_tokens must be multiples of 8 (16-byte GEMM rows)", who);
   if (!w_shards || !A || !dY || !dX || !dW) return set_error(ZERO_ERR_INVALID_ARG, "%s: NULL argument", who);
   const BackwardWorkspace ws = backward_workspace(n_ranks, rows_out, k_in, m_tokens);
-  if (!workspace || workspace_bytes < ws.total)
+  if (!workspace || workspace_bytes < ws.min_total)
     return set_error(ZERO_ERR_INVALID_ARG, "%s: workspace of %llu bytes is below the %llu needed", who,
-                     workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.total);
+                     workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.min_total);
   if (!aligned16(dW) || !aligned16(workspace))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: dW and workspace must be 16-byte aligned", who);
   GradPtrs wp, ap, dyp;
@@ -128,23 +137,39 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (backward_in_place(n_ranks, rows_out, k_in, m_tokens)) {
-    // dX_q = dY_q W with W read as its row shards: one launch over all ranks' rows when each
-    // rank's M is a whole number of 128-row tiles, else one launch per rank
     const uint16_t* const* dy = reinterpret_cast<const uint16_t* const*>(dY);
-    const uint16_t* const* wsh = reinterpret_cast<const uint16_t* const*>(w_shards);
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    uint16_t* xt = reinterpret_cast<uint16_t*>(base + ws.xt);
     int rc;
-    if (m_tokens % 128 == 0) {
-      rc = launch_fsdp_bwd_dx(n_ranks, dy, m_tokens, n_ranks, wsh, rows_out, k_in, dX, st);
-      if (rc) return rc;
+    if (workspace_bytes >= ws.total) {
+      // W^T [K, R] (the backward all-gather, transposed) and X^T [K, N M] in one launch
+      uint16_t* wt = reinterpret_cast<uint16_t*>(base + ws.wt);
+      cudaError_t e = launch_transpose_cat2(wp, n_ranks, rows_out / n_ranks, k_in, wt, ap, n_ranks, m_tokens, k_in,
+                                            xt, st);
+      if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
+      // dX_q [M, K] = dY_q [M, R] * (W^T [K, R])^T, both operands K-major
+      const uint16_t* wt1[1] = {wt};
+      if (m_tokens % 128 == 0) {
+        if ((rc = launch_fsdp_gemm_row_split(n_ranks, dy, dX, m_tokens, wt, k_in, rows_out, 1.0f, st))) return rc;
+      } else {
+        for (int q = 0; q < n_ranks; ++q)
+          if ((rc = launch_fsdp_gemm(1, wt1, k_in, rows_out, dy[q], m_tokens, dX[q], nullptr, 1.0f, st))) return rc;
+      }
     } else {
-      for (int q = 0; q < n_ranks; ++q)
-        if ((rc = launch_fsdp_bwd_dx(n_ranks, dy + q, m_tokens, 1, wsh, rows_out, k_in, dX + q, st))) return rc;
+      // dX_q = dY_q W with W read as its row shards: one launch over all ranks' rows when
+      // each rank's M is a whole number of 128-row tiles, else one launch per rank
+      const uint16_t* const* wsh = reinterpret_cast<const uint16_t* const*>(w_shards);
+      if (m_tokens % 128 == 0) {
+        if ((rc = launch_fsdp_bwd_dx(n_ranks, dy, m_tokens, n_ranks, wsh, rows_out, k_in, dX, st))) return rc;
+      } else {
+        for (int q = 0; q < n_ranks; ++q)
+          if ((rc = launch_fsdp_bwd_dx(n_ranks, dy + q, m_tokens, 1, wsh, rows_out, k_in, dX + q, st))) return rc;
+      }
+      cudaError_t e = launch_transpose_cat(ap, n_ranks, m_tokens, k_in, xt, st);
+      if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
     }
     // dW = (1/N) sum_q dY_q^T X_q: the K loop runs over every rank's tokens in turn, dY
     // read in place, X from its rank-concatenated transpose
-    uint16_t* xt = static_cast<uint16_t*>(workspace);
-    cudaError_t e = launch_transpose_cat(ap, n_ranks, m_tokens, k_in, xt, st);
-    if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
     return launch_fsdp_bwd_dw(n_ranks, dy, xt, m_tokens, rows_out, k_in, dW, st);
   }
   uint8_t* base = static_cast<uint8_t*>(workspace);

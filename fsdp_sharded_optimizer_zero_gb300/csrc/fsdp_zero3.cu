@@ -6,9 +6,12 @@
 // backward); after the backward the weight gradient is reduce-scattered so each rank keeps
 // the rows of its own shard, and each rank's Adam updates that shard alone.
 //
-// Here every "gather" reads the N shards where they lie: either inside the GEMM's operand
+// Here the forward's gather reads the N shards where they lie: inside the GEMM's operand
 // loads (the default: no copy of W exists at all), or, with FSDP_GATHER_MATERIALIZE, by a
 // gather kernel into a workspace slot that plays the all-gather's receive buffer. The
+// backward's gather always lands W^T [K, R] in a slot (a transposing gather, in the same
+// launch as the X^T layout the dW GEMM reads), so that dX is a K-major GEMM on the CTA-pair
+// kernel: on GB300 an MN-major operand costs a GEMM 5-14 %, more than the transpose. The
 // reduce of the reduce-scatter happens inside the dW GEMM's fp32 accumulation (its K loop
 // runs over every rank's tokens), so rank r's reduce-scattered gradient is simply rows
 // [r R/N, (r+1) R/N) of dW, contiguous with its flat-parameter shard.
@@ -42,7 +45,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 struct Zero3Workspace {
   int slots;                // 2 with backward prefetch, else 1
   uint64_t xt_off[2];       // X^T [k_in, N M] bf16 of the unit in the slot
-  uint64_t w_off[2];        // gathered W [rows_out, k_in] bf16 (FSDP_GATHER_MATERIALIZE)
+  uint64_t w_off[2];        // the unit's gathered W^T [k_in, rows_out] (backward) or W (materialised forward)
   uint64_t total;
 };
 
@@ -56,7 +59,7 @@ Zero3Workspace zero3_workspace(int n, int n_units, const fsdp_unit_state* u, int
   }
   w.slots = (flags & FSDP_BACKWARD_PREFETCH) ? 2 : 1;
   const uint64_t xt = align256(2 * kmax * static_cast<uint64_t>(n) * static_cast<uint64_t>(m));
-  const uint64_t ww = (flags & FSDP_GATHER_MATERIALIZE) ? align256(2 * wmax) : 0;
+  const uint64_t ww = align256(2 * wmax);
   uint64_t off = 0;
   for (int s = 0; s < w.slots; ++s) {
     w.xt_off[s] = off;
@@ -99,10 +102,11 @@ int check_units(int n, int n_units, const fsdp_unit_state* u, int64_t m, int fla
     const fsdp_unit_state& s = u[i];
     if (s.rows_out < 1 || s.k_in < 1 || s.rows_out > (1 << 30) || s.k_in > (1 << 30))
       return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: sizes outside 1..2^30", kWho, i);
-    if (s.rows_out % n || (s.rows_out / n) % 64 || s.k_in % 64)
+    if (s.rows_out % n || s.rows_out % 64 || s.k_in % 8)
       return set_error(ZERO_ERR_INVALID_ARG,
-                       "%s: unit %d: needs rows_out / n_ranks and k_in multiples of 64 (got %lld / %d, %lld)", kWho, i,
-                       (long long)s.rows_out, n, (long long)s.k_in);
+                       "%s: unit %d: needs rows_out a multiple of 64 and of n_ranks, k_in a multiple of 8 (got %lld, "
+                       "%d, %lld)",
+                       kWho, i, (long long)s.rows_out, n, (long long)s.k_in);
     if (!(flags & FSDP_GATHER_MATERIALIZE) && !fsdp_fused_gather_ok(n, s.rows_out))
       return set_error(ZERO_ERR_INVALID_ARG,
                        "%s: unit %d: shards of %lld rows do not tile the GEMM for the fused gather; pass "
@@ -206,13 +210,21 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
   }
 
   // ---- backward, last -> unit 0 ----
-  // unit i's operands: its gathered W (materialised mode) and X_i^T [k_in, N M]
+  // unit i's operands: W_i^T [k_in, rows_out] gathered from its shards and X_i^T [k_in, N M],
+  // both laid out by one launch
   auto prepare = [&](int i, cudaStream_t s) {
     int r = ZERO_OK;
     if (overlap && i + ws.slots < L && (r = wait(s, ev_done(i + ws.slots)))) return r;  // slot reuse
-    if (materialize && (r = gather(i, s))) return r;
-    const zero_bf16* x1[1] = {units[i].x};
-    if ((r = fsdp_transpose_cat(1, x1, nm, units[i].k_in, xt_slot(i), reinterpret_cast<zero_stream_t>(s)))) return r;
+    const fsdp_unit_state& u = units[i];
+    GradPtrs wsrc, xsrc;
+    memset(&wsrc, 0, sizeof(wsrc));
+    memset(&xsrc, 0, sizeof(xsrc));
+    const uint16_t* const* sh = shards_of(i);
+    for (int q = 0; q < n; ++q) wsrc.p[q] = sh[q];
+    xsrc.p[0] = u.x;
+    const cudaError_t e =
+        launch_transpose_cat2(wsrc, n, u.rows_out / n, u.k_in, w_slot(i), xsrc, 1, nm, u.k_in, xt_slot(i), s);
+    if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", kWho, cudaGetErrorString(e));
     return overlap ? record(ev_ready(i), s) : ZERO_OK;
   };
   if (overlap) {
@@ -227,11 +239,10 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
     } else if ((rc = prepare(i, st))) {
       return rc;
     }
-    const uint16_t* w1[1] = {w_slot(i)};
-    const uint16_t* const* wp = materialize ? w1 : shards_of(i);
-    const int pieces = materialize ? 1 : n;
+    // dY_{i-1} [N M, K] = bf16(dY_i [N M, R] * (W_i^T [K, R])^T), both operands K-major
+    const uint16_t* wt1[1] = {w_slot(i)};
     zero_bf16* dx = i > 0 ? units[i - 1].dy : dx_out;
-    if (dx && (rc = launch_fsdp_bwd_dx_bf16(pieces, wp, s.rows_out, s.k_in, s.dy, nm, dx, st))) return rc;
+    if (dx && (rc = launch_fsdp_gemm(1, wt1, s.k_in, s.rows_out, s.dy, nm, nullptr, dx, 1.0f, st))) return rc;
     if ((rc = launch_fsdp_bwd_dw_alpha(s.dy, nm, xt_slot(i), s.rows_out, s.k_in, s.dw,
                                        1.0f / static_cast<float>(n), st)))
       return rc;

@@ -60,6 +60,11 @@ cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t st)
 // transposed and concatenated into one row-major [cols, n * rows] buffer
 cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int64_t cols, uint16_t* dst,
                                  cudaStream_t st);
+// two such independent problems in one launch when both are aligned for the pipelined
+// kernel (16-byte rows and buffers), else two launches; same results as two calls
+cudaError_t launch_transpose_cat2(const GradPtrs& srcs0, int n0, int64_t rows0, int64_t cols0, uint16_t* dst0,
+                                  const GradPtrs& srcs1, int n1, int64_t rows1, int64_t cols1, uint16_t* dst1,
+                                  cudaStream_t st);
 
 // ---- FSDP GEMM (fsdp_gemm.cu) ----
 // Y[M, R] = alpha * A[M, K] * W^T with W given as n_ranks row shards of R/n_ranks rows
@@ -87,12 +92,9 @@ int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces
                        cudaStream_t st);
 int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* Xt, int64_t m_tokens,
                        int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st);
-// The same two products over one contiguous operand for all ranks (rank q's rows at q M):
-// dX [NM, K] = dY [NM, R] W written as bf16 only (W read in place from w_pieces MN-major
-// pieces along K, or as one gathered W); dW [R, K] = alpha dY^T [R, NM] (X^T [K, NM])^T
-// with dY read in place as one MN-major piece. Bit-identical to the per-rank forms above.
-int launch_fsdp_bwd_dx_bf16(int w_pieces, const uint16_t* const* w, int64_t rows_out, int64_t k_in,
-                            const uint16_t* dY, int64_t nm, uint16_t* dX_bf16, cudaStream_t st);
+// dW over one contiguous dY for all ranks (rank q's rows at q M): dW [R, K] = alpha dY^T
+// [R, NM] (X^T [K, NM])^T with dY read in place as one MN-major piece. Bit-identical to the
+// per-rank form above.
 int launch_fsdp_bwd_dw_alpha(const uint16_t* dY, int64_t nm, const uint16_t* Xt, int64_t rows_out, int64_t k_in,
                              float* dW, float alpha, cudaStream_t st);
 unsigned int fsdp_gemm_read_clear_error();

@@ -6,6 +6,8 @@
 // 4-element units per thread-iteration, so every global access of a warp is one
 // contiguous run: reduce-scatter 2N + 4 bytes per parameter, Adam 28 (+2 with the cast),
 // all-gather 6, row gather 4 per weight element, transpose 4 per element.
+#include <string.h>
+
 #include <algorithm>
 #include <type_traits>
 
@@ -273,27 +275,39 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// requires cols % 8 == 0, total_rows % 8 == 0 and 16-byte-aligned sources and destination
-__global__ void __launch_bounds__(256) transpose_cat_pipe_kernel(GradPtrs srcs, int64_t rows, int64_t cols,
-                                                                 int64_t total_rows, uint16_t* __restrict__ dst) {
+// One transpose-and-concatenate problem of the pipelined kernel. Requires cols % 8 == 0,
+// total_rows % 8 == 0 and 16-byte-aligned sources and destination.
+struct TransposeJob {
+  GradPtrs srcs;
+  int64_t rows, cols, total_rows, col_tiles, ntiles;
+  uint16_t* dst;
+};
+// Up to two independent problems in one launch (the backward's W^T and X^T): tiles
+// [0, j[0].ntiles) belong to the first, the rest to the second.
+struct TransposeJobs {
+  TransposeJob j[2];
+};
+
+__global__ void __launch_bounds__(256) transpose_cat_pipe_kernel(const __grid_constant__ TransposeJobs jobs) {
   __shared__ __align__(128) uint16_t ring[kPipeStages][64 * 64];
   const int t = threadIdx.x;
-  const int64_t col_tiles = (cols + 63) / 64, row_tiles = (total_rows + 63) / 64;
-  const int64_t ntiles = col_tiles * row_tiles;
+  const int64_t nt0 = jobs.j[0].ntiles, ntiles = nt0 + jobs.j[1].ntiles;
   // issue the copies of tile idx into ring slot `slot` (one commit group per call, empty
   // when idx is past the end, so every thread's group count stays in step)
   auto issue = [&](int64_t idx, int slot) {
     if (idx < ntiles) {
-      const int64_t c0 = (idx % col_tiles) * 64, r0 = (idx / col_tiles) * 64;
+      const TransposeJob& J = jobs.j[idx < nt0 ? 0 : 1];
+      const int64_t li = idx < nt0 ? idx : idx - nt0;
+      const int64_t c0 = (li % J.col_tiles) * 64, r0 = (li / J.col_tiles) * 64;
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int v = t + 256 * k, rr = v >> 3, ch = v & 7;  // 64 rows x 8 chunks of 16 B
         const int64_t gr = r0 + rr, gc = c0 + ch * 8;
-        const bool in = gr < total_rows && gc < cols;
-        const uint16_t* src = srcs.p[0];
+        const bool in = gr < J.total_rows && gc < J.cols;
+        const uint16_t* src = J.srcs.p[0];
         if (in) {
-          const int64_t q = gr / rows, lr = gr - q * rows;
-          src = srcs.p[q] + lr * cols + gc;
+          const int64_t q = gr / J.rows, lr = gr - q * J.rows;
+          src = J.srcs.p[q] + lr * J.cols + gc;
         }
         cp_async16(smem_u32(&ring[slot][rr * 64 + ((ch ^ ((rr >> 3) & 7)) * 8)]), src, in ? 16u : 0u);
       }
@@ -308,7 +322,9 @@ __global__ void __launch_bounds__(256) transpose_cat_pipe_kernel(GradPtrs srcs, 
     cp_async_wait<kPipeStages - 1>();  // this thread's copies of tile idx have landed
     __syncthreads();                    // and everyone else's
     const uint16_t* T = ring[i % kPipeStages];
-    const int64_t c0 = (idx % col_tiles) * 64, r0 = (idx / col_tiles) * 64;
+    const TransposeJob& J = jobs.j[idx < nt0 ? 0 : 1];
+    const int64_t li = idx < nt0 ? idx : idx - nt0;
+    const int64_t c0 = (li % J.col_tiles) * 64, r0 = (li / J.col_tiles) * 64;
     // two output rows (source columns cc, cc + 1) x 8 output columns (source rows rv..rv+7)
     const int cc = (t >> 3) * 2, rv = (t & 7) * 8;
     uint32_t w[8];
@@ -320,9 +336,9 @@ __global__ void __launch_bounds__(256) transpose_cat_pipe_kernel(GradPtrs srcs, 
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int64_t dc = c0 + cc + h;
-      if (dc < cols && r0 + rv < total_rows) {  // total_rows % 8 == 0: all 8 in range
+      if (dc < J.cols && r0 + rv < J.total_rows) {  // total_rows % 8 == 0: all 8 in range
         const uint32_t sel = h ? 0x7632u : 0x5410u;
-        __stcs(reinterpret_cast<uint4*>(dst + dc * total_rows + r0 + rv),
+        __stcs(reinterpret_cast<uint4*>(J.dst + dc * J.total_rows + r0 + rv),
                make_uint4(__byte_perm(w[0], w[1], sel), __byte_perm(w[2], w[3], sel), __byte_perm(w[4], w[5], sel),
                           __byte_perm(w[6], w[7], sel)));
       }
@@ -402,24 +418,60 @@ cudaError_t launch_gather_rows(const GradPtrs& shards, int n, uint64_t shard_ele
   return cudaGetLastError();
 }
 
+namespace {
+
+// the pipelined kernel's job for one problem, or false when its shapes or buffers are not
+// aligned for it
+bool pipe_job(const GradPtrs& srcs, int n, int64_t rows, int64_t cols, uint16_t* dst, TransposeJob* j) {
+  const int64_t total_rows = rows * n;
+  bool vec = cols % 8 == 0 && total_rows % 8 == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
+  for (int q = 0; q < n; ++q) vec = vec && (reinterpret_cast<uintptr_t>(srcs.p[q]) & 15) == 0;
+  if (!vec) return false;
+  j->srcs = srcs;
+  j->rows = rows;
+  j->cols = cols;
+  j->total_rows = total_rows;
+  j->col_tiles = (cols + 63) / 64;
+  j->ntiles = j->col_tiles * ((total_rows + 63) / 64);
+  j->dst = dst;
+  return true;
+}
+
+cudaError_t launch_pipe(const TransposeJobs& jobs, cudaStream_t st) {
+  const int64_t ntiles = jobs.j[0].ntiles + jobs.j[1].ntiles;
+  if (ntiles == 0) return cudaSuccess;
+  const unsigned int grid =
+      static_cast<unsigned int>(std::min<int64_t>(ntiles, static_cast<int64_t>(num_sms()) * kPipeBlocksPerSm));
+  transpose_cat_pipe_kernel<<<grid, 256, 0, st>>>(jobs);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int64_t cols, uint16_t* dst,
                                  cudaStream_t st) {
   const int64_t total_rows = rows * n;
   if (total_rows == 0 || cols == 0) return cudaSuccess;
-  bool vec = cols % 8 == 0 && total_rows % 8 == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
-  for (int q = 0; q < n; ++q) vec = vec && (reinterpret_cast<uintptr_t>(srcs.p[q]) & 15) == 0;
-  if (vec) {
-    const int64_t ntiles = ((cols + 63) / 64) * ((total_rows + 63) / 64);
-    const unsigned int grid =
-        static_cast<unsigned int>(std::min<int64_t>(ntiles, static_cast<int64_t>(num_sms()) * kPipeBlocksPerSm));
-    transpose_cat_pipe_kernel<<<grid, 256, 0, st>>>(srcs, rows, cols, total_rows, dst);
-    return cudaGetLastError();
-  }
+  TransposeJobs jobs;
+  memset(&jobs, 0, sizeof(jobs));
+  if (pipe_job(srcs, n, rows, cols, dst, &jobs.j[0])) return launch_pipe(jobs, st);
   const int64_t gy = std::min<int64_t>((total_rows + kTR - 1) / kTR, 65535), gx = (cols + kTC - 1) / kTC;
   if (gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
   transpose_cat_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(
-      srcs, rows, cols, total_rows, dst, vec ? 1 : 0);
+      srcs, rows, cols, total_rows, dst, 0);
   return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_cat2(const GradPtrs& srcs0, int n0, int64_t rows0, int64_t cols0, uint16_t* dst0,
+                                  const GradPtrs& srcs1, int n1, int64_t rows1, int64_t cols1, uint16_t* dst1,
+                                  cudaStream_t st) {
+  TransposeJobs jobs;
+  memset(&jobs, 0, sizeof(jobs));
+  if (rows0 * n0 > 0 && cols0 > 0 && rows1 * n1 > 0 && cols1 > 0 &&
+      pipe_job(srcs0, n0, rows0, cols0, dst0, &jobs.j[0]) && pipe_job(srcs1, n1, rows1, cols1, dst1, &jobs.j[1]))
+    return launch_pipe(jobs, st);
+  cudaError_t e = launch_transpose_cat(srcs0, n0, rows0, cols0, dst0, st);
+  return e == cudaSuccess ? launch_transpose_cat(srcs1, n1, rows1, cols1, dst1, st) : e;
 }
 
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t st) {

@@ -287,9 +287,12 @@ ZERO_API int fsdp_transpose_cat(int n_srcs, const zero_bf16* const srcs[], int64
                                 zero_stream_t stream);
 
 /* Bytes of device workspace fsdp_unit_backward needs for transposed operand copies, each
- * rounded up to 256 bytes. When R/N, k_in and m_tokens are multiples of 64 and N <= 16
- * the GEMMs read W's shards and dY in place (as MN-major tensor-core operands) and only
- * X^T (2*K*N*M) is needed; otherwise W^T (2*R*K), dY^T (2*R*N*M) and X^T. */
+ * rounded up to 256 bytes. When R/N, k_in and m_tokens are multiples of 64 and N <= 16,
+ * dY is read in place (an MN-major tensor-core operand) and the workspace holds X^T
+ * (2*K*N*M) and W^T (2*R*K), the backward all-gather of W laid out transposed; a workspace
+ * that holds X^T alone is also accepted, and W is then read in place from its shards as an
+ * MN-major operand (same results, about 4 % slower on GB300). Other shapes need W^T,
+ * dY^T (2*R*N*M) and X^T. This call returns the size of the fastest path. */
 ZERO_API int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t k_in, int64_t m_tokens,
                                           uint64_t* bytes);
 
@@ -302,7 +305,8 @@ ZERO_API int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t
  * dX[q]: out, row-major [m_tokens, k_in] fp32: dX_q = dY_q W;
  * dW: out, row-major [rows_out, k_in] fp32: dW = (1/N) sum_q dY_q^T X_q; rank r's
  *     reduce-scattered shard is rows [r*R/N, (r+1)*R/N).
- * workspace: device buffer of fsdp_unit_backward_workspace() bytes (caller-owned scratch).
+ * workspace: device buffer of fsdp_unit_backward_workspace() bytes (caller-owned scratch),
+ *     or at least the X^T part of it for the shapes that read dY in place (see above).
  * Requires rows_out % N == 0 and k_in, rows_out, N*m_tokens multiples of 8; all buffers
  * 16-byte aligned. fp32 accumulation on the tensor cores in an unspecified order: each dX
  * entry is within (R+1) 2^-23 sum|dy w| and each dW entry within (N M + 1) 2^-23 (1/N)
@@ -354,17 +358,17 @@ typedef struct {
 } fsdp_unit_state;
 
 /* flags of fsdp_zero3_step */
-#define FSDP_GATHER_MATERIALIZE 1 /* gather each unit's W into a workspace slot (the all-gather's receive
-                                     buffer: sharded model + the unit in use), reused after the unit; without
-                                     it the GEMMs read every tile straight from its shard */
+#define FSDP_GATHER_MATERIALIZE 1 /* forward: gather each unit's W into a workspace slot (the all-gather's
+                                     receive buffer: sharded model + the unit in use), reused after the unit;
+                                     without it the forward GEMM reads every tile straight from its shard.
+                                     The backward always gathers W^T into the slot (below). */
 #define FSDP_BACKWARD_PREFETCH 2  /* issue unit i-1's gather and X^T layout on prefetch_stream while unit i's
                                      backward GEMMs run on `stream` */
 
 /* Bytes of device workspace fsdp_zero3_step needs for these units, M tokens per rank and
- * flags: X^T [k_in, N*M] bf16 of the largest unit (two slots with FSDP_BACKWARD_PREFETCH),
- * plus the gathered W [rows_out, k_in] bf16 of the largest unit (two slots with prefetch)
- * under FSDP_GATHER_MATERIALIZE; each slot rounded up to 256 bytes. Only the units' sizes
- * are read. */
+ * flags: one slot (two with FSDP_BACKWARD_PREFETCH) holding X^T [k_in, N*M] bf16 of the
+ * widest input and the gathered W^T (or W) of the largest unit, 2*rows_out*k_in bytes; each
+ * part rounded up to 256 bytes. Only the units' sizes are read. */
 ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit_state* units, int64_t m_tokens,
                                        int flags, uint64_t* bytes);
 
@@ -373,8 +377,9 @@ ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit
  *   forward, unit 0 -> last: gather W_i (fused into the GEMM's loads, or into a workspace
  *     slot), X_{i+1} = bf16(X_i W_i^T) for every rank (the last unit's output goes to y_out;
  *     with y_out NULL that product is skipped), W_i freed;
- *   backward, last -> unit 0: gather W_i again, dY_{i-1} = bf16(dY_i W_i) (unit 0: into
- *     dx_out, skipped when NULL), dW_i = (1/N) sum_q dY_{i,q}^T X_{i,q} (the reduce of the
+ *   backward, last -> unit 0: gather W_i again, as W_i^T into a workspace slot (with
+ *     X_i^T, in one launch), dY_{i-1} = bf16(dY_i W_i) (unit 0: into dx_out, skipped when
+ *     NULL) with both GEMM operands K-major, dW_i = (1/N) sum_q dY_{i,q}^T X_{i,q} (the reduce of the
  *     reduce-scatter inside the fp32 tensor-core accumulation, rank r keeping its rows),
  *     then each rank's Adam on its shard (zero_adam_step, ZERO_ALL_RANKS: every rank's
  *     shard in one launch) writing the new bf16 shards of W_i — after W_i's last use;
@@ -385,8 +390,8 @@ ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit
  * Results do not depend on the flags (same bits). dX / dY products are fp32 sums of exact
  * bf16 products in an unspecified order (bounds as fsdp_unit_backward), rounded once to
  * bf16; Adam is bit-exact as zero_adam_step.
- * Requires 1 <= N <= 16, 1 <= n_units <= 64, N*M % 8 == 0; per unit k_in % 64 == 0,
- * (rows_out / N) % 64 == 0, and without FSDP_GATHER_MATERIALIZE the fused gather's shard
+ * Requires 1 <= N <= 16, 1 <= n_units <= 64, N*M % 8 == 0; per unit rows_out a multiple of
+ * 64 and of N, k_in % 8 == 0, and without FSDP_GATHER_MATERIALIZE the fused gather's shard
  * rule ((rows_out / N) % 128 == 0; 256 under zero_set_gemm_kernel(1)); 16-byte-aligned
  * buffers; workspace of fsdp_zero3_step_workspace() bytes. prefetch_stream may be NULL
  * (then everything runs on `stream`). */

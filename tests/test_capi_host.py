@@ -136,15 +136,16 @@ def test_newer_entry_points_reject_bad_arguments_before_launch(z):
     assert lib.zero_fused_step_fp32_grads(p.handle, 4, good, 256, 512, 768, 1024, C.byref(adam), 1, None) == -1
     # backward: rows % N, K % 8, workspace size, NULL rank pointer
     ws = C.c_uint64()
-    # W and dY in place (R/N, K and M multiples of 64): X^T only; otherwise W^T, dY^T, X^T
+    # dY in place (R/N, K and M multiples of 64): X^T and W^T (X^T alone is also accepted);
+    # otherwise W^T, dY^T, X^T
     assert lib.fsdp_unit_backward_workspace(4, 512, 256, 128, C.byref(ws)) == 0
-    assert ws.value == 2 * 256 * 512
+    assert ws.value == 2 * 256 * 512 + 2 * 512 * 256
     assert lib.fsdp_unit_backward_workspace(4, 512, 256, 40, C.byref(ws)) == 0
     assert ws.value == 2 * 512 * 256 + 2 * 512 * 160 + 2 * 256 * 160
     assert lib.fsdp_unit_backward_workspace(17, 17 * 64, 256, 128, C.byref(ws)) == 0
     assert ws.value > 2 * 256 * 17 * 128  # more than 16 ranks: one GEMM operand cannot hold every piece
     assert lib.fsdp_unit_backward_workspace(4, 512, 192, 128, C.byref(ws)) == 0
-    assert ws.value == 2 * 192 * 512
+    assert ws.value == 2 * 192 * 512 + 2 * 512 * 192
     assert lib.fsdp_unit_backward_workspace(4, 512, 200, 128, C.byref(ws)) == 0
     assert ws.value > 2 * 200 * 512  # K not a multiple of 64
     assert lib.fsdp_unit_backward_workspace(0, 512, 256, 128, C.byref(ws)) == -1
@@ -243,8 +244,10 @@ def test_zero3_step_rejects_bad_arguments_before_launch(z):
     good = [(512, 256), (1024, 512)]
     plans = [z.zero_plan(r * k, n, "zero3", 1 << 20) for r, k in good]
     ws = C.c_uint64()
+    # one slot (two with the backward prefetch): X^T of the widest input and W^T of the
+    # largest unit
     assert lib.fsdp_zero3_step_workspace(n, 2, units(good), m, 0, C.byref(ws)) == 0
-    assert ws.value == 2 * 512 * n * m
+    assert ws.value == 2 * 512 * n * m + 2 * 1024 * 512
     assert lib.fsdp_zero3_step_workspace(n, 2, units(good), m, 3, C.byref(ws)) == 0
     assert ws.value == 2 * (2 * 512 * n * m + 2 * 1024 * 512)
 
@@ -254,9 +257,11 @@ def test_zero3_step_rejects_bad_arguments_before_launch(z):
     # chain: unit 1's k_in must be unit 0's rows_out
     assert call(units([(512, 256), (1024, 256)], plans)) == -1
     assert b"is not unit 0's rows_out" in lib.zero_last_error()
-    # shard rows a multiple of 64, k_in a multiple of 64
-    assert call(units([(512, 200), (1024, 512)], plans)) == -1
-    assert call(units([(4 * 96, 256)], plans[:1]), nu=1) == -1
+    # rows_out a multiple of 64 (dW reads dY as an MN-major operand), k_in a multiple of 8
+    assert call(units([(512, 252), (1024, 512)], plans)) == -1
+    assert b"multiple of 64" in lib.zero_last_error()
+    assert call(units([(4 * 72, 256)], plans[:1]), nu=1) == -1
+    assert b"multiple of 64" in lib.zero_last_error()
     # shards of 64 rows do not tile the fused gather: FSDP_GATHER_MATERIALIZE needed
     p64 = [z.zero_plan(256 * 256, n, "zero3", 1 << 20)]  # kept alive: destroying a plan clears the message
     assert call(units([(256, 256)], p64), nu=1) == -1

@@ -264,10 +264,11 @@ def run_backward(z, n, rows, k, m, key=0, ints=False):
 
 
 def test_backward_workspace_sizes(z):
-    # W and dY are read in place when R/N, M and K are multiples of 64 (and N <= 16): the
-    # workspace holds X^T alone; otherwise W^T, dY^T and X^T
-    assert z.fsdp_unit_backward_workspace(8, 14336, 4096, 2048) == 2 * 4096 * 8 * 2048
-    assert z.fsdp_unit_backward_workspace(5, 320, 192, 192) == 2 * 192 * 5 * 192
+    # dY is read in place when R/N, M and K are multiples of 64 (and N <= 16): the
+    # workspace holds X^T and W^T (X^T alone also works, with W read in place); otherwise
+    # W^T, dY^T and X^T
+    assert z.fsdp_unit_backward_workspace(8, 14336, 4096, 2048) == 2 * 4096 * 8 * 2048 + 2 * 14336 * 4096
+    assert z.fsdp_unit_backward_workspace(5, 320, 192, 192) == 2 * 192 * 5 * 192 + 2 * 320 * 192
     assert z.fsdp_unit_backward_workspace(5, 320, 200, 192) > 2 * 200 * 5 * 192
     assert z.fsdp_unit_backward_workspace(4, 512, 256, 40) > 2 * 256 * 4 * 40
     assert z.fsdp_unit_backward_workspace(8, 2048, 512, 96) > 2 * 512 * 8 * 96
@@ -385,6 +386,34 @@ def test_backward_mistral_down_sampled(z):
     bound = (n * m + 1) * 2.0 ** -23 * bd / n + 2.0 ** -24 * np.abs(ex)
     got = f32(dW[torch.from_numpy(rr).to(DEV), torch.from_numpy(cc).to(DEV)]).astype(np.float64)
     assert np.all(np.abs(got - ex) <= bound), "dW"
+
+
+@pytest.mark.parametrize("n,rows,k,m", [(4, 512, 256, 128), (5, 320, 192, 192), (8, 2048, 512, 64),
+                                        (8, 3584, 128, 512)])
+def test_backward_x_only_workspace_reads_w_in_place_same_bits(z, n, rows, k, m):
+    """A workspace that holds X^T alone is accepted: W is then read in place from its
+    shards (MN-major) instead of from its transpose, with the same dX and dW bits."""
+    shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=5)
+    A = [synth.activations(m, k, device=DEV, seed_key=q) for q in range(n)]
+    dY = [synth.upstream_grad(m, rows, device=DEV, seed_key=q) for q in range(n)]
+    out = []
+    full = z.fsdp_unit_backward_workspace(n, rows, k, m)
+    x_only = (2 * k * n * m + 255) // 256 * 256
+    for size in (full, x_only):
+        dX = [torch.full((m, k), float("nan"), device=DEV) for _ in range(n)]
+        dW = torch.full((rows, k), float("nan"), device=DEV)
+        ws = torch.empty(size, dtype=torch.uint8, device=DEV)
+        z.fsdp_unit_backward(shards, A, dY, dX, dW, ws)
+        z.zero_device_status()
+        out.append((dX, dW))
+    (dXa, dWa), (dXb, dWb) = out
+    assert torch.equal(dWa.view(torch.int32), dWb.view(torch.int32))
+    for a, b in zip(dXa, dXb):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    ws = torch.empty(x_only - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(z.ZeroError) as e:
+        z.fsdp_unit_backward(shards, A, dY, out[0][0], out[0][1], ws)
+    assert e.value.code == -1
 
 
 def test_backward_rejects_small_workspace(z):
