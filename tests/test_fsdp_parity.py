@@ -356,11 +356,11 @@ def test_backward_mistral_up_sampled(z):
 
 
 def test_backward_mistral_down_sampled(z):
-    """W_down [4096, 14336] in 8 row shards of 512 rows (read in place as the dX GEMM's
-    MN-major B), 1024 tokens per rank: sampled dX and dW entries against float64 dot
-    products under the bounds."""
+    """W_down [4096, 14336] in 8 row shards of 512 rows (gathered as W^T for the dX GEMM),
+    1024 tokens per rank: sampled dX and dW entries against float64 dot products under the
+    bounds."""
     n, rows, k, m = 8, 4096, 14336, 1024
-    assert z.fsdp_unit_backward_workspace(n, rows, k, m) == 2 * k * n * m  # the in-place path
+    assert z.fsdp_unit_backward_workspace(n, rows, k, m) == 2 * k * n * m + 2 * rows * k  # dY in place
     shards, A, dY, dX, dW = run_backward(z, n, rows, k, m, key=9)
     rng = np.random.default_rng(2)
     w_full = torch.cat(shards, 0)
