@@ -660,6 +660,21 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
                                          "workspace_bytes": ws_x.numel(),
                                          "note": "workspace of X^T alone: W's shards read in place as an MN-major "
                                                  "operand of the dX GEMM (one-CTA kernel)"}
+        del shards, A, dY, dX, dW, ws, ws_x
+        # the same for W_down [4096, 14336]: X (the MLP's H) is the wider operand, so dY^T is
+        # laid out and X read in place
+        R, K = 4096, 14336
+        shards = synth.weight_shards(R, K, n, device=dev, seed_key=13)
+        A = [synth.activations(Mb, K, device=dev, seed_key=q) for q in range(n)]
+        dY = [synth.upstream_grad(Mb, R, device=dev, seed_key=q) for q in range(n)]
+        dX = [torch.empty(Mb, K, device=dev) for _ in range(n)]
+        dW = torch.empty(R, K, device=dev)
+        ws = torch.empty(z.fsdp_unit_backward_workspace(n, R, K, Mb), dtype=torch.uint8, device=dev)
+        ms = time_launches(lambda: z.fsdp_unit_backward(shards, A, dY, dX, dW, ws, stream=stream), 5, stream)
+        res["backward_down"] = {"ms": ms, "tflops": flop / ms / 1e9, "frac": flop / ms / 1e9 / tf_peak,
+                                "ranks": n, "tokens_per_rank": Mb, "workspace_bytes": ws.numel(),
+                                "note": "W^T and dY^T laid out by one transpose launch; dX on the CTA-pair kernel; "
+                                        "dW reads X in place (MN-major)"}
     except Exception as e:  # the GEMM leg must not hide the step's line
         res["error"] = str(e)[:300]
     return res

@@ -918,6 +918,14 @@ bool fsdp_fused_gather_ok(int n_ranks, int64_t rows_out) {
   return n_ranks == 1 || (rows_out / n_ranks) % (g_gemm_kernel.load() == 1 ? BN : 128) == 0;
 }
 
+int launch_fsdp_bwd_dw_x_mn(int x_pieces, const uint16_t* dYt, const uint16_t* const* X, int64_t piece_rows,
+                            int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st) {
+  const uint16_t* a1[1] = {dYt};
+  float* y1[1] = {dW};
+  return launch_gemm<false>({1, a1, false, rows_out}, {x_pieces, X, true, piece_rows}, nullptr, rows_out, k_in,
+                            piece_rows * x_pieces, y1, 1, nullptr, alpha, st, "fsdp_unit_backward");
+}
+
 int launch_fsdp_bwd_dw_alpha(const uint16_t* dY, int64_t nm, const uint16_t* Xt, int64_t rows_out, int64_t k_in,
                              float* dW, float alpha, cudaStream_t st) {
   const uint16_t* dy1[1] = {dY};

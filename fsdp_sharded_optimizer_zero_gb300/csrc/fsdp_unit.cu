@@ -16,10 +16,12 @@
 //                   workspace holds it), or read in place as an MN-major B with the shard
 //                   picked by K block (when the workspace holds only X^T). One launch over
 //                   all ranks' row pieces when M % 128 == 0, else one per rank;
-//   dW = (1/N) sum_q dY_q^T X_q   with dY_q an MN-major A, the K loop over every rank's
-//                   tokens, and X^T [K, N M] laid out in the workspace (a second MN-major
-//                   operand costs more than that transpose). W^T and X^T are laid out by
-//                   ONE launch of the transpose kernel;
+//   dW = (1/N) sum_q dY_q^T X_q   with the K loop over every rank's tokens: one of dY and X
+//                   is read in place as an MN-major operand and the other laid out
+//                   transposed in the workspace (two MN-major operands cost more than one
+//                   transpose). The narrower one is transposed: X^T [K, N M] when K <= R
+//                   (W_up: 134 against 470 MB), dY^T [R, N M] otherwise (W_down). W^T and that
+//                   transpose are laid out by ONE launch of the transpose kernel;
 // so the sum over ranks happens inside the fp32 tensor-core accumulation, and the 1/N scale
 // is applied in the epilogue. On GB300 each MN-major operand costs its GEMM 5-14 %, so
 // W^T's 44 us transpose (W_up) buys back more than it costs: 2.534 against 2.652 ms per
@@ -28,6 +30,8 @@
 // [K, R], dY^T [R, N M] and X^T [K, N M] in the workspace, then K-major GEMMs (on the
 // CTA-pair kernel). Every path gives the same bits.
 #include <string.h>
+
+#include <algorithm>
 
 #include "internal.h"
 
@@ -55,9 +59,9 @@ BackwardWorkspace backward_workspace(int n, int64_t rows_out, int64_t k_in, int6
   BackwardWorkspace w{0, 0, 0, 0, 0};
   const uint64_t R = static_cast<uint64_t>(rows_out), K = static_cast<uint64_t>(k_in);
   const uint64_t NM = static_cast<uint64_t>(n) * static_cast<uint64_t>(m_tokens);
-  if (backward_in_place(n, rows_out, k_in, m_tokens)) {  // X^T, then W^T (or W in place)
-    w.xt = 0;
-    w.wt = align256(2 * K * NM);
+  if (backward_in_place(n, rows_out, k_in, m_tokens)) {  // X^T or dY^T, then W^T (or W in place)
+    w.xt = w.dyt = 0;                                    // the one of the two that is laid out
+    w.wt = align256(2 * std::min(K, R) * NM);
     w.min_total = w.wt;
     w.total = w.wt + align256(2 * R * K);
     return w;
@@ -139,13 +143,17 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
   if (backward_in_place(n_ranks, rows_out, k_in, m_tokens)) {
     const uint16_t* const* dy = reinterpret_cast<const uint16_t* const*>(dY);
     uint8_t* base = static_cast<uint8_t*>(workspace);
-    uint16_t* xt = reinterpret_cast<uint16_t*>(base + ws.xt);
+    // the dW GEMM's laid-out operand: X^T [K, N M] when K <= R, else dY^T [R, N M]
+    const bool t_dy = k_in > rows_out;
+    uint16_t* tr = reinterpret_cast<uint16_t*>(base + ws.xt);
+    const GradPtrs& tsrc = t_dy ? dyp : ap;
+    const int64_t tcols = t_dy ? rows_out : k_in;
     int rc;
     if (workspace_bytes >= ws.total) {
-      // W^T [K, R] (the backward all-gather, transposed) and X^T [K, N M] in one launch
+      // W^T [K, R] (the backward all-gather, transposed) and the dW operand in one launch
       uint16_t* wt = reinterpret_cast<uint16_t*>(base + ws.wt);
-      cudaError_t e = launch_transpose_cat2(wp, n_ranks, rows_out / n_ranks, k_in, wt, ap, n_ranks, m_tokens, k_in,
-                                            xt, st);
+      cudaError_t e = launch_transpose_cat2(wp, n_ranks, rows_out / n_ranks, k_in, wt, tsrc, n_ranks, m_tokens, tcols,
+                                            tr, st);
       if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
       // dX_q [M, K] = dY_q [M, R] * (W^T [K, R])^T, both operands K-major
       const uint16_t* wt1[1] = {wt};
@@ -165,12 +173,15 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
         for (int q = 0; q < n_ranks; ++q)
           if ((rc = launch_fsdp_bwd_dx(n_ranks, dy + q, m_tokens, 1, wsh, rows_out, k_in, dX + q, st))) return rc;
       }
-      cudaError_t e = launch_transpose_cat(ap, n_ranks, m_tokens, k_in, xt, st);
+      cudaError_t e = launch_transpose_cat(tsrc, n_ranks, m_tokens, tcols, tr, st);
       if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
     }
-    // dW = (1/N) sum_q dY_q^T X_q: the K loop runs over every rank's tokens in turn, dY
-    // read in place, X from its rank-concatenated transpose
-    return launch_fsdp_bwd_dw(n_ranks, dy, xt, m_tokens, rows_out, k_in, dW, st);
+    // dW = (1/N) sum_q dY_q^T X_q: the K loop runs over every rank's tokens in turn, one
+    // operand read in place (MN-major), the other from its rank-concatenated transpose
+    if (t_dy)
+      return launch_fsdp_bwd_dw_x_mn(n_ranks, tr, reinterpret_cast<const uint16_t* const*>(A), m_tokens, rows_out,
+                                     k_in, dW, 1.0f / static_cast<float>(n_ranks), st);
+    return launch_fsdp_bwd_dw(n_ranks, dy, tr, m_tokens, rows_out, k_in, dW, st);
   }
   uint8_t* base = static_cast<uint8_t*>(workspace);
   uint16_t* wt = reinterpret_cast<uint16_t*>(base + ws.wt);

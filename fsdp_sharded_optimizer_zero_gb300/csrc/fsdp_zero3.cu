@@ -10,18 +10,19 @@
 // loads (the default: no copy of W exists at all), or, with FSDP_GATHER_MATERIALIZE, by a
 // gather kernel into a workspace slot that plays the all-gather's receive buffer. The
 // backward's gather always lands W^T [K, R] in a slot (a transposing gather, in the same
-// launch as the X^T layout the dW GEMM reads), so that dX is a K-major GEMM on the CTA-pair
-// kernel: on GB300 an MN-major operand costs a GEMM 5-14 %, more than the transpose. The
+// launch as the dW GEMM's laid-out operand: X^T [K, N M], or dY^T [R, N M] when K > R, the
+// other one read in place), so that dX is a K-major GEMM on the CTA-pair kernel: on GB300 an
+// MN-major operand costs a GEMM 5-14 %, more than the transpose. The
 // reduce of the reduce-scatter happens inside the dW GEMM's fp32 accumulation (its K loop
 // runs over every rank's tokens), so rank r's reduce-scattered gradient is simply rows
 // [r R/N, (r+1) R/N) of dW, contiguous with its flat-parameter shard.
 //
 // Overlap ([Interview] follow-up "FSDP 怎么把通信藏起来?": the all-gather on its own CUDA
 // stream, the backward prefetching the next unit's): with FSDP_BACKWARD_PREFETCH and a
-// prefetch stream, unit i-1's gather and its X^T layout (the dW GEMM's operand) are issued
-// on the prefetch stream as soon as unit i's backward starts, into the other of two slots;
-// events order each slot's reuse and each unit's start. Forward prefetch stays off (the
-// pages' default).
+// prefetch stream, unit i-1's gather and its dW operand layout are issued on the prefetch
+// stream once unit i's dX GEMM is enqueued (when that operand is dY^T, it waits for the dX
+// GEMM that writes dY_{i-1}), into the other of two slots; events order each slot's reuse
+// and each unit's start. Forward prefetch stays off (the pages' default).
 //
 // Ordering inside a unit's backward: dX (reads W_i) and dW, then Adam writes the new W_i
 // shards. Unit i's W is not read again in this step (unit i-1's backward reads W_{i-1} and
@@ -44,7 +45,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 struct Zero3Workspace {
   int slots;                // 2 with backward prefetch, else 1
-  uint64_t xt_off[2];       // X^T [k_in, N M] bf16 of the unit in the slot
+  uint64_t xt_off[2];       // the unit's X^T [k_in, N M] or dY^T [rows_out, N M] bf16 (the narrower)
   uint64_t w_off[2];        // the unit's gathered W^T [k_in, rows_out] (backward) or W (materialised forward)
   uint64_t total;
 };
@@ -54,7 +55,7 @@ Zero3Workspace zero3_workspace(int n, int n_units, const fsdp_unit_state* u, int
   memset(&w, 0, sizeof(w));
   uint64_t kmax = 0, wmax = 0;
   for (int i = 0; i < n_units; ++i) {
-    kmax = std::max<uint64_t>(kmax, static_cast<uint64_t>(u[i].k_in));
+    kmax = std::max<uint64_t>(kmax, static_cast<uint64_t>(std::min(u[i].k_in, u[i].rows_out)));
     wmax = std::max<uint64_t>(wmax, static_cast<uint64_t>(u[i].rows_out) * static_cast<uint64_t>(u[i].k_in));
   }
   w.slots = (flags & FSDP_BACKWARD_PREFETCH) ? 2 : 1;
@@ -102,10 +103,12 @@ int check_units(int n, int n_units, const fsdp_unit_state* u, int64_t m, int fla
     const fsdp_unit_state& s = u[i];
     if (s.rows_out < 1 || s.k_in < 1 || s.rows_out > (1 << 30) || s.k_in > (1 << 30))
       return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: sizes outside 1..2^30", kWho, i);
-    if (s.rows_out % n || s.rows_out % 64 || s.k_in % 8)
+    // the dW GEMM reads the wider of dY [N M, rows_out] and X [N M, k_in] in place as an
+    // MN-major operand, whose rows must be whole 64-column chunks
+    if (s.rows_out % n || s.rows_out % 8 || s.k_in % 8 || std::max(s.rows_out, s.k_in) % 64)
       return set_error(ZERO_ERR_INVALID_ARG,
-                       "%s: unit %d: needs rows_out a multiple of 64 and of n_ranks, k_in a multiple of 8 (got %lld, "
-                       "%d, %lld)",
+                       "%s: unit %d: needs rows_out a multiple of n_ranks and of 8, k_in a multiple of 8, and the "
+                       "larger of the two a multiple of 64 (got %lld, %d, %lld)",
                        kWho, i, (long long)s.rows_out, n, (long long)s.k_in);
     if (!(flags & FSDP_GATHER_MATERIALIZE) && !fsdp_fused_gather_ok(n, s.rows_out))
       return set_error(ZERO_ERR_INVALID_ARG,
@@ -167,11 +170,15 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
   uint8_t* base = static_cast<uint8_t*>(workspace);
   auto xt_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.xt_off[i % ws.slots]); };
   auto w_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.w_off[i % ws.slots]); };
-  // events: [0] forward done, [1 + i] unit i's operands ready, [1 + L + i] unit i's backward done
+  // events: [0] forward done, [1 + i] unit i's operands ready, [1 + L + i] unit i's backward
+  // done, [1 + 2L + i] unit i's dX GEMM done (it writes dY_{i-1})
   cudaEvent_t* ev = nullptr;
-  if (overlap && (rc = get_events(static_cast<size_t>(2 * L + 1), &ev))) return rc;
+  if (overlap && (rc = get_events(static_cast<size_t>(3 * L + 1), &ev))) return rc;
   const auto ev_ready = [&](int i) { return ev[1 + i]; };
   const auto ev_done = [&](int i) { return ev[1 + L + i]; };
+  const auto ev_dx = [&](int i) { return ev[1 + 2 * L + i]; };
+  // the dW GEMM's laid-out operand: X^T when k_in <= rows_out, else dY^T
+  const auto t_dy = [&](int i) { return units[i].k_in > units[i].rows_out; };
 
   // the N row shards of unit i (rank r's rows at r R/N), or its gathered copy
   const uint16_t* shard_ptrs[kGemmMaxPieces];
@@ -210,20 +217,22 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
   }
 
   // ---- backward, last -> unit 0 ----
-  // unit i's operands: W_i^T [k_in, rows_out] gathered from its shards and X_i^T [k_in, N M],
-  // both laid out by one launch
+  // unit i's operands: W_i^T [k_in, rows_out] gathered from its shards and the narrower of
+  // X_i^T [k_in, N M] and dY_i^T [rows_out, N M], both laid out by one launch
   auto prepare = [&](int i, cudaStream_t s) {
     int r = ZERO_OK;
     if (overlap && i + ws.slots < L && (r = wait(s, ev_done(i + ws.slots)))) return r;  // slot reuse
+    if (overlap && t_dy(i) && i + 1 < L && (r = wait(s, ev_dx(i + 1)))) return r;       // dY_i written
     const fsdp_unit_state& u = units[i];
-    GradPtrs wsrc, xsrc;
+    GradPtrs wsrc, tsrc;
     memset(&wsrc, 0, sizeof(wsrc));
-    memset(&xsrc, 0, sizeof(xsrc));
+    memset(&tsrc, 0, sizeof(tsrc));
     const uint16_t* const* sh = shards_of(i);
     for (int q = 0; q < n; ++q) wsrc.p[q] = sh[q];
-    xsrc.p[0] = u.x;
+    tsrc.p[0] = t_dy(i) ? u.dy : u.x;
+    const int64_t tcols = t_dy(i) ? u.rows_out : u.k_in;
     const cudaError_t e =
-        launch_transpose_cat2(wsrc, n, u.rows_out / n, u.k_in, w_slot(i), xsrc, 1, nm, u.k_in, xt_slot(i), s);
+        launch_transpose_cat2(wsrc, n, u.rows_out / n, u.k_in, w_slot(i), tsrc, 1, nm, tcols, xt_slot(i), s);
     if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", kWho, cudaGetErrorString(e));
     return overlap ? record(ev_ready(i), s) : ZERO_OK;
   };
@@ -235,7 +244,6 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
     const fsdp_unit_state& s = units[i];
     if (overlap) {
       if ((rc = wait(st, ev_ready(i)))) return rc;
-      if (i > 0 && (rc = prepare(i - 1, pf))) return rc;  // overlaps this unit's GEMMs
     } else if ((rc = prepare(i, st))) {
       return rc;
     }
@@ -243,9 +251,20 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
     const uint16_t* wt1[1] = {w_slot(i)};
     zero_bf16* dx = i > 0 ? units[i - 1].dy : dx_out;
     if (dx && (rc = launch_fsdp_gemm(1, wt1, s.k_in, s.rows_out, s.dy, nm, nullptr, dx, 1.0f, st))) return rc;
-    if ((rc = launch_fsdp_bwd_dw_alpha(s.dy, nm, xt_slot(i), s.rows_out, s.k_in, s.dw,
-                                       1.0f / static_cast<float>(n), st)))
-      return rc;
+    if (overlap) {
+      if ((rc = record(ev_dx(i), st))) return rc;
+      if (i > 0 && (rc = prepare(i - 1, pf))) return rc;  // overlaps this unit's dW GEMM and Adam
+    }
+    // dW = (1/N) dY_i^T X_i: X^T laid out and dY read in place, or dY^T laid out and X read
+    // in place, whichever of the two is narrower
+    const float inv_n = 1.0f / static_cast<float>(n);
+    if (t_dy(i)) {
+      const uint16_t* x1[1] = {s.x};
+      rc = launch_fsdp_bwd_dw_x_mn(1, xt_slot(i), x1, nm, s.rows_out, s.k_in, s.dw, inv_n, st);
+    } else {
+      rc = launch_fsdp_bwd_dw_alpha(s.dy, nm, xt_slot(i), s.rows_out, s.k_in, s.dw, inv_n, st);
+    }
+    if (rc) return rc;
     // each rank's Adam on its shard (rows r R/N .. of dW): every rank's shard in one launch
     if ((rc = zero_adam_step(s.plan, ZERO_ALL_RANKS, s.dw, s.master, s.m, s.v, s.w, hp, step, stream))) return rc;
     if (overlap && (rc = record(ev_done(i), st))) return rc;

@@ -92,6 +92,12 @@ int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces
                        cudaStream_t st);
 int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* Xt, int64_t m_tokens,
                        int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st);
+// dW = alpha sum_q dY_q^T X_q with dY^T [R, N M] laid out (a K-major A) and X read in place
+// as an MN-major B in x_pieces pieces of piece_rows token rows (each rank's X_q, or one
+// contiguous [N M, K]), the K loop over the tokens: the cheaper form when X is the wider of
+// the two (K > R). Same bits as the form above.
+int launch_fsdp_bwd_dw_x_mn(int x_pieces, const uint16_t* dYt, const uint16_t* const* X, int64_t piece_rows,
+                            int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st);
 // dW over one contiguous dY for all ranks (rank q's rows at q M): dW [R, K] = alpha dY^T
 // [R, NM] (X^T [K, NM])^T with dY read in place as one MN-major piece. Bit-identical to the
 // per-rank form above.

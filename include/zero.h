@@ -288,11 +288,13 @@ ZERO_API int fsdp_transpose_cat(int n_srcs, const zero_bf16* const srcs[], int64
 
 /* Bytes of device workspace fsdp_unit_backward needs for transposed operand copies, each
  * rounded up to 256 bytes. When R/N, k_in and m_tokens are multiples of 64 and N <= 16,
- * dY is read in place (an MN-major tensor-core operand) and the workspace holds X^T
- * (2*K*N*M) and W^T (2*R*K), the backward all-gather of W laid out transposed; a workspace
- * that holds X^T alone is also accepted, and W is then read in place from its shards as an
- * MN-major operand (same results, about 4 % slower on GB300). Other shapes need W^T,
- * dY^T (2*R*N*M) and X^T. This call returns the size of the fastest path. */
+ * the dW GEMM reads the wider of dY and X in place (an MN-major tensor-core operand) and
+ * the workspace holds the transpose of the narrower one (X^T, 2*K*N*M bytes, when K <= R;
+ * else dY^T, 2*R*N*M) followed by W^T (2*R*K), the backward all-gather of W laid out
+ * transposed; a workspace that holds the first part alone is also accepted, and W is then
+ * read in place from its shards as an MN-major operand (same results, about 4 % slower on
+ * GB300). Other shapes need W^T, dY^T and X^T. This call returns the size of the fastest
+ * path. */
 ZERO_API int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t k_in, int64_t m_tokens,
                                           uint64_t* bytes);
 
@@ -366,9 +368,10 @@ typedef struct {
                                      backward GEMMs run on `stream` */
 
 /* Bytes of device workspace fsdp_zero3_step needs for these units, M tokens per rank and
- * flags: one slot (two with FSDP_BACKWARD_PREFETCH) holding X^T [k_in, N*M] bf16 of the
- * widest input and the gathered W^T (or W) of the largest unit, 2*rows_out*k_in bytes; each
- * part rounded up to 256 bytes. Only the units' sizes are read. */
+ * flags: one slot (two with FSDP_BACKWARD_PREFETCH) holding the dW GEMM's laid-out operand
+ * (X^T [k_in, N*M] or dY^T [rows_out, N*M], the narrower: 2*min(rows_out, k_in)*N*M bytes,
+ * the largest over the units) and the gathered W^T (or W) of the largest unit,
+ * 2*rows_out*k_in bytes; each part rounded up to 256 bytes. Only the units' sizes are read. */
 ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit_state* units, int64_t m_tokens,
                                        int flags, uint64_t* bytes);
 
@@ -379,7 +382,8 @@ ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit
  *     with y_out NULL that product is skipped), W_i freed;
  *   backward, last -> unit 0: gather W_i again, as W_i^T into a workspace slot (with
  *     X_i^T, in one launch), dY_{i-1} = bf16(dY_i W_i) (unit 0: into dx_out, skipped when
- *     NULL) with both GEMM operands K-major, dW_i = (1/N) sum_q dY_{i,q}^T X_{i,q} (the reduce of the
+ *     NULL) with both GEMM operands K-major, dW_i = (1/N) sum_q dY_{i,q}^T X_{i,q} (the narrower
+ *     of X_i and dY_i laid out transposed in the same launch as W_i^T, the other read in place; the reduce of the
  *     reduce-scatter inside the fp32 tensor-core accumulation, rank r keeping its rows),
  *     then each rank's Adam on its shard (zero_adam_step, ZERO_ALL_RANKS: every rank's
  *     shard in one launch) writing the new bf16 shards of W_i — after W_i's last use;
@@ -391,7 +395,8 @@ ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit
  * bf16 products in an unspecified order (bounds as fsdp_unit_backward), rounded once to
  * bf16; Adam is bit-exact as zero_adam_step.
  * Requires 1 <= N <= 16, 1 <= n_units <= 64, N*M % 8 == 0; per unit rows_out a multiple of
- * 64 and of N, k_in % 8 == 0, and without FSDP_GATHER_MATERIALIZE the fused gather's shard
+ * N and of 8, k_in % 8 == 0, the larger of rows_out and k_in a multiple of 64 (the dW GEMM
+ * reads that operand, dY or X, in place), and without FSDP_GATHER_MATERIALIZE the fused gather's shard
  * rule ((rows_out / N) % 128 == 0; 256 under zero_set_gemm_kernel(1)); 16-byte-aligned
  * buffers; workspace of fsdp_zero3_step_workspace() bytes. prefetch_stream may be NULL
  * (then everything runs on `stream`). */

@@ -360,7 +360,7 @@ def test_backward_mistral_down_sampled(z):
     1024 tokens per rank: sampled dX and dW entries against float64 dot products under the
     bounds."""
     n, rows, k, m = 8, 4096, 14336, 1024
-    assert z.fsdp_unit_backward_workspace(n, rows, k, m) == 2 * k * n * m + 2 * rows * k  # dY in place
+    assert z.fsdp_unit_backward_workspace(n, rows, k, m) == 2 * rows * n * m + 2 * rows * k  # X read in place
     shards, A, dY, dX, dW = run_backward(z, n, rows, k, m, key=9)
     rng = np.random.default_rng(2)
     w_full = torch.cat(shards, 0)
@@ -389,16 +389,17 @@ def test_backward_mistral_down_sampled(z):
 
 
 @pytest.mark.parametrize("n,rows,k,m", [(4, 512, 256, 128), (5, 320, 192, 192), (8, 2048, 512, 64),
-                                        (8, 3584, 128, 512)])
+                                        (8, 3584, 128, 512), (4, 256, 1024, 128), (8, 512, 2048, 64)])
 def test_backward_x_only_workspace_reads_w_in_place_same_bits(z, n, rows, k, m):
-    """A workspace that holds X^T alone is accepted: W is then read in place from its
-    shards (MN-major) instead of from its transpose, with the same dX and dW bits."""
+    """A workspace that holds only the dW operand's transpose (X^T, or dY^T when k > rows)
+    is accepted: W is then read in place from its shards (MN-major) instead of from its
+    transpose, with the same dX and dW bits."""
     shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=5)
     A = [synth.activations(m, k, device=DEV, seed_key=q) for q in range(n)]
     dY = [synth.upstream_grad(m, rows, device=DEV, seed_key=q) for q in range(n)]
     out = []
     full = z.fsdp_unit_backward_workspace(n, rows, k, m)
-    x_only = (2 * k * n * m + 255) // 256 * 256
+    x_only = (2 * min(k, rows) * n * m + 255) // 256 * 256
     for size in (full, x_only):
         dX = [torch.full((m, k), float("nan"), device=DEV) for _ in range(n)]
         dW = torch.full((rows, k), float("nan"), device=DEV)
@@ -414,6 +415,29 @@ def test_backward_x_only_workspace_reads_w_in_place_same_bits(z, n, rows, k, m):
     with pytest.raises(z.ZeroError) as e:
         z.fsdp_unit_backward(shards, A, dY, out[0][0], out[0][1], ws)
     assert e.value.code == -1
+
+
+@pytest.mark.parametrize("n,rows,k,m", [(8, 512, 2048, 128), (4, 1024, 256, 192)])
+def test_backward_dw_equals_k_major_product_of_transposes(z, n, rows, k, m):
+    """dW does not depend on which operand is laid out: fsdp_unit_backward's dW (dY^T laid
+    out and X read in place when k > rows, else X^T laid out and dY read in place) equals,
+    bit for bit, the K-major product dY^T (X^T)^T of both transposes through
+    fsdp_unit_forward, scaled by 1/N (exact for N a power of two)."""
+    shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=8)
+    A = [synth.activations(m, k, device=DEV, seed_key=q) for q in range(n)]
+    dY = [synth.upstream_grad(m, rows, device=DEV, seed_key=q) for q in range(n)]
+    dX = [torch.empty(m, k, device=DEV) for _ in range(n)]
+    dW = torch.empty(rows, k, device=DEV)
+    ws = torch.empty(z.fsdp_unit_backward_workspace(n, rows, k, m), dtype=torch.uint8, device=DEV)
+    z.fsdp_unit_backward(shards, A, dY, dX, dW, ws)
+    dyt = torch.empty(rows, n * m, dtype=torch.bfloat16, device=DEV)
+    xt = torch.empty(k, n * m, dtype=torch.bfloat16, device=DEV)
+    z.fsdp_transpose_cat(dY, dyt)
+    z.fsdp_transpose_cat(A, xt)
+    ref = torch.empty(rows, k, device=DEV)
+    z.fsdp_unit_forward([xt], dyt, ref)
+    z.zero_device_status()
+    assert torch.equal(dW.view(torch.int32), (ref * (1.0 / n)).view(torch.int32))
 
 
 def test_backward_rejects_small_workspace(z):
