@@ -520,9 +520,9 @@ def zero3_units(z, synth, dev, n, m, shapes=ZERO3_SHAPES):
 def zero3_leg(z, synth, dev, tf_peak, hbm_peak, stream):
     """One ZeRO-3 training step over 4 FSDP units with the Mistral-7B MLP shapes, N = 8
     ranks of 1024 tokens (8192 in all): forward, backward in reverse with each rank's Adam
-    on its shard after the unit's backward. Timed serial and with the next unit's gather /
-    X^T layout prefetched on a second stream, with the gather fused into the GEMM loads and
-    materialised into a workspace slot."""
+    on its shard after the unit's backward. Timed serial, with the next unit's gather and
+    dW operand layout prefetched on a second stream, with each unit's Adam on that stream
+    beside the next units' GEMMs, and with the forward gather materialised."""
     import torch
     n, m = 8, 1024
     res = {"units": [list(s) for s in ZERO3_SHAPES], "n_ranks": n, "tokens_per_rank": m}
@@ -536,9 +536,10 @@ def zero3_leg(z, synth, dev, tf_peak, hbm_peak, stream):
         adam_bytes = sum(30 * R * K for R, K in ZERO3_SHAPES)
         res["gemm_flop_per_step"] = flop
         res["adam_bytes_per_step"] = adam_bytes
-        for name, flags, pf in (("serial", 0, None), ("prefetch", z.FSDP_BACKWARD_PREFETCH, side),
-                                ("materialized_serial", z.FSDP_GATHER_MATERIALIZE, None),
-                                ("materialized_prefetch", z.FSDP_GATHER_MATERIALIZE | z.FSDP_BACKWARD_PREFETCH, side)):
+        P, O, G = z.FSDP_BACKWARD_PREFETCH, z.FSDP_OVERLAP_OPTIMIZER, z.FSDP_GATHER_MATERIALIZE
+        for name, flags, pf in (("serial", 0, None), ("prefetch", P, side), ("overlap_optimizer", O, side),
+                                ("prefetch_overlap_optimizer", P | O, side),
+                                ("materialized_serial", G, None), ("materialized_prefetch", G | P, side)):
             ws = torch.empty(z.fsdp_zero3_step_workspace(n, ZERO3_SHAPES, m, flags), dtype=torch.uint8, device=dev)
             t = [0]
 
@@ -553,6 +554,7 @@ def zero3_leg(z, synth, dev, tf_peak, hbm_peak, stream):
             del ws
         z.zero_device_status(stream)
         res["prefetch_gain"] = res["serial"]["ms"] / res["prefetch"]["ms"] - 1.0
+        res["overlap_optimizer_gain"] = res["serial"]["ms"] / res["overlap_optimizer"]["ms"] - 1.0
         res["materialized_prefetch_gain"] = (res["materialized_serial"]["ms"] / res["materialized_prefetch"]["ms"]
                                              - 1.0)
         res["note"] = ("tflops counts the 12 GEMMs' flops (6 N M R K per unit) over the whole step, which also holds "
@@ -1116,11 +1118,11 @@ def run_case(args):
         out.update(R=R, K=K, n_ranks=n, gather_ms=ms_g, transpose_ms=ms_t, bytes=byts,
                    gather_gbs=byts / ms_g / 1e6, transpose_gbs=byts / ms_t / 1e6)
     elif args.case == "zero3_step":
-        # one ZeRO-3 step over the 4 Mistral-shaped units, N = 8 ranks x 1024 tokens, with the
-        # prefetch stream (about 7 GB on the device), 3 steps
+        # one ZeRO-3 step over the 4 Mistral-shaped units, N = 8 ranks x 1024 tokens, each
+        # unit's Adam on a second stream (about 7 GB on the device), 3 steps
         n, m = 8, 1024
         units = zero3_units(z, synth, dev, n, m)
-        flags = z.FSDP_BACKWARD_PREFETCH
+        flags = z.FSDP_OVERLAP_OPTIMIZER
         ws = torch.empty(z.fsdp_zero3_step_workspace(n, ZERO3_SHAPES, m, flags), dtype=torch.uint8, device=dev)
         y = torch.empty(n * m, ZERO3_SHAPES[-1][0], dtype=torch.bfloat16, device=dev)
         dx = torch.empty(n * m, ZERO3_SHAPES[0][1], dtype=torch.bfloat16, device=dev)

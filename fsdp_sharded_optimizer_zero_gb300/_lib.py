@@ -67,6 +67,7 @@ class fsdp_unit_state(C.Structure):
 
 FSDP_GATHER_MATERIALIZE = 1
 FSDP_BACKWARD_PREFETCH = 2
+FSDP_OVERLAP_OPTIMIZER = 4
 
 
 class zero_adam(C.Structure):

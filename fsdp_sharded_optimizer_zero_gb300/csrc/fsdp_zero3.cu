@@ -26,7 +26,11 @@
 //
 // Ordering inside a unit's backward: dX (reads W_i) and dW, then Adam writes the new W_i
 // shards. Unit i's W is not read again in this step (unit i-1's backward reads W_{i-1} and
-// the dY that unit i produced from the old W_i), so the update can follow each unit.
+// the dY that unit i produced from the old W_i), so the update can follow each unit. With
+// FSDP_OVERLAP_OPTIMIZER that Adam runs on the prefetch stream once unit i's dW is done,
+// beside the following units' GEMMs: the update kernel is HBM bound and uses no shared
+// memory, so it fits on the SMs next to a persistent GEMM, which leaves most of the DRAM
+// bandwidth idle.
 #include <string.h>
 
 #include <algorithm>
@@ -97,7 +101,7 @@ int check_units(int n, int n_units, const fsdp_unit_state* u, int64_t m, int fla
   if (!u) return set_error(ZERO_ERR_INVALID_ARG, "%s: units is NULL", kWho);
   if (m < 1 || (static_cast<int64_t>(n) * m) % 8)
     return set_error(ZERO_ERR_INVALID_ARG, "%s: n_ranks * m_tokens must be a positive multiple of 8", kWho);
-  if (flags & ~(FSDP_GATHER_MATERIALIZE | FSDP_BACKWARD_PREFETCH))
+  if (flags & ~(FSDP_GATHER_MATERIALIZE | FSDP_BACKWARD_PREFETCH | FSDP_OVERLAP_OPTIMIZER))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: unknown flags 0x%x", kWho, flags);
   for (int i = 0; i < n_units; ++i) {
     const fsdp_unit_state& s = u[i];
@@ -162,18 +166,19 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
                      kWho, workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.total);
   const bool materialize = (flags & FSDP_GATHER_MATERIALIZE) != 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaStream_t pf = ((flags & FSDP_BACKWARD_PREFETCH) && prefetch_stream)
-                        ? reinterpret_cast<cudaStream_t>(prefetch_stream)
-                        : st;
+  cudaStream_t side = prefetch_stream ? reinterpret_cast<cudaStream_t>(prefetch_stream) : st;
+  cudaStream_t pf = (flags & FSDP_BACKWARD_PREFETCH) ? side : st;
   const bool overlap = pf != st;
+  const bool adam_side = (flags & FSDP_OVERLAP_OPTIMIZER) && side != st;
   const int64_t nm = static_cast<int64_t>(n) * m_tokens;
   uint8_t* base = static_cast<uint8_t*>(workspace);
   auto xt_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.xt_off[i % ws.slots]); };
   auto w_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.w_off[i % ws.slots]); };
   // events: [0] forward done, [1 + i] unit i's operands ready, [1 + L + i] unit i's backward
-  // done, [1 + 2L + i] unit i's dX GEMM done (it writes dY_{i-1})
+  // GEMMs done (its slot is free), [1 + 2L + i] unit i's dX GEMM done (it writes dY_{i-1}),
+  // [1 + 3L] the side stream's last launch
   cudaEvent_t* ev = nullptr;
-  if (overlap && (rc = get_events(static_cast<size_t>(3 * L + 1), &ev))) return rc;
+  if ((overlap || adam_side) && (rc = get_events(static_cast<size_t>(3 * L + 2), &ev))) return rc;
   const auto ev_ready = [&](int i) { return ev[1 + i]; };
   const auto ev_done = [&](int i) { return ev[1 + L + i]; };
   const auto ev_dx = [&](int i) { return ev[1 + 2 * L + i]; };
@@ -265,10 +270,22 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
       rc = launch_fsdp_bwd_dw_alpha(s.dy, nm, xt_slot(i), s.rows_out, s.k_in, s.dw, inv_n, st);
     }
     if (rc) return rc;
-    // each rank's Adam on its shard (rows r R/N .. of dW): every rank's shard in one launch
-    if ((rc = zero_adam_step(s.plan, ZERO_ALL_RANKS, s.dw, s.master, s.m, s.v, s.w, hp, step, stream))) return rc;
-    if (overlap && (rc = record(ev_done(i), st))) return rc;
+    if ((overlap || adam_side) && (rc = record(ev_done(i), st))) return rc;
+    // each rank's Adam on its shard (rows r R/N .. of dW): every rank's shard in one launch,
+    // on `stream` or, overlapped, on the side stream after this unit's dW
+    if (adam_side) {
+      if ((rc = wait(side, ev_done(i))) ||
+          (rc = zero_adam_step(s.plan, ZERO_ALL_RANKS, s.dw, s.master, s.m, s.v, s.w, hp, step,
+                               reinterpret_cast<zero_stream_t>(side))))
+        return rc;
+    } else if ((rc = zero_adam_step(s.plan, ZERO_ALL_RANKS, s.dw, s.master, s.m, s.v, s.w, hp, step, stream))) {
+      return rc;
+    }
   }
-  // every prefetch-stream launch was awaited by `stream` (unit 0's operands were the last)
+  // join: `stream` waits for the side stream's last launch (its last Adam; without Adam on
+  // it, unit 0's operands, which `stream` has already awaited)
+  if (overlap || adam_side) {
+    if ((rc = record(ev[1 + 3 * L], side)) || (rc = wait(st, ev[1 + 3 * L]))) return rc;
+  }
   return ZERO_OK;
 }

@@ -364,8 +364,10 @@ typedef struct {
                                      receive buffer: sharded model + the unit in use), reused after the unit;
                                      without it the forward GEMM reads every tile straight from its shard.
                                      The backward always gathers W^T into the slot (below). */
-#define FSDP_BACKWARD_PREFETCH 2  /* issue unit i-1's gather and X^T layout on prefetch_stream while unit i's
-                                     backward GEMMs run on `stream` */
+#define FSDP_BACKWARD_PREFETCH 2  /* issue unit i-1's gather and dW operand layout on prefetch_stream while
+                                     unit i's backward GEMMs run on `stream` */
+#define FSDP_OVERLAP_OPTIMIZER 4  /* run unit i's Adam on prefetch_stream once its dW is done, beside the
+                                     following units' backward GEMMs on `stream` */
 
 /* Bytes of device workspace fsdp_zero3_step needs for these units, M tokens per rank and
  * flags: one slot (two with FSDP_BACKWARD_PREFETCH) holding the dW GEMM's laid-out operand
@@ -387,9 +389,11 @@ ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit
  *     reduce-scatter inside the fp32 tensor-core accumulation, rank r keeping its rows),
  *     then each rank's Adam on its shard (zero_adam_step, ZERO_ALL_RANKS: every rank's
  *     shard in one launch) writing the new bf16 shards of W_i — after W_i's last use;
- *   with FSDP_BACKWARD_PREFETCH, unit i-1's gather and X^T layout run on prefetch_stream
- *     while unit i computes ([Interview] follow-up "FSDP 怎么把通信藏起来?": the all-gather
- *     on its own stream, the backward prefetching the next unit's).
+ *   with FSDP_BACKWARD_PREFETCH, unit i-1's gather and dW operand layout run on
+ *     prefetch_stream while unit i computes ([Interview] follow-up "FSDP 怎么把通信藏起来?":
+ *     the all-gather on its own stream, the backward prefetching the next unit's);
+ *   with FSDP_OVERLAP_OPTIMIZER, unit i's Adam runs on prefetch_stream after its dW, while
+ *     the backward of the units below it runs on `stream`.
  * All work is ordered on `stream` by the time the call returns (prefetch_stream joins it).
  * Results do not depend on the flags (same bits). dX / dY products are fp32 sums of exact
  * bf16 products in an unspecified order (bounds as fsdp_unit_backward), rounded once to

@@ -164,17 +164,18 @@ def test_zero3_step_every_buffer_vs_oracle(z, n, shapes, m, flags):
     units = make_units(z, n, shapes, m, key=len(shapes) + n)
     for t in (1, 2):  # the second step's forward reads the shards the first one wrote
         before = snapshot(units)
-        y_out, dx_out = run_step(z, units, m, t, flags | z.FSDP_BACKWARD_PREFETCH)
+        y_out, dx_out = run_step(z, units, m, t, flags | z.FSDP_BACKWARD_PREFETCH | z.FSDP_OVERLAP_OPTIMIZER)
         check_step(z, n, m, before, units, y_out, dx_out, t)
 
 
 @pytest.mark.parametrize("n,shapes,m", [(4, [(512, 256), (1024, 512), (512, 1024)], 96), (2, [(256, 64), (256, 256)], 200)])
 def test_zero3_step_flags_give_the_same_bits(z, n, shapes, m):
-    """Fused or materialised gather, serial or with the prefetch stream: same bits in every
-    buffer, over two steps."""
+    """Fused or materialised gather, serial, with the prefetch stream, with Adam on the side
+    stream: same bits in every buffer, over two steps."""
     base = make_units(z, n, shapes, m, key=7)
     results = []
-    for flags, prefetch in ((0, False), (2, True), (1, False), (3, True), (2, False)):
+    for flags, prefetch in ((0, False), (2, True), (1, False), (3, True), (2, False), (4, True), (6, True), (7, True),
+                            (4, False)):
         units = clone_units(base)
         for t in (1, 2):
             y_out, dx_out = run_step(z, units, m, t, flags, prefetch=prefetch)
