@@ -490,9 +490,21 @@ def extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args):
                                    "bytes": b_mg, "params_per_s": P / ms_mg * 1e3}
     del grads32, master, m, v, param
     torch.cuda.empty_cache()
-    legs["fsdp_unit_forward"] = fsdp_leg(z, synth, dev, tf_burst, peak_src, stream)
+    # the tensor-core legs are compared with the burst bf16 peak (a short cuBLAS loop on a
+    # cool GPU): let the GPU idle for a moment after the seconds of HBM streaming above, and
+    # record the SM clocks each of them ran at
+    gpu = torch.cuda.current_device()
+    time.sleep(args.leg_idle_s)
+    with ClockSampler(gpu) as clk:
+        legs["fsdp_unit_forward"] = fsdp_leg(z, synth, dev, tf_burst, peak_src, stream)
+    legs["fsdp_unit_forward"]["clocks"] = clk.summary()
+    legs["fsdp_unit_forward"]["idle_before_s"] = args.leg_idle_s
     torch.cuda.empty_cache()
-    legs["fsdp_zero3_step"] = zero3_leg(z, synth, dev, tf_burst, hbm_peak, stream)
+    time.sleep(args.leg_idle_s)
+    with ClockSampler(gpu) as clk:
+        legs["fsdp_zero3_step"] = zero3_leg(z, synth, dev, tf_burst, hbm_peak, stream)
+    legs["fsdp_zero3_step"]["clocks"] = clk.summary()
+    legs["fsdp_zero3_step"]["idle_before_s"] = args.leg_idle_s
     return legs
 
 
@@ -1168,6 +1180,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--leg-idle-s", type=float, default=2.0,
+                    help="seconds the GPU idles before each tensor-core leg group")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.sweep:
         args.warmup = 3
