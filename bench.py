@@ -505,6 +505,15 @@ def extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args):
         legs["fsdp_zero3_step"] = zero3_leg(z, synth, dev, tf_burst, hbm_peak, stream)
     legs["fsdp_zero3_step"]["clocks"] = clk.summary()
     legs["fsdp_zero3_step"]["idle_before_s"] = args.leg_idle_s
+    # beside each fraction of the burst bf16 peak, the fraction of the sustained one (the
+    # same cuBLAS GEMM looped for seconds under the power cap): these legs run for tens of
+    # milliseconds after seconds of other work, and the tensor-core kernels reach the power
+    # cap themselves
+    tf_sust = peaks()[2]
+    for leg in (legs["fsdp_unit_forward"], legs["fsdp_zero3_step"]):
+        for v in leg.values():
+            if isinstance(v, dict) and "tflops" in v:
+                v["frac_of_sustained_bf16_peak"] = v["tflops"] / tf_sust
     return legs
 
 
