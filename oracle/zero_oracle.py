@@ -487,6 +487,21 @@ def mlp_unit_forward(x_bf16, gate_shards, up_shards, down_shards=None, h_bf16=No
     return g, u, h, y
 
 
+def silu_gate_backward(dh_bf16, g_bf16, u_bf16):
+    """Backward of H = silu(G) * U (the MLP unit's SiLU-gate product; [Interview] Fig. 2:
+    the unit's backward after its forward) from the activations the forward saved and the
+    upstream dH, all bf16, in float64:
+        s = 1 / (1 + exp(-g)),  silu(g) = g s,  silu'(g) = s (1 + g (1 - s)),
+        dU = dH silu(G),  dG = dH U silu'(G).
+    Returns (dG, dU) in float64."""
+    dh = bf16_to_f32(dh_bf16).astype(np.float64)
+    g = bf16_to_f32(g_bf16).astype(np.float64)
+    u = bf16_to_f32(u_bf16).astype(np.float64)
+    with np.errstate(over="ignore"):
+        s = 1.0 / (1.0 + np.exp(-g))
+    return dh * u * (s * (1.0 + g * (1.0 - s))), dh * (g * s)
+
+
 def transpose_cat(srcs) -> np.ndarray:
     """The FSDP backward's operand layout: dst[c][q*rows + r] = srcs[q][r][c] — the sources
     transposed and placed side by side (W^T from W's row shards is the backward all-gather,

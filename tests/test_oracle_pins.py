@@ -545,6 +545,48 @@ def test_mlp_unit_forward_bruteforce():
             assert y[i, j] == pytest.approx(sum(h[i, k] * wd[j, k] for k in range(f)), rel=1e-12, abs=1e-300)
 
 
+def test_silu_gate_backward_matches_torch_autograd():
+    """The SiLU-gate backward against torch's automatic differentiation of silu(g) * u in
+    float64 (a library routine that differentiates the forward; it shares nothing with the
+    oracle's closed form), on bf16 inputs over the range activations take."""
+    rng = np.random.default_rng(41)
+    n = 20000
+    g = bf16_of(np.concatenate([rng.normal(0, 3, n - 6), [0.0, -30.0, 30.0, -1.278, 1e-3, -88.0]]))
+    u = bf16_of(rng.normal(0, 2, n))
+    dh = bf16_of(rng.normal(0, 1, n))
+    dg, du = O.silu_gate_backward(dh, g, u)
+    gt = torch.tensor(O.bf16_to_f32(g).astype(np.float64), requires_grad=True)
+    ut = torch.tensor(O.bf16_to_f32(u).astype(np.float64), requires_grad=True)
+    (torch.nn.functional.silu(gt) * ut).backward(torch.tensor(O.bf16_to_f32(dh).astype(np.float64)))
+    assert np.allclose(dg, gt.grad.numpy(), rtol=1e-12, atol=1e-300)
+    assert np.allclose(du, ut.grad.numpy(), rtol=1e-12, atol=1e-300)
+
+
+def test_silu_gate_backward_is_the_derivative_of_the_forward():
+    """Central differences of the oracle's own forward silu(g) * u (O.silu) reproduce the
+    backward: d/dg and d/du of dh * silu(g) * u."""
+    g = np.linspace(-12, 12, 481)
+    g_b, u_b, dh_b = bf16_of(g), bf16_of(np.full_like(g, 1.5)), bf16_of(np.full_like(g, -0.75))
+    gf, uf, dhf = (O.bf16_to_f32(x).astype(np.float64) for x in (g_b, u_b, dh_b))
+    dg, du = O.silu_gate_backward(dh_b, g_b, u_b)
+    h = 1e-6
+    num_dg = dhf * uf * (O.silu(gf + h) - O.silu(gf - h)) / (2 * h)
+    num_du = dhf * O.silu(gf)
+    assert np.allclose(dg, num_dg, rtol=1e-7, atol=1e-9)
+    assert np.allclose(du, num_du, rtol=1e-14, atol=1e-300)
+
+
+def test_silu_gate_backward_closed_forms():
+    """g = 0: silu = 0 and silu' = 1/2, so dU = 0 and dG = dh u / 2; large |g|: silu' -> 1
+    (g -> +inf) and -> 0 (g -> -inf)."""
+    dh, u = bf16_of(np.array([0.5, -2.0, 3.0])), bf16_of(np.array([4.0, 1.5, -0.25]))
+    dg, du = O.silu_gate_backward(dh, bf16_of(np.zeros(3)), u)
+    assert np.array_equal(du, np.zeros(3))
+    assert np.array_equal(dg, O.bf16_to_f32(dh) * O.bf16_to_f32(u) * 0.5)
+    dg, _ = O.silu_gate_backward(bf16_of(np.ones(2)), bf16_of(np.array([80.0, -80.0])), bf16_of(np.ones(2)))
+    assert dg[0] == pytest.approx(1.0, rel=1e-15) and abs(dg[1]) < 1e-30
+
+
 # ---------------------------------------------------------------------------------------
 # mutation tests: a planted mistake in the oracle must fail one of the pins above
 # ---------------------------------------------------------------------------------------
@@ -608,3 +650,25 @@ def test_mutation_dropped_padding_is_caught(monkeypatch):
     monkeypatch.setattr(O, "make_layout", no_pad)
     with pytest.raises(AssertionError):
         test_layout_bruteforce(13, 4, 3)
+
+
+def _silu_gate_backward_wrong_derivative(dh_bf16, g_bf16, u_bf16):
+    dh, g, u = (O.bf16_to_f32(x).astype(np.float64) for x in (dh_bf16, g_bf16, u_bf16))
+    s = 1.0 / (1.0 + np.exp(-g))
+    return dh * u * (s * (1.0 + g * s)), dh * (g * s)  # (1 - s) dropped
+
+
+@pytest.mark.parametrize("bad", [_silu_gate_backward_wrong_derivative])
+def test_mutations_of_silu_gate_backward_are_caught(bad, monkeypatch):
+    monkeypatch.setattr(O, "silu_gate_backward", bad)
+    with pytest.raises(AssertionError):
+        test_silu_gate_backward_matches_torch_autograd()
+    with pytest.raises(AssertionError):
+        test_silu_gate_backward_is_the_derivative_of_the_forward()
+
+
+def test_mutation_swapped_silu_gate_outputs_is_caught(monkeypatch):
+    good = O.silu_gate_backward
+    monkeypatch.setattr(O, "silu_gate_backward", lambda dh, g, u: good(dh, g, u)[::-1])
+    with pytest.raises(AssertionError):
+        test_silu_gate_backward_closed_forms()
