@@ -505,19 +505,82 @@ def extra_legs(z, synth, dev, hbm_peak, tf_burst, peak_src, args):
         legs["fsdp_zero3_step"] = zero3_leg(z, synth, dev, tf_burst, hbm_peak, stream)
     legs["fsdp_zero3_step"]["clocks"] = clk.summary()
     legs["fsdp_zero3_step"]["idle_before_s"] = args.leg_idle_s
+    torch.cuda.empty_cache()
+    time.sleep(args.leg_idle_s)
+    with ClockSampler(gpu) as clk:
+        legs["fsdp_zero3_mlp_step"] = zero3_mlp_leg(z, synth, dev, tf_burst, stream)
+    legs["fsdp_zero3_mlp_step"]["clocks"] = clk.summary()
+    legs["fsdp_zero3_mlp_step"]["idle_before_s"] = args.leg_idle_s
     # beside each fraction of the burst bf16 peak, the fraction of the sustained one (the
     # same cuBLAS GEMM looped for seconds under the power cap): these legs run for tens of
     # milliseconds after seconds of other work, and the tensor-core kernels reach the power
     # cap themselves
     tf_sust = peaks()[2]
-    for leg in (legs["fsdp_unit_forward"], legs["fsdp_zero3_step"]):
-        for v in leg.values():
+    for leg in (legs["fsdp_unit_forward"], legs["fsdp_zero3_step"], legs["fsdp_zero3_mlp_step"]):
+        for v in [leg] + list(leg.values()):
             if isinstance(v, dict) and "tflops" in v:
                 v["frac_of_sustained_bf16_peak"] = v["tflops"] / tf_sust
     return legs
 
 
 ZERO3_SHAPES = [(14336, 4096), (4096, 14336), (14336, 4096), (4096, 14336)]
+MLP_UNITS = 2  # Mistral-7B MLP units (d_model 4096, d_ff 14336) in the MLP stack leg
+
+
+def zero3_mlp_units(z, synth, dev, n, m, n_units=MLP_UNITS, d=4096, f=14336):
+    """A stack of Mistral-7B MLP units (W_gate, W_up [14336, 4096], W_down [4096, 14336],
+    each in n row shards with its ZeRO-3 state), n ranks of m tokens."""
+    import torch
+    nm = n * m
+    bf = dict(dtype=torch.bfloat16, device=dev)
+
+    def weight(rows, cols, key):
+        w = torch.cat(synth.weight_shards(rows, cols, n, device=dev, seed_key=key), 0).contiguous()
+        return {"plan": z.zero_plan(rows * cols, n, "zero3", 50 * MIB), "w": w, "master": w.float().reshape(-1),
+                "m": torch.zeros(rows * cols, device=dev), "v": torch.zeros(rows * cols, device=dev)}
+    units = [{"d_model": d, "d_ff": f, "gate": weight(f, d, 40 + 3 * i), "up": weight(f, d, 41 + 3 * i),
+              "down": weight(d, f, 42 + 3 * i), "x": torch.empty(nm, d, **bf), "gu": torch.empty(nm, 2 * f, **bf),
+              "h": torch.empty(nm, f, **bf), "dy": torch.empty(nm, d, **bf), "dh": torch.empty(nm, f, **bf),
+              "dgu": torch.empty(nm, 2 * f, **bf), "dw_gu": torch.empty(2 * f, d, device=dev),
+              "dw_down": torch.empty(d, f, device=dev)} for i in range(n_units)]
+    units[0]["x"].copy_(synth.activations(nm, d, device=dev))
+    units[-1]["dy"].copy_(synth.upstream_grad(nm, d, device=dev))
+    return units
+
+
+def zero3_mlp_leg(z, synth, dev, tf_peak, stream):
+    """One ZeRO-3 training step over a stack of Mistral-7B MLP units, N = 8 ranks of 1024
+    tokens: forward (gate-up kernel saving G | U, down projection), backward in reverse
+    (dH, dW_down, SiLU-gate backward, dX over both projections, dW_gate | dW_up), each
+    rank's Adam on its three shards."""
+    import torch
+    n, m = 8, 1024
+    res = {"units": MLP_UNITS, "d_model": 4096, "d_ff": 14336, "n_ranks": n, "tokens_per_rank": m}
+    try:
+        units = zero3_mlp_units(z, synth, dev, n, m)
+        nm = n * m
+        y = torch.empty(nm, 4096, dtype=torch.bfloat16, device=dev)
+        dx = torch.empty(nm, 4096, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(z.fsdp_zero3_mlp_step_workspace(n, [(4096, 14336)] * MLP_UNITS, m), dtype=torch.uint8,
+                         device=dev)
+        t = [0]
+
+        def step():
+            t[0] += 1
+            z.fsdp_zero3_mlp_step(units, m, HP, t[0], y_out=y, dx_out=dx, workspace=ws, stream=stream)
+
+        ms = time_launches(step, 10, stream)
+        z.zero_device_status(stream)
+        flop = MLP_UNITS * 3 * 3 * 2.0 * nm * 4096 * 14336  # 3 matrices, forward + 2 backward GEMMs each
+        res.update(ms=ms, tflops=flop / ms / 1e9, frac_of_bf16_peak=flop / ms / 1e9 / tf_peak,
+                   gemm_flop_per_step=flop, workspace_bytes=ws.numel(),
+                   adam_bytes_per_step=MLP_UNITS * 3 * 30 * 4096 * 14336,
+                   silu_backward_bytes_per_step=MLP_UNITS * 10 * nm * 14336,
+                   note="tflops counts the GEMM flops over the whole step, which also holds the Adam launches, the "
+                        "SiLU-gate backward and the W^T / operand transposes")
+    except Exception as e:  # the leg must not hide the step's line
+        res["error"] = str(e)[:300]
+    return res
 
 
 def zero3_units(z, synth, dev, n, m, shapes=ZERO3_SHAPES):
@@ -1153,6 +1216,20 @@ def run_case(args):
                                                      stream=stream, prefetch_stream=side), 2, stream)
         flop = sum(6.0 * n * m * R * K for R, K in ZERO3_SHAPES)
         out.update(n_ranks=n, tokens_per_rank=m, ms=ms, tflops=flop / ms / 1e9)
+    elif args.case == "zero3_mlp_step":
+        # one ZeRO-3 step over 2 Mistral-7B MLP units, N = 8 ranks x 1024 tokens (about
+        # 10 GB on the device), 3 steps
+        n, m = 8, 1024
+        units = zero3_mlp_units(z, synth, dev, n, m)
+        ws = torch.empty(z.fsdp_zero3_mlp_step_workspace(n, [(4096, 14336)] * MLP_UNITS, m), dtype=torch.uint8,
+                         device=dev)
+        y = torch.empty(n * m, 4096, dtype=torch.bfloat16, device=dev)
+        dx = torch.empty(n * m, 4096, dtype=torch.bfloat16, device=dev)
+        hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+        ms = time_launches(lambda: z.fsdp_zero3_mlp_step(units, m, hp, 1, y_out=y, dx_out=dx, workspace=ws,
+                                                         stream=stream), 2, stream)
+        flop = MLP_UNITS * 9 * 2.0 * n * m * 4096 * 14336
+        out.update(n_ranks=n, tokens_per_rank=m, units=MLP_UNITS, ms=ms, tflops=flop / ms / 1e9)
     elif args.case == "backward_up":
         # FSDP unit backward of W_up [14336, 4096] in 8 row shards, 2048 tokens per rank
         # (dY 470 MB, X 134 MB, dX 268 MB, dW 235 MB, X^T workspace 134 MB): 3 launches
@@ -1177,7 +1254,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="one measured case: fused_small | fused_tma_small | megatron_small | e2e_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
-                         "backward_up | rank_view_small | zero3_step (ncu-sized) | "
+                         "backward_up | rank_view_small | zero3_step | zero3_mlp_step (ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)

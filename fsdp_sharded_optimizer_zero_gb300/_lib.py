@@ -34,7 +34,8 @@ EXPORTS = (
     "zero_reduce_scatter", "zero_adam_step", "zero_fused_step", "zero_fused_step_host", "zero_fused_step_fp32_grads",
     "zero_fused_step_buckets", "zero_allgather_params", "ddp_allreduce",
     "fsdp_gather_rows", "fsdp_unit_forward", "fsdp_transpose_cat", "fsdp_unit_backward_workspace", "fsdp_unit_backward", "fsdp_mlp_forward",
-    "fsdp_zero3_step_workspace", "fsdp_zero3_step", "fsdp_unit_forward_static_scratch",
+    "fsdp_zero3_step_workspace", "fsdp_zero3_step", "fsdp_zero3_mlp_step_workspace", "fsdp_zero3_mlp_step",
+    "fsdp_unit_forward_static_scratch",
     "zero_last_error", "zero_device_status", "zero_selftest_bounded_wait", "zero_set_fused_kernel", "zero_set_gemm_kernel", "zero_version",
 )
 
@@ -63,6 +64,18 @@ class fsdp_unit_state(C.Structure):
     _fields_ = [("rows_out", C.c_int64), ("k_in", C.c_int64), ("plan", C.c_void_p), ("w", C.c_void_p),
                 ("master", C.c_void_p), ("m", C.c_void_p), ("v", C.c_void_p), ("x", C.c_void_p), ("dy", C.c_void_p),
                 ("dw", C.c_void_p)]
+
+
+class fsdp_weight_state(C.Structure):
+    _fields_ = [("plan", C.c_void_p), ("w", C.c_void_p), ("master", C.c_void_p), ("m", C.c_void_p),
+                ("v", C.c_void_p)]
+
+
+class fsdp_mlp_unit_state(C.Structure):
+    _fields_ = [("d_model", C.c_int64), ("d_ff", C.c_int64), ("gate", fsdp_weight_state), ("up", fsdp_weight_state),
+                ("down", fsdp_weight_state), ("x", C.c_void_p), ("gu", C.c_void_p), ("h", C.c_void_p),
+                ("dy", C.c_void_p), ("dh", C.c_void_p), ("dgu", C.c_void_p), ("dw_gu", C.c_void_p),
+                ("dw_down", C.c_void_p)]
 
 
 FSDP_GATHER_MATERIALIZE = 1
@@ -111,6 +124,9 @@ def _load():
         "fsdp_zero3_step_workspace": (I, [I, I, C.POINTER(fsdp_unit_state), I64, I, C.POINTER(U64)]),
         "fsdp_zero3_step": (I, [I, I, C.POINTER(fsdp_unit_state), I64, VP, VP, C.POINTER(zero_adam), I64, I, VP, U64,
                                 VP, VP]),
+        "fsdp_zero3_mlp_step_workspace": (I, [I, I, C.POINTER(fsdp_mlp_unit_state), I64, C.POINTER(U64)]),
+        "fsdp_zero3_mlp_step": (I, [I, I, C.POINTER(fsdp_mlp_unit_state), I64, VP, VP, C.POINTER(zero_adam), I64, VP,
+                                    U64, VP]),
         "zero_set_gemm_kernel": (I, [I]),
         "zero_version": (I, []),
     }
@@ -463,6 +479,62 @@ def fsdp_zero3_step(units, m_tokens: int, hp, step: int, y_out=None, dx_out=None
         C.byref(a), step, flags, _dev(workspace, torch.uint8, "workspace"),
         0 if workspace is None else workspace.numel(), _stream(stream),
         None if prefetch_stream is None else _stream(prefetch_stream)))
+
+
+def _weight_state(ws: fsdp_weight_state, w: dict, rows: int, cols: int, name: str):
+    if tuple(w["w"].shape) != (rows, cols):
+        raise ValueError(f"{name}.w must be [{rows}, {cols}] (got {tuple(w['w'].shape)})")
+    ws.plan = w["plan"].handle
+    ws.w = _dev(w["w"], torch.bfloat16, f"{name}.w")
+    for k in ("master", "m", "v"):
+        _need(w[k], rows * cols, f"{name}.{k}")
+        setattr(ws, k, _dev(w[k], torch.float32, f"{name}.{k}"))
+
+
+def _mlp_unit_array(units, nm=None):
+    arr = (fsdp_mlp_unit_state * len(units))()
+    for i, u in enumerate(units):
+        d, f = int(u["d_model"]), int(u["d_ff"])
+        arr[i].d_model, arr[i].d_ff = d, f
+        if nm is None:
+            continue
+        _weight_state(arr[i].gate, u["gate"], f, d, f"units[{i}].gate")
+        _weight_state(arr[i].up, u["up"], f, d, f"units[{i}].up")
+        _weight_state(arr[i].down, u["down"], d, f, f"units[{i}].down")
+        for k, cols in (("x", d), ("gu", 2 * f), ("h", f), ("dy", d), ("dh", f), ("dgu", 2 * f)):
+            if u[k].dim() != 2 or tuple(u[k].shape) != (nm, cols):
+                raise ValueError(f"units[{i}].{k} must be [{nm}, {cols}] (got {tuple(u[k].shape)})")
+            setattr(arr[i], k, _dev(u[k], torch.bfloat16, f"units[{i}].{k}"))
+        _need(u["dw_gu"], 2 * f * d, f"units[{i}].dw_gu")
+        _need(u["dw_down"], d * f, f"units[{i}].dw_down")
+        arr[i].dw_gu = _dev(u["dw_gu"], torch.float32, f"units[{i}].dw_gu")
+        arr[i].dw_down = _dev(u["dw_down"], torch.float32, f"units[{i}].dw_down")
+    return arr
+
+
+def fsdp_zero3_mlp_step_workspace(n_ranks: int, shapes, m_tokens: int) -> int:
+    """Workspace bytes of fsdp_zero3_mlp_step for MLP units of the given (d_model, d_ff)."""
+    arr = _mlp_unit_array([{"d_model": d, "d_ff": f} for d, f in shapes])
+    b = C.c_uint64()
+    _check(_lib.fsdp_zero3_mlp_step_workspace(n_ranks, len(arr), arr, m_tokens, C.byref(b)))
+    return b.value
+
+
+def fsdp_zero3_mlp_step(units, m_tokens: int, hp, step: int, y_out=None, dx_out=None, workspace=None, stream=None):
+    """units: one dict per MLP unit with d_model, d_ff; gate / up / down as dicts of plan,
+    w, master, m, v; and x, gu, h, dy, dh, dgu (bf16) and dw_gu, dw_down (fp32)."""
+    if not units:
+        raise ValueError("units is empty")
+    n = units[0]["gate"]["plan"].n_ranks
+    nm = n * m_tokens
+    arr = _mlp_unit_array(units, nm)
+    _need(y_out, nm * int(units[-1]["d_model"]), "y_out")
+    _need(dx_out, nm * int(units[0]["d_model"]), "dx_out")
+    a = _adam(hp)
+    _check(_lib.fsdp_zero3_mlp_step(
+        n, len(arr), arr, m_tokens, _dev(y_out, torch.bfloat16, "y_out"), _dev(dx_out, torch.bfloat16, "dx_out"),
+        C.byref(a), step, _dev(workspace, torch.uint8, "workspace"), 0 if workspace is None else workspace.numel(),
+        _stream(stream)))
 
 
 def fsdp_mlp_forward(gate_shards, up_shards, down_shards, X, H, Y, scratch_down=None, stream=None,

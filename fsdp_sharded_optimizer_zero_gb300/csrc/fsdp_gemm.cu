@@ -94,6 +94,7 @@ struct GemmParams {
   CUtensorMap w2[kMaxShards];    // gate-up mode: the up projection's shards (w holds the gate's)
   float* y;                      // [M, R] fp32
   uint16_t* yb;                  // [M, R] bf16 or null (gate-up mode: H = silu(gate) * up)
+  uint16_t* gu;                  // gate-up mode, nullable: [M, 2R] bf16, the gate and up projections G | U
   CUtensorMap ymap[kMaxShards];  // Y row piece s [y_shard_rows, R] fp32, box 32 x 32, 128B swizzle (y_tma)
   float alpha;                   // output scale (1: none)
   int m, r, k, shard_rows, n_shards;
@@ -184,6 +185,30 @@ __device__ __forceinline__ void store_gate_up_chunk(const GemmParams& p, int row
   } else {
     for (int j = 0; j < 32; ++j)
       if (col0 + j < p.r) brow[col0 + j] = f32_to_bf16_bits(h[j]);
+  }
+  if (p.gu) {  // the saved activations of the backward: bf16 G at column c, U at column R + c
+    uint16_t* grow = p.gu + static_cast<size_t>(row) * 2 * p.r;
+    if (col0 + 32 <= p.r && (p.r & 7) == 0) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        __stcs(reinterpret_cast<uint4*>(grow + col0 + j),
+               make_uint4(pack_bf16x2(__uint_as_float(g[j]), __uint_as_float(g[j + 1])),
+                          pack_bf16x2(__uint_as_float(g[j + 2]), __uint_as_float(g[j + 3])),
+                          pack_bf16x2(__uint_as_float(g[j + 4]), __uint_as_float(g[j + 5])),
+                          pack_bf16x2(__uint_as_float(g[j + 6]), __uint_as_float(g[j + 7]))));
+        __stcs(reinterpret_cast<uint4*>(grow + p.r + col0 + j),
+               make_uint4(pack_bf16x2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])),
+                          pack_bf16x2(__uint_as_float(u[j + 2]), __uint_as_float(u[j + 3])),
+                          pack_bf16x2(__uint_as_float(u[j + 4]), __uint_as_float(u[j + 5])),
+                          pack_bf16x2(__uint_as_float(u[j + 6]), __uint_as_float(u[j + 7]))));
+      }
+    } else {
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < p.r) {
+          grow[col0 + j] = f32_to_bf16_bits(__uint_as_float(g[j]));
+          grow[p.r + col0 + j] = f32_to_bf16_bits(__uint_as_float(u[j]));
+        }
+    }
   }
 }
 
@@ -742,7 +767,7 @@ struct Operand {
 template <bool GATE_UP>
 int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, int64_t m_tokens, int64_t rows_out,
                 int64_t k_in, float* const* Y, int y_pieces, uint16_t* Y_bf16, float alpha, cudaStream_t st,
-                const char* who) {
+                const char* who, uint16_t* GU = nullptr) {
   constexpr int TN = GATE_UP ? 128 : BN;
   if (m_tokens > INT32_MAX / 2 || rows_out > INT32_MAX / 2 || k_in > INT32_MAX / 2)
     return set_error(ZERO_ERR_INVALID_ARG, "%s: sizes must be below 2^30", who);
@@ -816,6 +841,7 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
   p.a_mn = A.mn ? 1 : 0;
   p.b_mn = B.mn ? 1 : 0;
   p.yb = Y_bf16;
+  p.gu = GATE_UP ? GU : nullptr;
   p.alpha = alpha;
   p.m = static_cast<int>(m_tokens);
   p.r = static_cast<int>(rows_out);
@@ -888,10 +914,10 @@ int launch_fsdp_gemm_row_split(int a_shards, const uint16_t* const* A, float* co
 
 int launch_fsdp_gate_up(int n_shards, const uint16_t* const* gate_shards, const uint16_t* const* up_shards,
                         int64_t d_ff, int64_t d_model, const uint16_t* X, int64_t m_tokens, uint16_t* H,
-                        cudaStream_t st) {
+                        cudaStream_t st, uint16_t* GU) {
   const uint16_t* a1[1] = {X};
   return launch_gemm<true>({1, a1, false, m_tokens}, {n_shards, gate_shards, false, d_ff / n_shards}, up_shards,
-                           m_tokens, d_ff, d_model, nullptr, 1, H, 1.0f, st, "fsdp_mlp_forward");
+                           m_tokens, d_ff, d_model, nullptr, 1, H, 1.0f, st, "fsdp_mlp_forward", GU);
 }
 
 int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces_rows, int dy_pieces,

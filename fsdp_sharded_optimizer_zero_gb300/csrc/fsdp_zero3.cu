@@ -289,3 +289,205 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
   }
   return ZERO_OK;
 }
+
+// ======================================================================================
+// The same step over Mistral-style MLP units (H = silu(X W_gate^T) * (X W_up^T), Y = H
+// W_down^T), each of the three weights with its own ZeRO-3 state. Forward: the gate-up
+// kernel (both projections in one N = 256 MMA stream, SiLU-gate epilogue) also saves G | U
+// for the backward, then the down projection. Backward, per unit: W_down^T gathered, dH,
+// dW_down and W_down's Adam; the SiLU-gate backward; [W_gate; W_up]^T gathered (the 2N
+// shards of both in one transposing launch), dX over the concatenated K of both
+// projections, dW_gate | dW_up in one GEMM, and their Adam. Serial on one stream: on one
+// GPU the side-stream forms of the linear step above measured slower.
+// ======================================================================================
+
+namespace {
+
+const char* const kWhoMlp = "fsdp_zero3_mlp_step";
+
+struct MlpWorkspace {
+  uint64_t wt_off, t_off, total;  // the gathered W^T slot, the dW operand slot
+};
+
+// bytes of the dW GEMM's laid-out operand for dW [R, K] over nm tokens: the transpose of
+// the narrower of dY [nm, R] and X [nm, K]
+uint64_t narrower_bytes(int64_t R, int64_t K, int64_t nm) {
+  return 2ull * static_cast<uint64_t>(std::min(R, K)) * static_cast<uint64_t>(nm);
+}
+
+MlpWorkspace mlp_workspace(int n, int L, const fsdp_mlp_unit_state* u, int64_t m) {
+  const int64_t nm = static_cast<int64_t>(n) * m;
+  uint64_t wt = 0, t = 0;
+  for (int i = 0; i < L; ++i) {
+    const int64_t d = u[i].d_model, f = u[i].d_ff;
+    wt = std::max<uint64_t>(wt, 4ull * static_cast<uint64_t>(f) * static_cast<uint64_t>(d));
+    t = std::max(t, std::max(narrower_bytes(d, f, nm), narrower_bytes(2 * f, d, nm)));
+  }
+  MlpWorkspace w;
+  w.wt_off = 0;
+  w.t_off = align256(wt);
+  w.total = w.t_off + align256(t);
+  return w;
+}
+
+int check_weight(const fsdp_weight_state& w, int64_t rows, int64_t cols, int n, int i, const char* name) {
+  if (!w.plan) return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: %s.plan is NULL", kWhoMlp, i, name);
+  zero_layout L;
+  zero_plan_query(w.plan, &L);
+  if (L.psi != static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols) || L.n_ranks != n || L.stage != ZERO_STAGE_3)
+    return set_error(ZERO_ERR_INVALID_ARG,
+                     "%s: unit %d: %s.plan must be zero_plan(%lld * %lld, n_ranks, ZERO_STAGE_3, ...)", kWhoMlp, i,
+                     name, (long long)rows, (long long)cols);
+  if (!w.w || !w.master || !w.m || !w.v)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: a buffer of %s is NULL", kWhoMlp, i, name);
+  if (!aligned16(w.w) || !aligned16(w.master) || !aligned16(w.m) || !aligned16(w.v))
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: buffers of %s must be 16-byte aligned", kWhoMlp, i, name);
+  return ZERO_OK;
+}
+
+int check_mlp_units(int n, int L, const fsdp_mlp_unit_state* u, int64_t m, bool buffers) {
+  if (n < 1 || n > kGemmMaxPieces)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: n_ranks %d outside 1..%d", kWhoMlp, n, kGemmMaxPieces);
+  if (L < 1 || L > 64) return set_error(ZERO_ERR_INVALID_ARG, "%s: n_units %d outside 1..64", kWhoMlp, L);
+  if (!u) return set_error(ZERO_ERR_INVALID_ARG, "%s: units is NULL", kWhoMlp);
+  if (m < 1 || (static_cast<int64_t>(n) * m) % 8)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: n_ranks * m_tokens must be a positive multiple of 8", kWhoMlp);
+  for (int i = 0; i < L; ++i) {
+    const fsdp_mlp_unit_state& s = u[i];
+    const int64_t d = s.d_model, f = s.d_ff;
+    if (d < 64 || f < 64 || d > (1 << 28) || f > (1 << 28) || d % 64 || f % 64)
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: d_model and d_ff must be multiples of 64 (got %lld, %lld)",
+                       kWhoMlp, i, (long long)d, (long long)f);
+    if (f % n || (f / n) % 128)
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: d_ff / n_ranks must be a multiple of 128 (got %lld / %d)",
+                       kWhoMlp, i, (long long)f, n);
+    if (!fsdp_fused_gather_ok(n, d))
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: W_down's shards of %lld rows do not tile the fused gather",
+                       kWhoMlp, i, (long long)(d % n ? -1 : d / n));
+    if (i + 1 < L && u[i + 1].d_model != d)
+      return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d's d_model %lld differs from unit %d's %lld", kWhoMlp, i + 1,
+                       (long long)u[i + 1].d_model, i, (long long)d);
+    if (!buffers) continue;
+    int rc;
+    if ((rc = check_weight(s.gate, f, d, n, i, "gate")) || (rc = check_weight(s.up, f, d, n, i, "up")) ||
+        (rc = check_weight(s.down, d, f, n, i, "down")))
+      return rc;
+    const void* bufs[] = {s.x, s.gu, s.h, s.dy, s.dh, s.dgu, s.dw_gu, s.dw_down};
+    for (const void* b : bufs) {
+      if (!b) return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: an activation or gradient buffer is NULL", kWhoMlp, i);
+      if (!aligned16(b))
+        return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: activation and gradient buffers must be 16-byte aligned",
+                         kWhoMlp, i);
+    }
+  }
+  return ZERO_OK;
+}
+
+// dW [R, K] = alpha sum over nm tokens of dY^T X, with the narrower operand's transpose in
+// t (laid out by the caller): dY^T [R, nm] when K > R (X read in place), else X^T [K, nm]
+// (dY read in place)
+int dw_gemm(const uint16_t* dy, const uint16_t* x, const uint16_t* t, int64_t R, int64_t K, int64_t nm, float* dw,
+            float alpha, cudaStream_t st) {
+  if (K > R) {
+    const uint16_t* x1[1] = {x};
+    return launch_fsdp_bwd_dw_x_mn(1, t, x1, nm, R, K, dw, alpha, st);
+  }
+  return launch_fsdp_bwd_dw_alpha(dy, nm, t, R, K, dw, alpha, st);
+}
+
+}  // namespace
+
+extern "C" int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsdp_mlp_unit_state* units,
+                                             int64_t m_tokens, uint64_t* bytes) {
+  if (!bytes) return set_error(ZERO_ERR_INVALID_ARG, "fsdp_zero3_mlp_step_workspace: bytes is NULL");
+  int rc = check_mlp_units(n_ranks, n_units, units, m_tokens, false);
+  if (rc) return rc;
+  *bytes = mlp_workspace(n_ranks, n_units, units, m_tokens).total;
+  return ZERO_OK;
+}
+
+extern "C" int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit_state* units, int64_t m_tokens,
+                                   zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step,
+                                   void* workspace, uint64_t workspace_bytes, zero_stream_t stream) {
+  const int n = n_ranks, L = n_units;
+  int rc = check_mlp_units(n, L, units, m_tokens, true);
+  if (rc) return rc;
+  if ((rc = check_adam_args(hp, step, kWhoMlp))) return rc;
+  if ((y_out && !aligned16(y_out)) || (dx_out && !aligned16(dx_out)))
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: y_out and dx_out must be 16-byte aligned", kWhoMlp);
+  const MlpWorkspace ws = mlp_workspace(n, L, units, m_tokens);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < ws.total)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: workspace of %llu bytes (16-byte aligned) is below the %llu needed",
+                     kWhoMlp, workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.total);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t nm = static_cast<int64_t>(n) * m_tokens;
+  uint16_t* wt = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + ws.wt_off);
+  uint16_t* tr = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + ws.t_off);
+  const float inv_n = 1.0f / static_cast<float>(n);
+
+  // the N row shards of a weight (rank r's rows at r rows/N), into ptrs[first .. first + N)
+  auto shards = [&](const fsdp_weight_state& w, int64_t rows, int64_t cols, const uint16_t** ptrs, int first) {
+    const int64_t per = (rows / n) * cols;
+    for (int r = 0; r < n; ++r) ptrs[first + r] = w.w + r * per;
+  };
+  auto transposes = [&](const GradPtrs& wsrc, int wn, int64_t wrows, int64_t wcols, const uint16_t* t_src,
+                        int64_t t_cols) {
+    GradPtrs tsrc;
+    memset(&tsrc, 0, sizeof(tsrc));
+    tsrc.p[0] = t_src;
+    const cudaError_t e = launch_transpose_cat2(wsrc, wn, wrows, wcols, wt, tsrc, 1, nm, t_cols, tr, st);
+    return e == cudaSuccess ? ZERO_OK : set_error(ZERO_ERR_CUDA, "%s: transpose: %s", kWhoMlp, cudaGetErrorString(e));
+  };
+
+  // ---- forward, unit 0 -> last ----
+  for (int i = 0; i < L; ++i) {
+    const fsdp_mlp_unit_state& s = units[i];
+    const int64_t d = s.d_model, f = s.d_ff;
+    const uint16_t *gsh[kGemmMaxPieces], *ush[kGemmMaxPieces], *dsh[kGemmMaxPieces];
+    shards(s.gate, f, d, gsh, 0);
+    shards(s.up, f, d, ush, 0);
+    shards(s.down, d, f, dsh, 0);
+    if ((rc = launch_fsdp_gate_up(n, gsh, ush, f, d, s.x, nm, s.h, st, s.gu))) return rc;
+    zero_bf16* out = i + 1 < L ? units[i + 1].x : y_out;
+    if (out && (rc = launch_fsdp_gemm(n, dsh, d, f, s.h, nm, nullptr, out, 1.0f, st))) return rc;
+  }
+
+  // ---- backward, last -> unit 0 ----
+  for (int i = L - 1; i >= 0; --i) {
+    const fsdp_mlp_unit_state& s = units[i];
+    const int64_t d = s.d_model, f = s.d_ff;
+    GradPtrs wsrc;
+    memset(&wsrc, 0, sizeof(wsrc));
+    // W_down^T [f, d] and the dW_down operand (dW_down [d, f] = dY^T H: dY^T when f > d)
+    shards(s.down, d, f, wsrc.p, 0);
+    if ((rc = transposes(wsrc, n, d / n, f, f > d ? s.dy : s.h, f > d ? d : f))) return rc;
+    // dH [nm, f] = bf16(dY [nm, d] * (W_down^T [f, d])^T)
+    const uint16_t* wt1[1] = {wt};
+    if ((rc = launch_fsdp_gemm(1, wt1, f, d, s.dy, nm, nullptr, s.dh, 1.0f, st))) return rc;
+    if ((rc = dw_gemm(s.dy, s.h, tr, d, f, nm, s.dw_down, inv_n, st))) return rc;
+    if ((rc = zero_adam_step(s.down.plan, ZERO_ALL_RANKS, s.dw_down, s.down.master, s.down.m, s.down.v, s.down.w, hp,
+                             step, stream)))
+      return rc;
+    // dG | dU from dH and the saved G | U
+    cudaError_t e = launch_silu_gate_backward(s.dh, s.gu, s.dgu, nm, f, st);
+    if (e != cudaSuccess)
+      return set_error(ZERO_ERR_CUDA, "%s: SiLU-gate backward: %s", kWhoMlp, cudaGetErrorString(e));
+    // [W_gate; W_up]^T [d, 2f] (the 2N shards of both) and the dW_gu operand (dW_gu [2f, d]
+    // = [dG | dU]^T X: [dG | dU]^T when d > 2f)
+    memset(&wsrc, 0, sizeof(wsrc));
+    shards(s.gate, f, d, wsrc.p, 0);
+    shards(s.up, f, d, wsrc.p, n);
+    if ((rc = transposes(wsrc, 2 * n, f / n, d, d > 2 * f ? s.dgu : s.x, d > 2 * f ? 2 * f : d))) return rc;
+    // dX [nm, d] = bf16([dG | dU] [nm, 2f] * ([W_gate; W_up]^T [d, 2f])^T): the sum of both
+    // projections' input gradients over the concatenated K
+    zero_bf16* dx = i > 0 ? units[i - 1].dy : dx_out;
+    if (dx && (rc = launch_fsdp_gemm(1, wt1, d, 2 * f, s.dgu, nm, nullptr, dx, 1.0f, st))) return rc;
+    if ((rc = dw_gemm(s.dgu, s.x, tr, 2 * f, d, nm, s.dw_gu, inv_n, st))) return rc;
+    if ((rc = zero_adam_step(s.gate.plan, ZERO_ALL_RANKS, s.dw_gu, s.gate.master, s.gate.m, s.gate.v, s.gate.w, hp,
+                             step, stream)) ||
+        (rc = zero_adam_step(s.up.plan, ZERO_ALL_RANKS, s.dw_gu + f * d, s.up.master, s.up.m, s.up.v, s.up.w, hp,
+                             step, stream)))
+      return rc;
+  }
+  return ZERO_OK;
+}

@@ -60,6 +60,10 @@ cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t st)
 // transposed and concatenated into one row-major [cols, n * rows] buffer
 cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int64_t cols, uint16_t* dst,
                                  cudaStream_t st);
+// SiLU-gate backward of H = silu(G) * U: dG | dU [rows, 2 d_ff] bf16 from dH [rows, d_ff]
+// and the saved G | U [rows, 2 d_ff], elementwise in fp32
+cudaError_t launch_silu_gate_backward(const uint16_t* dh, const uint16_t* gu, uint16_t* dgu, int64_t rows, int64_t d_ff,
+                                      cudaStream_t st);
 // two such independent problems in one launch when both are aligned for the pipelined
 // kernel (16-byte rows and buffers), else two launches; same results as two calls
 cudaError_t launch_transpose_cat2(const GradPtrs& srcs0, int n0, int64_t rows0, int64_t cols0, uint16_t* dst0,
@@ -77,9 +81,11 @@ int launch_fsdp_gemm_row_split(int a_shards, const uint16_t* const* A, float* co
                                const uint16_t* W, int64_t rows_out, int64_t k_in, float alpha, cudaStream_t st);
 // H[M, d_ff] (bf16) = silu(X W_gate^T) * (X W_up^T), gate and up given as n_ranks row
 // shards each (d_ff / n_ranks rows, a multiple of 128, or n_ranks = 1 with full weights).
+// GU (nullable, [M, 2 d_ff] bf16) also receives the two projections G | U, rounded from the
+// same fp32 accumulators (the activations the backward needs).
 int launch_fsdp_gate_up(int n_ranks, const uint16_t* const* gate_shards, const uint16_t* const* up_shards,
                         int64_t d_ff, int64_t d_model, const uint16_t* X, int64_t m_tokens, uint16_t* H,
-                        cudaStream_t st);
+                        cudaStream_t st, uint16_t* GU = nullptr);
 // Backward GEMMs reading operands in place as MN-major tiles:
 // dX_q[M, K] = dY_q W for the dy_pieces row pieces of dY / dX (dy_pieces = 1: one rank),
 // with W read in place from its n_ranks row shards (R / n_ranks a multiple of 64);

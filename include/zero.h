@@ -409,6 +409,66 @@ ZERO_API int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* un
                              void* workspace, uint64_t workspace_bytes, zero_stream_t stream,
                              zero_stream_t prefetch_stream);
 
+/* The ZeRO-3 state of one weight [rows, cols] of an FSDP unit. */
+typedef struct {
+  const zero_plan_t* plan; /* zero_plan(rows * cols, N, ZERO_STAGE_3, any bucket): rank r's shard = rows
+                              [r*rows/N, (r+1)*rows/N), flat elements [r*S, (r+1)*S) */
+  zero_bf16* w;            /* [rows, cols] bf16, the N row shards back to back; the step writes the new shards */
+  float *master, *m, *v;   /* [rows * cols] fp32 each, rank r's shard at r*S; updated in place */
+} fsdp_weight_state;
+
+/* One Mistral-style FSDP MLP unit: H = silu(X W_gate^T) * (X W_up^T), Y = H W_down^T, for all
+ * N simulated ranks (M tokens each; rank q's rows of every [N*M, .] buffer are [q*M, (q+1)*M)). */
+typedef struct {
+  int64_t d_model, d_ff;
+  fsdp_weight_state gate, up; /* W_gate, W_up [d_ff, d_model] */
+  fsdp_weight_state down;     /* W_down [d_model, d_ff] */
+  zero_bf16* x;     /* [N*M, d_model]: the input. Unit 0: the caller's batch (read); unit i > 0: written by
+                       the forward (unit i-1's output) */
+  zero_bf16* gu;    /* out, [N*M, 2*d_ff]: G | U = X W_gate^T | X W_up^T, rounded from the fp32 accumulators
+                       (the activations the backward reads) */
+  zero_bf16* h;     /* out, [N*M, d_ff]: H, the down projection's input */
+  zero_bf16* dy;    /* [N*M, d_model]: the gradient of the unit's output. Last unit: the caller's (read);
+                       unit i < last: written by unit i+1's backward */
+  zero_bf16* dh;    /* out, [N*M, d_ff]: dH = dY W_down */
+  zero_bf16* dgu;   /* out, [N*M, 2*d_ff]: dG | dU, the SiLU-gate backward of dH */
+  float* dw_gu;     /* out, [2*d_ff, d_model]: (1/N) sum_q [dG | dU]_q^T X_q = dW_gate (rows 0..d_ff-1)
+                       stacked on dW_up (rows d_ff..): each rank's reduce-scattered rows feed its Adam */
+  float* dw_down;   /* out, [d_model, d_ff]: (1/N) sum_q dY_q^T H_q */
+} fsdp_mlp_unit_state;
+
+/* Bytes of device workspace fsdp_zero3_mlp_step needs: one slot for the gathered W^T of the
+ * unit in use (W_down^T, then [W_gate; W_up]^T: 4*d_ff*d_model bytes at most) and one for
+ * the dW GEMMs' laid-out operand (the narrower of dY and H, then of [dG | dU] and X, as a
+ * transpose: 2*min(.)*N*M bytes), the largest over the units, each rounded up to 256 bytes. */
+ZERO_API int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsdp_mlp_unit_state* units,
+                                           int64_t m_tokens, uint64_t* bytes);
+
+/* One ZeRO-3 training step of a stack of n_units FSDP MLP units for all N ranks, each unit
+ * following its life on a card ([Interview] Fig. 2; "FSDP" item: gather before use, free
+ * after, reduce-scatter the gradient):
+ *   forward, unit 0 -> last: G | U and H = silu(G) * U in one tensor-core kernel (the gate
+ *     and up shards gathered inside its loads), then X_{i+1} = bf16(H W_down^T) (the last
+ *     unit's output to y_out; skipped when NULL);
+ *   backward, last -> unit 0: W_down gathered again as W_down^T; dH = bf16(dY W_down);
+ *     dW_down = (1/N) sum_q dY_q^T H_q; each rank's Adam on its W_down shard; dG | dU by the
+ *     SiLU-gate backward (s = 1/(1 + exp(-g)): dU = dH g s, dG = dH U s (1 + g (1 - s)), fp32
+ *     from the saved bf16 G, U and dH, rounded to bf16); [W_gate; W_up] gathered as its
+ *     transpose; dY_{i-1} = bf16([dG | dU] [W_gate; W_up]) (unit 0: into dx_out, skipped
+ *     when NULL); dW_gate | dW_up = (1/N) sum_q [dG | dU]_q^T X_q; each rank's Adam on its
+ *     W_gate and W_up shards. Every weight's update follows its last read.
+ * The reduce over ranks happens inside the fp32 accumulation of each dW GEMM; rank r's
+ * reduce-scattered gradient is its rows. GEMM outputs are fp32 sums of exact bf16 products
+ * in an unspecified order, rounded once to bf16 where the output is bf16; Adam is bit-exact as
+ * zero_adam_step. All work is ordered on `stream`.
+ * Requires 1 <= N <= 16, 1 <= n_units <= 64, N*M % 8 == 0, d_model and d_ff multiples of 64,
+ * unit i+1's d_model equal to unit i's, (d_ff / N) % 128 == 0 and d_model / N tiling the fused
+ * gather ((d_model / N) % 128 == 0; 256 under zero_set_gemm_kernel(1)); 16-byte-aligned
+ * buffers; workspace of fsdp_zero3_mlp_step_workspace() bytes. */
+ZERO_API int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit_state* units, int64_t m_tokens,
+                                 zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step,
+                                 void* workspace, uint64_t workspace_bytes, zero_stream_t stream);
+
 /* Allocation-free variant of fsdp_unit_forward, for callers that cannot allocate device
  * memory where they run the unit (e.g. a plug-in inside a framework that owns all device
  * memory through its own pool, or a latency-critical path that cannot take cudaMalloc's
