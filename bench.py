@@ -1216,20 +1216,20 @@ def run_case(args):
                                                      stream=stream, prefetch_stream=side), 2, stream)
         flop = sum(6.0 * n * m * R * K for R, K in ZERO3_SHAPES)
         out.update(n_ranks=n, tokens_per_rank=m, ms=ms, tflops=flop / ms / 1e9)
-    elif args.case == "zero3_mlp_step":
+    elif args.case in ("zero3_mlp_step", "zero3_mlp_small"):
         # one ZeRO-3 step over 2 Mistral-7B MLP units, N = 8 ranks x 1024 tokens (about
-        # 10 GB on the device), 3 steps
-        n, m = 8, 1024
-        units = zero3_mlp_units(z, synth, dev, n, m)
-        ws = torch.empty(z.fsdp_zero3_mlp_step_workspace(n, [(4096, 14336)] * MLP_UNITS, m), dtype=torch.uint8,
+        # 10 GB on the device), 3 steps; zero3_mlp_small: one unit, 8 x 256 tokens (2.7 GB)
+        n, m, nu = (8, 1024, MLP_UNITS) if args.case == "zero3_mlp_step" else (8, 256, 1)
+        units = zero3_mlp_units(z, synth, dev, n, m, n_units=nu)
+        ws = torch.empty(z.fsdp_zero3_mlp_step_workspace(n, [(4096, 14336)] * nu, m), dtype=torch.uint8,
                          device=dev)
         y = torch.empty(n * m, 4096, dtype=torch.bfloat16, device=dev)
         dx = torch.empty(n * m, 4096, dtype=torch.bfloat16, device=dev)
         hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
         ms = time_launches(lambda: z.fsdp_zero3_mlp_step(units, m, hp, 1, y_out=y, dx_out=dx, workspace=ws,
                                                          stream=stream), 2, stream)
-        flop = MLP_UNITS * 9 * 2.0 * n * m * 4096 * 14336
-        out.update(n_ranks=n, tokens_per_rank=m, units=MLP_UNITS, ms=ms, tflops=flop / ms / 1e9)
+        flop = nu * 9 * 2.0 * n * m * 4096 * 14336
+        out.update(n_ranks=n, tokens_per_rank=m, units=nu, ms=ms, tflops=flop / ms / 1e9)
     elif args.case == "backward_up":
         # FSDP unit backward of W_up [14336, 4096] in 8 row shards, 2048 tokens per rank
         # (dY 470 MB, X 134 MB, dX 268 MB, dW 235 MB, X^T workspace 134 MB): 3 launches
@@ -1254,7 +1254,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="one measured case: fused_small | fused_tma_small | megatron_small | e2e_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
-                         "backward_up | rank_view_small | zero3_step | zero3_mlp_step (ncu-sized) | "
+                         "backward_up | rank_view_small | zero3_step | zero3_mlp_step | zero3_mlp_small (ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
