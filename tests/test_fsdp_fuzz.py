@@ -79,3 +79,50 @@ def test_random_backward_pair_kernel_everywhere_bit_identical(z, i):
     for q in range(n):
         assert torch.equal(outs[0][0][q], outs[1][0][q]), f"dX of rank {q}: n={n} rows={rows} k={k} m={m}"
     assert torch.equal(outs[0][1], outs[1][1]), f"dW: n={n} rows={rows} k={k} m={m}"
+
+
+def zero3_case(i):
+    """A random stack of linear units for fsdp_zero3_step: N, unit count, chained shapes
+    (rows_out a multiple of 64 and of N, k_in of 8, the larger of the two of 64), tokens per
+    rank (N M a multiple of 8, ragged K blocks in dW), flags."""
+    rng = np.random.default_rng(5000 + i)
+    n = int(rng.choice([1, 2, 3, 4, 8]))
+    flags = int(rng.choice([0, 1, 2, 3, 4, 6, 7]))
+    fused_rows = n * 128 * int(rng.integers(1, 4))  # shards that tile the fused gather
+    shapes, k = [], 64 * int(rng.integers(1, 9))
+    for _ in range(int(rng.integers(1, 4))):
+        r = fused_rows if not flags & 1 or rng.random() < 0.5 else 64 * n * int(rng.integers(1, 5))
+        shapes.append((r, k))
+        k = r
+    m = int(rng.integers(8, 200))
+    while (n * m) % 8:
+        m += 1
+    return n, shapes, m, flags
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_random_zero3_step(z, i):
+    import test_fsdp_zero3 as Z3
+    n, shapes, m, flags = zero3_case(i)
+    units = Z3.make_units(z, n, shapes, m, key=50 + i)
+    for t in (1, 2):
+        before = Z3.snapshot(units)
+        y, dx = Z3.run_step(z, units, m, t, flags, prefetch=bool(flags & 6))
+        Z3.check_step(z, n, m, before, units, y, dx, t)
+
+
+@pytest.mark.parametrize("i", range(4))
+def test_random_zero3_mlp_step(z, i):
+    import test_fsdp_zero3_mlp as ZM
+    rng = np.random.default_rng(6000 + i)
+    n = int(rng.choice([1, 2, 4]))
+    d = n * 128 * int(rng.integers(1, 4))
+    f = n * 128 * int(rng.integers(1, 4))
+    m = int(rng.integers(8, 120))
+    while (n * m) % 8:
+        m += 1
+    units = ZM.make_units(z, n, d, f, int(rng.integers(1, 3)), m, key=60 + i)
+    for t in (1, 2):
+        before = ZM.snapshot(units)
+        y, dx = ZM.run_step(z, units, m, t)
+        ZM.check_step(n, m, before, units, y, dx, t)
