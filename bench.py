@@ -563,21 +563,29 @@ def zero3_mlp_leg(z, synth, dev, tf_peak, stream):
         dx = torch.empty(nm, 4096, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(z.fsdp_zero3_mlp_step_workspace(n, [(4096, 14336)] * MLP_UNITS, m), dtype=torch.uint8,
                          device=dev)
-        t = [0]
-
-        def step():
-            t[0] += 1
-            z.fsdp_zero3_mlp_step(units, m, HP, t[0], y_out=y, dx_out=dx, workspace=ws, stream=stream)
-
-        ms = time_launches(step, 10, stream)
-        z.zero_device_status(stream)
         flop = MLP_UNITS * 3 * 3 * 2.0 * nm * 4096 * 14336  # 3 matrices, forward + 2 backward GEMMs each
-        res.update(ms=ms, tflops=flop / ms / 1e9, frac_of_bf16_peak=flop / ms / 1e9 / tf_peak,
+        # the fused optimizer (the default) writes no dW; the separate form reads it back
+        no_dw = [{k: v for k, v in u.items() if k not in ("dw_gu", "dw_down")} for u in units]
+        for name, flags, us in (("fused_optimizer", 0, no_dw), ("separate_optimizer", z.FSDP_SEPARATE_OPTIMIZER,
+                                                                 units)):
+            t = [0]
+
+            def step():
+                t[0] += 1
+                z.fsdp_zero3_mlp_step(us, m, HP, t[0], y_out=y, dx_out=dx, workspace=ws, stream=stream, flags=flags)
+
+            ms = time_launches(step, 10, stream)
+            res[name] = {"ms": ms, "tflops": flop / ms / 1e9, "frac_of_bf16_peak": flop / ms / 1e9 / tf_peak}
+        z.zero_device_status(stream)
+        res.update(ms=res["fused_optimizer"]["ms"], tflops=res["fused_optimizer"]["tflops"],
+                   frac_of_bf16_peak=res["fused_optimizer"]["frac_of_bf16_peak"],
+                   fused_optimizer_gain=res["separate_optimizer"]["ms"] / res["fused_optimizer"]["ms"] - 1.0,
                    gemm_flop_per_step=flop, workspace_bytes=ws.numel(),
                    adam_bytes_per_step=MLP_UNITS * 3 * 30 * 4096 * 14336,
                    silu_backward_bytes_per_step=MLP_UNITS * 10 * nm * 14336,
-                   note="tflops counts the GEMM flops over the whole step, which also holds the Adam launches, the "
-                        "SiLU-gate backward and the W^T / operand transposes")
+                   note="tflops counts the GEMM flops over the whole step, which also holds each rank's Adam (fused "
+                        "into the dW GEMMs' epilogues, or separate), the SiLU-gate backward and the W^T / operand "
+                        "transposes")
     except Exception as e:  # the leg must not hide the step's line
         res["error"] = str(e)[:300]
     return res
@@ -620,16 +628,20 @@ def zero3_leg(z, synth, dev, tf_peak, hbm_peak, stream):
         adam_bytes = sum(30 * R * K for R, K in ZERO3_SHAPES)
         res["gemm_flop_per_step"] = flop
         res["adam_bytes_per_step"] = adam_bytes
-        P, O, G = z.FSDP_BACKWARD_PREFETCH, z.FSDP_OVERLAP_OPTIMIZER, z.FSDP_GATHER_MATERIALIZE
-        for name, flags, pf in (("serial", 0, None), ("prefetch", P, side), ("overlap_optimizer", O, side),
-                                ("prefetch_overlap_optimizer", P | O, side),
+        P, O, G, S = (z.FSDP_BACKWARD_PREFETCH, z.FSDP_OVERLAP_OPTIMIZER, z.FSDP_GATHER_MATERIALIZE,
+                      z.FSDP_SEPARATE_OPTIMIZER)
+        # the fused optimizer (the default) writes no dW; the separate forms read it back
+        no_dw = [{k: v for k, v in u.items() if k != "dw"} for u in units]
+        for name, flags, pf in (("serial", 0, None), ("separate_optimizer", S, None), ("prefetch", P, side),
+                                ("overlap_optimizer", O, side), ("prefetch_overlap_optimizer", P | O, side),
                                 ("materialized_serial", G, None), ("materialized_prefetch", G | P, side)):
             ws = torch.empty(z.fsdp_zero3_step_workspace(n, ZERO3_SHAPES, m, flags), dtype=torch.uint8, device=dev)
             t = [0]
+            us = units if flags & (S | O) else no_dw
 
             def step():
                 t[0] += 1
-                z.fsdp_zero3_step(units, m, HP, t[0], y_out=y, dx_out=dx, flags=flags, workspace=ws, stream=stream,
+                z.fsdp_zero3_step(us, m, HP, t[0], y_out=y, dx_out=dx, flags=flags, workspace=ws, stream=stream,
                                   prefetch_stream=pf)
 
             ms = time_launches(step, 10, stream)
@@ -637,12 +649,14 @@ def zero3_leg(z, synth, dev, tf_peak, hbm_peak, stream):
                          "workspace_bytes": ws.numel()}
             del ws
         z.zero_device_status(stream)
+        res["fused_optimizer_gain"] = res["separate_optimizer"]["ms"] / res["serial"]["ms"] - 1.0
         res["prefetch_gain"] = res["serial"]["ms"] / res["prefetch"]["ms"] - 1.0
         res["overlap_optimizer_gain"] = res["serial"]["ms"] / res["overlap_optimizer"]["ms"] - 1.0
         res["materialized_prefetch_gain"] = (res["materialized_serial"]["ms"] / res["materialized_prefetch"]["ms"]
                                              - 1.0)
         res["note"] = ("tflops counts the 12 GEMMs' flops (6 N M R K per unit) over the whole step, which also holds "
-                       "4 Adam launches (30 B per parameter) and 4 X^T layouts")
+                       "each rank's Adam (fused into the dW GEMMs' epilogues unless separate) and the operand "
+                       "layouts")
     except Exception as e:  # the leg must not hide the step's line
         res["error"] = str(e)[:300]
     return res
@@ -1203,10 +1217,11 @@ def run_case(args):
                    gather_gbs=byts / ms_g / 1e6, transpose_gbs=byts / ms_t / 1e6)
     elif args.case == "zero3_step":
         # one ZeRO-3 step over the 4 Mistral-shaped units, N = 8 ranks x 1024 tokens, each
-        # unit's Adam on a second stream (about 7 GB on the device), 3 steps
+        # rank's Adam fused into the dW GEMMs (about 7 GB on the device), 3 steps
         n, m = 8, 1024
         units = zero3_units(z, synth, dev, n, m)
-        flags = z.FSDP_OVERLAP_OPTIMIZER
+        flags = 0  # each rank's Adam fused into the dW GEMMs
+        units = [{k: v for k, v in u.items() if k != "dw"} for u in units]
         ws = torch.empty(z.fsdp_zero3_step_workspace(n, ZERO3_SHAPES, m, flags), dtype=torch.uint8, device=dev)
         y = torch.empty(n * m, ZERO3_SHAPES[-1][0], dtype=torch.bfloat16, device=dev)
         dx = torch.empty(n * m, ZERO3_SHAPES[0][1], dtype=torch.bfloat16, device=dev)
@@ -1226,6 +1241,7 @@ def run_case(args):
         y = torch.empty(n * m, 4096, dtype=torch.bfloat16, device=dev)
         dx = torch.empty(n * m, 4096, dtype=torch.bfloat16, device=dev)
         hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
+        units = [{k: v for k, v in u.items() if k not in ("dw_gu", "dw_down")} for u in units]  # fused Adam
         ms = time_launches(lambda: z.fsdp_zero3_mlp_step(units, m, hp, 1, y_out=y, dx_out=dx, workspace=ws,
                                                          stream=stream), 2, stream)
         flop = nu * 9 * 2.0 * n * m * 4096 * 14336

@@ -81,6 +81,7 @@ class fsdp_mlp_unit_state(C.Structure):
 FSDP_GATHER_MATERIALIZE = 1
 FSDP_BACKWARD_PREFETCH = 2
 FSDP_OVERLAP_OPTIMIZER = 4
+FSDP_SEPARATE_OPTIMIZER = 8
 
 
 class zero_adam(C.Structure):
@@ -125,8 +126,8 @@ def _load():
         "fsdp_zero3_step": (I, [I, I, C.POINTER(fsdp_unit_state), I64, VP, VP, C.POINTER(zero_adam), I64, I, VP, U64,
                                 VP, VP]),
         "fsdp_zero3_mlp_step_workspace": (I, [I, I, C.POINTER(fsdp_mlp_unit_state), I64, C.POINTER(U64)]),
-        "fsdp_zero3_mlp_step": (I, [I, I, C.POINTER(fsdp_mlp_unit_state), I64, VP, VP, C.POINTER(zero_adam), I64, VP,
-                                    U64, VP]),
+        "fsdp_zero3_mlp_step": (I, [I, I, C.POINTER(fsdp_mlp_unit_state), I64, VP, VP, C.POINTER(zero_adam), I64, I,
+                                    VP, U64, VP]),
         "zero_set_gemm_kernel": (I, [I]),
         "zero_version": (I, []),
     }
@@ -445,10 +446,10 @@ def _unit_array(units, shapes_only=False):
             raise ValueError(f"units[{i}].x must be [N*M, {k}] (got {tuple(u['x'].shape)})")
         if u["dy"].dim() != 2 or tuple(u["dy"].shape) != (nm, rows):
             raise ValueError(f"units[{i}].dy must be [{nm}, {rows}] (got {tuple(u['dy'].shape)})")
-        _need(u["dw"], rows * k, f"units[{i}].dw")
+        _need(u.get("dw"), rows * k, f"units[{i}].dw")
         arr[i].x = _dev(u["x"], torch.bfloat16, f"units[{i}].x")
         arr[i].dy = _dev(u["dy"], torch.bfloat16, f"units[{i}].dy")
-        arr[i].dw = _dev(u["dw"], torch.float32, f"units[{i}].dw")
+        arr[i].dw = _dev(u.get("dw"), torch.float32, f"units[{i}].dw")
     return arr
 
 
@@ -505,10 +506,10 @@ def _mlp_unit_array(units, nm=None):
             if u[k].dim() != 2 or tuple(u[k].shape) != (nm, cols):
                 raise ValueError(f"units[{i}].{k} must be [{nm}, {cols}] (got {tuple(u[k].shape)})")
             setattr(arr[i], k, _dev(u[k], torch.bfloat16, f"units[{i}].{k}"))
-        _need(u["dw_gu"], 2 * f * d, f"units[{i}].dw_gu")
-        _need(u["dw_down"], d * f, f"units[{i}].dw_down")
-        arr[i].dw_gu = _dev(u["dw_gu"], torch.float32, f"units[{i}].dw_gu")
-        arr[i].dw_down = _dev(u["dw_down"], torch.float32, f"units[{i}].dw_down")
+        _need(u.get("dw_gu"), 2 * f * d, f"units[{i}].dw_gu")
+        _need(u.get("dw_down"), d * f, f"units[{i}].dw_down")
+        arr[i].dw_gu = _dev(u.get("dw_gu"), torch.float32, f"units[{i}].dw_gu")
+        arr[i].dw_down = _dev(u.get("dw_down"), torch.float32, f"units[{i}].dw_down")
     return arr
 
 
@@ -520,9 +521,11 @@ def fsdp_zero3_mlp_step_workspace(n_ranks: int, shapes, m_tokens: int) -> int:
     return b.value
 
 
-def fsdp_zero3_mlp_step(units, m_tokens: int, hp, step: int, y_out=None, dx_out=None, workspace=None, stream=None):
+def fsdp_zero3_mlp_step(units, m_tokens: int, hp, step: int, y_out=None, dx_out=None, workspace=None, stream=None,
+                        flags: int = 0):
     """units: one dict per MLP unit with d_model, d_ff; gate / up / down as dicts of plan,
-    w, master, m, v; and x, gu, h, dy, dh, dgu (bf16) and dw_gu, dw_down (fp32)."""
+    w, master, m, v; and x, gu, h, dy, dh, dgu (bf16) and dw_gu, dw_down (fp32, or None
+    when the optimizer is fused, the default)."""
     if not units:
         raise ValueError("units is empty")
     n = units[0]["gate"]["plan"].n_ranks
@@ -533,8 +536,8 @@ def fsdp_zero3_mlp_step(units, m_tokens: int, hp, step: int, y_out=None, dx_out=
     a = _adam(hp)
     _check(_lib.fsdp_zero3_mlp_step(
         n, len(arr), arr, m_tokens, _dev(y_out, torch.bfloat16, "y_out"), _dev(dx_out, torch.bfloat16, "dx_out"),
-        C.byref(a), step, _dev(workspace, torch.uint8, "workspace"), 0 if workspace is None else workspace.numel(),
-        _stream(stream)))
+        C.byref(a), step, flags, _dev(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
 def fsdp_mlp_forward(gate_shards, up_shards, down_shards, X, H, Y, scratch_down=None, stream=None,

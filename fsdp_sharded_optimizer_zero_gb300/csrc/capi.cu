@@ -241,6 +241,10 @@ int zgb::check_adam_args(const zero_adam* hp, int64_t step, const char* who) {
   return make_scalars(hp, step, 1, who, &sc);
 }
 
+int zgb::make_adam_scalars(const zero_adam* hp, int64_t step, const char* who, AdamScalars* sc) {
+  return make_scalars(hp, step, 1, who, sc);
+}
+
 namespace {
 
 int load_grads(const zero_bf16* const grads[], int n, uint64_t off, const char* who, GradPtrs* gp) {

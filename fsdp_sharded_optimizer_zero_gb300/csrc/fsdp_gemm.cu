@@ -104,6 +104,7 @@ struct GemmParams {
   int y_tma;                     // write Y through shared memory and TMA stores
   CUtensorMap ybmap;             // bf16-only output: Y_bf16 [M, R], box 64 x 32, 128B swizzle (yb_tma)
   int yb_tma;                    // no fp32 Y: write bf16 Y through shared memory and TMA stores
+  AdamFuse adam;                 // plain mode with the fused optimizer: the state the output indexes
 };
 constexpr uint32_t kMnChunk = 64 * BK * 2;  // one 64-column chunk of an MN-major stage operand: 8 KiB
 
@@ -165,6 +166,73 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, in
   }
 }
 
+// Fused optimizer. Measured on GB300 (the ZeRO-3 steps, against the same Adam as its own
+// launch): per-lane row loads of the state ran 6-14 % slower, whatever their order; staging
+// the chunk and walking rows with one column per lane (coalesced 128-byte lines), 16 rows
+// in flight, 4 % slower; 32 rows in flight, level; plus L2 prefetches two chunks ahead,
+// -3 to +1 %. The epilogue is bound by the state loads' latency: 128 threads hold ~48 KB in
+// flight per SM against the ~100 KB that HBM's bandwidth-latency product asks for.
+//
+// fused optimizer on one 32 x 32 chunk of the fp32 result, staged in shared memory (buf,
+// 128-byte rows, 16-byte piece j of row i at slot j ^ (i % 8)): result (i, c) is the
+// reduced gradient of parameter (row0 + i - split) * R + col0 + c of the weight set the
+// chunk's rows belong to (a chunk's 32 rows never straddle the split: it is a multiple of
+// 128). The warp walks the chunk's rows with one column per lane, so every state access
+// is one contiguous 128-byte line; all 32 rows' loads are in flight before their arithmetic.
+// adam_elem: the same operations as the Adam kernels (same bits).
+constexpr int kAdamRows = 32;  // rows of a staged chunk whose state loads are in flight together
+// L2 prefetch of the optimizer state the chunk at columns col0 .. col0 + 31 of rows
+// row0 .. row0 + 31 will read: lane i takes row row0 + i, one 128-byte line per array
+__device__ __forceinline__ void adam_prefetch_chunk(const GemmParams& p, int row0, int col0, int lane) {
+  const int row = row0 + lane;
+  if (col0 >= p.r || row >= p.m) return;
+  const int set = row0 >= p.adam.split ? 1 : 0;
+  const size_t idx = static_cast<size_t>(row - (set ? p.adam.split : 0)) * p.r + col0;
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p.adam.master[set] + idx));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p.adam.m[set] + idx));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p.adam.v[set] + idx));
+}
+__device__ __forceinline__ void adam_chunk_rows(const GemmParams& p, const uint8_t* buf, int row0, int col0,
+                                                int lane) {
+  const int col = col0 + lane;
+  if (col >= p.r || row0 >= p.m) return;
+  const int set = row0 >= p.adam.split ? 1 : 0;
+  const size_t first = static_cast<size_t>(row0 - (set ? p.adam.split : 0)) * p.r + col;
+  float* W = p.adam.master[set] + first;
+  float* M = p.adam.m[set] + first;
+  float* V = p.adam.v[set] + first;
+  uint16_t* P = p.adam.w[set] + first;
+  const size_t R = static_cast<size_t>(p.r);
+  const int rows = min(32, p.m - row0);
+  const uint32_t piece = static_cast<uint32_t>(lane) >> 2, word = static_cast<uint32_t>(lane) & 3u;
+#pragma unroll 1
+  for (int i0 = 0; i0 < rows; i0 += kAdamRows) {
+    float g[kAdamRows], w[kAdamRows], m[kAdamRows], v[kAdamRows];
+#pragma unroll
+    for (int k = 0; k < kAdamRows; ++k) {
+      const int i = i0 + k;
+      if (i < rows) {
+        g[k] = *reinterpret_cast<const float*>(buf + i * 128 + ((piece ^ (static_cast<uint32_t>(i) & 7u)) * 16) +
+                                               word * 4);
+        w[k] = __ldcs(W + i * R);
+        m[k] = __ldcs(M + i * R);
+        v[k] = __ldcs(V + i * R);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kAdamRows; ++k) {
+      const int i = i0 + k;
+      if (i < rows) {
+        adam_elem(g[k], w[k], m[k], v[k], p.adam.sc);
+        __stcs(W + i * R, w[k]);
+        __stcs(M + i * R, m[k]);
+        __stcs(V + i * R, v[k]);
+        P[i * R] = f32_to_bf16_bits(w[k]);
+      }
+    }
+  }
+}
+
 // gate-up epilogue: h = silu(g) * u = g / (1 + exp(-g)) * u in fp32, stored as bf16 (RNE)
 __device__ __forceinline__ void store_gate_up_chunk(const GemmParams& p, int row, int col0, const uint32_t (&g)[32],
                                                     const uint32_t (&u)[32]) {
@@ -216,7 +284,7 @@ __device__ __forceinline__ void store_gate_up_chunk(const GemmParams& p, int row
 // is complete: warp quarter q reads TMEM lanes [32q, 32q + 32) (tile rows 32q + lane) at
 // taddr, stages its chunks in its 8 KiB of shared memory at epi for TMA stores, and writes
 // rows m0 + 32q + lane, columns n0 .. n0 + TN of Y (row piece ash, local row ml) or of H.
-template <bool GATE_UP>
+template <bool GATE_UP, bool ADAM = false>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, uint8_t* epi, uint32_t& epi_chunk,
                                               int m0, int n0, int ash, int ml, int q, int lane) {
   constexpr int TN = Mode<GATE_UP>::TN;
@@ -268,14 +336,41 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
       ++epi_chunk;
     }
   } else {
+    if constexpr (ADAM) {  // the first two chunks' state on its way to L2
+      adam_prefetch_chunk(p, m0 + q * 32, n0, lane);
+      adam_prefetch_chunk(p, m0 + q * 32, n0 + 32, lane);
+    }
 #pragma unroll 1
     for (int c = 0; c < TN; c += 32) {
       uint32_t r[32];
       tmem_ld_32cols(taddr + c, r);
       if (n0 + c >= p.r) continue;  // warp-uniform
+      if constexpr (ADAM) {
+        if (c + 64 < TN) adam_prefetch_chunk(p, m0 + q * 32, n0 + c + 64, lane);
+      }
       if (p.alpha != 1.0f) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), p.alpha));
+      }
+      if constexpr (ADAM) {
+        // stage the chunk as the fp32 TMA-store path does, optionally store it as Y, then
+        // run the optimizer over it row by row
+        uint8_t* buf = epi + (epi_chunk & 1u) * 4096u;
+        if (lane == 0 && epi_chunk >= 2) bulk_wait_group_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+              make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (p.y_tma && lane == 0) {
+          tma_store_2d(&p.ymap[ash], n0 + c, ml + q * 32, smem_u32(buf));
+          bulk_commit_group();
+        }
+        ++epi_chunk;
+        adam_chunk_rows(p, buf, m0 + q * 32, n0 + c, lane);
+        continue;
       }
       if (p.y_tma) {
         // lane = row of a 32 x 32 chunk: 128-byte rows, 16-byte pieces placed with the
@@ -296,8 +391,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
         }
         ++epi_chunk;
         if (p.yb && row < p.m) store_row_chunk(p, row, n0 + c, r, false);
-      } else if (row < p.m) {
-        store_row_chunk(p, row, n0 + c, r, true);
+      } else if (row < p.m && (p.y || p.yb)) {
+        store_row_chunk(p, row, n0 + c, r, p.y != nullptr);
       }
     }
   }
@@ -308,7 +403,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
 // the stage) share every A tile through one N = 256 MMA per K step; their two 128-column
 // accumulators sit side by side in one 256-column TMEM buffer and the epilogue writes
 // H = silu(gate) * up for a 128 x 128 tile.
-template <bool GATE_UP>
+template <bool GATE_UP, bool ADAM = false>
 __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr int TN = Mode<GATE_UP>::TN;                      // output tile columns
   constexpr uint32_t BT_BYTES = Mode<GATE_UP>::BT_BYTES;    // one B tile (two in gate-up mode)
@@ -471,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
       const int ml = m0 - ash * p.y_shard_rows;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * ACC;
       uint8_t* epi = smem + STAGES * STAGE_BYTES + static_cast<uint32_t>(q) * 2u * 4096u;
-      epilogue_tile<GATE_UP>(p, taddr, epi, epi_chunk, m0, n0, ash, ml, q, lane);
+      epilogue_tile<GATE_UP, ADAM>(p, taddr, epi, epi_chunk, m0, n0, ash, ml, q, lane);
       tc_fence_before();
       mbar_arrive(smem_u32(&acce_bar[a]));
     }
@@ -528,7 +623,7 @@ __device__ __forceinline__ void pair_tile_coords(int tile, int num_m, int num_n,
   nb = in_band / rows;
 }
 
-template <bool GATE_UP>
+template <bool GATE_UP, bool ADAM = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fsdp_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   constexpr int TN = Mode<GATE_UP>::TN;  // output tile columns: 256, or 128 of H in gate-up mode
@@ -681,7 +776,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int ash = min(m0 / p.y_shard_rows, y_pieces - 1);  // the Y row piece (rows past M: clipped)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * PAIR_ACC;
       uint8_t* epi = smem + PAIR_STAGES * PAIR_STAGE + static_cast<uint32_t>(q) * 2u * 4096u;
-      epilogue_tile<GATE_UP>(p, taddr, epi, epi_chunk, m0, nb * TN, ash, m0 - ash * p.y_shard_rows, q, lane);
+      epilogue_tile<GATE_UP, ADAM>(p, taddr, epi, epi_chunk, m0, nb * TN, ash, m0 - ash * p.y_shard_rows, q, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acce_bar[a]), 0));
@@ -704,7 +799,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 std::atomic<int> g_gemm_kernel{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-OncePerDevice g_attr_once[2];
+OncePerDevice g_attr_once[4];  // gate-up, plain, each with and without the fused optimizer
 
 int get_encode() {
   std::call_once(g_encode_once, [] {
@@ -762,12 +857,64 @@ struct Operand {
   int64_t piece_rows;
 };
 
+// One of the kernels: gate-up or plain, plain with the fused optimizer (ADAM), on CTA
+// pairs or one CTA per tile.
+template <bool GATE_UP, bool ADAM>
+int launch_variant(const GemmParams& p, bool pair, int64_t m_tokens, int64_t rows_out, cudaStream_t st,
+                   const char* who) {
+  constexpr int TN = GATE_UP ? 128 : BN;
+  constexpr int V = (GATE_UP ? 1 : 0) + (ADAM ? 2 : 0);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+  const cudaError_t attr = g_attr_once[V].run(dev, [] {
+    cudaError_t a = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP, ADAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Mode<GATE_UP>::SMEM);
+    if (a == cudaSuccess)
+      a = cudaFuncSetAttribute(fsdp_gemm_pair_kernel<GATE_UP, ADAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PAIR_SMEM);
+    return a;
+  });
+  if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(attr));
+  if (pair) {
+    // one 256-row tile per CTA pair at a time, as many pairs as can be resident at once: a
+    // persistent grid larger than that runs its last clusters as a second wave (a 4-CTA
+    // variant with 38 clusters where 36 fit ran at half speed). On GB300 all 76 pairs fit.
+    static int max_pairs[4][64];
+    static std::once_flag pairs_once[4][64];
+    std::call_once(pairs_once[V][dev & 63], [&] {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * std::max(1, num_sms() / 2), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = PAIR_SMEM;
+      int nc = 0;
+      if (cudaOccupancyMaxActiveClusters(&nc, fsdp_gemm_pair_kernel<GATE_UP, ADAM>, &cfg) != cudaSuccess || nc < 1) {
+        (void)cudaGetLastError();
+        nc = std::max(1, num_sms() / 2);
+      }
+      max_pairs[V][dev & 63] = std::min(nc, std::max(1, num_sms() / 2));
+    });
+    const int64_t tiles = ((m_tokens + 255) / 256) * ((rows_out + TN - 1) / TN);
+    const unsigned int pairs = static_cast<unsigned int>(std::min<int64_t>(tiles, max_pairs[V][dev & 63]));
+    fsdp_gemm_pair_kernel<GATE_UP, ADAM><<<2 * pairs, kThreads, PAIR_SMEM, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
+    return ZERO_OK;
+  }
+  const int64_t tiles = ((m_tokens + BM - 1) / BM) * ((rows_out + TN - 1) / TN);
+  const unsigned int grid = static_cast<unsigned int>(std::min<int64_t>(tiles, num_sms()));
+  fsdp_gemm_kernel<GATE_UP, ADAM><<<grid, kThreads, Mode<GATE_UP>::SMEM, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
+  return ZERO_OK;
+}
+
 // Y (y_pieces row pieces) = alpha * A * B^T, M x R, inner dimension K. GATE_UP: B and B2
 // are the gate and up shards (K-major) and Y_bf16 receives H = silu(gate) * up.
 template <bool GATE_UP>
 int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, int64_t m_tokens, int64_t rows_out,
                 int64_t k_in, float* const* Y, int y_pieces, uint16_t* Y_bf16, float alpha, cudaStream_t st,
-                const char* who, uint16_t* GU = nullptr) {
+                const char* who, uint16_t* GU = nullptr, const AdamFuse* adam = nullptr) {
   constexpr int TN = GATE_UP ? 128 : BN;
   if (m_tokens > INT32_MAX / 2 || rows_out > INT32_MAX / 2 || k_in > INT32_MAX / 2)
     return set_error(ZERO_ERR_INVALID_ARG, "%s: sizes must be below 2^30", who);
@@ -817,7 +964,20 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
   }
   const int64_t y_rows = m_tokens / y_pieces;
   const bool no_f32 = Y == nullptr || Y[0] == nullptr;
-  if (!GATE_UP && no_f32) {  // bf16-only output through TMA stores
+  if (adam) {
+    // the fused optimizer consumes the fp32 result in the epilogue; Y (fp32) may still be
+    // written beside it, a bf16-only output may not
+    bool ok = !GATE_UP && y_pieces == 1 && !Y_bf16 && rows_out % 8 == 0;
+    for (int s = 0; ok && s < 2; ++s)
+      ok = (reinterpret_cast<uintptr_t>(adam->master[s]) | reinterpret_cast<uintptr_t>(adam->m[s]) |
+            reinterpret_cast<uintptr_t>(adam->v[s]) | reinterpret_cast<uintptr_t>(adam->w[s])) % 16 == 0 &&
+           adam->master[s] && adam->m[s] && adam->v[s] && adam->w[s];
+    if (!ok)
+      return set_error(ZERO_ERR_UNSUPPORTED,
+                       "%s: the fused optimizer needs one fp32 output piece, rows of a multiple of 8 and 16-byte-"
+                       "aligned state",
+                       who);
+  } else if (!GATE_UP && no_f32) {  // bf16-only output through TMA stores
     if (!Y_bf16 || y_pieces != 1 || rows_out % 8 || (reinterpret_cast<uintptr_t>(Y_bf16) & 15))
       return set_error(ZERO_ERR_UNSUPPORTED,
                        "%s: a bf16-only output needs one 16-byte-aligned Y_bf16 with rows_out %% 8 == 0", who);
@@ -842,6 +1002,7 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
   p.b_mn = B.mn ? 1 : 0;
   p.yb = Y_bf16;
   p.gu = GATE_UP ? GU : nullptr;
+  if (adam) p.adam = *adam;
   p.alpha = alpha;
   p.m = static_cast<int>(m_tokens);
   p.r = static_cast<int>(rows_out);
@@ -849,49 +1010,8 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
   p.shard_rows = static_cast<int>(B.piece_rows);
   p.n_shards = B.pieces;
 
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
-  const cudaError_t attr = g_attr_once[GATE_UP ? 1 : 0].run(dev, [] {
-    cudaError_t a = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Mode<GATE_UP>::SMEM);
-    if (a == cudaSuccess)
-      a = cudaFuncSetAttribute(fsdp_gemm_pair_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               PAIR_SMEM);
-    return a;
-  });
-  if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(attr));
-  if (pair) {
-    // one 256-row tile per CTA pair at a time, as many pairs as can be resident at once: a
-    // persistent grid larger than that runs its last clusters as a second wave (a 4-CTA
-    // variant with 38 clusters where 36 fit ran at half speed). On GB300 all 76 pairs fit.
-    static int max_pairs[2][64];
-    static std::once_flag pairs_once[2][64];
-    std::call_once(pairs_once[GATE_UP ? 1 : 0][dev & 63], [&] {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * std::max(1, num_sms() / 2), 1, 1);
-      cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = PAIR_SMEM;
-      int nc = 0;
-      if (cudaOccupancyMaxActiveClusters(&nc, fsdp_gemm_pair_kernel<GATE_UP>, &cfg) != cudaSuccess || nc < 1) {
-        (void)cudaGetLastError();
-        nc = std::max(1, num_sms() / 2);
-      }
-      max_pairs[GATE_UP ? 1 : 0][dev & 63] = std::min(nc, std::max(1, num_sms() / 2));
-    });
-    const int64_t tiles = ((m_tokens + 255) / 256) * ((rows_out + TN - 1) / TN);
-    const unsigned int pairs = static_cast<unsigned int>(std::min<int64_t>(tiles, max_pairs[GATE_UP ? 1 : 0][dev & 63]));
-    fsdp_gemm_pair_kernel<GATE_UP><<<2 * pairs, kThreads, PAIR_SMEM, st>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
-    return ZERO_OK;
-  }
-  const int64_t tiles = ((m_tokens + BM - 1) / BM) * ((rows_out + TN - 1) / TN);
-  const unsigned int grid = static_cast<unsigned int>(std::min<int64_t>(tiles, num_sms()));
-  fsdp_gemm_kernel<GATE_UP><<<grid, kThreads, Mode<GATE_UP>::SMEM, st>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
-  return ZERO_OK;
+  if (adam) return launch_variant<false, true>(p, pair, m_tokens, rows_out, st, who);
+  return launch_variant<GATE_UP, false>(p, pair, m_tokens, rows_out, st, who);
 }
 
 }  // namespace
@@ -945,20 +1065,21 @@ bool fsdp_fused_gather_ok(int n_ranks, int64_t rows_out) {
 }
 
 int launch_fsdp_bwd_dw_x_mn(int x_pieces, const uint16_t* dYt, const uint16_t* const* X, int64_t piece_rows,
-                            int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st) {
+                            int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st,
+                            const AdamFuse* adam) {
   const uint16_t* a1[1] = {dYt};
   float* y1[1] = {dW};
   return launch_gemm<false>({1, a1, false, rows_out}, {x_pieces, X, true, piece_rows}, nullptr, rows_out, k_in,
-                            piece_rows * x_pieces, y1, 1, nullptr, alpha, st, "fsdp_unit_backward");
+                            piece_rows * x_pieces, y1, 1, nullptr, alpha, st, "fsdp_unit_backward", nullptr, adam);
 }
 
 int launch_fsdp_bwd_dw_alpha(const uint16_t* dY, int64_t nm, const uint16_t* Xt, int64_t rows_out, int64_t k_in,
-                             float* dW, float alpha, cudaStream_t st) {
+                             float* dW, float alpha, cudaStream_t st, const AdamFuse* adam) {
   const uint16_t* dy1[1] = {dY};
   const uint16_t* xt1[1] = {Xt};
   float* y1[1] = {dW};
   return launch_gemm<false>({1, dy1, true, nm}, {1, xt1, false, k_in}, nullptr, rows_out, k_in, nm, y1, 1, nullptr,
-                            alpha, st, "fsdp_zero3_step");
+                            alpha, st, "fsdp_zero3_step", nullptr, adam);
 }
 
 int set_gemm_kernel(int which) {

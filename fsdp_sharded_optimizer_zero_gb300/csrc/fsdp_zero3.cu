@@ -24,13 +24,17 @@
 // GEMM that writes dY_{i-1}), into the other of two slots; events order each slot's reuse
 // and each unit's start. Forward prefetch stays off (the pages' default).
 //
-// Ordering inside a unit's backward: dX (reads W_i) and dW, then Adam writes the new W_i
-// shards. Unit i's W is not read again in this step (unit i-1's backward reads W_{i-1} and
-// the dY that unit i produced from the old W_i), so the update can follow each unit. With
-// FSDP_OVERLAP_OPTIMIZER that Adam runs on the prefetch stream once unit i's dW is done,
-// beside the following units' GEMMs: the update kernel is HBM bound and uses no shared
-// memory, so it fits on the SMs next to a persistent GEMM, which leaves most of the DRAM
-// bandwidth idle.
+// Ordering inside a unit's backward: dX (reads W_i), then dW with each rank's Adam, which
+// writes the new W_i shards. Unit i's W is not read again in this step (unit i-1's backward
+// reads W_{i-1} and the dY that unit i produced from the old W_i), so the update can follow
+// each unit. By default the update is fused into the dW GEMM's epilogue: rank r's
+// reduce-scattered gradient is rows [r R/N, (r+1) R/N) of dW, the same flat elements as its
+// shard, so the epilogue applies Adam to each fp32 result as it leaves the accumulator
+// (the same operations as zero_adam_step, the same bits). dW then needs no HBM round trip
+// (it is written only when the caller passes dw), and the update's state traffic runs
+// beside the GEMM's tensor work instead of after it. FSDP_SEPARATE_OPTIMIZER keeps
+// zero_adam_step as its own launch after the dW GEMM; FSDP_OVERLAP_OPTIMIZER puts that
+// launch on the prefetch stream, beside the following units' GEMMs.
 #include <string.h>
 
 #include <algorithm>
@@ -101,7 +105,7 @@ int check_units(int n, int n_units, const fsdp_unit_state* u, int64_t m, int fla
   if (!u) return set_error(ZERO_ERR_INVALID_ARG, "%s: units is NULL", kWho);
   if (m < 1 || (static_cast<int64_t>(n) * m) % 8)
     return set_error(ZERO_ERR_INVALID_ARG, "%s: n_ranks * m_tokens must be a positive multiple of 8", kWho);
-  if (flags & ~(FSDP_GATHER_MATERIALIZE | FSDP_BACKWARD_PREFETCH | FSDP_OVERLAP_OPTIMIZER))
+  if (flags & ~(FSDP_GATHER_MATERIALIZE | FSDP_BACKWARD_PREFETCH | FSDP_OVERLAP_OPTIMIZER | FSDP_SEPARATE_OPTIMIZER))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: unknown flags 0x%x", kWho, flags);
   for (int i = 0; i < n_units; ++i) {
     const fsdp_unit_state& s = u[i];
@@ -130,7 +134,9 @@ int check_units(int n, int n_units, const fsdp_unit_state* u, int64_t m, int fla
         L.stage != ZERO_STAGE_3)
       return set_error(ZERO_ERR_INVALID_ARG,
                        "%s: unit %d: the plan must be zero_plan(rows_out * k_in, n_ranks, ZERO_STAGE_3, ...)", kWho, i);
-    if (!s.w || !s.master || !s.m || !s.v || !s.x || !s.dy || !s.dw)
+    // dw is read by a separate optimizer launch; with the fused update it is optional
+    const bool need_dw = (flags & (FSDP_OVERLAP_OPTIMIZER | FSDP_SEPARATE_OPTIMIZER)) != 0;
+    if (!s.w || !s.master || !s.m || !s.v || !s.x || !s.dy || (need_dw && !s.dw))
       return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: a buffer is NULL", kWho, i);
     if (!aligned16(s.w) || !aligned16(s.master) || !aligned16(s.m) || !aligned16(s.v) || !aligned16(s.x) ||
         !aligned16(s.dy) || !aligned16(s.dw))
@@ -170,6 +176,9 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
   cudaStream_t pf = (flags & FSDP_BACKWARD_PREFETCH) ? side : st;
   const bool overlap = pf != st;
   const bool adam_side = (flags & FSDP_OVERLAP_OPTIMIZER) && side != st;
+  const bool adam_separate = (flags & (FSDP_OVERLAP_OPTIMIZER | FSDP_SEPARATE_OPTIMIZER)) != 0;
+  AdamScalars sc;
+  if ((rc = make_adam_scalars(hp, step, kWho, &sc))) return rc;
   const int64_t nm = static_cast<int64_t>(n) * m_tokens;
   uint8_t* base = static_cast<uint8_t*>(workspace);
   auto xt_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.xt_off[i % ws.slots]); };
@@ -261,19 +270,23 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
       if (i > 0 && (rc = prepare(i - 1, pf))) return rc;  // overlaps this unit's dW GEMM and Adam
     }
     // dW = (1/N) dY_i^T X_i: X^T laid out and dY read in place, or dY^T laid out and X read
-    // in place, whichever of the two is narrower
+    // in place, whichever of the two is narrower; by default with each rank's Adam on its
+    // rows in the epilogue
     const float inv_n = 1.0f / static_cast<float>(n);
+    const AdamFuse fuse = {{s.master, s.master}, {s.m, s.m}, {s.v, s.v}, {s.w, s.w}, s.rows_out, sc};
+    const AdamFuse* af = adam_separate ? nullptr : &fuse;
     if (t_dy(i)) {
       const uint16_t* x1[1] = {s.x};
-      rc = launch_fsdp_bwd_dw_x_mn(1, xt_slot(i), x1, nm, s.rows_out, s.k_in, s.dw, inv_n, st);
+      rc = launch_fsdp_bwd_dw_x_mn(1, xt_slot(i), x1, nm, s.rows_out, s.k_in, s.dw, inv_n, st, af);
     } else {
-      rc = launch_fsdp_bwd_dw_alpha(s.dy, nm, xt_slot(i), s.rows_out, s.k_in, s.dw, inv_n, st);
+      rc = launch_fsdp_bwd_dw_alpha(s.dy, nm, xt_slot(i), s.rows_out, s.k_in, s.dw, inv_n, st, af);
     }
     if (rc) return rc;
     if ((overlap || adam_side) && (rc = record(ev_done(i), st))) return rc;
-    // each rank's Adam on its shard (rows r R/N .. of dW): every rank's shard in one launch,
-    // on `stream` or, overlapped, on the side stream after this unit's dW
-    if (adam_side) {
+    // with a separate optimizer: each rank's Adam on its shard (rows r R/N .. of dW), every
+    // rank's shard in one launch, on `stream` or, overlapped, on the side stream
+    if (!adam_separate) {
+    } else if (adam_side) {
       if ((rc = wait(side, ev_done(i))) ||
           (rc = zero_adam_step(s.plan, ZERO_ALL_RANKS, s.dw, s.master, s.m, s.v, s.w, hp, step,
                                reinterpret_cast<zero_stream_t>(side))))
@@ -345,7 +358,7 @@ int check_weight(const fsdp_weight_state& w, int64_t rows, int64_t cols, int n, 
   return ZERO_OK;
 }
 
-int check_mlp_units(int n, int L, const fsdp_mlp_unit_state* u, int64_t m, bool buffers) {
+int check_mlp_units(int n, int L, const fsdp_mlp_unit_state* u, int64_t m, bool buffers, bool need_dw = false) {
   if (n < 1 || n > kGemmMaxPieces)
     return set_error(ZERO_ERR_INVALID_ARG, "%s: n_ranks %d outside 1..%d", kWhoMlp, n, kGemmMaxPieces);
   if (L < 1 || L > 64) return set_error(ZERO_ERR_INVALID_ARG, "%s: n_units %d outside 1..64", kWhoMlp, L);
@@ -373,8 +386,11 @@ int check_mlp_units(int n, int L, const fsdp_mlp_unit_state* u, int64_t m, bool 
         (rc = check_weight(s.down, d, f, n, i, "down")))
       return rc;
     const void* bufs[] = {s.x, s.gu, s.h, s.dy, s.dh, s.dgu, s.dw_gu, s.dw_down};
-    for (const void* b : bufs) {
-      if (!b) return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: an activation or gradient buffer is NULL", kWhoMlp, i);
+    for (int k = 0; k < 8; ++k) {
+      const void* b = bufs[k];
+      // dw_gu and dw_down (the last two) are optional when the optimizer is fused
+      if (!b && (k < 6 || need_dw))
+        return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: an activation or gradient buffer is NULL", kWhoMlp, i);
       if (!aligned16(b))
         return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: activation and gradient buffers must be 16-byte aligned",
                          kWhoMlp, i);
@@ -387,12 +403,12 @@ int check_mlp_units(int n, int L, const fsdp_mlp_unit_state* u, int64_t m, bool 
 // t (laid out by the caller): dY^T [R, nm] when K > R (X read in place), else X^T [K, nm]
 // (dY read in place)
 int dw_gemm(const uint16_t* dy, const uint16_t* x, const uint16_t* t, int64_t R, int64_t K, int64_t nm, float* dw,
-            float alpha, cudaStream_t st) {
+            float alpha, cudaStream_t st, const AdamFuse* af) {
   if (K > R) {
     const uint16_t* x1[1] = {x};
-    return launch_fsdp_bwd_dw_x_mn(1, t, x1, nm, R, K, dw, alpha, st);
+    return launch_fsdp_bwd_dw_x_mn(1, t, x1, nm, R, K, dw, alpha, st, af);
   }
-  return launch_fsdp_bwd_dw_alpha(dy, nm, t, R, K, dw, alpha, st);
+  return launch_fsdp_bwd_dw_alpha(dy, nm, t, R, K, dw, alpha, st, af);
 }
 
 }  // namespace
@@ -407,12 +423,16 @@ extern "C" int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsd
 }
 
 extern "C" int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit_state* units, int64_t m_tokens,
-                                   zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step,
+                                   zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step, int flags,
                                    void* workspace, uint64_t workspace_bytes, zero_stream_t stream) {
   const int n = n_ranks, L = n_units;
-  int rc = check_mlp_units(n, L, units, m_tokens, true);
+  if (flags & ~FSDP_SEPARATE_OPTIMIZER)
+    return set_error(ZERO_ERR_INVALID_ARG, "%s: unknown flags 0x%x", kWhoMlp, flags);
+  const bool separate = (flags & FSDP_SEPARATE_OPTIMIZER) != 0;
+  int rc = check_mlp_units(n, L, units, m_tokens, true, separate);
   if (rc) return rc;
-  if ((rc = check_adam_args(hp, step, kWhoMlp))) return rc;
+  AdamScalars sc;
+  if ((rc = make_adam_scalars(hp, step, kWhoMlp, &sc))) return rc;
   if ((y_out && !aligned16(y_out)) || (dx_out && !aligned16(dx_out)))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: y_out and dx_out must be 16-byte aligned", kWhoMlp);
   const MlpWorkspace ws = mlp_workspace(n, L, units, m_tokens);
@@ -464,9 +484,12 @@ extern "C" int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit
     // dH [nm, f] = bf16(dY [nm, d] * (W_down^T [f, d])^T)
     const uint16_t* wt1[1] = {wt};
     if ((rc = launch_fsdp_gemm(1, wt1, f, d, s.dy, nm, nullptr, s.dh, 1.0f, st))) return rc;
-    if ((rc = dw_gemm(s.dy, s.h, tr, d, f, nm, s.dw_down, inv_n, st))) return rc;
-    if ((rc = zero_adam_step(s.down.plan, ZERO_ALL_RANKS, s.dw_down, s.down.master, s.down.m, s.down.v, s.down.w, hp,
-                             step, stream)))
+    // dW_down with W_down's Adam fused into its epilogue (or as its own launch)
+    const AdamFuse fd = {{s.down.master, s.down.master}, {s.down.m, s.down.m}, {s.down.v, s.down.v},
+                         {s.down.w, s.down.w}, d, sc};
+    if ((rc = dw_gemm(s.dy, s.h, tr, d, f, nm, s.dw_down, inv_n, st, separate ? nullptr : &fd))) return rc;
+    if (separate && (rc = zero_adam_step(s.down.plan, ZERO_ALL_RANKS, s.dw_down, s.down.master, s.down.m, s.down.v,
+                                         s.down.w, hp, step, stream)))
       return rc;
     // dG | dU from dH and the saved G | U
     cudaError_t e = launch_silu_gate_backward(s.dh, s.gu, s.dgu, nm, f, st);
@@ -482,11 +505,15 @@ extern "C" int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit
     // projections' input gradients over the concatenated K
     zero_bf16* dx = i > 0 ? units[i - 1].dy : dx_out;
     if (dx && (rc = launch_fsdp_gemm(1, wt1, d, 2 * f, s.dgu, nm, nullptr, dx, 1.0f, st))) return rc;
-    if ((rc = dw_gemm(s.dgu, s.x, tr, 2 * f, d, nm, s.dw_gu, inv_n, st))) return rc;
-    if ((rc = zero_adam_step(s.gate.plan, ZERO_ALL_RANKS, s.dw_gu, s.gate.master, s.gate.m, s.gate.v, s.gate.w, hp,
-                             step, stream)) ||
-        (rc = zero_adam_step(s.up.plan, ZERO_ALL_RANKS, s.dw_gu + f * d, s.up.master, s.up.m, s.up.v, s.up.w, hp,
-                             step, stream)))
+    // dW_gate | dW_up with both weights' Adam fused into its epilogue (rows < d_ff: W_gate)
+    const AdamFuse fgu = {{s.gate.master, s.up.master}, {s.gate.m, s.up.m}, {s.gate.v, s.up.v}, {s.gate.w, s.up.w},
+                          f, sc};
+    if ((rc = dw_gemm(s.dgu, s.x, tr, 2 * f, d, nm, s.dw_gu, inv_n, st, separate ? nullptr : &fgu))) return rc;
+    if (separate &&
+        ((rc = zero_adam_step(s.gate.plan, ZERO_ALL_RANKS, s.dw_gu, s.gate.master, s.gate.m, s.gate.v, s.gate.w, hp,
+                              step, stream)) ||
+         (rc = zero_adam_step(s.up.plan, ZERO_ALL_RANKS, s.dw_gu + f * d, s.up.master, s.up.m, s.up.v, s.up.w, hp,
+                              step, stream))))
       return rc;
   }
   return ZERO_OK;

@@ -71,6 +71,19 @@ cudaError_t launch_transpose_cat2(const GradPtrs& srcs0, int n0, int64_t rows0, 
                                   cudaStream_t st);
 
 // ---- FSDP GEMM (fsdp_gemm.cu) ----
+// Adam fused into a weight-gradient GEMM's epilogue: output element (row, col) of the
+// [rows, r] fp32 result is the reduced gradient of parameter (row - split*s) * r + col of
+// weight set s = (row >= split), whose fp32 master / m / v are updated and whose bf16 value
+// is written, in the same operation order as zero_adam_step (same bits). Two sets serve a
+// result that stacks two weights (W_gate rows, then W_up rows).
+struct AdamFuse {
+  float* master[2];
+  float* m[2];
+  float* v[2];
+  uint16_t* w[2];
+  int64_t split;  // rows of set 0 (>= rows for one set)
+  AdamScalars sc;
+};
 // Y[M, R] = alpha * A[M, K] * W^T with W given as n_ranks row shards of R/n_ranks rows
 // each (n_ranks = 1 with the full W for the materialised path). Both operands K-major.
 int launch_fsdp_gemm(int n_ranks, const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in,
@@ -103,12 +116,13 @@ int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* X
 // contiguous [N M, K]), the K loop over the tokens: the cheaper form when X is the wider of
 // the two (K > R). Same bits as the form above.
 int launch_fsdp_bwd_dw_x_mn(int x_pieces, const uint16_t* dYt, const uint16_t* const* X, int64_t piece_rows,
-                            int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st);
+                            int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st,
+                            const AdamFuse* adam = nullptr);
 // dW over one contiguous dY for all ranks (rank q's rows at q M): dW [R, K] = alpha dY^T
 // [R, NM] (X^T [K, NM])^T with dY read in place as one MN-major piece. Bit-identical to the
 // per-rank form above.
 int launch_fsdp_bwd_dw_alpha(const uint16_t* dY, int64_t nm, const uint16_t* Xt, int64_t rows_out, int64_t k_in,
-                             float* dW, float alpha, cudaStream_t st);
+                             float* dW, float alpha, cudaStream_t st, const AdamFuse* adam = nullptr);
 unsigned int fsdp_gemm_read_clear_error();
 int set_gemm_kernel(int which);  // 0 = default, 1 = one-CTA kernel everywhere, 2 = CTA-pair kernel everywhere
 
@@ -142,6 +156,8 @@ bool fsdp_fused_gather_ok(int n_ranks, int64_t rows_out);
 int set_error(int code, const char* fmt, ...);
 // Adam hyper-parameters and step validated as the step calls do (ZERO_ERR_INVALID_ARG)
 int check_adam_args(const zero_adam* hp, int64_t step, const char* who);
+// ... and turned into the scalars every Adam kernel takes (bias corrections of `step`)
+int make_adam_scalars(const zero_adam* hp, int64_t step, const char* who, AdamScalars* sc);
 int num_sms();
 
 }  // namespace zgb

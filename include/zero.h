@@ -356,7 +356,8 @@ typedef struct {
   zero_bf16* dy;           /* [N*M, rows_out] bf16: the gradient of the unit's output. Last unit: the caller's
                               loss gradient (read); unit i < last: written by unit i+1's backward (its dX) */
   float* dw;               /* out, [rows_out, k_in] fp32: dW = (1/N) sum_q dY_q^T X_q; rank r's reduce-scattered
-                              gradient = rows [r*R/N, (r+1)*R/N), which its Adam consumes */
+                              gradient = rows [r*R/N, (r+1)*R/N), which its Adam consumes. May be NULL (not
+                              written) unless the optimizer runs as its own launch */
 } fsdp_unit_state;
 
 /* flags of fsdp_zero3_step */
@@ -366,8 +367,13 @@ typedef struct {
                                      The backward always gathers W^T into the slot (below). */
 #define FSDP_BACKWARD_PREFETCH 2  /* issue unit i-1's gather and dW operand layout on prefetch_stream while
                                      unit i's backward GEMMs run on `stream` */
-#define FSDP_OVERLAP_OPTIMIZER 4  /* run unit i's Adam on prefetch_stream once its dW is done, beside the
-                                     following units' backward GEMMs on `stream` */
+#define FSDP_OVERLAP_OPTIMIZER 4  /* run unit i's Adam as its own launch on prefetch_stream once its dW is
+                                     done, beside the following units' backward GEMMs on `stream` */
+#define FSDP_SEPARATE_OPTIMIZER 8 /* run each Adam as its own launch (zero_adam_step) after the dW GEMM on
+                                     `stream`. Without this flag or the one above, each rank's Adam is fused
+                                     into the dW GEMM's epilogue: it updates the shard's fp32 state and writes
+                                     its bf16 values from the fp32 result as it leaves the accumulator (the
+                                     same operations, the same bits), and dW is written only if given */
 
 /* Bytes of device workspace fsdp_zero3_step needs for these units, M tokens per rank and
  * flags: one slot (two with FSDP_BACKWARD_PREFETCH) holding the dW GEMM's laid-out operand
@@ -387,8 +393,9 @@ ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit
  *     NULL) with both GEMM operands K-major, dW_i = (1/N) sum_q dY_{i,q}^T X_{i,q} (the narrower
  *     of X_i and dY_i laid out transposed in the same launch as W_i^T, the other read in place; the reduce of the
  *     reduce-scatter inside the fp32 tensor-core accumulation, rank r keeping its rows),
- *     then each rank's Adam on its shard (zero_adam_step, ZERO_ALL_RANKS: every rank's
- *     shard in one launch) writing the new bf16 shards of W_i — after W_i's last use;
+ *     then each rank's Adam on its shard (the operations of zero_adam_step, fused into the
+ *     dW GEMM's epilogue by default) writing the new bf16 shards of W_i — after W_i's last
+ *     use;
  *   with FSDP_BACKWARD_PREFETCH, unit i-1's gather and dW operand layout run on
  *     prefetch_stream while unit i computes ([Interview] follow-up "FSDP 怎么把通信藏起来?":
  *     the all-gather on its own stream, the backward prefetching the next unit's);
@@ -433,8 +440,9 @@ typedef struct {
   zero_bf16* dh;    /* out, [N*M, d_ff]: dH = dY W_down */
   zero_bf16* dgu;   /* out, [N*M, 2*d_ff]: dG | dU, the SiLU-gate backward of dH */
   float* dw_gu;     /* out, [2*d_ff, d_model]: (1/N) sum_q [dG | dU]_q^T X_q = dW_gate (rows 0..d_ff-1)
-                       stacked on dW_up (rows d_ff..): each rank's reduce-scattered rows feed its Adam */
-  float* dw_down;   /* out, [d_model, d_ff]: (1/N) sum_q dY_q^T H_q */
+                       stacked on dW_up (rows d_ff..): each rank's reduce-scattered rows feed its Adam.
+                       May be NULL (not written) unless FSDP_SEPARATE_OPTIMIZER */
+  float* dw_down;   /* out, [d_model, d_ff]: (1/N) sum_q dY_q^T H_q; NULL as dw_gu */
 } fsdp_mlp_unit_state;
 
 /* Bytes of device workspace fsdp_zero3_mlp_step needs: one slot for the gathered W^T of the
@@ -451,12 +459,13 @@ ZERO_API int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsdp_
  *     and up shards gathered inside its loads), then X_{i+1} = bf16(H W_down^T) (the last
  *     unit's output to y_out; skipped when NULL);
  *   backward, last -> unit 0: W_down gathered again as W_down^T; dH = bf16(dY W_down);
- *     dW_down = (1/N) sum_q dY_q^T H_q; each rank's Adam on its W_down shard; dG | dU by the
+ *     dW_down = (1/N) sum_q dY_q^T H_q with each rank's Adam on its W_down shard in the GEMM's
+ *     epilogue (or, with FSDP_SEPARATE_OPTIMIZER in flags, as its own launch); dG | dU by the
  *     SiLU-gate backward (s = 1/(1 + exp(-g)): dU = dH g s, dG = dH U s (1 + g (1 - s)), fp32
  *     from the saved bf16 G, U and dH, rounded to bf16); [W_gate; W_up] gathered as its
  *     transpose; dY_{i-1} = bf16([dG | dU] [W_gate; W_up]) (unit 0: into dx_out, skipped
- *     when NULL); dW_gate | dW_up = (1/N) sum_q [dG | dU]_q^T X_q; each rank's Adam on its
- *     W_gate and W_up shards. Every weight's update follows its last read.
+ *     when NULL); dW_gate | dW_up = (1/N) sum_q [dG | dU]_q^T X_q with each rank's Adam on its
+ *     W_gate and W_up shards in the same way. Every weight's update follows its last read.
  * The reduce over ranks happens inside the fp32 accumulation of each dW GEMM; rank r's
  * reduce-scattered gradient is its rows. GEMM outputs are fp32 sums of exact bf16 products
  * in an unspecified order, rounded once to bf16 where the output is bf16; Adam is bit-exact as
@@ -466,7 +475,7 @@ ZERO_API int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsdp_
  * gather ((d_model / N) % 128 == 0; 256 under zero_set_gemm_kernel(1)); 16-byte-aligned
  * buffers; workspace of fsdp_zero3_mlp_step_workspace() bytes. */
 ZERO_API int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit_state* units, int64_t m_tokens,
-                                 zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step,
+                                 zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step, int flags,
                                  void* workspace, uint64_t workspace_bytes, zero_stream_t stream);
 
 /* Allocation-free variant of fsdp_unit_forward, for callers that cannot allocate device

@@ -273,7 +273,7 @@ def test_zero3_step_rejects_bad_arguments_before_launch(z):
     assert call(units(good, p2)) == -1
     assert call(units(good)) == -1                               # no plans
     assert call(units(good, plans, fill=0x10008)) == -1          # misaligned buffers
-    assert call(units(good, plans), flags=8) == -1               # unknown flag
+    assert call(units(good, plans), flags=16) == -1              # unknown flag
     assert call(units(good, plans), step=0) == -1                # Adam step counts from 1
     bad = z._lib.zero_adam(1e-4, 1.0, 0.999, 1e-8, 0.0)
     assert call(units(good, plans), hp=bad) == -1                # beta1 outside [0, 1)

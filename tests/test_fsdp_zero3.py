@@ -170,12 +170,13 @@ def test_zero3_step_every_buffer_vs_oracle(z, n, shapes, m, flags):
 
 @pytest.mark.parametrize("n,shapes,m", [(4, [(512, 256), (1024, 512), (512, 1024)], 96), (2, [(256, 64), (256, 256)], 200)])
 def test_zero3_step_flags_give_the_same_bits(z, n, shapes, m):
-    """Fused or materialised gather, serial, with the prefetch stream, with Adam on the side
-    stream: same bits in every buffer, over two steps."""
+    """Fused or materialised gather, serial, with the prefetch stream, with Adam fused into
+    the dW GEMM (the default), as its own launch or on the side stream: same bits in every
+    buffer, over two steps."""
     base = make_units(z, n, shapes, m, key=7)
     results = []
     for flags, prefetch in ((0, False), (2, True), (1, False), (3, True), (2, False), (4, True), (6, True), (7, True),
-                            (4, False)):
+                            (4, False), (8, False), (10, True), (9, True)):
         units = clone_units(base)
         for t in (1, 2):
             y_out, dx_out = run_step(z, units, m, t, flags, prefetch=prefetch)
@@ -189,6 +190,27 @@ def test_zero3_step_flags_give_the_same_bits(z, n, shapes, m):
                 assert torch.equal(a[key].view(torch.int16), b[key].view(torch.int16)), key
             for key in ("master", "m", "v", "dw"):
                 assert torch.equal(a[key].view(torch.int32), b[key].view(torch.int32)), key
+
+
+def test_zero3_step_without_dw_output_same_update(z):
+    """With the optimizer fused into the dW GEMM (the default), dW need not be written: a
+    step with dw = None leaves master, m, v, the shards and every activation bit for bit as
+    a step that writes dW, over two steps."""
+    n, shapes, m = 4, [(512, 256), (1024, 512), (512, 1024)], 100
+    a = make_units(z, n, shapes, m, key=13)
+    b = clone_units(a)
+    for u in b:
+        u.pop("dw")
+    for t in (1, 2):
+        ya, dxa = run_step(z, a, m, t, 0)
+        yb, dxb = run_step(z, b, m, t, 0)
+        assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
+        assert torch.equal(dxa.view(torch.int16), dxb.view(torch.int16))
+    for ua, ub in zip(a, b):
+        for key in ("w", "x", "dy"):
+            assert torch.equal(ua[key].view(torch.int16), ub[key].view(torch.int16)), key
+        for key in ("master", "m", "v"):
+            assert torch.equal(ua[key].view(torch.int32), ub[key].view(torch.int32)), key
 
 
 def test_zero3_step_units_equal_standalone_calls(z):

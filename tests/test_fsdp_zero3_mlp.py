@@ -64,14 +64,14 @@ def make_units(z, n, d, f, n_units, m, key):
     return units
 
 
-def run_step(z, units, m, step):
+def run_step(z, units, m, step, flags=0):
     n = units[0]["gate"]["plan"].n_ranks
     nm = n * m
     shapes = [(u["d_model"], u["d_ff"]) for u in units]
     ws = torch.empty(z.fsdp_zero3_mlp_step_workspace(n, shapes, m), dtype=torch.uint8, device=DEV)
     y = torch.full((nm, shapes[-1][0]), float("nan"), dtype=torch.bfloat16, device=DEV)
     dx = torch.full((nm, shapes[0][0]), float("nan"), dtype=torch.bfloat16, device=DEV)
-    z.fsdp_zero3_mlp_step(units, m, HP, step, y_out=y, dx_out=dx, workspace=ws)
+    z.fsdp_zero3_mlp_step(units, m, HP, step, y_out=y, dx_out=dx, workspace=ws, flags=flags)
     z.zero_device_status()
     return y, dx
 
@@ -203,6 +203,46 @@ def test_zero3_mlp_step_every_buffer_vs_oracle(z, n, d, f, n_units, m):
         before = snapshot(units)
         y, dx = run_step(z, units, m, t)
         check_step(n, m, before, units, y, dx, t)
+
+
+def clone(units):
+    out = []
+    for u in units:
+        c = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in u.items()}
+        for w in ("gate", "up", "down"):
+            c[w] = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in u[w].items()}
+        out.append(c)
+    return out
+
+
+def test_zero3_mlp_optimizer_fused_or_separate_same_bits(z):
+    """Adam fused into the dW GEMMs' epilogues (the default, here once with dW written and
+    once without) and Adam as its own launches (FSDP_SEPARATE_OPTIMIZER) leave every
+    buffer bit for bit the same, over two steps."""
+    n, d, f, m = 4, 512, 512, 100
+    base = make_units(z, n, d, f, 2, m, key=21)
+    runs = {"fused": clone(base), "fused_no_dw": clone(base), "separate": clone(base)}
+    for u in runs["fused_no_dw"]:
+        u.pop("dw_gu")
+        u.pop("dw_down")
+    outs = {}
+    for name, units in runs.items():
+        for t in (1, 2):
+            outs[name] = run_step(z, units, m, t, flags=z.FSDP_SEPARATE_OPTIMIZER if name == "separate" else 0)
+    ref = runs["separate"]
+    for name in ("fused", "fused_no_dw"):
+        for a, b in zip(outs[name], outs["separate"]):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
+        for ua, ub in zip(runs[name], ref):
+            for key in ("x", "gu", "h", "dy", "dh", "dgu"):
+                assert torch.equal(ua[key].view(torch.int16), ub[key].view(torch.int16)), (name, key)
+            for w in ("gate", "up", "down"):
+                assert torch.equal(ua[w]["w"].view(torch.int16), ub[w]["w"].view(torch.int16)), (name, w)
+                for key in ("master", "m", "v"):
+                    assert torch.equal(ua[w][key].view(torch.int32), ub[w][key].view(torch.int32)), (name, w, key)
+    for ua, ub in zip(runs["fused"], ref):
+        for key in ("dw_gu", "dw_down"):
+            assert torch.equal(ua[key].view(torch.int32), ub[key].view(torch.int32)), key
 
 
 def test_zero3_mlp_forward_equals_the_mlp_forward_call(z):
