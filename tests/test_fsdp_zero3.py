@@ -245,3 +245,43 @@ def test_zero3_step_units_equal_standalone_calls(z):
     z.zero_device_status()
     assert torch.equal(master.view(torch.int32), units[1]["master"].view(torch.int32))
     assert torch.equal(w.view(torch.int16), units[1]["w"].view(-1).view(torch.int16))
+
+
+@pytest.mark.parametrize("flags", [0, 2, 6, 8, 3])
+def test_zero3_step_replays_from_a_cuda_graph(z, flags):
+    """The step is plain stream work (host-encoded tensor maps by value, no allocation, the
+    prefetch stream forked and joined through events), so it can be captured once in a CUDA
+    graph: two replays leave every buffer bit for bit as two eager calls of the same step."""
+    n, shapes, m = 4, [(512, 256), (1024, 512), (512, 1024)], 100
+    a = make_units(z, n, shapes, m, key=17)
+    b = clone_units(a)
+    side = torch.cuda.Stream()
+    ws = {k: torch.empty(z.fsdp_zero3_step_workspace(n, shapes, m, flags), dtype=torch.uint8, device=DEV)
+          for k in ("a", "b", "c")}
+    out = {k: (torch.empty(n * m, shapes[-1][0], dtype=torch.bfloat16, device=DEV),
+               torch.empty(n * m, shapes[0][1], dtype=torch.bfloat16, device=DEV)) for k in ("a", "b", "c")}
+
+    def run(units, k, stream):
+        z.fsdp_zero3_step(units, m, HP, 1, y_out=out[k][0], dx_out=out[k][1], flags=flags, workspace=ws[k],
+                          stream=stream, prefetch_stream=side)
+
+    run(clone_units(a), "c", torch.cuda.current_stream())  # warm-up: events, kernel attributes
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            run(b, "b", cap)
+    for _ in range(2):
+        run(a, "a", torch.cuda.current_stream())
+        g.replay()
+        torch.cuda.synchronize()
+        z.zero_device_status()
+        for x, y in zip(out["a"], out["b"]):
+            assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+        for ua, ub in zip(a, b):
+            for key in ("w", "x", "dy"):
+                assert torch.equal(ua[key].view(torch.int16), ub[key].view(torch.int16)), key
+            for key in ("master", "m", "v", "dw"):
+                assert torch.equal(ua[key].view(torch.int32), ub[key].view(torch.int32)), key

@@ -267,3 +267,46 @@ def test_zero3_mlp_step_rejects_bad_shapes(z):
     assert e.value.code == -1
     with pytest.raises(z.ZeroError):
         z.fsdp_zero3_mlp_step_workspace(4, [(512, 512), (256, 512)], 64)  # d_model changes
+
+
+@pytest.mark.parametrize("flags", [0, 8])
+def test_zero3_mlp_step_replays_from_a_cuda_graph(z, flags):
+    """Captured once in a CUDA graph, two replays of the MLP step leave every buffer bit for
+    bit as two eager calls of the same step."""
+    n, d, f, m = 2, 256, 512, 64
+    a = make_units(z, n, d, f, 2, m, key=27)
+    b = clone(a)
+    shapes = [(d, f)] * 2
+    ws = {k: torch.empty(z.fsdp_zero3_mlp_step_workspace(n, shapes, m), dtype=torch.uint8, device=DEV)
+          for k in ("a", "b", "c")}
+    out = {k: (torch.empty(n * m, d, dtype=torch.bfloat16, device=DEV),
+               torch.empty(n * m, d, dtype=torch.bfloat16, device=DEV)) for k in ("a", "b", "c")}
+
+    def run(units, k, stream):
+        z.fsdp_zero3_mlp_step(units, m, HP, 1, y_out=out[k][0], dx_out=out[k][1], workspace=ws[k], stream=stream,
+                              flags=flags)
+
+    run(clone(a), "c", torch.cuda.current_stream())  # warm-up: kernel attributes
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            run(b, "b", cap)
+    for _ in range(2):
+        run(a, "a", torch.cuda.current_stream())
+        g.replay()
+        torch.cuda.synchronize()
+        z.zero_device_status()
+        for x, y in zip(out["a"], out["b"]):
+            assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+        for ua, ub in zip(a, b):
+            for key in ("x", "gu", "h", "dy", "dh", "dgu"):
+                assert torch.equal(ua[key].view(torch.int16), ub[key].view(torch.int16)), key
+            for key in ("dw_gu", "dw_down"):
+                assert torch.equal(ua[key].view(torch.int32), ub[key].view(torch.int32)), key
+            for w in ("gate", "up", "down"):
+                assert torch.equal(ua[w]["w"].view(torch.int16), ub[w]["w"].view(torch.int16)), w
+                for key in ("master", "m", "v"):
+                    assert torch.equal(ua[w][key].view(torch.int32), ub[w][key].view(torch.int32)), (w, key)
