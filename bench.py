@@ -561,8 +561,8 @@ def zero3_mlp_leg(z, synth, dev, tf_peak, stream):
         nm = n * m
         y = torch.empty(nm, 4096, dtype=torch.bfloat16, device=dev)
         dx = torch.empty(nm, 4096, dtype=torch.bfloat16, device=dev)
-        ws = torch.empty(z.fsdp_zero3_mlp_step_workspace(n, [(4096, 14336)] * MLP_UNITS, m), dtype=torch.uint8,
-                         device=dev)
+        wsb = z.fsdp_zero3_mlp_step_workspace(n, [(4096, 14336)] * MLP_UNITS, m)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
         flop = MLP_UNITS * 3 * 3 * 2.0 * nm * 4096 * 14336  # 3 matrices, forward + 2 backward GEMMs each
         # the fused optimizer (the default) writes no dW; the separate form reads it back
         no_dw = [{k: v for k, v in u.items() if k not in ("dw_gu", "dw_down")} for u in units]
@@ -580,12 +580,12 @@ def zero3_mlp_leg(z, synth, dev, tf_peak, stream):
         res.update(ms=res["fused_optimizer"]["ms"], tflops=res["fused_optimizer"]["tflops"],
                    frac_of_bf16_peak=res["fused_optimizer"]["frac_of_bf16_peak"],
                    fused_optimizer_gain=res["separate_optimizer"]["ms"] / res["fused_optimizer"]["ms"] - 1.0,
-                   gemm_flop_per_step=flop, workspace_bytes=ws.numel(),
+                   gemm_flop_per_step=flop, workspace_bytes=wsb,
                    adam_bytes_per_step=MLP_UNITS * 3 * 30 * 4096 * 14336,
                    silu_backward_bytes_per_step=MLP_UNITS * 10 * nm * 14336,
                    note="tflops counts the GEMM flops over the whole step, which also holds each rank's Adam (fused "
-                        "into the dW GEMMs' epilogues, or separate), the SiLU-gate backward and the W^T / operand "
-                        "transposes")
+                        "into the dW GEMMs' epilogues, or separate) and the SiLU-gate backward; every backward operand "
+                        "is read in place (no transpose)")
     except Exception as e:  # the leg must not hide the step's line
         res["error"] = str(e)[:300]
     return res
@@ -612,9 +612,10 @@ def zero3_units(z, synth, dev, n, m, shapes=ZERO3_SHAPES):
 def zero3_leg(z, synth, dev, tf_peak, hbm_peak, stream):
     """One ZeRO-3 training step over 4 FSDP units with the Mistral-7B MLP shapes, N = 8
     ranks of 1024 tokens (8192 in all): forward, backward in reverse with each rank's Adam
-    on its shard after the unit's backward. Timed serial, with the next unit's gather and
-    dW operand layout prefetched on a second stream, with each unit's Adam on that stream
-    beside the next units' GEMMs, and with the forward gather materialised."""
+    on its shard after the unit's backward (fused into the dW GEMM's epilogue, or its own
+    launch). Timed serial (every gather fused into the GEMMs' loads), with each unit's Adam
+    on a second stream beside the next units' GEMMs, and with the gathers materialised into
+    a workspace slot, serially or with the next unit's gather prefetched on that stream."""
     import torch
     n, m = 8, 1024
     res = {"units": [list(s) for s in ZERO3_SHAPES], "n_ranks": n, "tokens_per_rank": m}
@@ -632,10 +633,12 @@ def zero3_leg(z, synth, dev, tf_peak, hbm_peak, stream):
                       z.FSDP_SEPARATE_OPTIMIZER)
         # the fused optimizer (the default) writes no dW; the separate forms read it back
         no_dw = [{k: v for k, v in u.items() if k != "dw"} for u in units]
-        for name, flags, pf in (("serial", 0, None), ("separate_optimizer", S, None), ("prefetch", P, side),
-                                ("overlap_optimizer", O, side), ("prefetch_overlap_optimizer", P | O, side),
-                                ("materialized_serial", G, None), ("materialized_prefetch", G | P, side)):
-            ws = torch.empty(z.fsdp_zero3_step_workspace(n, ZERO3_SHAPES, m, flags), dtype=torch.uint8, device=dev)
+        for name, flags, pf in (("serial", 0, None), ("separate_optimizer", S, None),
+                                ("overlap_optimizer", O, side), ("materialized_serial", G, None),
+                                ("materialized_prefetch", G | P, side),
+                                ("materialized_prefetch_overlap_optimizer", G | P | O, side)):
+            wsb = z.fsdp_zero3_step_workspace(n, ZERO3_SHAPES, m, flags)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
             t = [0]
             us = units if flags & (S | O) else no_dw
 
@@ -646,17 +649,16 @@ def zero3_leg(z, synth, dev, tf_peak, hbm_peak, stream):
 
             ms = time_launches(step, 10, stream)
             res[name] = {"ms": ms, "tflops": flop / ms / 1e9, "frac_of_bf16_peak": flop / ms / 1e9 / tf_peak,
-                         "workspace_bytes": ws.numel()}
+                         "workspace_bytes": wsb}
             del ws
         z.zero_device_status(stream)
         res["fused_optimizer_gain"] = res["separate_optimizer"]["ms"] / res["serial"]["ms"] - 1.0
-        res["prefetch_gain"] = res["serial"]["ms"] / res["prefetch"]["ms"] - 1.0
         res["overlap_optimizer_gain"] = res["serial"]["ms"] / res["overlap_optimizer"]["ms"] - 1.0
         res["materialized_prefetch_gain"] = (res["materialized_serial"]["ms"] / res["materialized_prefetch"]["ms"]
                                              - 1.0)
         res["note"] = ("tflops counts the 12 GEMMs' flops (6 N M R K per unit) over the whole step, which also holds "
-                       "each rank's Adam (fused into the dW GEMMs' epilogues unless separate) and the operand "
-                       "layouts")
+                       "each rank's Adam (fused into the dW GEMMs' epilogues unless separate); every backward operand "
+                       "is read in place (no transpose), the gathers fused into the loads unless materialised")
     except Exception as e:  # the leg must not hide the step's line
         res["error"] = str(e)[:300]
     return res
@@ -707,7 +709,8 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
                                     "note": "fsdp_gemm_kernel<false>: one CTA per 128 x 256 tile, for comparison"}
         del shards, Yb, Y
         # row a6 on its own: the materialised all-gather of W_up's 8 row shards (4 B per
-        # element) and the backward's transpose of the same shards into W^T (4 B per element)
+        # element) and the transposed gather of the same shards into W^T (4 B per element;
+        # the backward's fallback path for shapes the in-place GEMMs do not take)
         hbm = peaks()[0]
         shards_up = synth.weight_shards(14336, 4096, n, device=dev, seed_key=11)
         wfull = torch.empty(14336, 4096, dtype=torch.bfloat16, device=dev)
@@ -735,9 +738,10 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         res["mlp_unit_prefetched_gather"] = {"ms": ms2, "tflops": flop / ms2 / 1e9,
                                              "note": "W_down gathered into scratch on a second stream during gate+up"}
         del gs_, us_, ds_, Hb, Ym, sd
-        # backward of W_up for 8 ranks of 2048 tokens: W^T (the backward gather, transposed)
-        # and X^T laid out in one launch, one dX GEMM over all ranks on the CTA-pair kernel,
-        # one rank-reduced dW GEMM reading dY in place
+        # backward of W_up for 8 ranks of 2048 tokens, every operand read where it lies: one
+        # dX GEMM over all ranks with W's row shards as an MN-major operand (the backward
+        # gather fused into the loads), one rank-reduced dW GEMM with dY and X as MN-major
+        # operands; no workspace
         R, K, Mb = 14336, 4096, 2048
         shards = synth.weight_shards(R, K, n, device=dev, seed_key=11)
         A = [synth.activations(Mb, K, device=dev, seed_key=q) for q in range(n)]
@@ -745,36 +749,38 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         dX = [torch.empty(Mb, K, device=dev) for _ in range(n)]
         dW = torch.empty(R, K, device=dev)
         wsb = z.fsdp_unit_backward_workspace(n, R, K, Mb)
-        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
         ms = time_launches(lambda: z.fsdp_unit_backward(shards, A, dY, dX, dW, ws, stream=stream), 5, stream)
         flop = 2.0 * (2.0 * n * Mb * R * K)
         res["backward_up"] = {"ms": ms, "tflops": flop / ms / 1e9, "frac": flop / ms / 1e9 / tf_peak,
                               "ranks": n, "tokens_per_rank": Mb,
-                              "launches": 3, "workspace_bytes": wsb,
-                              "note": "W^T and X^T laid out by one transpose launch; dX over all ranks with "
-                                      "both operands K-major (CTA-pair kernel); dW reads dY in place (MN-major)"}
-        # the same call with a workspace that holds X^T alone: W read in place (MN-major)
-        ws_x = torch.empty((2 * K * n * Mb + 255) // 256 * 256, dtype=torch.uint8, device=dev)
-        ms_x = time_launches(lambda: z.fsdp_unit_backward(shards, A, dY, dX, dW, ws_x, stream=stream), 5, stream)
-        res["backward_up_w_in_place"] = {"ms": ms_x, "tflops": flop / ms_x / 1e9, "frac": flop / ms_x / 1e9 / tf_peak,
-                                         "workspace_bytes": ws_x.numel(),
-                                         "note": "workspace of X^T alone: W's shards read in place as an MN-major "
-                                                 "operand of the dX GEMM (one-CTA kernel)"}
-        del shards, A, dY, dX, dW, ws, ws_x
-        # the same for W_down [4096, 14336]: X (the MLP's H) is the wider operand, so dY^T is
-        # laid out and X read in place
+                              "launches": 2, "workspace_bytes": wsb,
+                              "note": "every operand read in place (CTA-pair kernel): dX over all ranks with W's "
+                                      "shards as an MN-major operand; dW with dY and X as MN-major operands"}
+        # the same call on the one-CTA kernel, for comparison
+        z.zero_set_gemm_kernel(1)
+        try:
+            ms_1 = time_launches(lambda: z.fsdp_unit_backward(shards, A, dY, dX, dW, ws, stream=stream), 5, stream)
+        finally:
+            z.zero_set_gemm_kernel(0)
+        res["backward_up_one_cta_kernel"] = {"ms": ms_1, "tflops": flop / ms_1 / 1e9,
+                                             "frac": flop / ms_1 / 1e9 / tf_peak,
+                                             "note": "the same in-place GEMMs on fsdp_gemm_kernel (one CTA per "
+                                                     "128 x 256 tile)"}
+        del shards, A, dY, dX, dW, ws
+        # the same for W_down [4096, 14336] (X is the MLP's H)
         R, K = 4096, 14336
         shards = synth.weight_shards(R, K, n, device=dev, seed_key=13)
         A = [synth.activations(Mb, K, device=dev, seed_key=q) for q in range(n)]
         dY = [synth.upstream_grad(Mb, R, device=dev, seed_key=q) for q in range(n)]
         dX = [torch.empty(Mb, K, device=dev) for _ in range(n)]
         dW = torch.empty(R, K, device=dev)
-        ws = torch.empty(z.fsdp_unit_backward_workspace(n, R, K, Mb), dtype=torch.uint8, device=dev)
+        wsb = z.fsdp_unit_backward_workspace(n, R, K, Mb)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
         ms = time_launches(lambda: z.fsdp_unit_backward(shards, A, dY, dX, dW, ws, stream=stream), 5, stream)
         res["backward_down"] = {"ms": ms, "tflops": flop / ms / 1e9, "frac": flop / ms / 1e9 / tf_peak,
-                                "ranks": n, "tokens_per_rank": Mb, "workspace_bytes": ws.numel(),
-                                "note": "W^T and dY^T laid out by one transpose launch; dX on the CTA-pair kernel; "
-                                        "dW reads X in place (MN-major)"}
+                                "ranks": n, "tokens_per_rank": Mb, "workspace_bytes": wsb,
+                                "note": "every operand read in place, as backward_up"}
     except Exception as e:  # the GEMM leg must not hide the step's line
         res["error"] = str(e)[:300]
     return res
@@ -1204,8 +1210,9 @@ def run_case(args):
                    allreduce_bytes=psi * (2 * n + 4), adam_bytes=psi * 30, allgather_bytes=psi * 6)
     elif args.case == "gather_w_up":
         # W_up [14336, 4096] bf16 from 8 row shards: the materialised all-gather
-        # (fsdp_gather_rows) and the backward's transposed gather W^T (fsdp_transpose_cat);
-        # 235 MB moved per launch each, 3 launches each
+        # (fsdp_gather_rows) and the transposed gather W^T (fsdp_transpose_cat, which the
+        # backward's fallback path uses for shapes the in-place GEMMs do not take); 235 MB
+        # moved per launch each, 3 launches each
         n, R, K = 8, 14336, 4096
         shards = synth.weight_shards(R, K, n, device=dev)
         W = torch.empty(R, K, dtype=torch.bfloat16, device=dev)
@@ -1248,8 +1255,8 @@ def run_case(args):
         out.update(n_ranks=n, tokens_per_rank=m, units=nu, ms=ms, tflops=flop / ms / 1e9)
     elif args.case == "backward_up":
         # FSDP unit backward of W_up [14336, 4096] in 8 row shards, 2048 tokens per rank
-        # (dY 470 MB, X 134 MB, dX 268 MB, dW 235 MB, X^T workspace 134 MB): 3 launches
-        # (dX GEMM, X transpose, dW GEMM) per call, 4 calls
+        # (dY 470 MB, X 134 MB, dX 268 MB, dW 235 MB, no workspace): 2 launches (dX GEMM,
+        # dW GEMM) per call, 4 calls
         n, R, K, M = 8, 14336, 4096, 2048
         shards = synth.weight_shards(R, K, n, device=dev, seed_key=11)
         A = [synth.activations(M, K, device=dev, seed_key=q) for q in range(n)]

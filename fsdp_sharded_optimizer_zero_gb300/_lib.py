@@ -407,9 +407,9 @@ def fsdp_unit_backward_workspace(n_ranks: int, rows_out: int, k_in: int, m_token
     return b.value
 
 
-def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace, stream=None):
+def fsdp_unit_backward(w_shards, A, dY, dX, dW, workspace=None, stream=None):
     """A, dY, dX: per-rank lists; dW: [rows_out, k_in] fp32; workspace: a uint8 CUDA tensor
-    of at least fsdp_unit_backward_workspace(...) bytes."""
+    of at least fsdp_unit_backward_workspace(...) bytes (None where that is 0)."""
     n = len(w_shards)
     rs, k = _shards_shape(w_shards, "w_shards")
     rows = n * rs

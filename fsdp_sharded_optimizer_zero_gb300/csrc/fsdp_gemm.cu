@@ -403,8 +403,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
 // the stage) share every A tile through one N = 256 MMA per K step; their two 128-column
 // accumulators sit side by side in one 256-column TMEM buffer and the epilogue writes
 // H = silu(gate) * up for a 128 x 128 tile.
-template <bool GATE_UP, bool ADAM = false>
+// LAYOUT: bit 0 set = A MN-major, bit 1 = B MN-major (p.a_mn / p.b_mn, fixed at compile
+// time: with the layout a run-time flag, the single producer thread's per-K-step work grew
+// long enough to starve the tensor pipe of MN-major GEMMs by 10-30 %).
+template <bool GATE_UP, bool ADAM = false, int LAYOUT = 0>
 __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(!GATE_UP || LAYOUT == 0, "gate-up mode is K-major only");
+  constexpr bool A_MN = (LAYOUT & 1) != 0, B_MN = (LAYOUT & 2) != 0;
   constexpr int TN = Mode<GATE_UP>::TN;                      // output tile columns
   constexpr uint32_t BT_BYTES = Mode<GATE_UP>::BT_BYTES;    // one B tile (two in gate-up mode)
   constexpr uint32_t STAGE_BYTES = Mode<GATE_UP>::STAGE;
@@ -461,20 +466,22 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
     if (lane == 0) {
       int64_t last_issue[STAGES];
       for (int s = 0; s < STAGES; ++s) last_issue[s] = -1;
-      uint32_t it = 0;
+      uint32_t it = 0, s = 0, ph = 0;  // K steps issued; their stage and its phase parity
       bool stop = false;
       for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x) {
         int mb, nb;
         tile_coords(tile, num_m, num_n, mb, nb);
         const int m0 = mb * BM;
         const int n0 = nb * TN;
-        const int shard = p.b_mn ? 0 : n0 / p.shard_rows;
+        const int shard = B_MN ? 0 : n0 / p.shard_rows;
         const int nl = n0 - shard * p.shard_rows;
         const void* wmap = &p.w[shard];
-        const int ash = p.a_mn ? 0 : m0 / p.a_shard_rows;  // the A row shard holding this tile's rows
+        const int ash = A_MN ? 0 : m0 / p.a_shard_rows;  // the A row shard holding this tile's rows
         const int ml = m0 - ash * p.a_shard_rows;
+        // MN-major operands: the K piece holding K block kb and the block's first row in it,
+        // advanced one block at a time (pieces are whole K blocks when there are several)
+        int aks = 0, akl = 0, bks = 0, bkl = 0;
         for (int kb = 0; kb < num_k; ++kb, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (it >= STAGES &&
               !mbar_wait_bounded(smem_u32(&empty_bar[s]), ph ^ 1u, abort, &g_zgb_dev_error, kErrEmpty)) {
             stop = true;
@@ -483,20 +490,21 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
           const uint32_t fb = smem_u32(&full_bar[s]);
           uint8_t* sa = smem + s * STAGE_BYTES;
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          if (!GATE_UP && p.a_mn) {  // K rows kb*BK.. of the piece holding them, BM / 64 M chunks
-            const int ks = kb * BK / p.a_shard_rows, kl = kb * BK - ks * p.a_shard_rows;
-            tma_load_3d(smem_u32(sa), &p.a[ks], 0, kl, m0 / 64, fb);
+          if constexpr (A_MN) {  // K rows kb*BK.. of the piece holding them, BM / 64 M chunks
+            tma_load_3d(smem_u32(sa), &p.a[aks], 0, akl, m0 / 64, fb);
+            if ((akl += BK) == p.a_shard_rows) akl = 0, ++aks;
           } else {
             tma_load_2d(smem_u32(sa), &p.a[ash], kb * BK, ml, fb);
           }
-          if (!GATE_UP && p.b_mn) {  // the same for B: TN / 64 chunks of 64 columns
-            const int ks = kb * BK / p.shard_rows, kl = kb * BK - ks * p.shard_rows;
-            tma_load_3d(smem_u32(sa + A_BYTES), &p.w[ks], 0, kl, n0 / 64, fb);
+          if constexpr (B_MN) {  // the same for B: TN / 64 chunks of 64 columns
+            tma_load_3d(smem_u32(sa + A_BYTES), &p.w[bks], 0, bkl, n0 / 64, fb);
+            if ((bkl += BK) == p.shard_rows) bkl = 0, ++bks;
           } else {
             tma_load_2d(smem_u32(sa + A_BYTES), wmap, kb * BK, nl, fb);
           }
           if (GATE_UP) tma_load_2d(smem_u32(sa + A_BYTES + BT_BYTES), &p.w2[shard], kb * BK, nl, fb);
           last_issue[s] = it;
+          if (++s == STAGES) s = 0, ph ^= 1u;
         }
       }
       if (*abort) {
@@ -512,13 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
     if (lane == 0) {
       // K-major: the next 16 K columns start 32 bytes further (+2 in the address field);
       // MN-major: 16 K rows = two 8-row groups further, 2048 bytes (+128)
-      const bool a_mn = !GATE_UP && p.a_mn, b_mn = !GATE_UP && p.b_mn;
-      const uint32_t a_step = a_mn ? 128u : 2u, b_step = b_mn ? 128u : 2u;
+      constexpr uint32_t a_step = A_MN ? 128u : 2u, b_step = B_MN ? 128u : 2u;
       // gate-up mode: the gate and up tiles sit back to back in the stage (128 rows each, the
       // same 128-byte row pitch), so ONE N = 256 MMA over both reads the A tile once and
       // fills the two side-by-side 128-column accumulators (gate, then up)
-      const uint32_t idesc = idesc_bf16_f32(BM, GATE_UP ? 2 * TN : TN, a_mn, b_mn);
-      uint32_t it = 0, i = 0;
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, GATE_UP ? 2 * TN : TN, A_MN, B_MN);
+      uint32_t i = 0, s = 0, ph = 0;
       bool stop = false, issued = false;
       for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x, ++i) {
         const uint32_t a = i & 1u, u = i >> 1;
@@ -526,21 +533,21 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
           break;
         tc_fence_after();
         const uint32_t d = tmem_base + a * ACC;
-        for (int kb = 0; kb < num_k; ++kb, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        for (int kb = 0; kb < num_k; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, abort, &g_zgb_dev_error, kErrFull)) {
             stop = true;
             break;
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-          const uint64_t ad = a_mn ? sw128_mnmajor_desc(sa, kMnChunk) : sw128_kmajor_desc(sa);
-          const uint64_t bd = b_mn ? sw128_mnmajor_desc(sa + A_BYTES, kMnChunk) : sw128_kmajor_desc(sa + A_BYTES);
+          const uint64_t ad = A_MN ? sw128_mnmajor_desc(sa, kMnChunk) : sw128_kmajor_desc(sa);
+          const uint64_t bd = B_MN ? sw128_mnmajor_desc(sa + A_BYTES, kMnChunk) : sw128_kmajor_desc(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)  // K = 16 per MMA
             umma_bf16(d, ad + a_step * k, bd + b_step * k, idesc, (kb | k) != 0 ? 1u : 0u);
           umma_commit(smem_u32(&empty_bar[s]));
           issued = true;
+          if (++s == STAGES) s = 0, ph ^= 1u;
         }
         if (!stop) umma_commit(smem_u32(&accf_bar[a]));
       }
@@ -623,9 +630,11 @@ __device__ __forceinline__ void pair_tile_coords(int tile, int num_m, int num_n,
   nb = in_band / rows;
 }
 
-template <bool GATE_UP, bool ADAM = false>
+template <bool GATE_UP, bool ADAM = false, int LAYOUT = 0>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fsdp_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(!GATE_UP || LAYOUT == 0, "gate-up mode is K-major only");
+  constexpr bool A_MN = (LAYOUT & 1) != 0, B_MN = (LAYOUT & 2) != 0;  // as in fsdp_gemm_kernel
   constexpr int TN = Mode<GATE_UP>::TN;  // output tile columns: 256, or 128 of H in gate-up mode
   static_assert(TN == (GATE_UP ? 128 : 256), "the pair MMA is N = 256: 256-column tiles, or gate | up halves");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -676,7 +685,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, s = 0, ph = 0;  // K steps issued; their stage and its phase parity
       bool stop = false;
       for (int tile = pair; tile < tiles && !stop; tile += pairs) {
         int mb, nb;
@@ -685,13 +694,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nrow = nb * TN + (GATE_UP ? 0 : static_cast<int>(rank) * 128);
         // K-major pieces holding this CTA's rows; a half past the last row (M or R % 256 ==
         // 128) starts beyond the last piece and reads zeros
-        const int ash = p.a_mn ? 0 : min(m0 / p.a_shard_rows, p.a_shards - 1);
+        const int ash = A_MN ? 0 : min(m0 / p.a_shard_rows, p.a_shards - 1);
         const int ml = m0 - ash * p.a_shard_rows;
-        const int shard = p.b_mn ? 0 : min(nrow / p.shard_rows, p.n_shards - 1);
+        const int shard = B_MN ? 0 : min(nrow / p.shard_rows, p.n_shards - 1);
         const int nl = nrow - shard * p.shard_rows;
         const void* bmap = GATE_UP && rank ? &p.w2[shard] : &p.w[shard];
+        int aks = 0, akl = 0, bks = 0, bkl = 0;  // MN-major: K piece and row of K block kb
         for (int kb = 0; kb < num_k; ++kb, ++it) {
-          const uint32_t s = it % PAIR_STAGES, ph = (it / PAIR_STAGES) & 1u;
           if (it >= PAIR_STAGES &&
               !mbar_wait_bounded(smem_u32(&empty_bar[s]), ph ^ 1u, abort, &g_zgb_dev_error, kErrPairEmpty)) {
             stop = true;
@@ -700,18 +709,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[s]), 0);
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * PAIR_STAGE);
           uint8_t* sa = smem + s * PAIR_STAGE;
-          if (!GATE_UP && p.a_mn) {  // K rows kb*BK.. of the piece holding them, this CTA's two M chunks
-            const int ks = kb * BK / p.a_shard_rows, kl = kb * BK - ks * p.a_shard_rows;
-            tma_load_3d_pair(smem_u32(sa), &p.a[ks], 0, kl, m0 / 64, fb);
+          if constexpr (A_MN) {  // K rows kb*BK.. of the piece holding them, this CTA's two M chunks
+            tma_load_3d_pair(smem_u32(sa), &p.a[aks], 0, akl, m0 / 64, fb);
+            if ((akl += BK) == p.a_shard_rows) akl = 0, ++aks;
           } else {
             tma_load_2d_pair(smem_u32(sa), &p.a[ash], kb * BK, ml, fb);
           }
-          if (!GATE_UP && p.b_mn) {  // the same for B: this CTA's two chunks of 64 columns
-            const int ks = kb * BK / p.shard_rows, kl = kb * BK - ks * p.shard_rows;
-            tma_load_3d_pair(smem_u32(sa + PAIR_HALF), &p.w[ks], 0, kl, nrow / 64, fb);
+          if constexpr (B_MN) {  // the same for B: this CTA's two chunks of 64 columns
+            tma_load_3d_pair(smem_u32(sa + PAIR_HALF), &p.w[bks], 0, bkl, nrow / 64, fb);
+            if ((bkl += BK) == p.shard_rows) bkl = 0, ++bks;
           } else {
             tma_load_2d_pair(smem_u32(sa + PAIR_HALF), bmap, kb * BK, nl, fb);
           }
+          if (++s == PAIR_STAGES) s = 0, ph ^= 1u;
         }
       }
       // every stage this CTA filled is read by the even CTA's MMAs: wait until they released it
@@ -725,10 +735,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------- MMA issuer (even CTA) ----------------
     if (rank == 0 && lane == 0) {
       // K steps of 16 as in the one-CTA kernel: +32 B (K-major) or +2048 B (MN-major)
-      const bool a_mn = !GATE_UP && p.a_mn, b_mn = !GATE_UP && p.b_mn;
-      const uint32_t a_step = a_mn ? 128u : 2u, b_step = b_mn ? 128u : 2u;
-      const uint32_t idesc = idesc_bf16_f32(256, 256, a_mn, b_mn);
-      uint32_t it = 0, i = 0;
+      constexpr uint32_t a_step = A_MN ? 128u : 2u, b_step = B_MN ? 128u : 2u;
+      constexpr uint32_t idesc = idesc_bf16_f32(256, 256, A_MN, B_MN);
+      uint32_t i = 0, s = 0, ph = 0;
       bool stop = false, issued = false;
       for (int tile = pair; tile < tiles && !stop; tile += pairs, ++i) {
         const uint32_t a = i & 1u, u = i >> 1;
@@ -737,21 +746,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d = tmem_base + a * PAIR_ACC;
-        for (int kb = 0; kb < num_k; ++kb, ++it) {
-          const uint32_t s = it % PAIR_STAGES, ph = (it / PAIR_STAGES) & 1u;
+        for (int kb = 0; kb < num_k; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, abort, &g_zgb_dev_error, kErrPairFull)) {
             stop = true;
             break;
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * PAIR_STAGE);
-          const uint64_t ad = a_mn ? sw128_mnmajor_desc(sa, kMnChunk) : sw128_kmajor_desc(sa);
-          const uint64_t bd = b_mn ? sw128_mnmajor_desc(sa + PAIR_HALF, kMnChunk) : sw128_kmajor_desc(sa + PAIR_HALF);
+          const uint64_t ad = A_MN ? sw128_mnmajor_desc(sa, kMnChunk) : sw128_kmajor_desc(sa);
+          const uint64_t bd = B_MN ? sw128_mnmajor_desc(sa + PAIR_HALF, kMnChunk) : sw128_kmajor_desc(sa + PAIR_HALF);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             umma_bf16_pair(d, ad + a_step * k, bd + b_step * k, idesc, (kb | k) != 0 ? 1u : 0u);
           umma_commit_pair(smem_u32(&empty_bar[s]), 0x3);
           issued = true;
+          if (++s == PAIR_STAGES) s = 0, ph ^= 1u;
         }
         if (!stop) umma_commit_pair(smem_u32(&accf_bar[a]), 0x3);
       }
@@ -799,7 +808,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 std::atomic<int> g_gemm_kernel{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-OncePerDevice g_attr_once[4];  // gate-up, plain, each with and without the fused optimizer
+OncePerDevice g_attr_once[16];  // per kernel variant: gate-up, fused optimizer, operand layout
 
 int get_encode() {
   std::call_once(g_encode_once, [] {
@@ -857,22 +866,22 @@ struct Operand {
   int64_t piece_rows;
 };
 
-// One of the kernels: gate-up or plain, plain with the fused optimizer (ADAM), on CTA
-// pairs or one CTA per tile.
-template <bool GATE_UP, bool ADAM>
+// One of the kernels: gate-up or plain, plain with the fused optimizer (ADAM), for one
+// operand layout, on CTA pairs or one CTA per tile.
+template <bool GATE_UP, bool ADAM, int LAYOUT>
 int launch_variant(const GemmParams& p, bool pair, int64_t m_tokens, int64_t rows_out, cudaStream_t st,
                    const char* who) {
   constexpr int TN = GATE_UP ? 128 : BN;
-  constexpr int V = (GATE_UP ? 1 : 0) + (ADAM ? 2 : 0);
+  constexpr int V = (GATE_UP ? 1 : 0) + (ADAM ? 2 : 0) + 4 * LAYOUT;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
   const cudaError_t attr = g_attr_once[V].run(dev, [] {
-    cudaError_t a = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP, ADAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Mode<GATE_UP>::SMEM);
+    cudaError_t a = cudaFuncSetAttribute(fsdp_gemm_kernel<GATE_UP, ADAM, LAYOUT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Mode<GATE_UP>::SMEM);
     if (a == cudaSuccess)
-      a = cudaFuncSetAttribute(fsdp_gemm_pair_kernel<GATE_UP, ADAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               PAIR_SMEM);
+      a = cudaFuncSetAttribute(fsdp_gemm_pair_kernel<GATE_UP, ADAM, LAYOUT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM);
     return a;
   });
   if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(attr));
@@ -880,15 +889,16 @@ int launch_variant(const GemmParams& p, bool pair, int64_t m_tokens, int64_t row
     // one 256-row tile per CTA pair at a time, as many pairs as can be resident at once: a
     // persistent grid larger than that runs its last clusters as a second wave (a 4-CTA
     // variant with 38 clusters where 36 fit ran at half speed). On GB300 all 76 pairs fit.
-    static int max_pairs[4][64];
-    static std::once_flag pairs_once[4][64];
+    static int max_pairs[16][64];
+    static std::once_flag pairs_once[16][64];
     std::call_once(pairs_once[V][dev & 63], [&] {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * std::max(1, num_sms() / 2), 1, 1);
       cfg.blockDim = dim3(kThreads, 1, 1);
       cfg.dynamicSmemBytes = PAIR_SMEM;
       int nc = 0;
-      if (cudaOccupancyMaxActiveClusters(&nc, fsdp_gemm_pair_kernel<GATE_UP, ADAM>, &cfg) != cudaSuccess || nc < 1) {
+      if (cudaOccupancyMaxActiveClusters(&nc, fsdp_gemm_pair_kernel<GATE_UP, ADAM, LAYOUT>, &cfg) != cudaSuccess ||
+          nc < 1) {
         (void)cudaGetLastError();
         nc = std::max(1, num_sms() / 2);
       }
@@ -896,14 +906,14 @@ int launch_variant(const GemmParams& p, bool pair, int64_t m_tokens, int64_t row
     });
     const int64_t tiles = ((m_tokens + 255) / 256) * ((rows_out + TN - 1) / TN);
     const unsigned int pairs = static_cast<unsigned int>(std::min<int64_t>(tiles, max_pairs[V][dev & 63]));
-    fsdp_gemm_pair_kernel<GATE_UP, ADAM><<<2 * pairs, kThreads, PAIR_SMEM, st>>>(p);
+    fsdp_gemm_pair_kernel<GATE_UP, ADAM, LAYOUT><<<2 * pairs, kThreads, PAIR_SMEM, st>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
     return ZERO_OK;
   }
   const int64_t tiles = ((m_tokens + BM - 1) / BM) * ((rows_out + TN - 1) / TN);
   const unsigned int grid = static_cast<unsigned int>(std::min<int64_t>(tiles, num_sms()));
-  fsdp_gemm_kernel<GATE_UP, ADAM><<<grid, kThreads, Mode<GATE_UP>::SMEM, st>>>(p);
+  fsdp_gemm_kernel<GATE_UP, ADAM, LAYOUT><<<grid, kThreads, Mode<GATE_UP>::SMEM, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
   return ZERO_OK;
@@ -922,13 +932,12 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
       y_pieces > kMaxShards)
     return set_error(ZERO_ERR_UNSUPPORTED, "%s: at most %d pieces per operand", who, kMaxShards);
   if (GATE_UP && (A.mn || B.mn)) return set_error(ZERO_ERR_UNSUPPORTED, "%s: gate-up mode is K-major only", who);
-  // Kernel choice: the CTA-pair kernel runs every mode, but by default only K-major
-  // operands take it; with an MN-major operand (the backward's in-place GEMMs) the pair
-  // form measured no faster, and 2-4 % slower over a whole backward call, than the one-CTA
-  // kernel. Pair CTAs load 128-row halves of a K-major B, so B pieces need a multiple of
-  // 128 rows; the one-CTA kernel loads whole TN-row tiles.
-  const int choice = g_gemm_kernel.load();
-  const bool pair = choice == 2 || (choice == 0 && !A.mn && !B.mn);
+  // Kernel choice: the CTA-pair kernel unless the one-CTA kernel is asked for. With the
+  // operand layout a template parameter, an MN-major operand costs the pair kernel 0-3 %
+  // (Mistral W_up backward GEMMs: 1.013-1.050 ms for every layout), while the one-CTA
+  // kernel runs 7-15 % behind it. Pair CTAs load 128-row halves of a K-major B, so B
+  // pieces need a multiple of 128 rows; the one-CTA kernel loads whole TN-row tiles.
+  const bool pair = g_gemm_kernel.load() != 1;
   // A and Y pieces
   if (A.mn) {
     if (A.piece_rows * A.pieces != k_in || (A.pieces > 1 && A.piece_rows % BK) || m_tokens % 64 || y_pieces != 1)
@@ -1010,8 +1019,25 @@ int launch_gemm(const Operand& A, const Operand& B, const uint16_t* const* B2, i
   p.shard_rows = static_cast<int>(B.piece_rows);
   p.n_shards = B.pieces;
 
-  if (adam) return launch_variant<false, true>(p, pair, m_tokens, rows_out, st, who);
-  return launch_variant<GATE_UP, false>(p, pair, m_tokens, rows_out, st, who);
+  if constexpr (GATE_UP) {
+    return launch_variant<true, false, 0>(p, pair, m_tokens, rows_out, st, who);
+  } else {
+    const int layout = (A.mn ? 1 : 0) | (B.mn ? 2 : 0);
+    if (adam) {
+      switch (layout) {
+        case 0: return launch_variant<false, true, 0>(p, pair, m_tokens, rows_out, st, who);
+        case 1: return launch_variant<false, true, 1>(p, pair, m_tokens, rows_out, st, who);
+        case 2: return launch_variant<false, true, 2>(p, pair, m_tokens, rows_out, st, who);
+        default: return launch_variant<false, true, 3>(p, pair, m_tokens, rows_out, st, who);
+      }
+    }
+    switch (layout) {
+      case 0: return launch_variant<false, false, 0>(p, pair, m_tokens, rows_out, st, who);
+      case 1: return launch_variant<false, false, 1>(p, pair, m_tokens, rows_out, st, who);
+      case 2: return launch_variant<false, false, 2>(p, pair, m_tokens, rows_out, st, who);
+      default: return launch_variant<false, false, 3>(p, pair, m_tokens, rows_out, st, who);
+    }
+  }
 }
 
 }  // namespace
@@ -1048,13 +1074,21 @@ int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces
                             "fsdp_unit_backward");
 }
 
-int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* Xt, int64_t m_tokens,
-                       int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st) {
+int launch_fsdp_gemm_w_mn(int w_pieces, const uint16_t* const* W, int64_t w_piece_rows, int64_t n_out,
+                          const uint16_t* A, int64_t m, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st,
+                          const char* who) {
+  const uint16_t* a1[1] = {A};
+  float* y1[1] = {Y};
+  return launch_gemm<false>({1, a1, false, m}, {w_pieces, W, true, w_piece_rows}, nullptr, m, n_out,
+                            w_piece_rows * w_pieces, y1, 1, Y_bf16, alpha, st, who);
+}
+
+int launch_fsdp_bwd_dw_in_place(int pieces, const uint16_t* const* dY, const uint16_t* const* X, int64_t piece_rows,
+                                int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st,
+                                const AdamFuse* adam, const char* who) {
   float* y1[1] = {dW};
-  const uint16_t* xt1[1] = {Xt};
-  return launch_gemm<false>({n_ranks, dY, true, m_tokens}, {1, xt1, false, k_in}, nullptr, rows_out, k_in,
-                            m_tokens * n_ranks, y1, 1, nullptr, 1.0f / static_cast<float>(n_ranks), st,
-                            "fsdp_unit_backward");
+  return launch_gemm<false>({pieces, dY, true, piece_rows}, {pieces, X, true, piece_rows}, nullptr, rows_out, k_in,
+                            piece_rows * pieces, y1, 1, nullptr, alpha, st, who, nullptr, adam);
 }
 
 bool fsdp_fused_gather_ok(int n_ranks, int64_t rows_out) {
@@ -1062,24 +1096,6 @@ bool fsdp_fused_gather_ok(int n_ranks, int64_t rows_out) {
   // K-major forward: the pair kernel loads 128-row halves of each W tile, the one-CTA
   // kernel whole TN-row tiles, and each load must lie inside one shard
   return n_ranks == 1 || (rows_out / n_ranks) % (g_gemm_kernel.load() == 1 ? BN : 128) == 0;
-}
-
-int launch_fsdp_bwd_dw_x_mn(int x_pieces, const uint16_t* dYt, const uint16_t* const* X, int64_t piece_rows,
-                            int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st,
-                            const AdamFuse* adam) {
-  const uint16_t* a1[1] = {dYt};
-  float* y1[1] = {dW};
-  return launch_gemm<false>({1, a1, false, rows_out}, {x_pieces, X, true, piece_rows}, nullptr, rows_out, k_in,
-                            piece_rows * x_pieces, y1, 1, nullptr, alpha, st, "fsdp_unit_backward", nullptr, adam);
-}
-
-int launch_fsdp_bwd_dw_alpha(const uint16_t* dY, int64_t nm, const uint16_t* Xt, int64_t rows_out, int64_t k_in,
-                             float* dW, float alpha, cudaStream_t st, const AdamFuse* adam) {
-  const uint16_t* dy1[1] = {dY};
-  const uint16_t* xt1[1] = {Xt};
-  float* y1[1] = {dW};
-  return launch_gemm<false>({1, dy1, true, nm}, {1, xt1, false, k_in}, nullptr, rows_out, k_in, nm, y1, 1, nullptr,
-                            alpha, st, "fsdp_zero3_step", nullptr, adam);
 }
 
 int set_gemm_kernel(int which) {

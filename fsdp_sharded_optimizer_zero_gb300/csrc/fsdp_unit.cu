@@ -8,27 +8,21 @@
 //   dW   = (1/N) sum_q dY_q^T X_q                  (all ranks' contributions, reduced)
 // and rank r's reduce-scatter result is rows [r R/N, (r+1) R/N) of dW, a contiguous block.
 //
-// Both products run on the tcgen05 GEMM. When R / N, K and M are multiples of 64 (and
-// N <= 16) dY is read where it lies:
-//   dX_q = dY_q W   with dY_q a K-major A. W comes from its row shards either as W^T [K, R]
-//                   laid out in the workspace by the backward all-gather (a transposing
-//                   gather), a K-major B that the CTA-pair kernel runs (the default when the
-//                   workspace holds it), or read in place as an MN-major B with the shard
-//                   picked by K block (when the workspace holds only X^T). One launch over
-//                   all ranks' row pieces when M % 128 == 0, else one per rank;
-//   dW = (1/N) sum_q dY_q^T X_q   with the K loop over every rank's tokens: one of dY and X
-//                   is read in place as an MN-major operand and the other laid out
-//                   transposed in the workspace (two MN-major operands cost more than one
-//                   transpose). The narrower one is transposed: X^T [K, N M] when K <= R
-//                   (W_up: 134 against 470 MB), dY^T [R, N M] otherwise (W_down). W^T and that
-//                   transpose are laid out by ONE launch of the transpose kernel;
+// Both products run on the tcgen05 GEMM (CTA-pair kernel). When R / N, K and M are
+// multiples of 64 (and N <= 16) every operand is read where it lies, with no workspace:
+//   dX_q = dY_q W   with dY_q a K-major A and W read from its row shards as an MN-major B
+//                   (the backward all-gather fused into the loads, as in the forward: the
+//                   shard is picked by K block). One launch over all ranks' row pieces when
+//                   M % 128 == 0, else one per rank;
+//   dW = (1/N) sum_q dY_q^T X_q   with dY_q and X_q both read as MN-major operands and the
+//                   K loop over every rank's tokens in turn,
 // so the sum over ranks happens inside the fp32 tensor-core accumulation, and the 1/N scale
-// is applied in the epilogue. On GB300 each MN-major operand costs its GEMM 5-14 %, so
-// W^T's 44 us transpose (W_up) buys back more than it costs: 2.534 against 2.652 ms per
-// call on W_up, 8 ranks x 2048 tokens (median of 8 interleaved rounds, same bits). The
-// MN-major dW stays on the one-CTA kernel. Other shapes take the transposed path: W^T
-// [K, R], dY^T [R, N M] and X^T [K, N M] in the workspace, then K-major GEMMs (on the
-// CTA-pair kernel). Every path gives the same bits.
+// is applied in the epilogue. With the operand layouts compiled into the kernel, an
+// MN-major operand costs the pair kernel 0-3 % on GB300 (Mistral W_up, 8 ranks x 2048
+// tokens: dX 1.047 ms with W in place against 1.045 ms over a laid-out W^T, dW 1.016 ms
+// with both operands in place), so laying out W^T, X^T or dY^T (44-49 us each) no longer
+// pays. Other shapes take the transposed path: W^T [K, R], dY^T [R, N M] and X^T [K, N M]
+// in the workspace, then K-major GEMMs. Every path gives the same bits.
 #include <string.h>
 
 #include <algorithm>
@@ -46,11 +40,10 @@ struct BackwardWorkspace {
   uint64_t min_total;           // the smallest workspace the call accepts
 };
 
-// The backward reads W and dY in place (MN-major GEMM operands) when every K piece is a
-// whole number of 64-row K blocks (the W shards' R / N rows for dX, each rank's m_tokens
-// rows for dW) and the MN-major operands' rows are whole 64-column chunks (k_in % 64 == 0;
-// R % 64 follows from R / N). X is still transposed: each MN-major operand costs the GEMM
-// 8-14 % on GB300, and dW with both operands MN-major lost more than X^T's transpose.
+// The backward reads W, dY and X in place (MN-major GEMM operands) when every K piece is
+// a whole number of 64-row K blocks (the W shards' R / N rows for dX, each rank's m_tokens
+// rows for dW) and every MN-major operand's rows are whole 64-column chunks (k_in % 64 ==
+// 0; R % 64 follows from R / N).
 bool backward_in_place(int n, int64_t rows_out, int64_t k_in, int64_t m_tokens) {
   return n <= kGemmMaxPieces && (rows_out / n) % 64 == 0 && m_tokens % 64 == 0 && k_in % 64 == 0;
 }
@@ -59,13 +52,7 @@ BackwardWorkspace backward_workspace(int n, int64_t rows_out, int64_t k_in, int6
   BackwardWorkspace w{0, 0, 0, 0, 0};
   const uint64_t R = static_cast<uint64_t>(rows_out), K = static_cast<uint64_t>(k_in);
   const uint64_t NM = static_cast<uint64_t>(n) * static_cast<uint64_t>(m_tokens);
-  if (backward_in_place(n, rows_out, k_in, m_tokens)) {  // X^T or dY^T, then W^T (or W in place)
-    w.xt = w.dyt = 0;                                    // the one of the two that is laid out
-    w.wt = align256(2 * std::min(K, R) * NM);
-    w.min_total = w.wt;
-    w.total = w.wt + align256(2 * R * K);
-    return w;
-  }
+  if (backward_in_place(n, rows_out, k_in, m_tokens)) return w;  // no workspace
   w.wt = 0;
   w.dyt = align256(2 * R * K);
   w.xt = w.dyt + align256(2 * R * NM);
@@ -121,10 +108,10 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
                      "%s: k_in, rows_out and n_ranks * m_tokens must be multiples of 8 (16-byte GEMM rows)", who);
   if (!w_shards || !A || !dY || !dX || !dW) return set_error(ZERO_ERR_INVALID_ARG, "%s: NULL argument", who);
   const BackwardWorkspace ws = backward_workspace(n_ranks, rows_out, k_in, m_tokens);
-  if (!workspace || workspace_bytes < ws.min_total)
+  if (ws.min_total && (!workspace || workspace_bytes < ws.min_total))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: workspace of %llu bytes is below the %llu needed", who,
                      workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.min_total);
-  if (!aligned16(dW) || !aligned16(workspace))
+  if (!aligned16(dW) || (ws.min_total && !aligned16(workspace)))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: dW and workspace must be 16-byte aligned", who);
   GradPtrs wp, ap, dyp;
   memset(&wp, 0, sizeof(wp));
@@ -142,46 +129,19 @@ extern "C" int fsdp_unit_backward(int n_ranks, const zero_bf16* const w_shards[]
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (backward_in_place(n_ranks, rows_out, k_in, m_tokens)) {
     const uint16_t* const* dy = reinterpret_cast<const uint16_t* const*>(dY);
-    uint8_t* base = static_cast<uint8_t*>(workspace);
-    // the dW GEMM's laid-out operand: X^T [K, N M] when K <= R, else dY^T [R, N M]
-    const bool t_dy = k_in > rows_out;
-    uint16_t* tr = reinterpret_cast<uint16_t*>(base + ws.xt);
-    const GradPtrs& tsrc = t_dy ? dyp : ap;
-    const int64_t tcols = t_dy ? rows_out : k_in;
+    const uint16_t* const* wsh = reinterpret_cast<const uint16_t* const*>(w_shards);
     int rc;
-    if (workspace_bytes >= ws.total) {
-      // W^T [K, R] (the backward all-gather, transposed) and the dW operand in one launch
-      uint16_t* wt = reinterpret_cast<uint16_t*>(base + ws.wt);
-      cudaError_t e = launch_transpose_cat2(wp, n_ranks, rows_out / n_ranks, k_in, wt, tsrc, n_ranks, m_tokens, tcols,
-                                            tr, st);
-      if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
-      // dX_q [M, K] = dY_q [M, R] * (W^T [K, R])^T, both operands K-major
-      const uint16_t* wt1[1] = {wt};
-      if (m_tokens % 128 == 0) {
-        if ((rc = launch_fsdp_gemm_row_split(n_ranks, dy, dX, m_tokens, wt, k_in, rows_out, 1.0f, st))) return rc;
-      } else {
-        for (int q = 0; q < n_ranks; ++q)
-          if ((rc = launch_fsdp_gemm(1, wt1, k_in, rows_out, dy[q], m_tokens, dX[q], nullptr, 1.0f, st))) return rc;
-      }
+    // dX_q = dY_q W with W read as its row shards: one launch over all ranks' rows when
+    // each rank's M is a whole number of 128-row tiles, else one launch per rank
+    if (m_tokens % 128 == 0) {
+      if ((rc = launch_fsdp_bwd_dx(n_ranks, dy, m_tokens, n_ranks, wsh, rows_out, k_in, dX, st))) return rc;
     } else {
-      // dX_q = dY_q W with W read as its row shards: one launch over all ranks' rows when
-      // each rank's M is a whole number of 128-row tiles, else one launch per rank
-      const uint16_t* const* wsh = reinterpret_cast<const uint16_t* const*>(w_shards);
-      if (m_tokens % 128 == 0) {
-        if ((rc = launch_fsdp_bwd_dx(n_ranks, dy, m_tokens, n_ranks, wsh, rows_out, k_in, dX, st))) return rc;
-      } else {
-        for (int q = 0; q < n_ranks; ++q)
-          if ((rc = launch_fsdp_bwd_dx(n_ranks, dy + q, m_tokens, 1, wsh, rows_out, k_in, dX + q, st))) return rc;
-      }
-      cudaError_t e = launch_transpose_cat(tsrc, n_ranks, m_tokens, tcols, tr, st);
-      if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", who, cudaGetErrorString(e));
+      for (int q = 0; q < n_ranks; ++q)
+        if ((rc = launch_fsdp_bwd_dx(n_ranks, dy + q, m_tokens, 1, wsh, rows_out, k_in, dX + q, st))) return rc;
     }
-    // dW = (1/N) sum_q dY_q^T X_q: the K loop runs over every rank's tokens in turn, one
-    // operand read in place (MN-major), the other from its rank-concatenated transpose
-    if (t_dy)
-      return launch_fsdp_bwd_dw_x_mn(n_ranks, tr, reinterpret_cast<const uint16_t* const*>(A), m_tokens, rows_out,
-                                     k_in, dW, 1.0f / static_cast<float>(n_ranks), st);
-    return launch_fsdp_bwd_dw(n_ranks, dy, tr, m_tokens, rows_out, k_in, dW, st);
+    // dW = (1/N) sum_q dY_q^T X_q: both read in place, the K loop over every rank's tokens
+    return launch_fsdp_bwd_dw_in_place(n_ranks, dy, reinterpret_cast<const uint16_t* const*>(A), m_tokens, rows_out,
+                                       k_in, dW, 1.0f / static_cast<float>(n_ranks), st, nullptr, who);
   }
   uint8_t* base = static_cast<uint8_t*>(workspace);
   uint16_t* wt = reinterpret_cast<uint16_t*>(base + ws.wt);

@@ -6,23 +6,22 @@
 // backward); after the backward the weight gradient is reduce-scattered so each rank keeps
 // the rows of its own shard, and each rank's Adam updates that shard alone.
 //
-// Here the forward's gather reads the N shards where they lie: inside the GEMM's operand
-// loads (the default: no copy of W exists at all), or, with FSDP_GATHER_MATERIALIZE, by a
-// gather kernel into a workspace slot that plays the all-gather's receive buffer. The
-// backward's gather always lands W^T [K, R] in a slot (a transposing gather, in the same
-// launch as the dW GEMM's laid-out operand: X^T [K, N M], or dY^T [R, N M] when K > R, the
-// other one read in place), so that dX is a K-major GEMM on the CTA-pair kernel: on GB300 an
-// MN-major operand costs a GEMM 5-14 %, more than the transpose. The
-// reduce of the reduce-scatter happens inside the dW GEMM's fp32 accumulation (its K loop
-// runs over every rank's tokens), so rank r's reduce-scattered gradient is simply rows
+// Here both gathers (before the forward and again before the backward) read the N shards
+// where they lie: inside the GEMMs' operand loads (the default: no copy of W exists at
+// all; the backward's dX GEMM reads the shards as an MN-major operand, picking the shard by
+// K block), or, with FSDP_GATHER_MATERIALIZE, by a gather kernel into a workspace slot
+// that plays the all-gather's receive buffer. The dW GEMM reads dY and X where they lie
+// too (both MN-major), so the backward lays out no transpose. The reduce of the
+// reduce-scatter happens inside the dW GEMM's fp32 accumulation (its K loop runs over
+// every rank's tokens), so rank r's reduce-scattered gradient is simply rows
 // [r R/N, (r+1) R/N) of dW, contiguous with its flat-parameter shard.
 //
 // Overlap ([Interview] follow-up "FSDP 怎么把通信藏起来?": the all-gather on its own CUDA
-// stream, the backward prefetching the next unit's): with FSDP_BACKWARD_PREFETCH and a
-// prefetch stream, unit i-1's gather and its dW operand layout are issued on the prefetch
-// stream once unit i's dX GEMM is enqueued (when that operand is dY^T, it waits for the dX
-// GEMM that writes dY_{i-1}), into the other of two slots; events order each slot's reuse
-// and each unit's start. Forward prefetch stays off (the pages' default).
+// stream, the backward prefetching the next unit's): with FSDP_GATHER_MATERIALIZE,
+// FSDP_BACKWARD_PREFETCH and a prefetch stream, unit i-1's gather is issued on the
+// prefetch stream once unit i's dX GEMM is enqueued, into the other of two slots; events
+// order each slot's reuse and each unit's start. With the fused gather there is no copy to
+// prefetch and the flag changes nothing. Forward prefetch stays off (the pages' default).
 //
 // Ordering inside a unit's backward: dX (reads W_i), then dW with each rank's Adam, which
 // writes the new W_i shards. Unit i's W is not read again in this step (unit i-1's backward
@@ -52,31 +51,22 @@ uint64_t align256(uint64_t b) { return (b + 255) & ~uint64_t(255); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 struct Zero3Workspace {
-  int slots;                // 2 with backward prefetch, else 1
-  uint64_t xt_off[2];       // the unit's X^T [k_in, N M] or dY^T [rows_out, N M] bf16 (the narrower)
-  uint64_t w_off[2];        // the unit's gathered W^T [k_in, rows_out] (backward) or W (materialised forward)
+  int slots;           // gathered-W slots: 2 with a materialised gather and backward prefetch, 1
+                       // with a materialised gather, 0 with the fused gather
+  uint64_t w_off[2];   // the unit's gathered W [rows_out, k_in] bf16
   uint64_t total;
 };
 
-Zero3Workspace zero3_workspace(int n, int n_units, const fsdp_unit_state* u, int64_t m, int flags) {
+Zero3Workspace zero3_workspace(int n_units, const fsdp_unit_state* u, int flags) {
   Zero3Workspace w;
   memset(&w, 0, sizeof(w));
-  uint64_t kmax = 0, wmax = 0;
-  for (int i = 0; i < n_units; ++i) {
-    kmax = std::max<uint64_t>(kmax, static_cast<uint64_t>(std::min(u[i].k_in, u[i].rows_out)));
+  if (!(flags & FSDP_GATHER_MATERIALIZE)) return w;
+  uint64_t wmax = 0;
+  for (int i = 0; i < n_units; ++i)
     wmax = std::max<uint64_t>(wmax, static_cast<uint64_t>(u[i].rows_out) * static_cast<uint64_t>(u[i].k_in));
-  }
   w.slots = (flags & FSDP_BACKWARD_PREFETCH) ? 2 : 1;
-  const uint64_t xt = align256(2 * kmax * static_cast<uint64_t>(n) * static_cast<uint64_t>(m));
-  const uint64_t ww = align256(2 * wmax);
-  uint64_t off = 0;
-  for (int s = 0; s < w.slots; ++s) {
-    w.xt_off[s] = off;
-    off += xt;
-    w.w_off[s] = off;
-    off += ww;
-  }
-  w.total = off;
+  for (int s = 0; s < w.slots; ++s) w.w_off[s] = static_cast<uint64_t>(s) * align256(2 * wmax);
+  w.total = static_cast<uint64_t>(w.slots) * align256(2 * wmax);
   return w;
 }
 
@@ -111,12 +101,11 @@ int check_units(int n, int n_units, const fsdp_unit_state* u, int64_t m, int fla
     const fsdp_unit_state& s = u[i];
     if (s.rows_out < 1 || s.k_in < 1 || s.rows_out > (1 << 30) || s.k_in > (1 << 30))
       return set_error(ZERO_ERR_INVALID_ARG, "%s: unit %d: sizes outside 1..2^30", kWho, i);
-    // the dW GEMM reads the wider of dY [N M, rows_out] and X [N M, k_in] in place as an
-    // MN-major operand, whose rows must be whole 64-column chunks
-    if (s.rows_out % n || s.rows_out % 8 || s.k_in % 8 || std::max(s.rows_out, s.k_in) % 64)
+    // the backward reads W's shards (dX) and dY [N M, rows_out], X [N M, k_in] (dW) in place
+    // as MN-major operands: rows of whole 64-column chunks, shards of whole 64-row K blocks
+    if (s.rows_out % n || s.k_in % 64 || (s.rows_out / n) % 64)
       return set_error(ZERO_ERR_INVALID_ARG,
-                       "%s: unit %d: needs rows_out a multiple of n_ranks and of 8, k_in a multiple of 8, and the "
-                       "larger of the two a multiple of 64 (got %lld, %d, %lld)",
+                       "%s: unit %d: rows_out / n_ranks and k_in must each be a multiple of 64 (got %lld / %d, %lld)",
                        kWho, i, (long long)s.rows_out, n, (long long)s.k_in);
     if (!(flags & FSDP_GATHER_MATERIALIZE) && !fsdp_fused_gather_ok(n, s.rows_out))
       return set_error(ZERO_ERR_INVALID_ARG,
@@ -152,7 +141,7 @@ extern "C" int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_un
   if (!bytes) return set_error(ZERO_ERR_INVALID_ARG, "fsdp_zero3_step_workspace: bytes is NULL");
   int rc = check_units(n_ranks, n_units, units, m_tokens, flags, false);
   if (rc) return rc;
-  *bytes = zero3_workspace(n_ranks, n_units, units, m_tokens, flags).total;
+  *bytes = zero3_workspace(n_units, units, flags).total;
   return ZERO_OK;
 }
 
@@ -166,14 +155,14 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
   if ((rc = check_adam_args(hp, step, kWho))) return rc;
   if ((y_out && !aligned16(y_out)) || (dx_out && !aligned16(dx_out)))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: y_out and dx_out must be 16-byte aligned", kWho);
-  const Zero3Workspace ws = zero3_workspace(n, L, units, m_tokens, flags);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < ws.total)
+  const Zero3Workspace ws = zero3_workspace(L, units, flags);
+  if (ws.total && (!workspace || !aligned16(workspace) || workspace_bytes < ws.total))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: workspace of %llu bytes (16-byte aligned) is below the %llu needed",
                      kWho, workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.total);
   const bool materialize = (flags & FSDP_GATHER_MATERIALIZE) != 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaStream_t side = prefetch_stream ? reinterpret_cast<cudaStream_t>(prefetch_stream) : st;
-  cudaStream_t pf = (flags & FSDP_BACKWARD_PREFETCH) ? side : st;
+  cudaStream_t pf = materialize && (flags & FSDP_BACKWARD_PREFETCH) ? side : st;
   const bool overlap = pf != st;
   const bool adam_side = (flags & FSDP_OVERLAP_OPTIMIZER) && side != st;
   const bool adam_separate = (flags & (FSDP_OVERLAP_OPTIMIZER | FSDP_SEPARATE_OPTIMIZER)) != 0;
@@ -181,18 +170,15 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
   if ((rc = make_adam_scalars(hp, step, kWho, &sc))) return rc;
   const int64_t nm = static_cast<int64_t>(n) * m_tokens;
   uint8_t* base = static_cast<uint8_t*>(workspace);
-  auto xt_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.xt_off[i % ws.slots]); };
-  auto w_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.w_off[i % ws.slots]); };
-  // events: [0] forward done, [1 + i] unit i's operands ready, [1 + L + i] unit i's backward
-  // GEMMs done (its slot is free), [1 + 2L + i] unit i's dX GEMM done (it writes dY_{i-1}),
-  // [1 + 3L] the side stream's last launch
+  auto w_slot = [&](int i) { return reinterpret_cast<uint16_t*>(base + ws.w_off[i % std::max(ws.slots, 1)]); };
+  // events: [0] forward done, [1 + i] unit i's gathered W ready, [1 + L + i] unit i's dX
+  // GEMM done (its slot is free), [1 + 2L + i] unit i's dW GEMM done, [1 + 3L] the side
+  // stream's last launch
   cudaEvent_t* ev = nullptr;
   if ((overlap || adam_side) && (rc = get_events(static_cast<size_t>(3 * L + 2), &ev))) return rc;
   const auto ev_ready = [&](int i) { return ev[1 + i]; };
-  const auto ev_done = [&](int i) { return ev[1 + L + i]; };
-  const auto ev_dx = [&](int i) { return ev[1 + 2 * L + i]; };
-  // the dW GEMM's laid-out operand: X^T when k_in <= rows_out, else dY^T
-  const auto t_dy = [&](int i) { return units[i].k_in > units[i].rows_out; };
+  const auto ev_free = [&](int i) { return ev[1 + L + i]; };
+  const auto ev_done = [&](int i) { return ev[1 + 2 * L + i]; };
 
   // the N row shards of unit i (rank r's rows at r R/N), or its gathered copy
   const uint16_t* shard_ptrs[kGemmMaxPieces];
@@ -231,23 +217,11 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
   }
 
   // ---- backward, last -> unit 0 ----
-  // unit i's operands: W_i^T [k_in, rows_out] gathered from its shards and the narrower of
-  // X_i^T [k_in, N M] and dY_i^T [rows_out, N M], both laid out by one launch
+  // with a materialised gather, unit i's W gathered again into its slot
   auto prepare = [&](int i, cudaStream_t s) {
     int r = ZERO_OK;
-    if (overlap && i + ws.slots < L && (r = wait(s, ev_done(i + ws.slots)))) return r;  // slot reuse
-    if (overlap && t_dy(i) && i + 1 < L && (r = wait(s, ev_dx(i + 1)))) return r;       // dY_i written
-    const fsdp_unit_state& u = units[i];
-    GradPtrs wsrc, tsrc;
-    memset(&wsrc, 0, sizeof(wsrc));
-    memset(&tsrc, 0, sizeof(tsrc));
-    const uint16_t* const* sh = shards_of(i);
-    for (int q = 0; q < n; ++q) wsrc.p[q] = sh[q];
-    tsrc.p[0] = t_dy(i) ? u.dy : u.x;
-    const int64_t tcols = t_dy(i) ? u.rows_out : u.k_in;
-    const cudaError_t e =
-        launch_transpose_cat2(wsrc, n, u.rows_out / n, u.k_in, w_slot(i), tsrc, 1, nm, tcols, xt_slot(i), s);
-    if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: transpose: %s", kWho, cudaGetErrorString(e));
+    if (overlap && i + ws.slots < L && (r = wait(s, ev_free(i + ws.slots)))) return r;  // slot reuse
+    if ((r = gather(i, s))) return r;
     return overlap ? record(ev_ready(i), s) : ZERO_OK;
   };
   if (overlap) {
@@ -258,30 +232,31 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
     const fsdp_unit_state& s = units[i];
     if (overlap) {
       if ((rc = wait(st, ev_ready(i)))) return rc;
-    } else if ((rc = prepare(i, st))) {
+    } else if (materialize && (rc = prepare(i, st))) {
       return rc;
     }
-    // dY_{i-1} [N M, K] = bf16(dY_i [N M, R] * (W_i^T [K, R])^T), both operands K-major
-    const uint16_t* wt1[1] = {w_slot(i)};
+    // dY_{i-1} [N M, K] = bf16(dY_i [N M, R] * W_i [R, K]), W_i read as an MN-major operand
+    // from its N row shards (or its gathered copy)
     zero_bf16* dx = i > 0 ? units[i - 1].dy : dx_out;
-    if (dx && (rc = launch_fsdp_gemm(1, wt1, s.k_in, s.rows_out, s.dy, nm, nullptr, dx, 1.0f, st))) return rc;
+    const uint16_t* w1[1] = {materialize ? w_slot(i) : nullptr};
+    const uint16_t* const* wp = materialize ? w1 : shards_of(i);
+    const int w_pieces = materialize ? 1 : n;
+    if (dx && (rc = launch_fsdp_gemm_w_mn(w_pieces, wp, s.rows_out / w_pieces, s.k_in, s.dy, nm, nullptr, dx, 1.0f,
+                                          st, kWho)))
+      return rc;
     if (overlap) {
-      if ((rc = record(ev_dx(i), st))) return rc;
+      if ((rc = record(ev_free(i), st))) return rc;
       if (i > 0 && (rc = prepare(i - 1, pf))) return rc;  // overlaps this unit's dW GEMM and Adam
     }
-    // dW = (1/N) dY_i^T X_i: X^T laid out and dY read in place, or dY^T laid out and X read
-    // in place, whichever of the two is narrower; by default with each rank's Adam on its
-    // rows in the epilogue
+    // dW = (1/N) dY_i^T X_i with dY_i and X_i read in place; by default with each rank's
+    // Adam on its rows in the epilogue
     const float inv_n = 1.0f / static_cast<float>(n);
     const AdamFuse fuse = {{s.master, s.master}, {s.m, s.m}, {s.v, s.v}, {s.w, s.w}, s.rows_out, sc};
-    const AdamFuse* af = adam_separate ? nullptr : &fuse;
-    if (t_dy(i)) {
-      const uint16_t* x1[1] = {s.x};
-      rc = launch_fsdp_bwd_dw_x_mn(1, xt_slot(i), x1, nm, s.rows_out, s.k_in, s.dw, inv_n, st, af);
-    } else {
-      rc = launch_fsdp_bwd_dw_alpha(s.dy, nm, xt_slot(i), s.rows_out, s.k_in, s.dw, inv_n, st, af);
-    }
-    if (rc) return rc;
+    const uint16_t* dy1[1] = {s.dy};
+    const uint16_t* x1[1] = {s.x};
+    if ((rc = launch_fsdp_bwd_dw_in_place(1, dy1, x1, nm, s.rows_out, s.k_in, s.dw, inv_n, st,
+                                          adam_separate ? nullptr : &fuse, kWho)))
+      return rc;
     if ((overlap || adam_side) && (rc = record(ev_done(i), st))) return rc;
     // with a separate optimizer: each rank's Adam on its shard (rows r R/N .. of dW), every
     // rank's shard in one launch, on `stream` or, overlapped, on the side stream
@@ -296,7 +271,7 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
     }
   }
   // join: `stream` waits for the side stream's last launch (its last Adam; without Adam on
-  // it, unit 0's operands, which `stream` has already awaited)
+  // it, unit 0's gather, which `stream` has already awaited)
   if (overlap || adam_side) {
     if ((rc = record(ev[1 + 3 * L], side)) || (rc = wait(st, ev[1 + 3 * L]))) return rc;
   }
@@ -307,10 +282,12 @@ extern "C" int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* 
 // The same step over Mistral-style MLP units (H = silu(X W_gate^T) * (X W_up^T), Y = H
 // W_down^T), each of the three weights with its own ZeRO-3 state. Forward: the gate-up
 // kernel (both projections in one N = 256 MMA stream, SiLU-gate epilogue) also saves G | U
-// for the backward, then the down projection. Backward, per unit: W_down^T gathered, dH,
-// dW_down and W_down's Adam; the SiLU-gate backward; [W_gate; W_up]^T gathered (the 2N
-// shards of both in one transposing launch), dX over the concatenated K of both
-// projections, dW_gate | dW_up in one GEMM, and their Adam. Serial on one stream: on one
+// for the backward, then the down projection. Backward, per unit: dH from W_down's shards
+// read in place, dW_down (dY and H read in place) with W_down's Adam; the SiLU-gate
+// backward; dX over the concatenated K of both projections from the 2N shards of [W_gate;
+// W_up] read in place, dW_gate | dW_up in one GEMM (dG | dU and X read in place) with
+// their Adam. No transpose is laid out; only more than 8 ranks (2N pieces above the
+// GEMM's 16) gather [W_gate; W_up] into the workspace first. Serial on one stream: on one
 // GPU the side-stream forms of the linear step above measured slower.
 // ======================================================================================
 
@@ -319,27 +296,15 @@ namespace {
 const char* const kWhoMlp = "fsdp_zero3_mlp_step";
 
 struct MlpWorkspace {
-  uint64_t wt_off, t_off, total;  // the gathered W^T slot, the dW operand slot
+  uint64_t total;  // [W_gate; W_up] gathered [2 d_ff, d_model] bf16 when 2 n_ranks > 16, else 0
 };
 
-// bytes of the dW GEMM's laid-out operand for dW [R, K] over nm tokens: the transpose of
-// the narrower of dY [nm, R] and X [nm, K]
-uint64_t narrower_bytes(int64_t R, int64_t K, int64_t nm) {
-  return 2ull * static_cast<uint64_t>(std::min(R, K)) * static_cast<uint64_t>(nm);
-}
-
-MlpWorkspace mlp_workspace(int n, int L, const fsdp_mlp_unit_state* u, int64_t m) {
-  const int64_t nm = static_cast<int64_t>(n) * m;
-  uint64_t wt = 0, t = 0;
-  for (int i = 0; i < L; ++i) {
-    const int64_t d = u[i].d_model, f = u[i].d_ff;
-    wt = std::max<uint64_t>(wt, 4ull * static_cast<uint64_t>(f) * static_cast<uint64_t>(d));
-    t = std::max(t, std::max(narrower_bytes(d, f, nm), narrower_bytes(2 * f, d, nm)));
-  }
-  MlpWorkspace w;
-  w.wt_off = 0;
-  w.t_off = align256(wt);
-  w.total = w.t_off + align256(t);
+MlpWorkspace mlp_workspace(int n, int L, const fsdp_mlp_unit_state* u) {
+  MlpWorkspace w{0};
+  if (2 * n <= kGemmMaxPieces) return w;
+  for (int i = 0; i < L; ++i)
+    w.total = std::max<uint64_t>(w.total, align256(4ull * static_cast<uint64_t>(u[i].d_ff) *
+                                                   static_cast<uint64_t>(u[i].d_model)));
   return w;
 }
 
@@ -399,18 +364,6 @@ int check_mlp_units(int n, int L, const fsdp_mlp_unit_state* u, int64_t m, bool 
   return ZERO_OK;
 }
 
-// dW [R, K] = alpha sum over nm tokens of dY^T X, with the narrower operand's transpose in
-// t (laid out by the caller): dY^T [R, nm] when K > R (X read in place), else X^T [K, nm]
-// (dY read in place)
-int dw_gemm(const uint16_t* dy, const uint16_t* x, const uint16_t* t, int64_t R, int64_t K, int64_t nm, float* dw,
-            float alpha, cudaStream_t st, const AdamFuse* af) {
-  if (K > R) {
-    const uint16_t* x1[1] = {x};
-    return launch_fsdp_bwd_dw_x_mn(1, t, x1, nm, R, K, dw, alpha, st, af);
-  }
-  return launch_fsdp_bwd_dw_alpha(dy, nm, t, R, K, dw, alpha, st, af);
-}
-
 }  // namespace
 
 extern "C" int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsdp_mlp_unit_state* units,
@@ -418,7 +371,7 @@ extern "C" int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsd
   if (!bytes) return set_error(ZERO_ERR_INVALID_ARG, "fsdp_zero3_mlp_step_workspace: bytes is NULL");
   int rc = check_mlp_units(n_ranks, n_units, units, m_tokens, false);
   if (rc) return rc;
-  *bytes = mlp_workspace(n_ranks, n_units, units, m_tokens).total;
+  *bytes = mlp_workspace(n_ranks, n_units, units).total;
   return ZERO_OK;
 }
 
@@ -435,28 +388,19 @@ extern "C" int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit
   if ((rc = make_adam_scalars(hp, step, kWhoMlp, &sc))) return rc;
   if ((y_out && !aligned16(y_out)) || (dx_out && !aligned16(dx_out)))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: y_out and dx_out must be 16-byte aligned", kWhoMlp);
-  const MlpWorkspace ws = mlp_workspace(n, L, units, m_tokens);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < ws.total)
+  const MlpWorkspace ws = mlp_workspace(n, L, units);
+  if (ws.total && (!workspace || !aligned16(workspace) || workspace_bytes < ws.total))
     return set_error(ZERO_ERR_INVALID_ARG, "%s: workspace of %llu bytes (16-byte aligned) is below the %llu needed",
                      kWhoMlp, workspace ? (unsigned long long)workspace_bytes : 0ull, (unsigned long long)ws.total);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t nm = static_cast<int64_t>(n) * m_tokens;
-  uint16_t* wt = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + ws.wt_off);
-  uint16_t* tr = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + ws.t_off);
+  uint16_t* wgu = static_cast<uint16_t*>(workspace);  // gathered [W_gate; W_up] (more than 8 ranks)
   const float inv_n = 1.0f / static_cast<float>(n);
 
   // the N row shards of a weight (rank r's rows at r rows/N), into ptrs[first .. first + N)
   auto shards = [&](const fsdp_weight_state& w, int64_t rows, int64_t cols, const uint16_t** ptrs, int first) {
     const int64_t per = (rows / n) * cols;
     for (int r = 0; r < n; ++r) ptrs[first + r] = w.w + r * per;
-  };
-  auto transposes = [&](const GradPtrs& wsrc, int wn, int64_t wrows, int64_t wcols, const uint16_t* t_src,
-                        int64_t t_cols) {
-    GradPtrs tsrc;
-    memset(&tsrc, 0, sizeof(tsrc));
-    tsrc.p[0] = t_src;
-    const cudaError_t e = launch_transpose_cat2(wsrc, wn, wrows, wcols, wt, tsrc, 1, nm, t_cols, tr, st);
-    return e == cudaSuccess ? ZERO_OK : set_error(ZERO_ERR_CUDA, "%s: transpose: %s", kWhoMlp, cudaGetErrorString(e));
   };
 
   // ---- forward, unit 0 -> last ----
@@ -476,18 +420,19 @@ extern "C" int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit
   for (int i = L - 1; i >= 0; --i) {
     const fsdp_mlp_unit_state& s = units[i];
     const int64_t d = s.d_model, f = s.d_ff;
-    GradPtrs wsrc;
-    memset(&wsrc, 0, sizeof(wsrc));
-    // W_down^T [f, d] and the dW_down operand (dW_down [d, f] = dY^T H: dY^T when f > d)
-    shards(s.down, d, f, wsrc.p, 0);
-    if ((rc = transposes(wsrc, n, d / n, f, f > d ? s.dy : s.h, f > d ? d : f))) return rc;
-    // dH [nm, f] = bf16(dY [nm, d] * (W_down^T [f, d])^T)
-    const uint16_t* wt1[1] = {wt};
-    if ((rc = launch_fsdp_gemm(1, wt1, f, d, s.dy, nm, nullptr, s.dh, 1.0f, st))) return rc;
-    // dW_down with W_down's Adam fused into its epilogue (or as its own launch)
+    const uint16_t* wsh[2 * kGemmMaxPieces];
+    // dH [nm, f] = bf16(dY [nm, d] * W_down [d, f]), W_down read from its row shards
+    shards(s.down, d, f, wsh, 0);
+    if ((rc = launch_fsdp_gemm_w_mn(n, wsh, d / n, f, s.dy, nm, nullptr, s.dh, 1.0f, st, kWhoMlp))) return rc;
+    // dW_down [d, f] = (1/N) dY^T H with W_down's Adam fused into its epilogue (or as its
+    // own launch)
     const AdamFuse fd = {{s.down.master, s.down.master}, {s.down.m, s.down.m}, {s.down.v, s.down.v},
                          {s.down.w, s.down.w}, d, sc};
-    if ((rc = dw_gemm(s.dy, s.h, tr, d, f, nm, s.dw_down, inv_n, st, separate ? nullptr : &fd))) return rc;
+    const uint16_t* dy1[1] = {s.dy};
+    const uint16_t* h1[1] = {s.h};
+    if ((rc = launch_fsdp_bwd_dw_in_place(1, dy1, h1, nm, d, f, s.dw_down, inv_n, st, separate ? nullptr : &fd,
+                                          kWhoMlp)))
+      return rc;
     if (separate && (rc = zero_adam_step(s.down.plan, ZERO_ALL_RANKS, s.dw_down, s.down.master, s.down.m, s.down.v,
                                          s.down.w, hp, step, stream)))
       return rc;
@@ -495,20 +440,33 @@ extern "C" int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit
     cudaError_t e = launch_silu_gate_backward(s.dh, s.gu, s.dgu, nm, f, st);
     if (e != cudaSuccess)
       return set_error(ZERO_ERR_CUDA, "%s: SiLU-gate backward: %s", kWhoMlp, cudaGetErrorString(e));
-    // [W_gate; W_up]^T [d, 2f] (the 2N shards of both) and the dW_gu operand (dW_gu [2f, d]
-    // = [dG | dU]^T X: [dG | dU]^T when d > 2f)
-    memset(&wsrc, 0, sizeof(wsrc));
-    shards(s.gate, f, d, wsrc.p, 0);
-    shards(s.up, f, d, wsrc.p, n);
-    if ((rc = transposes(wsrc, 2 * n, f / n, d, d > 2 * f ? s.dgu : s.x, d > 2 * f ? 2 * f : d))) return rc;
-    // dX [nm, d] = bf16([dG | dU] [nm, 2f] * ([W_gate; W_up]^T [d, 2f])^T): the sum of both
-    // projections' input gradients over the concatenated K
+    // dX [nm, d] = bf16([dG | dU] [nm, 2f] * [W_gate; W_up] [2f, d]): the sum of both
+    // projections' input gradients over the concatenated K, [W_gate; W_up] read from the
+    // 2N shards of both (or, past 8 ranks, from its gathered copy)
     zero_bf16* dx = i > 0 ? units[i - 1].dy : dx_out;
-    if (dx && (rc = launch_fsdp_gemm(1, wt1, d, 2 * f, s.dgu, nm, nullptr, dx, 1.0f, st))) return rc;
-    // dW_gate | dW_up with both weights' Adam fused into its epilogue (rows < d_ff: W_gate)
+    if (dx) {
+      shards(s.gate, f, d, wsh, 0);
+      shards(s.up, f, d, wsh, n);
+      int pieces = 2 * n;
+      if (2 * n > kGemmMaxPieces) {
+        if ((rc = fsdp_gather_rows(n, wsh, f, d, wgu, stream)) ||
+            (rc = fsdp_gather_rows(n, wsh + n, f, d, wgu + f * d, stream)))
+          return rc;
+        wsh[0] = wgu;
+        pieces = 1;
+      }
+      if ((rc = launch_fsdp_gemm_w_mn(pieces, wsh, 2 * f / pieces, d, s.dgu, nm, nullptr, dx, 1.0f, st, kWhoMlp)))
+        return rc;
+    }
+    // dW_gate | dW_up [2f, d] = (1/N) [dG | dU]^T X with both weights' Adam fused into its
+    // epilogue (rows < d_ff: W_gate)
     const AdamFuse fgu = {{s.gate.master, s.up.master}, {s.gate.m, s.up.m}, {s.gate.v, s.up.v}, {s.gate.w, s.up.w},
                           f, sc};
-    if ((rc = dw_gemm(s.dgu, s.x, tr, 2 * f, d, nm, s.dw_gu, inv_n, st, separate ? nullptr : &fgu))) return rc;
+    const uint16_t* dgu1[1] = {s.dgu};
+    const uint16_t* x1[1] = {s.x};
+    if ((rc = launch_fsdp_bwd_dw_in_place(1, dgu1, x1, nm, 2 * f, d, s.dw_gu, inv_n, st, separate ? nullptr : &fgu,
+                                          kWhoMlp)))
+      return rc;
     if (separate &&
         ((rc = zero_adam_step(s.gate.plan, ZERO_ALL_RANKS, s.dw_gu, s.gate.master, s.gate.m, s.gate.v, s.gate.w, hp,
                               step, stream)) ||

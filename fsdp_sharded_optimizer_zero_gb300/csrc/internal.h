@@ -64,11 +64,6 @@ cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int6
 // and the saved G | U [rows, 2 d_ff], elementwise in fp32
 cudaError_t launch_silu_gate_backward(const uint16_t* dh, const uint16_t* gu, uint16_t* dgu, int64_t rows, int64_t d_ff,
                                       cudaStream_t st);
-// two such independent problems in one launch when both are aligned for the pipelined
-// kernel (16-byte rows and buffers), else two launches; same results as two calls
-cudaError_t launch_transpose_cat2(const GradPtrs& srcs0, int n0, int64_t rows0, int64_t cols0, uint16_t* dst0,
-                                  const GradPtrs& srcs1, int n1, int64_t rows1, int64_t cols1, uint16_t* dst1,
-                                  cudaStream_t st);
 
 // ---- FSDP GEMM (fsdp_gemm.cu) ----
 // Adam fused into a weight-gradient GEMM's epilogue: output element (row, col) of the
@@ -99,32 +94,34 @@ int launch_fsdp_gemm_row_split(int a_shards, const uint16_t* const* A, float* co
 int launch_fsdp_gate_up(int n_ranks, const uint16_t* const* gate_shards, const uint16_t* const* up_shards,
                         int64_t d_ff, int64_t d_model, const uint16_t* X, int64_t m_tokens, uint16_t* H,
                         cudaStream_t st, uint16_t* GU = nullptr);
-// Backward GEMMs reading operands in place as MN-major tiles:
-// dX_q[M, K] = dY_q W for the dy_pieces row pieces of dY / dX (dy_pieces = 1: one rank),
-// with W read in place from its n_ranks row shards (R / n_ranks a multiple of 64);
-// dW[R, K] = (1/n_ranks) sum_q dY_q^T X_q with dY read in place (every rank's m_tokens
-// rows, a multiple of 64, one K piece) and X as the rank-concatenated X^T [K, N M].
-// At most kGemmMaxPieces pieces per operand.
+// Backward GEMMs reading every operand where it lies: a tensor stored [K, M] (or [K, N])
+// for a GEMM that contracts over K is read as MN-major tiles, so no transpose is ever laid
+// out. Operands given as several pieces are split along K into whole 64-row K blocks (at
+// most kGemmMaxPieces pieces per operand); the results are bit-identical to the K-major
+// forms over transposed copies.
+// dX_q[M, K] = dY_q W (fp32) for the dy_pieces row pieces of dY / dX (dy_pieces = 1: one
+// rank), W read in place from its n_ranks row shards (R / n_ranks a multiple of 64).
 constexpr int kGemmMaxPieces = 16;
 int launch_fsdp_bwd_dx(int n_ranks, const uint16_t* const* dY, int64_t dy_pieces_rows, int dy_pieces,
                        const uint16_t* const* w_shards, int64_t rows_out, int64_t k_in, float* const* dX,
                        cudaStream_t st);
-int launch_fsdp_bwd_dw(int n_ranks, const uint16_t* const* dY, const uint16_t* Xt, int64_t m_tokens,
-                       int64_t rows_out, int64_t k_in, float* dW, cudaStream_t st);
-// dW = alpha sum_q dY_q^T X_q with dY^T [R, N M] laid out (a K-major A) and X read in place
-// as an MN-major B in x_pieces pieces of piece_rows token rows (each rank's X_q, or one
-// contiguous [N M, K]), the K loop over the tokens: the cheaper form when X is the wider of
-// the two (K > R). Same bits as the form above.
-int launch_fsdp_bwd_dw_x_mn(int x_pieces, const uint16_t* dYt, const uint16_t* const* X, int64_t piece_rows,
-                            int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st,
-                            const AdamFuse* adam = nullptr);
-// dW over one contiguous dY for all ranks (rank q's rows at q M): dW [R, K] = alpha dY^T
-// [R, NM] (X^T [K, NM])^T with dY read in place as one MN-major piece. Bit-identical to the
-// per-rank form above.
-int launch_fsdp_bwd_dw_alpha(const uint16_t* dY, int64_t nm, const uint16_t* Xt, int64_t rows_out, int64_t k_in,
-                             float* dW, float alpha, cudaStream_t st, const AdamFuse* adam = nullptr);
+// Y[m, n_out] = alpha A W, A [m, K] K-major, W [K, n_out] given as w_pieces row pieces of
+// w_piece_rows rows (K = w_pieces * w_piece_rows; n_out a multiple of 64): a unit's input
+// gradient from its weight's row shards, or from [W_gate; W_up]'s 2N shards. fp32 Y and/or
+// bf16 Y_bf16 (a bf16-only output needs n_out % 8 == 0).
+int launch_fsdp_gemm_w_mn(int w_pieces, const uint16_t* const* W, int64_t w_piece_rows, int64_t n_out,
+                          const uint16_t* A, int64_t m, float* Y, uint16_t* Y_bf16, float alpha, cudaStream_t st,
+                          const char* who);
+// dW[R, K] = alpha sum over the tokens of dY^T X, dY [T, R] and X [T, K] both read in place
+// as MN-major operands given as `pieces` token pieces of piece_rows rows (each rank's
+// tokens, or one piece for all T = pieces * piece_rows); the K loop runs over every token,
+// so the sum over ranks (the reduce of the reduce-scatter) happens in the fp32 accumulator.
+// R and K multiples of 64. With adam, each row's optimizer update runs in the epilogue.
+int launch_fsdp_bwd_dw_in_place(int pieces, const uint16_t* const* dY, const uint16_t* const* X, int64_t piece_rows,
+                                int64_t rows_out, int64_t k_in, float* dW, float alpha, cudaStream_t st,
+                                const AdamFuse* adam, const char* who);
 unsigned int fsdp_gemm_read_clear_error();
-int set_gemm_kernel(int which);  // 0 = default, 1 = one-CTA kernel everywhere, 2 = CTA-pair kernel everywhere
+int set_gemm_kernel(int which);  // 0 = default (CTA-pair kernel), 1 = one-CTA kernel everywhere, 2 = CTA-pair kernel
 
 // Runs a set-up step (a kernel attribute) once per device until it succeeds. Unlike
 // std::call_once, a failed attempt (say, under an error left pending by an earlier launch)

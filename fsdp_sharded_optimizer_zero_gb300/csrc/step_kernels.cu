@@ -282,8 +282,8 @@ struct TransposeJob {
   int64_t rows, cols, total_rows, col_tiles, ntiles;
   uint16_t* dst;
 };
-// Up to two independent problems in one launch (the backward's W^T and X^T): tiles
-// [0, j[0].ntiles) belong to the first, the rest to the second.
+// Up to two independent problems in one launch: tiles [0, j[0].ntiles) belong to the
+// first, the rest to the second (launch_transpose_cat passes one, the second empty).
 struct TransposeJobs {
   TransposeJob j[2];
 };
@@ -516,18 +516,6 @@ cudaError_t launch_transpose_cat(const GradPtrs& srcs, int n, int64_t rows, int6
   transpose_cat_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(
       srcs, rows, cols, total_rows, dst, 0);
   return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_cat2(const GradPtrs& srcs0, int n0, int64_t rows0, int64_t cols0, uint16_t* dst0,
-                                  const GradPtrs& srcs1, int n1, int64_t rows1, int64_t cols1, uint16_t* dst1,
-                                  cudaStream_t st) {
-  TransposeJobs jobs;
-  memset(&jobs, 0, sizeof(jobs));
-  if (rows0 * n0 > 0 && cols0 > 0 && rows1 * n1 > 0 && cols1 > 0 &&
-      pipe_job(srcs0, n0, rows0, cols0, dst0, &jobs.j[0]) && pipe_job(srcs1, n1, rows1, cols1, dst1, &jobs.j[1]))
-    return launch_pipe(jobs, st);
-  cudaError_t e = launch_transpose_cat(srcs0, n0, rows0, cols0, dst0, st);
-  return e == cudaSuccess ? launch_transpose_cat(srcs1, n1, rows1, cols1, dst1, st) : e;
 }
 
 cudaError_t launch_silu_gate_backward(const uint16_t* dh, const uint16_t* gu, uint16_t* dgu, int64_t rows, int64_t d_ff,

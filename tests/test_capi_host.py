@@ -136,16 +136,16 @@ def test_newer_entry_points_reject_bad_arguments_before_launch(z):
     assert lib.zero_fused_step_fp32_grads(p.handle, 4, good, 256, 512, 768, 1024, C.byref(adam), 1, None) == -1
     # backward: rows % N, K % 8, workspace size, NULL rank pointer
     ws = C.c_uint64()
-    # dY in place (R/N, K and M multiples of 64): X^T and W^T (X^T alone is also accepted);
+    # every operand read in place (R/N, K and M multiples of 64, N <= 16): no workspace;
     # otherwise W^T, dY^T, X^T
     assert lib.fsdp_unit_backward_workspace(4, 512, 256, 128, C.byref(ws)) == 0
-    assert ws.value == 2 * 256 * 512 + 2 * 512 * 256
+    assert ws.value == 0
     assert lib.fsdp_unit_backward_workspace(4, 512, 256, 40, C.byref(ws)) == 0
     assert ws.value == 2 * 512 * 256 + 2 * 512 * 160 + 2 * 256 * 160
     assert lib.fsdp_unit_backward_workspace(17, 17 * 64, 256, 128, C.byref(ws)) == 0
     assert ws.value > 2 * 256 * 17 * 128  # more than 16 ranks: one GEMM operand cannot hold every piece
     assert lib.fsdp_unit_backward_workspace(4, 512, 192, 128, C.byref(ws)) == 0
-    assert ws.value == 2 * 192 * 512 + 2 * 512 * 192
+    assert ws.value == 0
     assert lib.fsdp_unit_backward_workspace(4, 512, 200, 128, C.byref(ws)) == 0
     assert ws.value > 2 * 200 * 512  # K not a multiple of 64
     assert lib.fsdp_unit_backward_workspace(0, 512, 256, 128, C.byref(ws)) == -1
@@ -244,12 +244,16 @@ def test_zero3_step_rejects_bad_arguments_before_launch(z):
     good = [(512, 256), (1024, 512)]
     plans = [z.zero_plan(r * k, n, "zero3", 1 << 20) for r, k in good]
     ws = C.c_uint64()
-    # one slot (two with the backward prefetch): X^T of the widest input and W^T of the
-    # largest unit
+    # nothing with the fused gather (every backward operand read in place); with the
+    # materialised gather one slot for the largest unit's W, two with the backward prefetch
     assert lib.fsdp_zero3_step_workspace(n, 2, units(good), m, 0, C.byref(ws)) == 0
-    assert ws.value == 2 * 512 * n * m + 2 * 1024 * 512
+    assert ws.value == 0
+    assert lib.fsdp_zero3_step_workspace(n, 2, units(good), m, 2, C.byref(ws)) == 0
+    assert ws.value == 0
+    assert lib.fsdp_zero3_step_workspace(n, 2, units(good), m, 1, C.byref(ws)) == 0
+    assert ws.value == 2 * 1024 * 512
     assert lib.fsdp_zero3_step_workspace(n, 2, units(good), m, 3, C.byref(ws)) == 0
-    assert ws.value == 2 * (2 * 512 * n * m + 2 * 1024 * 512)
+    assert ws.value == 2 * (2 * 1024 * 512)
 
     def call(arr, nu=2, flags=0, wsb=1 << 30, step=1, hp=adam, mm=m, nr=n):
         return lib.fsdp_zero3_step(nr, nu, arr, mm, None, None, C.byref(hp), step, flags, 0x100000, wsb, None, None)
@@ -257,7 +261,8 @@ def test_zero3_step_rejects_bad_arguments_before_launch(z):
     # chain: unit 1's k_in must be unit 0's rows_out
     assert call(units([(512, 256), (1024, 256)], plans)) == -1
     assert b"is not unit 0's rows_out" in lib.zero_last_error()
-    # rows_out a multiple of 64 (dW reads dY as an MN-major operand), k_in a multiple of 8
+    # rows_out / N and k_in multiples of 64 (the backward reads W's shards, dY and X as
+    # MN-major operands)
     assert call(units([(512, 252), (1024, 512)], plans)) == -1
     assert b"multiple of 64" in lib.zero_last_error()
     assert call(units([(4 * 72, 256)], plans[:1]), nu=1) == -1
@@ -277,7 +282,7 @@ def test_zero3_step_rejects_bad_arguments_before_launch(z):
     assert call(units(good, plans), step=0) == -1                # Adam step counts from 1
     bad = z._lib.zero_adam(1e-4, 1.0, 0.999, 1e-8, 0.0)
     assert call(units(good, plans), hp=bad) == -1                # beta1 outside [0, 1)
-    assert call(units(good, plans), wsb=100) == -1               # workspace too small
+    assert call(units(good, plans), flags=1, wsb=100) == -1      # workspace too small (materialised gather)
     assert b"workspace" in lib.zero_last_error()
     assert call(units(good, plans), nr=17) == -1                 # at most 16 ranks
     assert call(units(good, plans), mm=3) == -1                  # N M a multiple of 8

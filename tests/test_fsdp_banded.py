@@ -103,10 +103,11 @@ def run_backward(z, n, rows, k, m, key, ints):
 
 
 # dX over all ranks is one row-split GEMM of N M = 4096 rows (32 blocks of 128: bands 24 + 8);
-# dW has R = 3584 rows (28 blocks: 24 + 4); both in place (R/N, M, K multiples of 64).
+# dW has R = 3584 rows (28 blocks: 24 + 4); every operand in place (R/N, M, K multiples of
+# 64), on the CTA-pair kernel (the default) and on the one-CTA kernel.
 # (4, 3200, 200, 896): K not a multiple of 64, so the transposed path's K-major GEMMs run
-# the same walk on the CTA-pair kernel.
-@pytest.mark.parametrize("kernel", [0, 2])
+# the same walk.
+@pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("n,rows,k,m", [(8, 3584, 128, 512), (4, 3200, 200, 896)])
 def test_backward_banded_walk_every_output(z, kernel, n, rows, k, m):
     z.zero_set_gemm_kernel(kernel)

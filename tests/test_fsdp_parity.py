@@ -264,11 +264,10 @@ def run_backward(z, n, rows, k, m, key=0, ints=False):
 
 
 def test_backward_workspace_sizes(z):
-    # dY is read in place when R/N, M and K are multiples of 64 (and N <= 16): the
-    # workspace holds X^T and W^T (X^T alone also works, with W read in place); otherwise
-    # W^T, dY^T and X^T
-    assert z.fsdp_unit_backward_workspace(8, 14336, 4096, 2048) == 2 * 4096 * 8 * 2048 + 2 * 14336 * 4096
-    assert z.fsdp_unit_backward_workspace(5, 320, 192, 192) == 2 * 192 * 5 * 192 + 2 * 320 * 192
+    # W, dY and X are read in place when R/N, M and K are multiples of 64 (and N <= 16): no
+    # workspace; otherwise W^T, dY^T and X^T
+    assert z.fsdp_unit_backward_workspace(8, 14336, 4096, 2048) == 0
+    assert z.fsdp_unit_backward_workspace(5, 320, 192, 192) == 0
     assert z.fsdp_unit_backward_workspace(5, 320, 200, 192) > 2 * 200 * 5 * 192
     assert z.fsdp_unit_backward_workspace(4, 512, 256, 40) > 2 * 256 * 4 * 40
     assert z.fsdp_unit_backward_workspace(8, 2048, 512, 96) > 2 * 512 * 8 * 96
@@ -356,11 +355,11 @@ def test_backward_mistral_up_sampled(z):
 
 
 def test_backward_mistral_down_sampled(z):
-    """W_down [4096, 14336] in 8 row shards of 512 rows (gathered as W^T for the dX GEMM),
+    """W_down [4096, 14336] in 8 row shards of 512 rows (read in place by the dX GEMM),
     1024 tokens per rank: sampled dX and dW entries against float64 dot products under the
     bounds."""
     n, rows, k, m = 8, 4096, 14336, 1024
-    assert z.fsdp_unit_backward_workspace(n, rows, k, m) == 2 * rows * n * m + 2 * rows * k  # X read in place
+    assert z.fsdp_unit_backward_workspace(n, rows, k, m) == 0  # every operand read in place
     shards, A, dY, dX, dW = run_backward(z, n, rows, k, m, key=9)
     rng = np.random.default_rng(2)
     w_full = torch.cat(shards, 0)
@@ -390,39 +389,40 @@ def test_backward_mistral_down_sampled(z):
 
 @pytest.mark.parametrize("n,rows,k,m", [(4, 512, 256, 128), (5, 320, 192, 192), (8, 2048, 512, 64),
                                         (8, 3584, 128, 512), (4, 256, 1024, 128), (8, 512, 2048, 64)])
-def test_backward_x_only_workspace_reads_w_in_place_same_bits(z, n, rows, k, m):
-    """A workspace that holds only the dW operand's transpose (X^T, or dY^T when k > rows)
-    is accepted: W is then read in place from its shards (MN-major) instead of from its
-    transpose, with the same dX and dW bits."""
+def test_backward_in_place_same_bits_on_both_kernels(z, n, rows, k, m):
+    """The in-place backward (W's shards, dY and X all read as MN-major operands, no
+    workspace: None is accepted, and a workspace passed anyway is not touched) gives the
+    same dX and dW bits on the CTA-pair kernel as on the one-CTA kernel, whose layouts
+    and K loops are compiled separately."""
+    assert z.fsdp_unit_backward_workspace(n, rows, k, m) == 0
     shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=5)
     A = [synth.activations(m, k, device=DEV, seed_key=q) for q in range(n)]
     dY = [synth.upstream_grad(m, rows, device=DEV, seed_key=q) for q in range(n)]
     out = []
-    full = z.fsdp_unit_backward_workspace(n, rows, k, m)
-    x_only = (2 * min(k, rows) * n * m + 255) // 256 * 256
-    for size in (full, x_only):
-        dX = [torch.full((m, k), float("nan"), device=DEV) for _ in range(n)]
-        dW = torch.full((rows, k), float("nan"), device=DEV)
-        ws = torch.empty(size, dtype=torch.uint8, device=DEV)
-        z.fsdp_unit_backward(shards, A, dY, dX, dW, ws)
-        z.zero_device_status()
-        out.append((dX, dW))
+    spare = torch.full((1 << 16,), 0x5A, dtype=torch.uint8, device=DEV)
+    try:
+        for kernel, ws in ((0, None), (1, spare)):
+            z.zero_set_gemm_kernel(kernel)
+            dX = [torch.full((m, k), float("nan"), device=DEV) for _ in range(n)]
+            dW = torch.full((rows, k), float("nan"), device=DEV)
+            z.fsdp_unit_backward(shards, A, dY, dX, dW, ws)
+            z.zero_device_status()
+            out.append((dX, dW))
+    finally:
+        z.zero_set_gemm_kernel(0)
     (dXa, dWa), (dXb, dWb) = out
     assert torch.equal(dWa.view(torch.int32), dWb.view(torch.int32))
     for a, b in zip(dXa, dXb):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
-    ws = torch.empty(x_only - 256, dtype=torch.uint8, device=DEV)
-    with pytest.raises(z.ZeroError) as e:
-        z.fsdp_unit_backward(shards, A, dY, out[0][0], out[0][1], ws)
-    assert e.value.code == -1
+    assert bool((spare == 0x5A).all())
 
 
 @pytest.mark.parametrize("n,rows,k,m", [(8, 512, 2048, 128), (4, 1024, 256, 192)])
 def test_backward_dw_equals_k_major_product_of_transposes(z, n, rows, k, m):
-    """dW does not depend on which operand is laid out: fsdp_unit_backward's dW (dY^T laid
-    out and X read in place when k > rows, else X^T laid out and dY read in place) equals,
-    bit for bit, the K-major product dY^T (X^T)^T of both transposes through
-    fsdp_unit_forward, scaled by 1/N (exact for N a power of two)."""
+    """dW does not depend on the operands' layout: fsdp_unit_backward's dW (dY and X both
+    read in place as MN-major operands) equals, bit for bit, the K-major product dY^T
+    (X^T)^T of both transposes through fsdp_unit_forward, scaled by 1/N (exact for N a
+    power of two)."""
     shards = synth.weight_shards(rows, k, n, device=DEV, seed_key=8)
     A = [synth.activations(m, k, device=DEV, seed_key=q) for q in range(n)]
     dY = [synth.upstream_grad(m, rows, device=DEV, seed_key=q) for q in range(n)]
