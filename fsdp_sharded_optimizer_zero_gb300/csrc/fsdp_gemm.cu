@@ -209,7 +209,7 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, in
 // 128). The warp walks the chunk's rows with one column per lane, so every state access
 // is one contiguous 128-byte line; all 32 rows' loads are in flight before their arithmetic.
 // adam_elem: the same operations as the Adam kernels (same bits).
-constexpr int kAdamRows = 32;  // rows of a staged chunk whose state loads are in flight together
+constexpr int kAdamRows = 32;  // rows of a staged chunk whose state loads are in flight together (one-CTA kernel)
 // L2 prefetch of the optimizer state the chunk at columns col0 .. col0 + 31 of rows
 // row0 .. row0 + 31 will read: lane i takes row row0 + i, one 128-byte line per array
 __device__ __forceinline__ void adam_prefetch_chunk(const GemmParams& p, int row0, int col0, int lane) {
@@ -221,6 +221,7 @@ __device__ __forceinline__ void adam_prefetch_chunk(const GemmParams& p, int row
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p.adam.m[set] + idx));
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p.adam.v[set] + idx));
 }
+template <int ROWS = kAdamRows>
 __device__ __forceinline__ void adam_chunk_rows(const GemmParams& p, const uint8_t* buf, int row0, int col0,
                                                 int lane) {
   const int col = col0 + lane;
@@ -235,24 +236,25 @@ __device__ __forceinline__ void adam_chunk_rows(const GemmParams& p, const uint8
   const int rows = min(32, p.m - row0);
   const uint32_t piece = static_cast<uint32_t>(lane) >> 2, word = static_cast<uint32_t>(lane) & 3u;
 #pragma unroll 1
-  for (int i0 = 0; i0 < rows; i0 += kAdamRows) {
-    float g[kAdamRows], w[kAdamRows], m[kAdamRows], v[kAdamRows];
+  for (int i0 = 0; i0 < rows; i0 += ROWS) {
+    float w[ROWS], m[ROWS], v[ROWS];
 #pragma unroll
-    for (int k = 0; k < kAdamRows; ++k) {
+    for (int k = 0; k < ROWS; ++k) {
       const int i = i0 + k;
       if (i < rows) {
-        g[k] = *reinterpret_cast<const float*>(buf + i * 128 + ((piece ^ (static_cast<uint32_t>(i) & 7u)) * 16) +
-                                               word * 4);
         w[k] = __ldcs(W + i * R);
         m[k] = __ldcs(M + i * R);
         v[k] = __ldcs(V + i * R);
       }
     }
 #pragma unroll
-    for (int k = 0; k < kAdamRows; ++k) {
+    for (int k = 0; k < ROWS; ++k) {
       const int i = i0 + k;
       if (i < rows) {
-        adam_elem(g[k], w[k], m[k], v[k], p.adam.sc);
+        // the gradient from the staged chunk when it is used: no register held across the loads
+        const float g = *reinterpret_cast<const float*>(buf + i * 128 +
+                                                        ((piece ^ (static_cast<uint32_t>(i) & 7u)) * 16) + word * 4);
+        adam_elem(g, w[k], m[k], v[k], p.adam.sc);
         __stcs(W + i * R, w[k]);
         __stcs(M + i * R, m[k]);
         __stcs(V + i * R, v[k]);
@@ -309,14 +311,21 @@ __device__ __forceinline__ void store_gate_up_chunk(const GemmParams& p, int row
   }
 }
 
-// Epilogue of one output tile, run by the four epilogue warps after the tile's accumulator
-// is complete: warp quarter q reads TMEM lanes [32q, 32q + 32) (tile rows 32q + lane) at
+// Epilogue of one output tile, run by the epilogue warps after the tile's accumulator is
+// complete: a warp of quarter q reads TMEM lanes [32q, 32q + 32) (tile rows 32q + lane) at
 // taddr, stages its chunks in its 8 KiB of shared memory at epi for TMA stores, and writes
 // rows m0 + 32q + lane, columns n0 .. n0 + TN of Y (row piece ash, local row ml) or of H.
-template <bool GATE_UP, bool ADAM = false>
+// With PARTS warps per quarter (the fused optimizer on the CTA pair), warp `part` of the
+// quarter takes the 32-column chunks part, part + PARTS, ...
+template <bool GATE_UP, bool ADAM = false, int PARTS = 1>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, uint8_t* epi, uint32_t& epi_chunk,
-                                              int m0, int n0, int ash, int ml, int q, int lane) {
+                                              int m0, int n0, int ash, int ml, int q, int lane, int part = 0) {
+  static_assert(PARTS == 1 || (ADAM && !GATE_UP), "columns are split between warps for the fused optimizer only");
   constexpr int TN = Mode<GATE_UP>::TN;
+#ifndef ZGB_PAIR_ADAM_ROWS
+#define ZGB_PAIR_ADAM_ROWS 16
+#endif
+  constexpr int kAdamInFlight = PARTS == 1 ? kAdamRows : ZGB_PAIR_ADAM_ROWS;  // registers: 320 threads with PARTS = 2
   const int row = m0 + q * 32 + lane;
   if constexpr (GATE_UP) {
 #pragma unroll 1
@@ -366,16 +375,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
     }
   } else {
     if constexpr (ADAM) {  // the first two chunks' state on its way to L2
-      adam_prefetch_chunk(p, m0 + q * 32, n0, lane);
-      adam_prefetch_chunk(p, m0 + q * 32, n0 + 32, lane);
+      adam_prefetch_chunk(p, m0 + q * 32, n0 + 32 * part, lane);
+      adam_prefetch_chunk(p, m0 + q * 32, n0 + 32 * (part + PARTS), lane);
     }
 #pragma unroll 1
-    for (int c = 0; c < TN; c += 32) {
+    for (int c = 32 * part; c < TN; c += 32 * PARTS) {
       uint32_t r[32];
       tmem_ld_32cols(taddr + c, r);
       if (n0 + c >= p.r) continue;  // warp-uniform
       if constexpr (ADAM) {
-        if (c + 64 < TN) adam_prefetch_chunk(p, m0 + q * 32, n0 + c + 64, lane);
+        if (c + 64 * PARTS < TN) adam_prefetch_chunk(p, m0 + q * 32, n0 + c + 64 * PARTS, lane);
       }
       if (p.alpha != 1.0f) {
 #pragma unroll
@@ -398,7 +407,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
           bulk_commit_group();
         }
         ++epi_chunk;
-        adam_chunk_rows(p, buf, m0 + q * 32, n0 + c, lane);
+        adam_chunk_rows<kAdamInFlight>(p, buf, m0 + q * 32, n0 + c, lane);
         continue;
       }
       if (p.y_tma) {
@@ -636,12 +645,21 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
 // Before leaving, each producer waits until the MMAs released every stage it filled, and
 // the two CTAs meet at a cluster barrier, so neither CTA's shared memory or barriers are
 // still targeted by the other; every mbarrier wait is bounded as in the one-CTA kernel.
-constexpr int PAIR_STAGES = 6;
 constexpr uint32_t PAIR_HALF = 128 * BK * 2;      // one CTA's 128 A rows, and its 128 B rows
 constexpr uint32_t PAIR_STAGE = 2 * PAIR_HALF;
 constexpr uint32_t PAIR_ACC = 256;                // TMEM columns of one accumulator (N = 256)
-constexpr uint32_t PAIR_EPI = 4u * 2u * 4096u;
-constexpr uint32_t PAIR_SMEM = PAIR_STAGES * PAIR_STAGE + PAIR_EPI + 1024;
+// Per variant: with the fused optimizer the epilogue does most of the kernel's instruction
+// issue (the Adam arithmetic of a 128 x 256 tile per CTA) and its state loads' latency, so
+// it runs 8 warps, two per TMEM lane quarter splitting the columns, with 16 rows of state
+// loads in flight each (200 registers at 320 threads); their staging buffers take one
+// operand stage (5 instead of 6; 5 measured within 1 % of 6 on the plain GEMMs).
+template <bool ADAM> struct PairCfg {
+  static constexpr int EPI_WARPS = ADAM ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int STAGES = ADAM ? 5 : 6;
+  static constexpr uint32_t EPI = EPI_WARPS * 2u * 4096u;
+  static constexpr uint32_t SMEM = STAGES * PAIR_STAGE + EPI + 1024;
+};
 
 constexpr unsigned int kErrPairEmpty = (4u << 8) | 1u;  // producer waiting for a free stage
 constexpr unsigned int kErrPairFull = (4u << 8) | 2u;   // MMA waiting for both CTAs' copies
@@ -660,9 +678,11 @@ __device__ __forceinline__ void pair_tile_coords(int tile, int num_m, int num_n,
 }
 
 template <bool GATE_UP, bool ADAM = false, int LAYOUT = 0>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<ADAM>::THREADS, 1)
     fsdp_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   static_assert(!GATE_UP || LAYOUT == 0, "gate-up mode is K-major only");
+  constexpr int PAIR_STAGES = PairCfg<ADAM>::STAGES;
+  constexpr int EPI_WARPS = PairCfg<ADAM>::EPI_WARPS;
   constexpr bool A_MN = (LAYOUT & 1) != 0, B_MN = (LAYOUT & 2) != 0;  // as in fsdp_gemm_kernel
   constexpr int TN = Mode<GATE_UP>::TN;  // output tile columns: 256, or 128 of H in gate-up mode
   static_assert(TN == (GATE_UP ? 128 : 256), "the pair MMA is N = 256: 256-column tiles, or gate | up halves");
@@ -692,7 +712,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&accf_bar[a]), 1);
-      mbar_init(smem_u32(&acce_bar[a]), 8);  // 4 epilogue warps in each CTA
+      mbar_init(smem_u32(&acce_bar[a]), 2 * EPI_WARPS);  // every epilogue warp of both CTAs
     }
     mbar_init(smem_u32(&drain_bar), 1);
     abort_flag = 0;
@@ -800,8 +820,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 2-5, both CTAs) ----------------
-    const int q = warp & 3;
+    // ---------------- epilogue (warps 2 .. 2 + EPI_WARPS - 1, both CTAs) ----------------
+    const int q = warp & 3;                 // the TMEM lane quarter this warp may read
+    const int part = (warp - 2) >> 2;       // which of the quarter's warps (column split)
     const int y_pieces = p.m / p.y_shard_rows;
     uint32_t i = 0, epi_chunk = 0;
     for (int tile = pair; tile < tiles; tile += pairs, ++i) {
@@ -813,8 +834,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int m0 = mb * 256 + static_cast<int>(rank) * 128;
       const int ash = min(m0 / p.y_shard_rows, y_pieces - 1);  // the Y row piece (rows past M: clipped)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * PAIR_ACC;
-      uint8_t* epi = smem + PAIR_STAGES * PAIR_STAGE + static_cast<uint32_t>(q) * 2u * 4096u;
-      epilogue_tile<GATE_UP, ADAM>(p, taddr, epi, epi_chunk, m0, nb * TN, ash, m0 - ash * p.y_shard_rows, q, lane);
+      uint8_t* epi = smem + PAIR_STAGES * PAIR_STAGE + static_cast<uint32_t>(warp - 2) * 2u * 4096u;
+      epilogue_tile<GATE_UP, ADAM, EPI_WARPS / 4>(p, taddr, epi, epi_chunk, m0, nb * TN, ash,
+                                                  m0 - ash * p.y_shard_rows, q, lane, part);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acce_bar[a]), 0));
@@ -910,7 +932,7 @@ int launch_variant(const GemmParams& p, bool pair, int64_t m_tokens, int64_t row
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Mode<GATE_UP>::SMEM);
     if (a == cudaSuccess)
       a = cudaFuncSetAttribute(fsdp_gemm_pair_kernel<GATE_UP, ADAM, LAYOUT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM);
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg<ADAM>::SMEM);
     return a;
   });
   if (attr != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: %s", who, cudaGetErrorString(attr));
@@ -923,8 +945,8 @@ int launch_variant(const GemmParams& p, bool pair, int64_t m_tokens, int64_t row
     std::call_once(pairs_once[V][dev & 63], [&] {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * std::max(1, num_sms() / 2), 1, 1);
-      cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = PAIR_SMEM;
+      cfg.blockDim = dim3(PairCfg<ADAM>::THREADS, 1, 1);
+      cfg.dynamicSmemBytes = PairCfg<ADAM>::SMEM;
       int nc = 0;
       if (cudaOccupancyMaxActiveClusters(&nc, fsdp_gemm_pair_kernel<GATE_UP, ADAM, LAYOUT>, &cfg) != cudaSuccess ||
           nc < 1) {
@@ -935,7 +957,8 @@ int launch_variant(const GemmParams& p, bool pair, int64_t m_tokens, int64_t row
     });
     const int64_t tiles = ((m_tokens + 255) / 256) * ((rows_out + TN - 1) / TN);
     const unsigned int pairs = static_cast<unsigned int>(std::min<int64_t>(tiles, max_pairs[V][dev & 63]));
-    fsdp_gemm_pair_kernel<GATE_UP, ADAM, LAYOUT><<<2 * pairs, kThreads, PAIR_SMEM, st>>>(p);
+    fsdp_gemm_pair_kernel<GATE_UP, ADAM, LAYOUT>
+        <<<2 * pairs, PairCfg<ADAM>::THREADS, PairCfg<ADAM>::SMEM, st>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ZERO_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
     return ZERO_OK;
