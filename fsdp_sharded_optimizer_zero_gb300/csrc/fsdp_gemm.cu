@@ -10,10 +10,11 @@
 //   fsdp_gemm_pair_kernel  a cluster of two CTAs per 256-row tile, tcgen05.mma.cta_group::2
 //                          (M = 256, N = 256) over both CTAs' shared memory: each CTA loads
 //                          half of A and half of B, a third fewer operand bytes per flop.
-//                          The default for K-major operands.
-//   fsdp_gemm_kernel       one CTA per 128 x 256 tile, tcgen05.mma.cta_group::1. The
-//                          default where an operand is MN-major (the backward's in-place
-//                          GEMMs), where the pair measured no faster.
+//                          The default, for every operand layout.
+//   fsdp_gemm_kernel       one CTA per 128 x 256 tile, tcgen05.mma.cta_group::1
+//                          (zero_set_gemm_kernel(1)).
+// Both are compiled per operand layout (template parameter LAYOUT: A and / or B stored
+// MN-major), so the producer and MMA threads carry no per-step layout logic.
 // One-CTA kernel structure (one CTA per SM, persistent over its output tiles):
 //   warp 0        TMA producer: A tile 128x64 and W tile 256x64 (bf16, 128-byte swizzle)
 //                 per 64-wide K block into a 4-stage shared-memory ring;

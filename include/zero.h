@@ -277,24 +277,21 @@ ZERO_API int fsdp_unit_forward(int n_ranks, const zero_bf16* const w_shards[], i
                       const zero_bf16* A, int64_t m_tokens, float* Y, zero_bf16* Y_bf16, zero_bf16* scratch_w,
                       zero_stream_t stream);
 
-/* The backward's operand layout step, as a call of its own: dst[c][q*rows + r] =
- * srcs[q][r][c] for q < n_srcs — the n_srcs row-major [rows, cols] bf16 sources
- * transposed and concatenated into one row-major [cols, n_srcs*rows] bf16 buffer (W^T
- * from W's row shards is the backward all-gather of [Interview] follow-up "手写 FSDP 的一层
- * linear"; the ranks' dY^T and X^T are the operands of the reduced dW). Any alignment;
- * 16-byte-aligned buffers with cols and n_srcs*rows multiples of 8 take 16-byte accesses. */
+/* The backward's operand layout step, as a call of its own (fsdp_unit_backward uses it on
+ * shapes its in-place GEMMs do not take): dst[c][q*rows + r] = srcs[q][r][c] for q <
+ * n_srcs — the n_srcs row-major [rows, cols] bf16 sources transposed and concatenated into
+ * one row-major [cols, n_srcs*rows] bf16 buffer (W^T from W's row shards is the backward
+ * all-gather of [Interview] follow-up "手写 FSDP 的一层 linear", landing transposed; the
+ * ranks' dY^T and X^T are the operands of the reduced dW). Any alignment; 16-byte-aligned
+ * buffers with cols and n_srcs*rows multiples of 8 take 16-byte accesses. */
 ZERO_API int fsdp_transpose_cat(int n_srcs, const zero_bf16* const srcs[], int64_t rows, int64_t cols, zero_bf16* dst,
                                 zero_stream_t stream);
 
-/* Bytes of device workspace fsdp_unit_backward needs for transposed operand copies, each
- * rounded up to 256 bytes. When R/N, k_in and m_tokens are multiples of 64 and N <= 16,
- * the dW GEMM reads the wider of dY and X in place (an MN-major tensor-core operand) and
- * the workspace holds the transpose of the narrower one (X^T, 2*K*N*M bytes, when K <= R;
- * else dY^T, 2*R*N*M) followed by W^T (2*R*K), the backward all-gather of W laid out
- * transposed; a workspace that holds the first part alone is also accepted, and W is then
- * read in place from its shards as an MN-major operand (same results, about 4 % slower on
- * GB300). Other shapes need W^T, dY^T and X^T. This call returns the size of the fastest
- * path. */
+/* Bytes of device workspace fsdp_unit_backward needs. When R/N, k_in and m_tokens are
+ * multiples of 64 and N <= 16, every operand is read where it lies (W from its row shards
+ * for dX, dY and X for dW, as MN-major tensor-core operands): 0 bytes. Other shapes need
+ * transposed copies W^T (2*R*K bytes), dY^T (2*R*N*M) and X^T (2*K*N*M), each rounded up
+ * to 256 bytes. */
 ZERO_API int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t k_in, int64_t m_tokens,
                                           uint64_t* bytes);
 
@@ -307,8 +304,8 @@ ZERO_API int fsdp_unit_backward_workspace(int n_ranks, int64_t rows_out, int64_t
  * dX[q]: out, row-major [m_tokens, k_in] fp32: dX_q = dY_q W;
  * dW: out, row-major [rows_out, k_in] fp32: dW = (1/N) sum_q dY_q^T X_q; rank r's
  *     reduce-scattered shard is rows [r*R/N, (r+1)*R/N).
- * workspace: device buffer of fsdp_unit_backward_workspace() bytes (caller-owned scratch),
- *     or at least the X^T part of it for the shapes that read dY in place (see above).
+ * workspace: device buffer of fsdp_unit_backward_workspace() bytes (caller-owned scratch);
+ *     may be NULL when that size is 0.
  * Requires rows_out % N == 0 and k_in, rows_out, N*m_tokens multiples of 8; all buffers
  * 16-byte aligned. fp32 accumulation on the tensor cores in an unspecified order: each dX
  * entry is within (R+1) 2^-23 sum|dy w| and each dW entry within (N M + 1) 2^-23 (1/N)
@@ -361,12 +358,12 @@ typedef struct {
 } fsdp_unit_state;
 
 /* flags of fsdp_zero3_step */
-#define FSDP_GATHER_MATERIALIZE 1 /* forward: gather each unit's W into a workspace slot (the all-gather's
-                                     receive buffer: sharded model + the unit in use), reused after the unit;
-                                     without it the forward GEMM reads every tile straight from its shard.
-                                     The backward always gathers W^T into the slot (below). */
-#define FSDP_BACKWARD_PREFETCH 2  /* issue unit i-1's gather and dW operand layout on prefetch_stream while
-                                     unit i's backward GEMMs run on `stream` */
+#define FSDP_GATHER_MATERIALIZE 1 /* gather each unit's W into a workspace slot (the all-gather's receive
+                                     buffer: sharded model + the unit in use) before its forward and again
+                                     before its backward; without it both GEMMs read every tile straight
+                                     from its shard */
+#define FSDP_BACKWARD_PREFETCH 2  /* with FSDP_GATHER_MATERIALIZE: issue unit i-1's gather on prefetch_stream
+                                     while unit i's backward runs on `stream`; without it, no effect */
 #define FSDP_OVERLAP_OPTIMIZER 4  /* run unit i's Adam as its own launch on prefetch_stream once its dW is
                                      done, beside the following units' backward GEMMs on `stream` */
 #define FSDP_SEPARATE_OPTIMIZER 8 /* run each Adam as its own launch (zero_adam_step) after the dW GEMM on
@@ -376,10 +373,9 @@ typedef struct {
                                      same operations, the same bits), and dW is written only if given */
 
 /* Bytes of device workspace fsdp_zero3_step needs for these units, M tokens per rank and
- * flags: one slot (two with FSDP_BACKWARD_PREFETCH) holding the dW GEMM's laid-out operand
- * (X^T [k_in, N*M] or dY^T [rows_out, N*M], the narrower: 2*min(rows_out, k_in)*N*M bytes,
- * the largest over the units) and the gathered W^T (or W) of the largest unit,
- * 2*rows_out*k_in bytes; each part rounded up to 256 bytes. Only the units' sizes are read. */
+ * flags: 0 without FSDP_GATHER_MATERIALIZE; with it, one slot (two with
+ * FSDP_BACKWARD_PREFETCH) for the gathered W of the largest unit, 2*rows_out*k_in bytes
+ * rounded up to 256. Only the units' sizes are read. */
 ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit_state* units, int64_t m_tokens,
                                        int flags, uint64_t* bytes);
 
@@ -388,15 +384,15 @@ ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit
  *   forward, unit 0 -> last: gather W_i (fused into the GEMM's loads, or into a workspace
  *     slot), X_{i+1} = bf16(X_i W_i^T) for every rank (the last unit's output goes to y_out;
  *     with y_out NULL that product is skipped), W_i freed;
- *   backward, last -> unit 0: gather W_i again, as W_i^T into a workspace slot (with
- *     X_i^T, in one launch), dY_{i-1} = bf16(dY_i W_i) (unit 0: into dx_out, skipped when
- *     NULL) with both GEMM operands K-major, dW_i = (1/N) sum_q dY_{i,q}^T X_{i,q} (the narrower
- *     of X_i and dY_i laid out transposed in the same launch as W_i^T, the other read in place; the reduce of the
- *     reduce-scatter inside the fp32 tensor-core accumulation, rank r keeping its rows),
+ *   backward, last -> unit 0: gather W_i again (fused into the dX GEMM's loads, which read
+ *     W_i's shards as an MN-major operand, or into the slot), dY_{i-1} = bf16(dY_i W_i)
+ *     (unit 0: into dx_out, skipped when NULL), dW_i = (1/N) sum_q dY_{i,q}^T X_{i,q} (dY_i
+ *     and X_i read in place as MN-major operands; the reduce of the reduce-scatter inside
+ *     the fp32 tensor-core accumulation, rank r keeping its rows),
  *     then each rank's Adam on its shard (the operations of zero_adam_step, fused into the
  *     dW GEMM's epilogue by default) writing the new bf16 shards of W_i — after W_i's last
  *     use;
- *   with FSDP_BACKWARD_PREFETCH, unit i-1's gather and dW operand layout run on
+ *   with FSDP_GATHER_MATERIALIZE and FSDP_BACKWARD_PREFETCH, unit i-1's gather runs on
  *     prefetch_stream while unit i computes ([Interview] follow-up "FSDP 怎么把通信藏起来?":
  *     the all-gather on its own stream, the backward prefetching the next unit's);
  *   with FSDP_OVERLAP_OPTIMIZER, unit i's Adam runs on prefetch_stream after its dW, while
@@ -406,11 +402,11 @@ ZERO_API int fsdp_zero3_step_workspace(int n_ranks, int n_units, const fsdp_unit
  * bf16 products in an unspecified order (bounds as fsdp_unit_backward), rounded once to
  * bf16; Adam is bit-exact as zero_adam_step.
  * Requires 1 <= N <= 16, 1 <= n_units <= 64, N*M % 8 == 0; per unit rows_out a multiple of
- * N and of 8, k_in % 8 == 0, the larger of rows_out and k_in a multiple of 64 (the dW GEMM
- * reads that operand, dY or X, in place), and without FSDP_GATHER_MATERIALIZE the fused gather's shard
- * rule ((rows_out / N) % 128 == 0; 256 under zero_set_gemm_kernel(1)); 16-byte-aligned
- * buffers; workspace of fsdp_zero3_step_workspace() bytes. prefetch_stream may be NULL
- * (then everything runs on `stream`). */
+ * N with rows_out / N and k_in multiples of 64 (the backward reads W's shards, dY and X in
+ * place), and without FSDP_GATHER_MATERIALIZE the fused gather's shard rule ((rows_out /
+ * N) % 128 == 0; 256 under zero_set_gemm_kernel(1)); 16-byte-aligned buffers; workspace of
+ * fsdp_zero3_step_workspace() bytes (NULL when 0). prefetch_stream may be NULL (then
+ * everything runs on `stream`). */
 ZERO_API int fsdp_zero3_step(int n_ranks, int n_units, const fsdp_unit_state* units, int64_t m_tokens,
                              zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step, int flags,
                              void* workspace, uint64_t workspace_bytes, zero_stream_t stream,
@@ -445,10 +441,10 @@ typedef struct {
   float* dw_down;   /* out, [d_model, d_ff]: (1/N) sum_q dY_q^T H_q; NULL as dw_gu */
 } fsdp_mlp_unit_state;
 
-/* Bytes of device workspace fsdp_zero3_mlp_step needs: one slot for the gathered W^T of the
- * unit in use (W_down^T, then [W_gate; W_up]^T: 4*d_ff*d_model bytes at most) and one for
- * the dW GEMMs' laid-out operand (the narrower of dY and H, then of [dG | dU] and X, as a
- * transpose: 2*min(.)*N*M bytes), the largest over the units, each rounded up to 256 bytes. */
+/* Bytes of device workspace fsdp_zero3_mlp_step needs: 0 for N <= 8, where every backward
+ * GEMM reads its operands in place (the dX GEMM takes the 2N shards of W_gate and W_up as
+ * its pieces); for N > 8 one slot for the gathered [W_gate; W_up] of the largest unit,
+ * 4*d_ff*d_model bytes rounded up to 256. */
 ZERO_API int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsdp_mlp_unit_state* units,
                                            int64_t m_tokens, uint64_t* bytes);
 
@@ -458,13 +454,14 @@ ZERO_API int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsdp_
  *   forward, unit 0 -> last: G | U and H = silu(G) * U in one tensor-core kernel (the gate
  *     and up shards gathered inside its loads), then X_{i+1} = bf16(H W_down^T) (the last
  *     unit's output to y_out; skipped when NULL);
- *   backward, last -> unit 0: W_down gathered again as W_down^T; dH = bf16(dY W_down);
+ *   backward, last -> unit 0 (every GEMM operand read where it lies, K-major or MN-major):
+ *     dH = bf16(dY W_down), W_down's shards gathered again inside the loads;
  *     dW_down = (1/N) sum_q dY_q^T H_q with each rank's Adam on its W_down shard in the GEMM's
  *     epilogue (or, with FSDP_SEPARATE_OPTIMIZER in flags, as its own launch); dG | dU by the
  *     SiLU-gate backward (s = 1/(1 + exp(-g)): dU = dH g s, dG = dH U s (1 + g (1 - s)), fp32
- *     from the saved bf16 G, U and dH, rounded to bf16); [W_gate; W_up] gathered as its
- *     transpose; dY_{i-1} = bf16([dG | dU] [W_gate; W_up]) (unit 0: into dx_out, skipped
- *     when NULL); dW_gate | dW_up = (1/N) sum_q [dG | dU]_q^T X_q with each rank's Adam on its
+ *     from the saved bf16 G, U and dH, rounded to bf16); dY_{i-1} = bf16([dG | dU] [W_gate;
+ *     W_up]) over the 2N shards of both (gathered into the workspace first when N > 8;
+ *     unit 0: into dx_out, skipped when NULL); dW_gate | dW_up = (1/N) sum_q [dG | dU]_q^T X_q with each rank's Adam on its
  *     W_gate and W_up shards in the same way. Every weight's update follows its last read.
  * The reduce over ranks happens inside the fp32 accumulation of each dW GEMM; rank r's
  * reduce-scattered gradient is its rows. GEMM outputs are fp32 sums of exact bf16 products
@@ -473,7 +470,7 @@ ZERO_API int fsdp_zero3_mlp_step_workspace(int n_ranks, int n_units, const fsdp_
  * Requires 1 <= N <= 16, 1 <= n_units <= 64, N*M % 8 == 0, d_model and d_ff multiples of 64,
  * unit i+1's d_model equal to unit i's, (d_ff / N) % 128 == 0 and d_model / N tiling the fused
  * gather ((d_model / N) % 128 == 0; 256 under zero_set_gemm_kernel(1)); 16-byte-aligned
- * buffers; workspace of fsdp_zero3_mlp_step_workspace() bytes. */
+ * buffers; workspace of fsdp_zero3_mlp_step_workspace() bytes (NULL when 0). */
 ZERO_API int fsdp_zero3_mlp_step(int n_ranks, int n_units, const fsdp_mlp_unit_state* units, int64_t m_tokens,
                                  zero_bf16* y_out, zero_bf16* dx_out, const zero_adam* hp, int64_t step, int flags,
                                  void* workspace, uint64_t workspace_bytes, zero_stream_t stream);
@@ -523,10 +520,9 @@ ZERO_API int zero_selftest_bounded_wait(uint32_t timeout_ms, zero_stream_t strea
 ZERO_API int zero_set_fused_kernel(int which);
 
 /* Select the tensor-core GEMM kernel of the FSDP calls. 0 = default: the CTA-pair kernel
- * (tcgen05.mma.cta_group::2, a cluster of two CTAs on two SMs per 256-row tile) wherever
- * both operands are K-major (every forward, the MLP unit, the backward's transposed path),
- * the one-CTA kernel where an operand is MN-major (the backward's in-place GEMMs). 1 = the
- * one-CTA kernel everywhere; 2 = the CTA-pair kernel everywhere. All give bit-identical
+ * (tcgen05.mma.cta_group::2, a cluster of two CTAs on two SMs per 256-row tile) for every
+ * GEMM, K-major or MN-major operands alike. 1 = the one-CTA kernel everywhere; 2 = the
+ * CTA-pair kernel everywhere (the same as 0). All give bit-identical
  * results (each output sums the same products in the same order). The fused gather needs
  * rows_out / n_ranks to be a multiple of 128 on the pair kernel, of 256 on the one-CTA
  * kernel. Process-wide; affects calls made after it returns. */
