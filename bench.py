@@ -1222,22 +1222,26 @@ def run_case(args):
         byts = 4 * R * K
         out.update(R=R, K=K, n_ranks=n, gather_ms=ms_g, transpose_ms=ms_t, bytes=byts,
                    gather_gbs=byts / ms_g / 1e6, transpose_gbs=byts / ms_t / 1e6)
-    elif args.case == "zero3_step":
+    elif args.case in ("zero3_step", "zero3_unit_small"):
         # one ZeRO-3 step over the 4 Mistral-shaped units, N = 8 ranks x 1024 tokens, each
-        # rank's Adam fused into the dW GEMMs (about 7 GB on the device), 3 steps
+        # rank's Adam fused into the dW GEMMs (about 7 GB on the device), 3 steps;
+        # zero3_unit_small: the second unit alone (W [4096, 14336], about 1.4 GB): per step
+        # its forward GEMM, dX GEMM and fused dW GEMM
         n, m = 8, 1024
-        units = zero3_units(z, synth, dev, n, m)
+        shapes = ZERO3_SHAPES if args.case == "zero3_step" else ZERO3_SHAPES[1:2]
+        units = zero3_units(z, synth, dev, n, m, shapes=shapes)
         flags = 0  # each rank's Adam fused into the dW GEMMs
         units = [{k: v for k, v in u.items() if k != "dw"} for u in units]
-        ws = torch.empty(z.fsdp_zero3_step_workspace(n, ZERO3_SHAPES, m, flags), dtype=torch.uint8, device=dev)
-        y = torch.empty(n * m, ZERO3_SHAPES[-1][0], dtype=torch.bfloat16, device=dev)
-        dx = torch.empty(n * m, ZERO3_SHAPES[0][1], dtype=torch.bfloat16, device=dev)
+        wsb = z.fsdp_zero3_step_workspace(n, shapes, m, flags)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
+        y = torch.empty(n * m, shapes[-1][0], dtype=torch.bfloat16, device=dev)
+        dx = torch.empty(n * m, shapes[0][1], dtype=torch.bfloat16, device=dev)
         side = torch.cuda.Stream()
         hp = {"lr": 1e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.0}
         ms = time_launches(lambda: z.fsdp_zero3_step(units, m, hp, 1, y_out=y, dx_out=dx, flags=flags, workspace=ws,
                                                      stream=stream, prefetch_stream=side), 2, stream)
-        flop = sum(6.0 * n * m * R * K for R, K in ZERO3_SHAPES)
-        out.update(n_ranks=n, tokens_per_rank=m, ms=ms, tflops=flop / ms / 1e9)
+        flop = sum(6.0 * n * m * R * K for R, K in shapes)
+        out.update(n_ranks=n, tokens_per_rank=m, units=len(shapes), ms=ms, tflops=flop / ms / 1e9)
     elif args.case in ("zero3_mlp_step", "zero3_mlp_small"):
         # one ZeRO-3 step over 2 Mistral-7B MLP units, N = 8 ranks x 1024 tokens (about
         # 10 GB on the device), 3 steps; zero3_mlp_small: one unit, 8 x 256 tokens (2.7 GB)
@@ -1277,7 +1281,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="one measured case: fused_small | fused_tma_small | megatron_small | e2e_small | legs_small | gather_w_up | gemm_small | gemm_w_up | mlp_unit | "
-                         "backward_up | rank_view_small | zero3_step | zero3_mlp_step | zero3_mlp_small (ncu-sized) | "
+                         "backward_up | rank_view_small | zero3_step | zero3_unit_small (ncu-sized) | zero3_mlp_step | "
+                         "zero3_mlp_small (ncu-sized) | "
                          "tiny | mistral_rank_view")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
