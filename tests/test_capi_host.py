@@ -287,3 +287,13 @@ def test_zero3_step_rejects_bad_arguments_before_launch(z):
     assert call(units(good, plans), nr=17) == -1                 # at most 16 ranks
     assert call(units(good, plans), mm=3) == -1                  # N M a multiple of 8
     assert call(units(good, plans), nu=0) == -1
+
+
+def test_zero3_mlp_step_workspace_sizes(z):
+    """The MLP step reads every backward operand in place up to 8 ranks (no workspace);
+    past 8 the 2N shards of [W_gate; W_up] exceed the GEMM's 16 pieces and the largest
+    unit's [W_gate; W_up] is gathered into the workspace (4 d_ff d_model bytes)."""
+    assert z.fsdp_zero3_mlp_step_workspace(8, [(4096, 14336)] * 2, 1024) == 0
+    assert z.fsdp_zero3_mlp_step_workspace(2, [(256, 1024)] * 3, 64) == 0
+    assert z.fsdp_zero3_mlp_step_workspace(12, [(1536, 1536)], 16) == 4 * 1536 * 1536
+    assert z.fsdp_zero3_mlp_step_workspace(16, [(2048, 2048), (2048, 4096)], 16) == 4 * 4096 * 2048
