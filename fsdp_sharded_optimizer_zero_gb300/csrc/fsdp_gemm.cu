@@ -641,8 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1) fsdp_gemm_kernel(const __grid_con
 //              which expects the stage bytes of both;
 //   even CTA   warp 1: issues the MMAs; tcgen05.commit multicasts to both CTAs' empty
 //              barriers (a stage is free in both) and accumulator barriers;
-//   both CTAs  warps 2-5: epilogue of the CTA's own 128 rows from its own TMEM; each warp
-//              then arrives on the even CTA's accumulator-empty barrier (8 arrivals).
+//   both CTAs  warps 2-5 (2-9 with the fused optimizer): epilogue of the CTA's own 128 rows
+//              from its own TMEM; each warp then arrives on the even CTA's
+//              accumulator-empty barrier (8 arrivals, 16).
 // Before leaving, each producer waits until the MMAs released every stage it filled, and
 // the two CTAs meet at a cluster barrier, so neither CTA's shared memory or barriers are
 // still targeted by the other; every mbarrier wait is bounded as in the one-CTA kernel.
@@ -652,8 +653,8 @@ constexpr uint32_t PAIR_ACC = 256;                // TMEM columns of one accumul
 // Per variant: with the fused optimizer the epilogue does most of the kernel's instruction
 // issue (the Adam arithmetic of a 128 x 256 tile per CTA) and its state loads' latency, so
 // it runs 8 warps, two per TMEM lane quarter splitting the columns, with 16 rows of state
-// loads in flight each (200 registers at 320 threads); their staging buffers take one
-// operand stage (5 instead of 6; 5 measured within 1 % of 6 on the plain GEMMs).
+// loads in flight each (168 registers at 320 threads, no spills); their staging buffers
+// take one operand stage (5 instead of 6; 5 measured within 1 % of 6 on the plain GEMMs).
 template <bool ADAM> struct PairCfg {
   static constexpr int EPI_WARPS = ADAM ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
@@ -855,8 +856,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<ADAM>::THREA
 }
 
 // ---- host side ----
-// 0: CTA-pair kernel for K-major operands, one-CTA kernel otherwise; 1: one-CTA kernel
-// everywhere; 2: CTA-pair kernel everywhere
+// 0 (default) and 2: the CTA-pair kernel for every GEMM; 1: the one-CTA kernel everywhere
 std::atomic<int> g_gemm_kernel{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
