@@ -213,6 +213,34 @@ def test_zero3_step_without_dw_output_same_update(z):
             assert torch.equal(ua[key].view(torch.int32), ub[key].view(torch.int32)), key
 
 
+@pytest.mark.parametrize("flags", [0, 8])
+def test_zero3_step_same_bits_on_both_gemm_kernels(z, flags):
+    """The step on the one-CTA GEMM kernel (zero_set_gemm_kernel(1): its own layout
+    instantiations, and its 4-warp fused-optimizer epilogue) leaves every buffer bit for bit
+    as on the default CTA-pair kernel, over two steps, with Adam fused (0) or separate (8).
+    Shard rows of 256 so that both kernels take the fused gather."""
+    n, shapes, m = 4, [(1024, 256), (1024, 1024), (1024, 1024)], 72
+    base = make_units(z, n, shapes, m, key=29)
+    out = []
+    try:
+        for kernel in (0, 1):
+            z.zero_set_gemm_kernel(kernel)
+            units = clone_units(base)
+            for t in (1, 2):
+                y, dx = run_step(z, units, m, t, flags)
+            out.append((units, y, dx))
+    finally:
+        z.zero_set_gemm_kernel(0)
+    (ua, ya, dxa), (ub, yb, dxb) = out
+    assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
+    assert torch.equal(dxa.view(torch.int16), dxb.view(torch.int16))
+    for a, b in zip(ua, ub):
+        for key in ("w", "x", "dy"):
+            assert torch.equal(a[key].view(torch.int16), b[key].view(torch.int16)), key
+        for key in ("master", "m", "v", "dw"):
+            assert torch.equal(a[key].view(torch.int32), b[key].view(torch.int32)), key
+
+
 def test_zero3_step_units_equal_standalone_calls(z):
     """One unit's part of the step equals the standalone calls: the forward output equals
     fsdp_unit_forward's bf16 output, dX equals RNE of fsdp_unit_backward's fp32 dX, dW is

@@ -248,6 +248,36 @@ def test_zero3_mlp_optimizer_fused_or_separate_same_bits(z):
             assert torch.equal(ua[key].view(torch.int32), ub[key].view(torch.int32)), key
 
 
+@pytest.mark.parametrize("flags", [0, 8])
+def test_zero3_mlp_step_same_bits_on_both_gemm_kernels(z, flags):
+    """The MLP step on the one-CTA GEMM kernel (zero_set_gemm_kernel(1)) leaves every buffer
+    bit for bit as on the default CTA-pair kernel, over two steps, Adam fused or separate."""
+    n, d, f, m = 2, 512, 512, 72
+    base = make_units(z, n, d, f, 2, m, key=31)
+    out = []
+    try:
+        for kernel in (0, 1):
+            z.zero_set_gemm_kernel(kernel)
+            units = clone(base)
+            for t in (1, 2):
+                y, dx = run_step(z, units, m, t, flags)
+            out.append((units, y, dx))
+    finally:
+        z.zero_set_gemm_kernel(0)
+    (ua, ya, dxa), (ub, yb, dxb) = out
+    assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
+    assert torch.equal(dxa.view(torch.int16), dxb.view(torch.int16))
+    for a, b in zip(ua, ub):
+        for key in ("x", "gu", "h", "dy", "dh", "dgu"):
+            assert torch.equal(a[key].view(torch.int16), b[key].view(torch.int16)), key
+        for key in ("dw_gu", "dw_down"):
+            assert torch.equal(a[key].view(torch.int32), b[key].view(torch.int32)), key
+        for w in ("gate", "up", "down"):
+            assert torch.equal(a[w]["w"].view(torch.int16), b[w]["w"].view(torch.int16)), w
+            for key in ("master", "m", "v"):
+                assert torch.equal(a[w][key].view(torch.int32), b[w][key].view(torch.int32)), (w, key)
+
+
 def test_zero3_mlp_forward_equals_the_mlp_forward_call(z):
     """The step's forward equals fsdp_mlp_forward on the same shards: H bit for bit, and
     the unit's bf16 output equals RNE of that call's fp32 Y."""
