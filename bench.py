@@ -901,6 +901,40 @@ def oracle_beside_legs(legs: dict, budget_s: float = 1.5):
                 "value": 4.0 * rows * R * K / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                 "sample": f"one rank's {rows} of 2048 tokens: dX and dW against the full 14336 x 4096 weight "
                           f"(float64); {k} calls"}
+    t_adam = n_params / legs["adam_step"]["cpu_oracle"]["value"] if isinstance(legs.get("adam_step"), dict) \
+        and "cpu_oracle" in legs["adam_step"] else None
+    z3 = legs.get("fsdp_zero3_step")
+    if isinstance(z3, dict) and "serial" in z3:
+        # one unit of the step, the oracle's way: forward, dX and dW on 16 token rows of one
+        # rank against the full 14336 x 4096 weight; Adam from its 4M-parameter timing
+        R, K, rows = 14336, 4096, 16
+        shards = [x.view(torch.int16).numpy().view(np.uint16) for x in synth.weight_shards(R, K, n)]
+        a = synth.activations(rows, K).view(torch.int16).numpy().view(np.uint16)
+        dy = synth.upstream_grad(rows, R).view(torch.int16).numpy().view(np.uint16)
+        t, k = _time_bounded(lambda: (O.fsdp_linear_forward(a, shards), O.fsdp_linear_backward(a, shards, dy, n)),
+                             budget_s)
+        z3["cpu_oracle"] = {"value": 6.0 * rows * R * K / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                            "adam_params_per_s": (n_params / t_adam) if t_adam else None,
+                            "sample": f"one 14336 x 4096 unit from 8 shards: forward, dX and dW on {rows} token rows "
+                                      f"of one rank (float64); {k} calls; Adam as in legs.adam_step"}
+    zm = legs.get("fsdp_zero3_mlp_step")
+    if isinstance(zm, dict) and "fused_optimizer" in zm:
+        # one Mistral MLP unit's forward (gate, up, SiLU gate, down) and its SiLU-gate
+        # backward on 16 token rows, the oracle's way
+        D, F, rows = 4096, 14336, 16
+        gs = [x.view(torch.int16).numpy().view(np.uint16) for x in synth.weight_shards(F, D, n, seed_key=1)]
+        us = [x.view(torch.int16).numpy().view(np.uint16) for x in synth.weight_shards(F, D, n, seed_key=2)]
+        ds = [x.view(torch.int16).numpy().view(np.uint16) for x in synth.weight_shards(D, F, n, seed_key=3)]
+        x = synth.activations(rows, D).view(torch.int16).numpy().view(np.uint16)
+        dh = synth.upstream_grad(rows, F).view(torch.int16).numpy().view(np.uint16)
+        gu = synth.activations(rows, 2 * F).view(torch.int16).numpy().view(np.uint16)
+        t, k = _time_bounded(lambda: (O.mlp_unit_forward(x, gs, us, ds),
+                                      O.silu_gate_backward(dh, gu[:, :F], gu[:, F:])), budget_s)
+        zm["cpu_oracle"] = {"value": 3 * 2.0 * rows * D * F / t / 1e12, "unit": "TFLOP/s", "cores": 1,
+                            "kind": "oracle", "adam_params_per_s": (n_params / t_adam) if t_adam else None,
+                            "sample": f"one Mistral MLP unit from 8 shards per weight: forward (gate, up, SiLU gate, "
+                                      f"down) and the SiLU-gate backward on {rows} token rows (float64); {k} calls; "
+                                      "Adam as in legs.adam_step"}
 
 
 def host_info() -> dict:
