@@ -717,10 +717,19 @@ def fsdp_leg(z, synth, dev, tf_peak, peak_src, stream):
         ms_g = time_launches(lambda: z.fsdp_gather_rows(shards_up, wfull, stream=stream), 20, stream)
         ms_t = time_launches(lambda: z.fsdp_transpose_cat(shards_up, wfull.view(4096, 14336), stream=stream), 20,
                              stream)
+        # a plain device-to-device copy of the same bytes, timed the same way: at 2 x 117 MB
+        # per launch, ramp-up and drain cap every copy below the long-copy peak
+        src_up = torch.cat(shards_up, 0)
+        ms_c = time_launches(lambda: wfull.copy_(src_up), 20, stream)
         b_gt = 4.0 * 14336 * 4096
-        res["gather_rows_w_up"] = {"ms": ms_g, "gbs": b_gt / ms_g / 1e6, "frac": b_gt / ms_g / 1e6 / hbm}
-        res["transpose_cat_w_up"] = {"ms": ms_t, "gbs": b_gt / ms_t / 1e6, "frac": b_gt / ms_t / 1e6 / hbm}
-        del shards_up, wfull
+        res["gather_rows_w_up"] = {"ms": ms_g, "gbs": b_gt / ms_g / 1e6, "frac": b_gt / ms_g / 1e6 / hbm,
+                                   "frac_of_same_size_copy": ms_c / ms_g}
+        res["transpose_cat_w_up"] = {"ms": ms_t, "gbs": b_gt / ms_t / 1e6, "frac": b_gt / ms_t / 1e6 / hbm,
+                                     "frac_of_same_size_copy": ms_c / ms_t}
+        res["copy_same_bytes_w_up"] = {"ms": ms_c, "gbs": b_gt / ms_c / 1e6, "frac": b_gt / ms_c / 1e6 / hbm,
+                                       "note": "torch copy_ of W_up's 117 MB (not this library's code): what a "
+                                               "plain copy of this size reaches, for the two rows above"}
+        del shards_up, wfull, src_up
         # the full MLP unit: gate + up in one kernel with the SiLU-gate epilogue, then down
         gs_ = synth.weight_shards(14336, 4096, n, device=dev, seed_key=12)
         us_ = synth.weight_shards(14336, 4096, n, device=dev, seed_key=11)
