@@ -28,8 +28,10 @@
 //                 is released, so the epilogue of tile i overlaps the main loop of tile i+1.
 // Other modes of both kernels: gate-up (two B operands, one N = 256 MMA per K step,
 // SiLU-gate epilogue writing bf16 H), A split by rows into pieces with matching Y pieces
-// (the backward's dX for all ranks in one launch), and MN-major A / B operands split along
-// K (the backward reading W and dY in place; see GemmParams).
+// (the backward's dX for all ranks in one launch), MN-major A / B operands split along
+// K (the backward reading W and dY in place; see GemmParams), and the fused optimizer
+// (template parameter ADAM): the weight-gradient GEMM's epilogue runs each rank's Adam on
+// its rows of the reduce-scattered result (adam_chunk_rows) instead of storing it.
 // Every mbarrier wait is bounded (error word + CTA abort flag, no trap); after an abort
 // the producer drains its copies and the MMA warp its MMAs before TMEM is released.
 #include <cuda.h>
