@@ -198,19 +198,21 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, in
   }
 }
 
-// Fused optimizer. Measured on GB300 (the ZeRO-3 steps, against the same Adam as its own
-// launch): per-lane row loads of the state ran 6-14 % slower, whatever their order; staging
-// the chunk and walking rows with one column per lane (coalesced 128-byte lines), 16 rows
-// in flight, 4 % slower; 32 rows in flight, level; plus L2 prefetches two chunks ahead,
-// -3 to +1 %. The epilogue is bound by the state loads' latency: 128 threads hold ~48 KB in
-// flight per SM against the ~100 KB that HBM's bandwidth-latency product asks for.
+// Fused optimizer. Measured on GB300 (the ZeRO-3 steps): per-lane row loads of the state
+// ran 6-14 % slower than the walk below, whatever their order; with the walk, 32 rows in
+// flight on the one-CTA kernel's 4 epilogue warps and 8 to 16 on the pair kernel's 8 are
+// best (fewer leave too few loads in flight, more spill); L2 prefetches two chunks ahead,
+// -3 to +1 %. On the pair kernel the epilogue runs about as long as the main loop beside
+// it, and its parts weigh a few per cent of the step each: the update's arithmetic (the
+// correctly rounded divisions and square root about half of that), the state's DRAM
+// traffic, and the state's stores.
 //
 // fused optimizer on one 32 x 32 chunk of the fp32 result, staged in shared memory (buf,
 // 128-byte rows, 16-byte piece j of row i at slot j ^ (i % 8)): result (i, c) is the
 // reduced gradient of parameter (row0 + i - split) * R + col0 + c of the weight set the
 // chunk's rows belong to (a chunk's 32 rows never straddle the split: it is a multiple of
 // 128). The warp walks the chunk's rows with one column per lane, so every state access
-// is one contiguous 128-byte line; all 32 rows' loads are in flight before their arithmetic.
+// is one contiguous 128-byte line; ROWS rows' loads are in flight before their arithmetic.
 // adam_elem: the same operations as the Adam kernels (same bits).
 constexpr int kAdamRows = 32;  // rows of a staged chunk whose state loads are in flight together (one-CTA kernel)
 // L2 prefetch of the optimizer state the chunk at columns col0 .. col0 + 31 of rows
