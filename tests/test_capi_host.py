@@ -68,6 +68,34 @@ def test_plan_matches_oracle(z, psi, n, bb, stage):
     assert L["fused_step_bytes"] == lay.psi_padded * (grad_bytes * n + 26)
 
 
+def test_plan_matches_oracle_on_random_sizes(z):
+    """400 seeded (psi, N, bucket bytes, stage) draws, psi from 1 to 2^40 on a log scale,
+    N from 1 to 64, buckets from 2N bytes (one element per rank) to 4 GiB: layout, bytes and
+    counts equal the oracle's, and the first, last and a middle bucket of the first and
+    last rank equal its bucket ranges."""
+    import numpy as np
+    rng = np.random.default_rng(20261202)
+    for _ in range(400):
+        psi = int(np.exp(rng.uniform(0.0, 40.0 * np.log(2.0))))
+        psi = max(psi, 1)
+        n = int(rng.integers(1, 65))
+        bb = int(rng.integers(2 * n, (4 << 30) + 1))
+        stage = STAGES[int(rng.integers(0, len(STAGES)))]
+        p = z.zero_plan(psi, n, stage, bb)
+        lay = O.make_layout(psi, n, bb)
+        L = p.layout
+        case = (psi, n, bb, stage)
+        assert (L["psi_padded"], L["shard_elems"], L["bucket_elems"], L["n_buckets"]) == \
+            (lay.psi_padded, lay.shard, lay.bucket_elems, lay.n_buckets), case
+        mb = O.model_state_bytes(stage, lay)
+        assert L["state_total_bytes"] == mb["total"], case
+        c = O.comm_elements(stage, lay)
+        assert L["comm_total"] == c["total"], case
+        for r in {0, n - 1}:
+            for k in {0, lay.n_buckets // 2, lay.n_buckets - 1}:
+                assert z.zero_bucket_range(p, r, k) == O.bucket_range(lay, r, k), case
+
+
 @pytest.mark.parametrize("psi,n,bb", [(13, 3, 6), (1000, 8, 48), (4099, 5, 1 << 10)])
 def test_bucket_ranges_match_oracle(z, psi, n, bb):
     p = z.zero_plan(psi, n, "zero2", bb)
